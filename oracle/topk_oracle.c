@@ -1,0 +1,182 @@
+/*
+ * Exact per-row top-k of BF16 logits: the plain CPU definition.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the oracle the CUDA path is checked
+ * against. Only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * load it; the product library never does, and the two share no code.
+ *
+ * What it computes follows the vLLM page "decode_topk_cute" (module docstring,
+ * "What this module computes"):
+ *   - for each row, the indices of its k largest elements, in any order; exact:
+ *     every index whose value exceeds the k-th largest, then enough of those
+ *     equal to it;
+ *   - a row of at most k elements returns 0 .. n-1 and -1 padding, without
+ *     looking at the values;
+ *   - token mode: an element is one BF16 logit;
+ *   - block mode: an element is the NaN-propagating maximum of an aligned group
+ *     of 8 logits; the row's newest block is pinned at +inf, and blocks that
+ *     score -inf are written as -1;
+ *   - values are compared through an order-preserving 16-bit key of their BF16
+ *     bits, so ties are exact.
+ * The key is the one the sglang PR #39305 page ("Exact bf16 consumer top-k
+ * adapted from DeepSelect", Modifications) writes as x ^ (x < 0 ? 0xFFFF :
+ * 0x8000): negatives reversed and below the positives, -0 below +0.
+ * Ties at the threshold go to the lowest indices (vLLM kimi_k3 "dsa/indexer"
+ * page, module docstring, IndexerSelect paragraph).
+ * NaN elements are never selected (sglang PR #39305, Modifications).
+ * The block-table transform is the one of IndexerSelect.emit on the kimi_k3
+ * indexer page: physical = table[row][i / page] * page + i % page.
+ *
+ * Readings where the pages leave a step open:
+ *   - valid_len outside [0, width] is clamped to that range;
+ *   - when a row has more than k elements but fewer than k non-NaN ones, the
+ *     result is every non-NaN element followed by -1 padding;
+ *   - the newest block is pinned even when its group holds a NaN;
+ *   - the maximum of {-0, +0} is +0 (the larger key).
+ *
+ * Method: for every candidate, one 64-bit word (key << 32) | (0xFFFFFFFF - i);
+ * sorting those words in descending order sorts by key descending, then index
+ * ascending. The first min(k, candidates) words are the selection.
+ */
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_TOKEN = 0, ORACLE_BLOCK8 = 1 };
+
+/* Order-preserving 16-bit key (sglang PR #39305, "distorted" value order). */
+static uint16_t order_key(uint16_t x) {
+    return (uint16_t)(x ^ ((x & 0x8000u) ? 0xFFFFu : 0x8000u));
+}
+
+/* BF16 NaN: exponent all ones and a non-zero mantissa. */
+static int is_nan_bf16(uint16_t x) { return (x & 0x7FFFu) > 0x7F80u; }
+
+static const uint16_t KEY_POS_INF = 0xFF80u; /* order_key(0x7F80), +inf */
+static const uint16_t KEY_NEG_INF = 0x007Fu; /* order_key(0xFF80), -inf */
+
+static int cmp_desc_u64(const void *a, const void *b) {
+    uint64_t x = *(const uint64_t *)a, y = *(const uint64_t *)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+typedef struct {
+    const uint16_t *logits;
+    int64_t row_stride;
+    int32_t rows, width;
+    const int32_t *valid_len;
+    int32_t k, mode;
+    const int32_t *table;
+    int32_t table_stride, page;
+    int32_t *out;
+    int32_t first_row, row_step;
+    int status;
+} job_t;
+
+/* Block-table transform of a logical element index (IndexerSelect.emit). */
+static int32_t transform(const job_t *j, int32_t r, int32_t i) {
+    if (!j->table) return i;
+    return j->table[(int64_t)r * j->table_stride + i / j->page] * j->page + i % j->page;
+}
+
+static int one_row(const job_t *j, int32_t r) {
+    const uint16_t *row = j->logits + (int64_t)r * j->row_stride;
+    int32_t *out = j->out + (int64_t)r * j->k;
+    int32_t L = j->valid_len[r];
+    if (L < 0) L = 0;
+    if (L > j->width) L = j->width;
+    int32_t n = (j->mode == ORACLE_BLOCK8) ? (L + 7) / 8 : L;
+
+    if (n <= j->k) { /* short row: 0 .. n-1 then -1, values never read */
+        for (int32_t s = 0; s < j->k; ++s) out[s] = s < n ? transform(j, r, s) : -1;
+        return 0;
+    }
+
+    uint64_t *cand = (uint64_t *)malloc((size_t)n * sizeof(uint64_t));
+    if (!cand) return 1;
+    int32_t m = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        uint16_t key;
+        if (j->mode == ORACLE_TOKEN) {
+            uint16_t x = row[i];
+            if (is_nan_bf16(x)) continue;
+            key = order_key(x);
+        } else {
+            int nan = 0;
+            key = 0;
+            int32_t end = 8 * i + 8 < L ? 8 * i + 8 : L;
+            for (int32_t t = 8 * i; t < end; ++t) {
+                if (is_nan_bf16(row[t])) nan = 1;
+                else if (order_key(row[t]) > key) key = order_key(row[t]);
+            }
+            if (i == n - 1) { nan = 0; key = KEY_POS_INF; } /* newest block */
+            if (nan) continue;
+        }
+        cand[m++] = ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+    }
+    qsort(cand, (size_t)m, sizeof(uint64_t), cmp_desc_u64);
+
+    int32_t sel = m < j->k ? m : j->k;
+    for (int32_t s = 0; s < sel; ++s) {
+        uint16_t key = (uint16_t)(cand[s] >> 32);
+        int32_t i = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[s]);
+        if (j->mode == ORACLE_BLOCK8 && key == KEY_NEG_INF) out[s] = -1;
+        else out[s] = transform(j, r, i);
+    }
+    for (int32_t s = sel; s < j->k; ++s) out[s] = -1;
+    free(cand);
+    return 0;
+}
+
+static void *worker(void *arg) {
+    job_t *j = (job_t *)arg;
+    for (int32_t r = j->first_row; r < j->rows; r += j->row_step)
+        if (one_row(j, r)) { j->status = 1; break; }
+    return NULL;
+}
+
+/*
+ * logits: BF16 bits, row r at logits + r * row_stride; valid_len: [rows];
+ * block_table: NULL (identity) or [rows, table_stride] page ids, page elements
+ * per page; out: [rows, k] int32. threads: worker threads over rows (<= 1: the
+ * calling thread only). Returns 0, or 1 on a bad argument or allocation failure.
+ */
+int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                     const int32_t *valid_len, int32_t k, int32_t mode,
+                     const int32_t *block_table, int32_t table_stride, int32_t page_size,
+                     int32_t *out, int32_t threads) {
+    if (rows < 0 || width < 0 || k < 1 || row_stride < width) return 1;
+    if (mode != ORACLE_TOKEN && mode != ORACLE_BLOCK8) return 1;
+    if (block_table && page_size < 1) return 1;
+    if (rows == 0) return 0;
+    if (!logits || !valid_len || !out) return 1;
+    if (threads < 1) threads = 1;
+    if (threads > rows) threads = rows;
+
+    job_t base = {logits, row_stride, rows, width, valid_len, k, mode,
+                  block_table, table_stride, page_size, out, 0, 1, 0};
+    if (threads == 1) {
+        worker(&base);
+        return base.status;
+    }
+    job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)threads);
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)threads);
+    if (!jobs || !tids) { free(jobs); free(tids); return 1; }
+    int32_t started = 0;
+    for (int32_t t = 0; t < threads; ++t) {
+        jobs[t] = base;
+        jobs[t].first_row = t;
+        jobs[t].row_step = threads;
+        if (pthread_create(&tids[t], NULL, worker, &jobs[t]) != 0) { jobs[t].status = 1; break; }
+        ++started;
+    }
+    int status = started == threads ? 0 : 1;
+    for (int32_t t = 0; t < started; ++t) {
+        pthread_join(tids[t], NULL);
+        status |= jobs[t].status;
+    }
+    free(jobs);
+    free(tids);
+    return status;
+}

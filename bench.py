@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Benchmark: exact BF16 top-k on GB300 (one JSON line on stdout).
+
+Headline workload (the consumer top-k of the sglang PR #39305 table): 2048 rows
+x 16384 BF16 logits, every row valid, k = 512, a per-row table of randomly
+permuted 64-token pages. A step is one launch of the whole path (bypass check,
+staging, keys, cutoff, filter, exact select, transformed write) over one batch.
+
+  value       rows/s with inputs resident in HBM (CUDA-graph replay, inputs
+              rotated over enough copies to exceed L2 between reuses)
+  e2e         rows/s through the C ABI with pinned HOST buffers: host->device
+              copy of the logits, valid lengths and table, the launch, and a
+              device->host copy of the indices, every step
+  roofline    algorithmic bytes per launch / mean launch time, against the
+              measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on the host cores (a bounded sample)
+  sweep       every configuration: microseconds/launch, rows/s, GB/s, fraction
+
+--impl reference times the CPU oracle itself on the same workload (the
+reference arm), on rank 0 only.
+Under torchrun (N > 1) every rank runs the same per-GPU batch on its own GPU
+(rows are independent: weak scaling, no collective on the data path); the
+step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+HEADLINE = dict(rows=2048, valid=16384, k=512)
+METRIC = "exact BF16 top-k rows/s (us/launch, HBM GB/s vs measured peak)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(case) -> int:
+    """Bytes a launch must move: every valid logit of rows with n > k, the valid
+    lengths, the output, and one table entry per selected index when a table is
+    given."""
+    rows = case.rows
+    b = case.logit_bytes() + 4 * rows + 4 * rows * case.k
+    if case.block_table is not None:
+        b += 4 * rows * case.k
+    return int(b)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7],
+                                 sw_power=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        sm = sorted(r["sm"] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0]["sm_max"],
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU timing
+
+class GpuCase:
+    """A workload resident on the GPU, rotated over copies to defeat L2."""
+
+    def __init__(self, case, torch, device, min_copies: int = 1, max_bytes: int = 1 << 31):
+        self.case = case
+        self.torch = torch
+        one = torch.from_numpy(np.ascontiguousarray(case.logits).view(np.int16)).to(device)
+        per = one.numel() * 2
+        copies = max(min_copies, -(-2 * L2_BYTES // max(per, 1)))
+        copies = max(1, min(copies, max_bytes // max(per, 1)))
+        self.copies = copies
+        self.logits = one.unsqueeze(0).expand(copies, *one.shape).contiguous()
+        del one
+        self.valid = torch.from_numpy(case.valid_len).to(device)
+        self.table = None if case.block_table is None else torch.from_numpy(case.block_table).to(device)
+        self.out = torch.empty((case.rows, case.k), dtype=torch.int32, device=device)
+
+    def launch(self, i: int, tk):
+        c = self.case
+        tk.select(self.logits[i % self.copies], self.valid, c.k, c.mode, self.table, c.page_size,
+                  out=self.out, width=c.width)
+
+
+def time_graph(gc, tk, torch, steps: int, warmup: int):
+    """Mean microseconds per launch over `steps` launches replayed from a CUDA
+    graph (events on the capture/replay stream)."""
+    stream = torch.cuda.Stream()
+    for i in range(max(3, warmup)):          # eager warm-up (also loads the library)
+        gc.launch(gc.copies - 1 - (i % gc.copies), tk)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            gc.launch(i, tk)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        graph.replay()                        # warm replay
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        stop.record(stream)
+    stop.synchronize()
+    return start.elapsed_time(stop) * 1e3 / steps
+
+
+def flush_l2(torch, device, scratch=[]):
+    if not scratch:
+        scratch.append(torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device))
+    scratch[0].fill_(1)
+
+
+def time_e2e(case, tk, torch, device, steps: int, warmup: int):
+    """rows/s through the public API with pinned host buffers, copies inside."""
+    h_logits = torch.from_numpy(np.ascontiguousarray(case.logits).view(np.int16)).pin_memory()
+    h_valid = torch.from_numpy(case.valid_len).pin_memory()
+    h_table = None if case.block_table is None else torch.from_numpy(case.block_table).pin_memory()
+    h_out = torch.empty((case.rows, case.k), dtype=torch.int32).pin_memory()
+    d_logits = torch.empty_like(h_logits, device=device)
+    d_valid = torch.empty_like(h_valid, device=device)
+    d_table = None if h_table is None else torch.empty_like(h_table, device=device)
+    d_out = torch.empty((case.rows, case.k), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_valid.copy_(h_valid, non_blocking=True)
+        if d_table is not None:
+            d_table.copy_(h_table, non_blocking=True)
+        tk.select(d_logits, d_valid, case.k, case.mode, d_table, case.page_size, out=d_out,
+                  width=case.width)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    stop.synchronize()
+    sec = start.elapsed_time(stop) / 1e3 / steps
+    bi = h_logits.numel() * 2 + h_valid.numel() * 4 + (0 if h_table is None else h_table.numel() * 4)
+    bo = h_out.numel() * 4
+    return case.rows / sec, bi, bo
+
+
+# ----------------------------------------------------------- CPU baseline
+
+def cpu_baseline(case, min_seconds: float = 2.0):
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.topk(case.logits[:8], case.valid_len[:8], case.k, case.mode,
+                None if case.block_table is None else case.block_table[:8], case.page_size,
+                width=case.width, threads=cores)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.topk(case.logits, case.valid_len, case.k, case.mode, case.block_table,
+                    case.page_size, width=case.width, threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    rows_per_s = reps * case.rows / el
+    return {"value": rows_per_s, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) over all {case.rows} rows of the workload "
+                      f"({el:.1f} s wall, {cores} threads)"}
+
+
+# ------------------------------------------------------------------- sweep
+
+def sweep_cases(full: bool):
+    cases = [("config1 token 4x4096 k512", lambda: W.config1(0))]
+    ks = W.CONFIG2_K if full else (512,)
+    for k in ks:
+        for valid in W.CONFIG2_VALID:
+            for rows in W.CONFIG2_ROWS:
+                cases.append((f"config2 consumer {rows}x16384 valid{valid} k{k}",
+                              lambda r=rows, v=valid, kk=k: W.config2(r, v, kk)))
+    cases += [("config3 crowded 64x150000 k512", lambda: W.config3(0)),
+              ("config4 block 32x1048576 k2048", lambda: W.config4(0)),
+              ("config5a wide 256x524288 k512", lambda: W.config5a(0)),
+              ("config5b wide 64x1048576 k512", lambda: W.config5b(0))]
+    return cases
+
+
+def run_sweep(tk, torch, device, steps, warmup, peak, full):
+    out = []
+    for name, make in sweep_cases(full):
+        case = make()
+        gc = GpuCase(case, torch, device)
+        us = time_graph(gc, tk, torch, steps, warmup)
+        ab = algorithmic_bytes(case)
+        gbs = ab / (us * 1e-6) / 1e9
+        out.append({"workload": name, "us_per_launch": round(us, 3),
+                    "rows_per_s": round(case.rows / (us * 1e-6), 1),
+                    "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                    "copies": gc.copies, "plan": tk.plan(case.rows, case.width, case.k, case.mode)})
+        del gc
+        torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep", choices=("none", "k512", "full"), default="k512")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    case = W.config2(HEADLINE["rows"], HEADLINE["valid"], HEADLINE["k"], seed=0)
+    workload = (f"consumer top-k: {case.rows} rows x {case.width} bf16, valid {HEADLINE['valid']}, "
+                f"k={case.k}, permuted 64-token page table")
+    peak, peak_kind = peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        base = cpu_baseline(case, min_seconds=max(2.0, 0.02 * args.steps))
+        v = base["value"]
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": case.rows / v * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16 keys (bf16 bits)", "data": "synthetic",
+            "config": {"workload": workload, "rows": case.rows, "width": case.width, "k": case.k},
+            "cpu_baseline": base,
+            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    import torch
+    import exact_bf16_top_gb300 as tk
+    tk._build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    gc = GpuCase(case, torch, device, min_copies=4)
+    # Warm-up and graph capture happen inside time_graph; time twice, keep the
+    # second (the first replay also pays one-time costs).
+    with ClockSampler(local_rank) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        us = time_graph(gc, tk, torch, args.steps, args.warmup)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    clk = clocks.summary()
+    if dist:
+        t = torch.tensor([us], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us = float(t.item())
+    rows_per_s = world * case.rows / (us * 1e-6)
+    ab = algorithmic_bytes(case)
+    achieved = ab / (us * 1e-6) / 1e9
+    e2e_v, bi, bo = time_e2e(case, tk, torch, device, args.e2e_steps, 3)
+    if dist:
+        t = torch.tensor([e2e_v], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        e2e_v = float(t.item()) * world
+    del gc
+    torch.cuda.empty_cache()
+
+    result = {
+        "metric": METRIC, "value": round(rows_per_s, 1), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
+        "us_per_launch": round(us, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u16 keys (bf16 bits), int32 indices", "data": "synthetic",
+        "config": {"workload": workload, "rows": case.rows, "width": case.width,
+                   "valid_len": HEADLINE["valid"], "k": case.k, "parallelism": f"rows x{world}",
+                   "l2": f"inputs rotated over {max(4, -(-2 * L2_BYTES // (case.rows * case.width * 2)))} "
+                         f"copies (> 2x the 129 MB L2 between reuses)",
+                   "timing": "CUDA graph of `steps` launches, events on the replay stream"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab},
+        "e2e": {"value": round(e2e_v, 1), "unit": "rows/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0 and args.sweep != "none":
+        result["sweep"] = run_sweep(tk, torch, device, max(20, args.steps // 4), 3, peak,
+                                    args.sweep == "full")
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+"""Exact per-row top-k of BF16 logits on GB300: Python binding of libtopk_bf16.
+
+Argument marshalling only: every step of the selection runs in the CUDA kernels
+of ``csrc/topk_bf16.cu`` behind the C ABI declared in ``include/topk_bf16.h``.
+Torch supplies device memory and the current stream. There is no CPU fallback:
+if the library is missing or the tensors are not on a CUDA device, the call
+raises.
+
+The operation (vLLM "decode_topk_cute", module docstring): for every row, the
+indices of its k largest elements (token mode: one BF16 logit; block mode: the
+NaN-propagating maximum of each aligned group of 8 logits, the newest block
+pinned at +inf, -inf blocks written as -1), ties at the k-th largest broken by
+the lowest index, NaN never selected, a row of at most k elements returning
+0..n-1 then -1, and an optional per-row block table applied to the indices.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build
+
+TOKEN = 0
+BLOCK8 = 1
+MAX_K = 2048
+MAX_WIDTH = 1 << 20
+NUM_COUNTERS = 16
+COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_forced", "tile_overshot", "tile_overflow",
+                 "tile_take_all", "compactions", "overflow_rounds", "cluster_merges", "rounds")
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
+           5: "CUDA error"}
+
+
+class TopkError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        super().__init__(f"topk_bf16: {_STATUS.get(status, status)}{(': ' + what) if what else ''}")
+        self.status = status
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("force_direct", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("counters", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libtopk_bf16.so (it must have been built: see ``_build.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"libtopk_bf16.so not built at {p}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        sel_args = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                    ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        lib.topk_bf16_select.argtypes = sel_args
+        lib.topk_bf16_select.restype = ctypes.c_int
+        lib.topk_bf16_select_ex.argtypes = sel_args + [ctypes.POINTER(_Options)]
+        lib.topk_bf16_select_ex.restype = ctypes.c_int
+        lib.topk_bf16_status_string.argtypes = [ctypes.c_int]
+        lib.topk_bf16_status_string.restype = ctypes.c_char_p
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.topk_bf16_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, i32p, i32p, i32p, i32p]
+        lib.topk_bf16_plan.restype = ctypes.c_int
+        lib.topk_bf16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
+        lib.topk_bf16_device_status.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int, what: str = ""):
+    if status != 0:
+        raise TopkError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_size: int = 64,
+           out=None, width: int | None = None, stream=None, *, force_direct: bool = False,
+           cluster: int = 0, counters=None):
+    """Exact top-k of every row of ``logits`` -> int32 [rows, k] on the same device.
+
+    logits: CUDA bfloat16 (or int16/uint16 holding BF16 bits) [rows, row_stride]
+    with unit inner stride, 16-byte aligned rows; valid_len: CUDA int32 [rows];
+    block_table: None or CUDA int32 [rows, pages] (unit inner stride);
+    width: logits per row that may be valid (default: logits.shape[1]);
+    stream: a torch.cuda.Stream (default: the current stream);
+    force_direct / cluster / counters: test hooks (see topk_bf16_select_ex).
+    """
+    import torch
+    if not (isinstance(logits, torch.Tensor) and logits.is_cuda):
+        raise TypeError("logits must be a CUDA tensor")
+    if logits.dtype not in (torch.bfloat16, torch.int16) and str(logits.dtype) != "torch.uint16":
+        raise TypeError("logits must be bfloat16 (or 16-bit BF16 bits)")
+    if logits.dim() != 2 or (logits.shape[1] > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be 2-D with unit inner stride")
+    rows, cols = logits.shape
+    width = cols if width is None else int(width)
+    if width > cols:
+        raise ValueError("width exceeds the logits' columns")
+    row_stride = logits.stride(0) if rows > 1 else -(-cols // 8) * 8
+    # The kernels read whole 16-byte vectors: each row must be readable up to
+    # the next multiple of 8 logits.
+    span = logits.storage_offset() + max(rows - 1, 0) * row_stride + -(-width // 8) * 8
+    if rows and span * 2 > logits.untyped_storage().nbytes():
+        raise ValueError("each row must be readable up to a multiple of 8 logits")
+    if not (valid_len.is_cuda and valid_len.dtype == torch.int32 and valid_len.numel() == rows
+            and valid_len.is_contiguous()):
+        raise ValueError("valid_len must be a contiguous CUDA int32 tensor with one entry per row")
+    table_stride = 0
+    if block_table is not None:
+        if not (block_table.is_cuda and block_table.dtype == torch.int32 and block_table.dim() == 2
+                and block_table.shape[0] == rows and block_table.stride(1) == 1):
+            raise ValueError("block_table must be CUDA int32 [rows, pages] with unit inner stride")
+        table_stride = block_table.stride(0) if rows > 1 else block_table.shape[1]
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    elif not (out.is_cuda and out.dtype == torch.int32 and out.shape == (rows, k) and out.is_contiguous()):
+        raise ValueError("out must be a contiguous CUDA int32 tensor [rows, k]")
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    lib = load()
+    with torch.cuda.device(logits.device):
+        args = (_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), int(mode),
+                _ptr(block_table), table_stride, int(page_size), _ptr(out),
+                ctypes.c_void_p(stream.cuda_stream))
+        if force_direct or cluster or counters is not None:
+            opt = _Options(1 if force_direct else 0, int(cluster),
+                           None if counters is None else counters.data_ptr())
+            st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
+        else:
+            st = lib.topk_bf16_select(*args)
+    _check(st)
+    return out
+
+
+def select_raw(logits_ptr: int, row_stride: int, rows: int, width: int, valid_len_ptr: int, k: int,
+               mode: int, table_ptr: int | None, table_stride: int, page_size: int, out_ptr: int,
+               stream_handle: int) -> None:
+    """The C entry point on raw device pointers (no checks beyond the library's)."""
+    _check(load().topk_bf16_select(logits_ptr, row_stride, rows, width, valid_len_ptr, k, mode,
+                                   table_ptr, table_stride, page_size, out_ptr,
+                                   ctypes.c_void_p(stream_handle)))
+
+
+def plan(rows: int, width: int, k: int, mode: int = TOKEN) -> dict:
+    """The launch the library would make: CTAs per row, threads, shared bytes, variant."""
+    c, t, s, v = (ctypes.c_int32() for _ in range(4))
+    _check(load().topk_bf16_plan(rows, width, k, mode, ctypes.byref(c), ctypes.byref(t),
+                                 ctypes.byref(s), ctypes.byref(v)))
+    return {"cluster": c.value, "threads": t.value, "smem_bytes": s.value,
+            "variant": "streamed" if v.value else "one-tile"}
+
+
+def device_status(clear: bool = True) -> int:
+    """Device-side status bits (bounded wait gave up = 1, bound check = 2); syncs the device."""
+    flags = ctypes.c_uint32()
+    _check(load().topk_bf16_device_status(ctypes.byref(flags), 1 if clear else 0))
+    return flags.value
+
+
+def status_string(status: int) -> str:
+    return load().topk_bf16_status_string(status).decode()

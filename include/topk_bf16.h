@@ -1,0 +1,148 @@
+/*
+ * topk_bf16.h - exact per-row top-k of BF16 logits on GB300 (sm_103a).
+ *
+ * The operation is the one the vLLM page "decode_topk_cute" states in its module
+ * docstring ("What this module computes"): for each row, the indices of its k
+ * largest elements, in any order. Exact: every index whose value exceeds the
+ * k-th largest, then enough of those equal to it; ties at the k-th largest go to
+ * the lowest indices (vLLM kimi_k3 "dsa/indexer", IndexerSelect: "ties at the
+ * threshold go to the lowest key indices"), so the selected set is unique. A row
+ * of at most k elements returns 0 .. n-1 and -1 padding without reading its
+ * values. Values are compared through the order-preserving 16-bit key of their
+ * BF16 bits, x ^ (x < 0 ? 0xFFFF : 0x8000) (sglang PR #39305, Modifications), so
+ * -0 ranks below +0 and denormals are ordered by value; NaN elements are never
+ * selected. The optional block table is applied as in IndexerSelect.emit of the
+ * kimi_k3 indexer page: physical = table[row][i / page] * page + i % page.
+ *
+ * Every entry point is a plain C function. Pointers named "device" must point to
+ * device memory of the current CUDA device; the library never frees, keeps or
+ * allocates memory on the caller's behalf and never synchronises the stream.
+ * All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream). Calls are thread-safe; the first call on a device sets kernel
+ * attributes once.
+ */
+#ifndef TOPK_BF16_H
+#define TOPK_BF16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TOPK_TOKEN = 0,   /* an element is one BF16 logit */
+    TOPK_BLOCK8 = 1   /* an element is the NaN-propagating maximum of an aligned
+                         group of 8 logits; the row's newest block (the one that
+                         holds logit valid_len-1) counts as +inf; a selected block
+                         whose value is -inf is written as -1
+                         (vLLM decode_topk_cute, module docstring, block mode) */
+} topk_mode_t;
+
+typedef enum {
+    TOPK_OK = 0,
+    TOPK_ERR_ARG = 1,    /* null pointer, rows < 0, bad mode, bad page size or table stride */
+    TOPK_ERR_ALIGN = 2,  /* logits not 16-byte aligned, or row_stride not a multiple of 8 */
+    TOPK_ERR_K = 3,      /* k outside [1, TOPK_MAX_K] */
+    TOPK_ERR_WIDTH = 4,  /* width outside [0, TOPK_MAX_WIDTH], or row_stride < width */
+    TOPK_ERR_CUDA = 5    /* a CUDA call failed (launch or attribute); see cudaGetLastError */
+} topk_status_t;
+
+#define TOPK_MAX_K 2048
+#define TOPK_MAX_WIDTH (1 << 20)
+
+/*
+ * Exact top-k of every row (the operation described at the top of this file).
+ *
+ * logits       device, BF16 bit patterns; row r starts at logits + r * row_stride.
+ *              The base must be 16-byte aligned and row_stride a multiple of 8, so
+ *              that every row is read as whole 16-byte vectors. The buffer must be
+ *              readable for rows * row_stride elements.
+ * row_stride   elements between consecutive rows (>= width).
+ * rows         number of rows (0 is a no-op that returns TOPK_OK).
+ * width        logits per row that may be valid, 0 .. TOPK_MAX_WIDTH.
+ * valid_len    device, int32 [rows]: valid logits of each row (a prefix); values
+ *              outside [0, width] are clamped on the device. n = valid_len in token
+ *              mode, ceil(valid_len / 8) in block mode.
+ * k            1 .. TOPK_MAX_K.
+ * mode         TOPK_TOKEN or TOPK_BLOCK8.
+ * block_table  NULL for logical indices, else device int32 [rows, table_stride]:
+ *              row r's page ids; selected element i is written as
+ *              block_table[r * table_stride + i / page_size] * page_size + i % page_size.
+ *              table_stride must be >= ceil(width_elements / page_size), where
+ *              width_elements is width (token) or ceil(width / 8) (block).
+ * page_size    elements per page, a power of two (64 in the pages' layout); ignored
+ *              when block_table is NULL.
+ * out          device, int32 [rows, k], fully written: the selected (transformed)
+ *              indices in any order, then -1 for the remaining slots. Must not
+ *              overlap the inputs.
+ * stream       cudaStream_t to enqueue on.
+ *
+ * Returns TOPK_OK once the work is enqueued, or an error status without
+ * enqueueing anything. Device-side data is never validated by trapping.
+ */
+topk_status_t topk_bf16_select(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                               int32_t width, const int32_t *valid_len, int32_t k,
+                               topk_mode_t mode, const int32_t *block_table,
+                               int32_t table_stride, int32_t page_size, int32_t *out,
+                               void *stream);
+
+/* Human-readable name of a status (a static string). */
+const char *topk_bf16_status_string(topk_status_t status);
+
+/*
+ * Options for topk_bf16_select_ex: test and diagnosis hooks. They change which
+ * internal path computes the result, never the result itself.
+ */
+typedef struct {
+    int32_t force_direct;   /* 1: skip the sampled cutoff; every tile takes the exact
+                               whole-tile radix path (the fallback) */
+    int32_t cluster;        /* 0: automatic; else CTAs per row: 1, 2, 4, 8 or 16 */
+    uint32_t *counters;     /* NULL, or device uint32 [TOPK_NUM_COUNTERS] that each
+                               launch adds its path counts to */
+} topk_bf16_options_t;
+
+/* Indices into topk_bf16_options_t.counters. */
+enum {
+    TOPK_CNT_BYPASS_ROWS = 0,    /* rows with n <= k */
+    TOPK_CNT_TILE_SAMPLED = 1,   /* tiles solved by the sampled cutoff */
+    TOPK_CNT_TILE_FORCED = 2,    /* tiles solved by the exact path because forced */
+    TOPK_CNT_TILE_OVERSHOT = 3,  /* sample cutoff above the k-th: exact path taken */
+    TOPK_CNT_TILE_OVERFLOW = 4,  /* too many survivors: exact path taken */
+    TOPK_CNT_TILE_TAKE_ALL = 5,  /* tiles with at most k candidates */
+    TOPK_CNT_COMPACTIONS = 6,    /* candidate-buffer compactions */
+    TOPK_CNT_OVERFLOW_ROUNDS = 7,/* streamed rounds that needed their own selection */
+    TOPK_CNT_CLUSTER_MERGES = 8, /* rows merged across a cluster of CTAs */
+    TOPK_CNT_ROUNDS = 9,         /* streamed rounds (tiles) in total */
+    TOPK_NUM_COUNTERS = 16
+};
+
+/* topk_bf16_select with options (NULL = defaults). Same arguments and errors,
+   plus TOPK_ERR_ARG for an unsupported cluster size. */
+topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                  int32_t width, const int32_t *valid_len, int32_t k,
+                                  topk_mode_t mode, const int32_t *block_table,
+                                  int32_t table_stride, int32_t page_size, int32_t *out,
+                                  void *stream, const topk_bf16_options_t *options);
+
+/*
+ * The launch topk_bf16_select would make for these sizes on the current device:
+ * CTAs per row, threads per CTA, dynamic shared memory bytes and the kernel
+ * variant (0 = one-tile rows, 1 = streamed rows). Any output pointer may be NULL.
+ */
+topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t mode,
+                             int32_t *cluster, int32_t *threads, int32_t *smem_bytes,
+                             int32_t *variant);
+
+/*
+ * Device-side status word of the current device: nonzero bits record a bounded
+ * wait that gave up (bit 0) or an internal bound check that failed (bit 1, debug
+ * builds). Synchronises the device. clear != 0 resets the word afterwards.
+ */
+topk_status_t topk_bf16_device_status(uint32_t *flags, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_BF16_H */

@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_bf16_top_gb300 as tk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "topk_bf16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tk._build.build()
+    return tk.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(topk_bf16_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("topk_bf16_select", "topk_bf16_status_string", "topk_bf16_select_ex",
+              "topk_bf16_plan", "topk_bf16_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", tk.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(topk_bf16_\w+)\b", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "topk_bf16.h"\nint main(void){return (int)TOPK_OK;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                    "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert tk.status_string(s)
+
+
+def _call(lib, logits=16, stride=8, rows=1, width=8, valid=16, k=1, mode=0, table=None,
+          table_stride=0, page=64, out=16):
+    return lib.topk_bf16_select(logits, stride, rows, width, valid, k, mode, table, table_stride,
+                                page, out, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), 3), (dict(k=2049), 3), (dict(rows=-1), 1), (dict(mode=2), 1),
+    (dict(width=(1 << 20) + 8, stride=(1 << 20) + 8), 4), (dict(width=16, stride=8), 4),
+    (dict(width=-1), 4), (dict(logits=None), 1), (dict(valid=None), 1), (dict(out=None), 1),
+    (dict(logits=18), 2), (dict(stride=12, width=8), 2), (dict(out=18), 2),
+    (dict(table=16, page=48, table_stride=1), 1), (dict(table=16, page=0, table_stride=1), 1),
+    (dict(table=16, page=4, table_stride=1), 1),
+])
+def test_bad_arguments_rejected_on_host(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert _call(lib, rows=0, logits=None, valid=None, out=None) == 0

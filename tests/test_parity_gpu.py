@@ -1,0 +1,137 @@
+"""Parity of the CUDA path with the CPU oracle: selected index sets must be
+bit-exact (sorted, after the block-table transform) on every configuration,
+the edge rows, every cluster size and the forced exact path."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import exact_bf16_top_gb300 as tk
+import oracle
+import workloads as W
+from gpu_util import assert_same_sets, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tk._build.build()
+    oracle.build()
+    tk.device_status(clear=True)
+    yield
+    assert tk.device_status(clear=True) == 0, "device status flags set"
+
+
+def check(case, **opts):
+    assert_same_sets(run_gpu(case, **opts), run_oracle(case), case.name + str(opts))
+
+
+def test_config1_token_4x4096():
+    check(W.config1(0))
+
+
+@pytest.mark.parametrize("rows", W.CONFIG2_ROWS)
+@pytest.mark.parametrize("valid", W.CONFIG2_VALID)
+@pytest.mark.parametrize("k", W.CONFIG2_K)
+def test_config2_consumer(rows, valid, k):
+    check(W.config2(rows, valid, k))
+
+
+def test_config3_crowded():
+    check(W.config3(0))
+
+
+def test_config4_block():
+    check(W.config4(0))
+
+
+def test_config5a_wide():
+    check(W.config5a(0))
+
+
+def test_config5b_wide():
+    check(W.config5b(0))
+
+
+@pytest.mark.parametrize("case", W.edge_cases(0), ids=lambda c: c.name)
+def test_edge_rows(case):
+    check(case)
+
+
+@pytest.mark.parametrize("case", W.edge_cases(0), ids=lambda c: c.name)
+def test_edge_rows_forced_exact(case):
+    check(case, force_direct=True)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("mode", [W.TOKEN, W.BLOCK8])
+@pytest.mark.parametrize("k", [1, 7, 512, 2048])
+def test_ragged_tiles_every_cluster(cluster, mode, k):
+    case = W.ragged_case(seed=10 + k + cluster, rows=6, width=100003, row_stride=100008, k=k,
+                         mode=mode, with_table=True)
+    check(case, cluster=cluster)
+
+
+@pytest.mark.parametrize("cluster", [0, 1, 4, 16])
+def test_ragged_forced_exact(cluster):
+    case = W.ragged_case(seed=3, rows=5, width=70001, row_stride=70008, k=512)
+    check(case, cluster=cluster, force_direct=True)
+
+
+@pytest.mark.parametrize("cluster", [0, 1, 2, 8])
+def test_crowded_every_cluster(cluster):
+    case = W.config3(0, rows=64, width=40000)
+    check(case, cluster=cluster)
+
+
+def test_edge_rows_wide_token():
+    """The edge rows at 150000 wide (streamed path, several rounds)."""
+    for case in W.edge_cases(1, width=150000, k=512):
+        check(case)
+        check(case, cluster=4)
+
+
+def test_repeatable():
+    case = W.config3(2, rows=16, width=150000)
+    first = run_gpu(case)
+    for _ in range(5):
+        assert np.array_equal(np.sort(run_gpu(case), 1), np.sort(first, 1))
+
+
+def test_path_counters_cover_every_path():
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for case in [W.config3(0, rows=64, width=60000), W.edge_cases(0)[0], W.edge_cases(0)[1],
+                 W.config4(0, rows=8, width=1 << 18)]:
+        run_gpu(case, counters=counters)
+        run_gpu(case, counters=counters, cluster=4)
+    run_gpu(W.edge_cases(0)[0], counters=counters, force_direct=True)
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    for name in ("bypass_rows", "tile_sampled", "tile_forced", "tile_take_all", "compactions",
+                 "cluster_merges", "rounds"):
+        assert c[name] > 0, (name, c)
+
+
+def test_output_written_in_place():
+    case = W.config2(32, 16384, 512)
+    logits = torch.from_numpy(case.logits.view(np.int16)).cuda()
+    valid = torch.from_numpy(case.valid_len).cuda()
+    table = torch.from_numpy(case.block_table).cuda()
+    out = torch.full((32, 512), 12345, dtype=torch.int32, device="cuda")
+    res = tk.select(logits, valid, 512, 0, table, 64, out=out)
+    assert res.data_ptr() == out.data_ptr()
+    assert_same_sets(out.cpu().numpy(), run_oracle(case))
+
+
+def test_strided_logits_and_nondefault_stream():
+    case = W.ragged_case(seed=8, rows=7, width=30000, row_stride=30016, k=300)
+    logits = torch.from_numpy(case.logits.view(np.int16)).cuda()
+    valid = torch.from_numpy(case.valid_len).cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = tk.select(logits[:, :30000], valid, case.k, width=case.width)
+    s.synchronize()
+    assert_same_sets(out.cpu().numpy(), run_oracle(case))

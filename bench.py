@@ -280,6 +280,26 @@ def run_sweep(tk, torch, device, steps, warmup, peak, full):
     return out
 
 
+def profile(args):
+    import torch
+    import exact_bf16_top_gb300 as tk
+    tk._build.build()
+    matches = [(n, m) for n, m in sweep_cases(True) if args.profile in n]
+    if not matches:
+        raise SystemExit(f"no workload matches {args.profile!r}")
+    name, make = matches[0]
+    case = make()
+    gc = GpuCase(case, torch, torch.device("cuda", 0), min_copies=2)
+    for i in range(args.warmup):
+        gc.launch(i + 1, tk)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        gc.launch(i, tk)
+    torch.cuda.synchronize()
+    print(json.dumps({"profiled": name, "launches": args.warmup + args.steps,
+                      "plan": tk.plan(case.rows, case.width, case.k, case.mode)}))
+
+
 # -------------------------------------------------------------------- main
 
 def main():
@@ -291,7 +311,12 @@ def main():
     ap.add_argument("--sweep", choices=("none", "k512", "full"), default="k512")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--profile", default=None,
+                    help="launch one sweep workload (a substring of its name) --steps times "
+                         "after --warmup launches, eagerly, and exit (for ncu)")
     args = ap.parse_args()
+    if args.profile:
+        return profile(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -10,7 +10,7 @@ SRC = os.path.join(PKG, "csrc", "topk_bf16.cu")
 HEADER = os.path.join(ROOT, "include", "topk_bf16.h")
 LIB_PATH = os.path.join(PKG, "libtopk_bf16.so")
 
-NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++20",
               "-shared", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
 

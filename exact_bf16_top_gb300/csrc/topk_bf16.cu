@@ -1421,7 +1421,7 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pl.cluster > 1 ? 1 : 0;  // a lone CTA per row needs no cluster
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, v.fn, args);
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;

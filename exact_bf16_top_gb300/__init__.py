@@ -26,8 +26,8 @@ BLOCK8 = 1
 MAX_K = 2048
 MAX_WIDTH = 1 << 20
 NUM_COUNTERS = 16
-COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_forced", "tile_overshot", "tile_overflow",
-                 "tile_take_all", "compactions", "overflow_rounds", "cluster_merges", "rounds")
+COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", "tile_overflow",
+                 "tile_take_all", "compactions", "refills", "cluster_merges", "rounds")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
            5: "CUDA error"}

@@ -12,30 +12,34 @@
 // mbarrier) that runs ahead across row boundaries, so the next row streams in
 // while the current one is being selected.
 //
-// A stage (a "tile": 256 threads x 8 vectors) is handled in one of two ways:
-//   * The first tile of a CTA's share is selected exactly. The cutoff comes from
-//     group representatives: each thread splits its logits into groups of g and
-//     takes one element of each group (the packed signed maximum of its BF16
-//     bits, which is the group maximum whenever the group holds a non-negative
-//     value). The k-th largest representative, found with a 12-bit histogram,
-//     is a lower bound on the tile's k-th largest key, because k distinct
-//     elements reach it; and keys above it sit in fewer than about k groups, so
-//     they are few. Keys above the cutoff go to a survivor list (one shared
-//     atomic per warp); the exact k-th comes from a histogram of survivors
-//     relative to the cutoff. When the representatives cannot bound the tile or
-//     the survivors overflow, the exact path (g = 1: every key is its own
-//     representative) decides it.
-//   * Later tiles keep every key at or above a running threshold.
-// Either way, a vector is first tested on its packed maximum; the vectors that
-// may hold a selected key are queued per warp (ballots), and the warp's lanes
-// then work through the queue together, so divergence does not multiply the
-// work. Selected keys are appended, in index order, to a candidate buffer at
-// slots from warp scans plus one CTA scan of per-run totals: no atomic per key.
-// A full buffer is compacted to its exact top-k, which raises the threshold;
-// CTAs of a cluster share their lower bounds on the row's k-th key through
-// distributed shared memory. The C buffers are merged with cluster-wide
-// histograms over distributed shared memory, and each CTA writes its part of
-// the answer through the block table, ties at the k-th key split in index order.
+// Every CTA keeps a candidate buffer of (key, index) pairs in shared memory, in
+// no particular order: it always holds every key of the CTA's share that can
+// still be selected, plus some that cannot. Ties at a cutoff are settled by
+// index only when they have to be (the lowest indices win): usually a handful
+// of entries ranked directly, a two-pass radix select over the indices when
+// there are many.
+//
+// The first stage ("tile": 256 threads x 8 vectors) of a CTA's share is
+// selected exactly. Its cutoff comes from group representatives: each thread
+// splits its logits into groups of g and takes one element of each group, the
+// packed signed maximum of its BF16 bits (the group maximum whenever the group
+// holds a non-negative value). The k-th largest representative, found with a
+// 12-bit histogram, bounds the tile's k-th key from below, because k distinct
+// elements reach it; keys above it sit in about k groups, so they are few. Those
+// survivors go to the buffer and their exact k-th comes from a histogram
+// relative to the cutoff. When the representatives cannot bound the tile, or
+// the survivors overflow, every key becomes its own representative (g = 1): the
+// exact path. Later tiles append every key at or above a running threshold,
+// which rises whenever the buffer is compacted to its top-k and, in a cluster,
+// when a peer CTA publishes its own bound through distributed shared memory.
+//
+// A vector is first tested on its packed maximum; the vectors that may hold a
+// wanted key are queued per warp (ballots), and the warp's lanes work through
+// the queue together, so divergence does not multiply the work; a warp
+// reserves its slots with one shared atomic, never one per key. The C buffers
+// of a row are merged with cluster-wide histograms over distributed shared
+// memory; ties at the row's k-th key are split across CTAs in index order, and
+// each CTA writes its part of the answer through the block table.
 // All selection arithmetic is on 16-bit integer keys; no floating point.
 
 #include <cuda_runtime.h>
@@ -53,14 +57,14 @@ constexpr int VPT = 8;                       // 16-byte vectors per thread per t
 constexpr int TILE_VEC = THREADS * VPT;      // 2048 vectors = 32 KiB per stage
 constexpr int QCAP = 32 * VPT;               // queue entries of one warp
 constexpr int HBINS = 4096;                  // 12-bit key bins
+constexpr int TIECAP = 256;                  // ties ranked directly
 constexpr uint32_t SUB_EXACT = 32;           // a bin fuller than this is resolved to the key
 constexpr uint32_t KEY_POS_INF = 0xFF80u;    // key of +inf
 constexpr uint32_t KEY_NEG_INF = 0x007Fu;    // key of -inf
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a stage wait gives up after 1 s
-constexpr uint32_t NO_ROOM = 0xFFFFFFFFu;
+constexpr uint32_t ALL = 0xFFFFFFFFu;        // "every tie" / "no cut"
 
 enum : uint32_t { ERR_WAIT = 1u, ERR_BOUNDS = 2u };
-enum { CTR_NGT = 0, CTR_NEQ = 1, CTR_SMAX = 2, CTR_BUFMAX = 3 };
 
 __device__ uint32_t g_device_status;
 
@@ -77,23 +81,24 @@ struct Params {
     int32_t force_direct;
 };
 
-template <int NSTAGE, int CAP, int SURV>
+template <int NSTAGE, int CAP>
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][TILE_VEC];           // streamed logits
-    uint32_t buf_idx[CAP];                   // candidate buffer, index order
+    uint32_t buf_idx[CAP];                   // candidate buffer (any order)
     uint16_t buf_key[CAP];
-    uint16_t surv[SURV];                     // survivors of a tile select
     uint32_t hist[HBINS];                    // 12-bit histogram (zero between uses)
     uint32_t hwin[2][256];                   // window histograms (zero between uses)
     uint32_t h_merge[2][256];                // this CTA's merge histograms (peers read them)
     uint32_t m_all[256];                     // merge: counts over the cluster
     uint32_t m_pre[2][256];                  // merge: counts over lower-ranked CTAs
+    uint32_t tie_idx[TIECAP];                // indices of ties being ranked
     uint32_t sub[16];                        // sub-bins of one 12-bit bin
-    uint32_t wsum[2][WARPS * VPT];           // run totals, [run * WARPS + warp]
     uint32_t red[2][WARPS];                  // block-scan warp totals
-    uint32_t sadj[WARPS][VPT];               // per-run slot offsets of a warp
     uint32_t bc[4];                          // broadcast words
-    uint32_t ctr[4];                         // counters (CTR_*)
+    uint32_t v_count;                        // buffer entries
+    uint32_t v_bufmax;                       // largest buffer key
+    uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
+    uint32_t v_ntie, v_emit, v_flag;
     uint32_t shared_thr;                     // lower bound on the row's k-th key (max)
     uint32_t shared_max;                     // largest candidate key of the cluster (max)
     uint32_t abort_flag;                     // a bounded wait gave up
@@ -306,7 +311,7 @@ struct TokenMode {
 struct BlockMode {
     static constexpr bool BLOCK = true;
     static constexpr int KPV = 1;
-    static constexpr int GMAX = 8;
+    static constexpr int GMAX = 4;
     static constexpr uint32_t KMIN = KEY_NEG_INF + 1;
     __device__ static __forceinline__ int32_t elem(int64_t v, int) { return static_cast<int32_t>(v); }
     __device__ static __forceinline__ uint32_t key(const uint4 &raw, int64_t v, int64_t V) {
@@ -396,31 +401,42 @@ __device__ __forceinline__ int32_t transform(const Params &p, int32_t row, int32
     return (page << p.page_shift) | (i & ((1 << p.page_shift) - 1));
 }
 
+// Warp-aggregated reservation of `n` slots (lane 0 adds; every lane gets base).
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t *ctr, uint32_t n) {
+    uint32_t base = 0;
+    if (lane_id() == 0 && n) base = atomicAdd(ctr, n);
+    return __shfl_sync(0xFFFFFFFFu, base, 0);
+}
+
 // --------------------------------------------------------- the CTA's machinery
 
-template <class M, int NSTAGE, int CAP, int SURV>
+template <class M, int NSTAGE, int CAP>
 struct Cta {
     static constexpr int KPV = M::KPV;
-    using S = Smem<NSTAGE, CAP, SURV>;
+    using S = Smem<NSTAGE, CAP>;
 
     S &s;
     const Params &p;
     uint32_t C, rank;
-    uint32_t parity = 0;   // alternates double-buffered scan scratch
+    uint32_t parity = 0;     // alternates double-buffered scan scratch
     // per row
     int32_t row = 0, L = 0;
     int64_t V = 0;
     uint32_t k = 0;
-    uint32_t count = 0;    // entries in the candidate buffer
-    uint32_t thr = 0;      // keep keys >= thr
-    uint32_t buf_lo = 0;   // every buffer key is >= buf_lo
-    uint32_t best_T = 0;   // largest exact k-th key found in this CTA's share (0: none)
+    uint32_t thr = 0;        // keep keys >= thr
+    uint32_t buf_lo = 0;     // every buffer key is >= buf_lo
+    uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
+    uint32_t known_T = 0;    // nonzero: the buffer's top-k cut is known (last_take ties at it)
+    uint32_t last_take = 0;
 
     __device__ Cta(S &s_, const Params &p_) : s(s_), p(p_) {}
 
+    __device__ __forceinline__ uint32_t volatile_load(const uint32_t *x) {
+        return *reinterpret_cast<const volatile uint32_t *>(x);
+    }
+
     __device__ __forceinline__ uint32_t effective_thr() {
-        if (C > 1) return max(thr, *reinterpret_cast<volatile uint32_t *>(&s.shared_thr));
-        return thr;
+        return C > 1 ? max(thr, volatile_load(&s.shared_thr)) : thr;
     }
 
     // Every CTA of the row learns that the row's k-th key is at least `bound`.
@@ -483,17 +499,28 @@ struct Cta {
         return total;
     }
 
-    // The q-th largest of keys[0 .. n), all within [lo, hi] (q <= n): a radix
-    // select over bins relative to lo, one pass when hi - lo < 256, else two.
-    // T = that key, above = keys greater than it. s.hwin is zero on entry and
-    // on exit.
-    __device__ void window_select(const uint16_t *keys, uint32_t n, uint32_t lo, uint32_t hi,
-                                  uint32_t q, uint32_t &T, uint32_t &above) {
+    // Bin of `key` in a window [lo, lo + (256 << shift)); a key outside it would
+    // break the caller's bounds, so it is recorded and clamped.
+    __device__ __forceinline__ static uint32_t window_bin(uint32_t key, uint32_t lo, int shift) {
+        const uint32_t o = (key - lo) >> shift;
+        if (key < lo || o > 255u) {
+            atomicOr(&g_device_status, ERR_BOUNDS);
+            return key < lo ? 0u : 255u;
+        }
+        return o;
+    }
+
+    // The q-th largest of buf_key[first .. first + n), all within [lo, hi]
+    // (q <= n): a radix select over bins relative to lo, one pass when
+    // hi - lo < 256, else two. T = that key, above = keys greater than it.
+    // s.hwin is zero on entry and on exit.
+    __device__ void window_select(uint32_t first, uint32_t n, uint32_t lo, uint32_t hi, uint32_t q,
+                                  uint32_t &T, uint32_t &above) {
         const int tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         for (uint32_t i = tid; i < n; i += THREADS)
-            atomicAdd(&s.hwin[0][window_bin(keys[i], lo, shift)], 1u);
+            atomicAdd(&s.hwin[0][window_bin(s.buf_key[first + i], lo, shift)], 1u);
         __syncthreads();
         uint32_t b1, above1, tot;
         find_bin256(s.hwin[0], q, b1, above1, tot);
@@ -503,7 +530,7 @@ struct Cta {
         } else {
             const uint32_t mask = (1u << shift) - 1u;
             for (uint32_t i = tid; i < n; i += THREADS) {
-                const uint32_t o = static_cast<uint32_t>(keys[i]) - lo;
+                const uint32_t o = static_cast<uint32_t>(s.buf_key[first + i]) - lo;
                 if ((o >> shift) == b1) atomicAdd(&s.hwin[1][o & mask], 1u);
             }
             __syncthreads();
@@ -517,22 +544,84 @@ struct Cta {
         s.hwin[1][tid] = 0u;
     }
 
-        // Bin of `key` in a window [lo, lo + (256 << shift)); keys outside it would
-    // break the caller's bounds, so they are recorded and clamped.
-    __device__ __forceinline__ static uint32_t window_bin(uint32_t key, uint32_t lo, int shift) {
-        const uint32_t o = (key - lo) >> shift;
-        if (key < lo || o > 255u) {
-            atomicOr(&g_device_status, ERR_BOUNDS);
-            return key < lo ? 0u : 255u;
+    // Rank the indices in s.tie_idx[0 .. e) (e <= TIECAP, distinct): the index
+    // with exactly q - 1 smaller ones. One __syncthreads.
+    __device__ uint32_t rank_cut(uint32_t e, uint32_t q) {
+        const uint32_t t = threadIdx.x;
+        if (t < e) {
+            const uint32_t mine = s.tie_idx[t];
+            uint32_t r = 0;
+            for (uint32_t u = 0; u < e; ++u) r += s.tie_idx[u] < mine;
+            if (r == q - 1) s.bc[3] = mine;
         }
-        return o;
+        __syncthreads();
+        return s.bc[3];
+    }
+
+    // Among buffer entries [0, n) with key == T (e of them, all distinct
+    // indices), the cut such that exactly q have an index <= cut: ALL when
+    // q >= e. Few ties are ranked directly; many by a two-pass radix select over
+    // 10-bit index digits (indices are below 2^20).
+    __device__ uint32_t tie_cut(uint32_t n, uint32_t T, uint32_t q) {
+        const int tid = threadIdx.x;
+        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
+        __syncthreads();
+        if (tid == 0) s.v_ntie = 0u;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
+            const uint32_t i = i0 + tid;
+            const bool tie = i < n && s.buf_key[i] == T;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, tie);
+            const uint32_t base = warp_reserve(&s.v_ntie, __popc(b));
+            const uint32_t slot = base + __popc(b & lt);
+            if (tie && slot < static_cast<uint32_t>(TIECAP)) s.tie_idx[slot] = s.buf_idx[i];
+        }
+        __syncthreads();
+        const uint32_t e = s.v_ntie;
+        if (q >= e) return ALL;
+        if (e <= static_cast<uint32_t>(TIECAP)) return rank_cut(e, q);
+        // Many ties: q-th smallest index, digit by digit.
+        uint32_t cut = 0, need = q;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int sh = pass == 0 ? 10 : 0;
+            for (uint32_t i = tid; i < n; i += THREADS) {
+                if (s.buf_key[i] != T) continue;
+                const uint32_t x = s.buf_idx[i];
+                if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
+                atomicAdd(&s.hist[(x >> sh) & 1023u], 1u);
+            }
+            __syncthreads();
+            // Ascending: thread t owns bins [4t, 4t + 4).
+            uint4 *h4 = reinterpret_cast<uint4 *>(s.hist) + tid;
+            const uint4 hv = *h4;
+            *h4 = make_uint4(0, 0, 0, 0);
+            const uint32_t v[4] = {hv.x, hv.y, hv.z, hv.w};
+            uint32_t total;
+            const uint32_t incl = block_incl_scan(v[0] + v[1] + v[2] + v[3], total);
+            uint32_t acc = incl - (v[0] + v[1] + v[2] + v[3]);
+            if (acc < need && need <= incl) {
+                bool done = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (!done && acc + v[i] >= need) {
+                        s.bc[0] = static_cast<uint32_t>(4 * tid + i);
+                        s.bc[1] = acc;
+                        done = true;
+                    }
+                    acc += v[i];
+                }
+            }
+            __syncthreads();
+            cut |= s.bc[0] << sh;
+            need -= s.bc[1];
+        }
+        return cut;
     }
 
     // Queue, per warp and in index order, the tile's vectors that may hold a
-    // key >= lim. Returns the queue length; run_start[j] = queue position of
-    // the first entry of run j (the warp's vectors j*THREADS + warp*32 + lane).
+    // key >= lim. Returns the queue length.
     __device__ __forceinline__ uint32_t build_queue(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                                    int nv, uint32_t lim, uint32_t (&run_start)[VPT]) {
+                                                    int nv, uint32_t lim) {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
         uint32_t q = 0;
@@ -541,7 +630,6 @@ struct Cta {
             const int pos = j * THREADS + static_cast<int>(threadIdx.x);
             const bool pass = pos < nv && M::may_reach(raw[j], ek[j], lim);
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            run_start[j] = q;
             if (pass) s.queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
             q += __popc(b);
         }
@@ -549,117 +637,70 @@ struct Cta {
         return q;
     }
 
-    // Append to the buffer, in index order, the tile's keys > T and the keys
-    // == T while fewer than `take` of them have been taken. Slots: warp scans
-    // over the queue plus one CTA scan of the per-run totals. If the result
-    // would not fit in `room` slots, nothing is written and NO_ROOM is returned.
-    __device__ uint32_t append_pass(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                    const uint4 *stg, int64_t tile_v0, int nv, uint32_t T,
-                                    uint32_t take, uint32_t room) {
-        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-        uint32_t run_start[VPT];
-        const uint32_t Q = build_queue(raw, ek, nv, take ? T : T + 1u, run_start);
-        const uint32_t nch = (Q + 31u) >> 5;
-        uint32_t pre[VPT];
-        uint32_t R[VPT];
+    // Clean keys of queued entry e of this warp (zeros past the queue).
+    __device__ __forceinline__ int queued_keys(const uint4 *stg, int64_t tile_v0, uint32_t e, uint32_t Q,
+                                               uint32_t (&ck)[4]) {
+        ck[0] = ck[1] = ck[2] = ck[3] = 0u;
+        if (e >= Q) return 0;
+        const uint32_t q = s.queue[threadIdx.x >> 5][e];
+        const int pos = static_cast<int>(q >> 5) * THREADS + static_cast<int>((threadIdx.x >> 5) * 32 + (q & 31u));
+        M::clean(stg[pos], tile_v0 + pos, V, L, ck);
+        return pos;
+    }
+
+    // Append every key >= lim of this warp's queued vectors, from queue entry
+    // `from` on, to the buffer (any order). Slots are reserved a warp at a time
+    // and only while they fit. Returns the first entry not appended (Q: all).
+    __device__ uint32_t append_keys(const uint4 *stg, int64_t tile_v0, uint32_t Q, uint32_t from,
+                                    uint32_t lim) {
+        const uint32_t lane = lane_id();
+        for (uint32_t e0 = from; e0 < Q; e0 += 32) {
+            uint32_t ck[4];
+            const int pos = queued_keys(stg, tile_v0, e0 + lane, Q, ck);
+            uint32_t cnt = 0, kmax = 0;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) R[j] = 0u;
-        uint32_t carry = 0, kmax = 0;
-#pragma unroll
-        for (int m = 0; m < VPT; ++m) {
-            pre[m] = 0u;
-            if (static_cast<uint32_t>(m) < nch) {
-                const uint32_t e = static_cast<uint32_t>(m) * 32u + lane;
-                uint32_t cnt = 0, je = VPT;
-                if (e < Q) {
-                    const uint32_t q = s.queue[warp][e];
-                    je = q >> 5;
-                    const int pos = static_cast<int>(je) * THREADS + static_cast<int>(warp) * 32 +
-                                    static_cast<int>(q & 31u);
-                    uint32_t ck[4];
-                    M::clean(stg[pos], tile_v0 + pos, V, L, ck);
-                    uint32_t gt = 0, eq = 0;
-#pragma unroll
-                    for (int h = 0; h < KPV; ++h) {
-                        const uint32_t key = key_at<M>(ck, h);
-                        gt += key > T;
-                        eq += key == T;
-                        kmax = (key > T || (take && key == T)) ? max(kmax, key) : kmax;
-                    }
-                    cnt = gt | (eq << 16);
-                }
-                const uint32_t incl = warp_incl_scan(cnt);
-                pre[m] = carry + incl - cnt;
-                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-#pragma unroll
-                for (int j = 0; j < VPT; ++j)
-                    R[j] += __reduce_add_sync(0xFFFFFFFFu, je == static_cast<uint32_t>(j) ? cnt : 0u);
+            for (int h = 0; h < KPV; ++h) {
+                const uint32_t key = key_at<M>(ck, h);
+                cnt += key >= lim;
+                kmax = key >= lim ? max(kmax, key) : kmax;
             }
-        }
-        if (lane == 0) {
+            const uint32_t incl = warp_incl_scan(cnt);
+            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t base = 0, ok = 1;
+            if (lane == 0 && total) {
+                uint32_t old = volatile_load(&s.v_count);
+                for (;;) {
+                    if (old + total > static_cast<uint32_t>(CAP)) {
+                        ok = 0;
+                        break;
+                    }
+                    const uint32_t prev = atomicCAS(&s.v_count, old, old + total);
+                    if (prev == old) {
+                        base = old;
+                        break;
+                    }
+                    old = prev;
+                }
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) return e0;  // full: the caller compacts and resumes here
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+            if (lane == 0 && kmax) atomicMax(&s.v_bufmax, kmax);
+            if (cnt) {
+                uint32_t slot = base + incl - cnt;
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) s.wsum[parity][j * WARPS + warp] = R[j];
-        }
-        __syncthreads();
-        // Runs in index order: run j of every warp, then run j + 1.
-        const uint32_t x0 = s.wsum[parity][lane], x1 = s.wsum[parity][lane + 32];
-        const uint32_t s0 = warp_incl_scan(x0);
-        const uint32_t t0 = __shfl_sync(0xFFFFFFFFu, s0, 31);
-        const uint32_t s1 = warp_incl_scan(x1) + t0;
-        const uint32_t total = __shfl_sync(0xFFFFFFFFu, s1, 31);
-        const uint32_t ex0 = s0 - x0, ex1 = s1 - x1;
-        uint32_t runpre = 0;
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const uint32_t f = static_cast<uint32_t>(j) * WARPS + warp;
-            const uint32_t base = j < 4 ? __shfl_sync(0xFFFFFFFFu, ex0, f) : __shfl_sync(0xFFFFFFFFu, ex1, f - 32u);
-            if (lane == 0) s.sadj[warp][j] = base - runpre;  // packed fields stay non-negative
-            runpre += R[j];
-        }
-        parity ^= 1u;
-        const uint32_t gt_total = total & 0xFFFFu, eq_total = total >> 16;
-        const uint32_t appended = gt_total + min(eq_total, take);
-        if (appended > room) return NO_ROOM;
-        kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-        if (lane == 0 && kmax) atomicMax(&s.ctr[CTR_BUFMAX], kmax);
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < VPT; ++m) {
-            if (static_cast<uint32_t>(m) < nch) {
-                const uint32_t e = static_cast<uint32_t>(m) * 32u + lane;
-                if (e < Q) {
-                    const uint32_t q = s.queue[warp][e];
-                    const uint32_t je = q >> 5;
-                    const int pos = static_cast<int>(je) * THREADS + static_cast<int>(warp) * 32 +
-                                    static_cast<int>(q & 31u);
-                    uint32_t ck[4];
-                    M::clean(stg[pos], tile_v0 + pos, V, L, ck);
-                    const uint32_t off = s.sadj[warp][je] + pre[m];
-                    uint32_t gt_before = off & 0xFFFFu, eq_before = off >> 16;
-#pragma unroll
-                    for (int h = 0; h < KPV; ++h) {
-                        const uint32_t key = key_at<M>(ck, h);
-                        uint32_t slot = NO_ROOM;
-                        if (key > T) {
-                            slot = count + gt_before + min(eq_before, take);
-                            ++gt_before;
-                        } else if (key == T) {
-                            if (eq_before < take) slot = count + gt_before + eq_before;
-                            ++eq_before;
-                        }
-                        if (slot != NO_ROOM) {
-                            if (slot < static_cast<uint32_t>(CAP)) {
-                                s.buf_key[slot] = static_cast<uint16_t>(key);
-                                s.buf_idx[slot] = M::elem(tile_v0 + pos, h);
-                            } else {
-                                atomicOr(&g_device_status, ERR_BOUNDS);
-                            }
-                        }
+                for (int h = 0; h < KPV; ++h) {
+                    const uint32_t key = key_at<M>(ck, h);
+                    if (key >= lim) {
+                        s.buf_key[slot] = static_cast<uint16_t>(key);
+                        s.buf_idx[slot] = M::elem(tile_v0 + pos, h);
+                        ++slot;
                     }
                 }
             }
         }
-        return appended;
+        return Q;
     }
 
     // Group representatives of this thread's tile, fed to f(key) (0 = none).
@@ -686,14 +727,6 @@ struct Cta {
                     f(key >= thr ? key : 0u);
                 }
             }
-        } else if constexpr (G == 2) {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                f(rep_key(smax_halves(raw[j].x), thr));
-                f(rep_key(smax_halves(raw[j].y), thr));
-                f(rep_key(smax_halves(raw[j].z), thr));
-                f(rep_key(smax_halves(raw[j].w), thr));
-            }
         } else if constexpr (G == 4) {
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
@@ -712,133 +745,156 @@ struct Cta {
         }
     }
 
-    template <int G>
-    __device__ __forceinline__ void reps_hist(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                              int64_t tile_v0, int nv) {
-        for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
-            if (key) atomicAdd(&s.hist[key >> 4], 1u);
-        });
-    }
-
-    template <int G>
-    __device__ __forceinline__ void reps_sub(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                             int64_t tile_v0, int nv, uint32_t bin) {
-        for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
-            if (key && (key >> 4) == bin) atomicAdd(&s.sub[key & 15u], 1u);
-        });
-    }
-
     template <class F>
-    __device__ __forceinline__ void dispatch_g(int g, F &&f) {
+    __device__ __forceinline__ void with_g(int g, F &&f) {
         if constexpr (M::BLOCK) {
-            switch (g) {
-                case 8: f.template operator()<8>(); break;
-                case 4: f.template operator()<4>(); break;
-                case 2: f.template operator()<2>(); break;
-                default: f.template operator()<1>(); break;
-            }
+            if (g == 4) f.template operator()<4>();
+            else f.template operator()<1>();
         } else {
-            switch (g) {
-                case 64: f.template operator()<64>(); break;
-                case 32: f.template operator()<32>(); break;
-                case 16: f.template operator()<16>(); break;
-                case 8: f.template operator()<8>(); break;
-                case 4: f.template operator()<4>(); break;
-                case 2: f.template operator()<2>(); break;
-                default: f.template operator()<1>(); break;
-            }
+            if (g == 64) f.template operator()<64>();
+            else if (g == 16) f.template operator()<16>();
+            else if (g == 4) f.template operator()<4>();
+            else f.template operator()<1>();
         }
     }
 
-    // Keys > c (and >= thr) of the tile into s.surv (unordered, one shared atomic
-    // per warp); keys == c counted; the largest such key. Results in s.ctr after
-    // the closing __syncthreads.
+    // Keys > c of the tile (and >= thr) appended to the buffer at `first` on (any
+    // order; slot overflow past `room` is counted but not written); keys == c
+    // counted, their indices kept in s.tie_idx while they fit. Counts in s.v_ngt,
+    // s.v_neq and the largest survivor in s.v_smax after the closing
+    // __syncthreads (all three zero on entry).
     __device__ void survivors(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
-                              int64_t tile_v0, int nv, uint32_t c) {
-        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-        uint32_t run_start[VPT];
-        const uint32_t Q = build_queue(raw, ek, nv, max(c, thr), run_start);
+                              int64_t tile_v0, int nv, uint32_t c, uint32_t first, uint32_t room) {
+        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
+        const uint32_t Q = build_queue(raw, ek, nv, max(c, thr));
         for (uint32_t e0 = 0; e0 < Q; e0 += 32) {
-            const uint32_t e = e0 + lane;
-            uint32_t ck[4] = {0u, 0u, 0u, 0u};
-            if (e < Q) {
-                const uint32_t q = s.queue[warp][e];
-                const int pos = static_cast<int>(q >> 5) * THREADS + static_cast<int>(warp) * 32 +
-                                static_cast<int>(q & 31u);
-                M::clean(stg[pos], tile_v0 + pos, V, L, ck);
-            }
-            uint32_t ngt = 0, neq = 0, kmax = 0;
+            uint32_t ck[4];
+            const int pos = queued_keys(stg, tile_v0, e0 + lane, Q, ck);
+            uint32_t ngt = 0, kmax = 0, eqmask = 0;
 #pragma unroll
             for (int h = 0; h < KPV; ++h) {
                 const uint32_t key = key_at<M>(ck, h);
                 const bool ok = key >= thr;
                 ngt += ok && key > c;
-                neq += ok && key == c;
+                eqmask |= (ok && key == c) ? (1u << h) : 0u;
                 kmax = (ok && key > c) ? max(kmax, key) : kmax;
             }
             const uint32_t incl = warp_incl_scan(ngt);
             uint32_t base = 0;
-            if (lane == 31 && incl) base = atomicAdd(&s.ctr[CTR_NGT], incl);
+            if (lane == 31 && incl) base = atomicAdd(&s.v_ngt, incl);
             base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - ngt;
-            const uint32_t eqs = __reduce_add_sync(0xFFFFFFFFu, neq);
             const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0) {
-                if (eqs) atomicAdd(&s.ctr[CTR_NEQ], eqs);
-                if (mx) atomicMax(&s.ctr[CTR_SMAX], mx);
-            }
+            if (lane == 0 && mx) atomicMax(&s.v_smax, mx);
             if (ngt) {
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
                     const uint32_t key = key_at<M>(ck, h);
                     if (key >= thr && key > c) {
-                        if (base < static_cast<uint32_t>(SURV)) s.surv[base] = static_cast<uint16_t>(key);
+                        if (base < room) {
+                            s.buf_key[first + base] = static_cast<uint16_t>(key);
+                            s.buf_idx[first + base] = M::elem(tile_v0 + pos, h);
+                        }
                         ++base;
                     }
                 }
+            }
+            const uint32_t neq = __popc(eqmask);
+            const uint32_t any = __ballot_sync(0xFFFFFFFFu, neq != 0);
+            if (any) {
+                const uint32_t einc = warp_incl_scan(neq);
+                uint32_t ebase = 0;
+                if (lane == 31) ebase = atomicAdd(&s.v_neq, einc);
+                ebase = __shfl_sync(0xFFFFFFFFu, ebase, 31) + einc - neq;
+#pragma unroll
+                for (int h = 0; h < KPV; ++h) {
+                    if (eqmask & (1u << h)) {
+                        if (ebase < static_cast<uint32_t>(TIECAP)) s.tie_idx[ebase] = M::elem(tile_v0 + pos, h);
+                        ++ebase;
+                    }
+                }
+                (void)lt;
             }
         }
         __syncthreads();
     }
 
-    // Exact top-k of the tile's keys >= thr, appended to the buffer in index
-    // order; raises thr when the tile held more than k.
+    // The `take` lowest-index keys equal to c in the tile, appended at
+    // first .. first + take in index order (tile order (j, thread, lane)), found
+    // with ordered scans of per-vector tie counts. For rows whose cutoff sits
+    // in a crowded bin.
+    __device__ void ordered_ties(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c, uint32_t take,
+                                 uint32_t first) {
+        uint32_t before = 0;
+        for (int j = 0; j < VPT; ++j) {
+            const int pos = j * THREADS + static_cast<int>(threadIdx.x);
+            uint32_t ck[4] = {0u, 0u, 0u, 0u};
+            if (pos < nv) M::clean(stg[pos], tile_v0 + pos, V, L, ck);
+            uint32_t eq = 0;
+#pragma unroll
+            for (int h = 0; h < KPV; ++h) eq += key_at<M>(ck, h) == c && c >= thr;
+            uint32_t total;
+            const uint32_t incl = block_incl_scan(eq, total);
+            uint32_t r = before + incl - eq;
+#pragma unroll
+            for (int h = 0; h < KPV; ++h) {
+                if (key_at<M>(ck, h) == c && c >= thr) {
+                    if (r < take) {
+                        s.buf_key[first + r] = static_cast<uint16_t>(c);
+                        s.buf_idx[first + r] = M::elem(tile_v0 + pos, h);
+                    }
+                    ++r;
+                }
+            }
+            before += total;
+            if (before >= take) break;  // uniform
+        }
+    }
+
+    // Exact top-k of the tile's keys >= thr into the buffer (see the file
+    // comment). Raises thr when the tile held more than k candidates.
     __device__ void tile_select(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
                                 int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
-        const int64_t nE64 = M::BLOCK ? nv
-                                      : min(static_cast<int64_t>(nv) * 8, static_cast<int64_t>(L) - 8 * tile_v0);
-        const uint32_t nE = static_cast<uint32_t>(nE64);
-        uint32_t T = thr - 1u, take = 0;
-        bool found = false;
-        if (nE <= k) {
-            count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-        } else {
-            // Group size: about 2k representatives (at least k).
+        const uint32_t first = s.v_count;
+        const uint32_t room = static_cast<uint32_t>(CAP) - first;
+        const uint32_t nE = static_cast<uint32_t>(
+            M::BLOCK ? nv : min(static_cast<int64_t>(nv) * 8, static_cast<int64_t>(L) - 8 * tile_v0));
+        known_T = 0;
+        if (nE > k) {
             int g = 1;
             if (!p.force_direct) {
-                while (g < M::GMAX && nE / static_cast<uint32_t>(2 * g) >= 2u * k) g *= 2;
-            } else {
-                count_event(p, TOPK_CNT_TILE_FORCED);
+                while (g < M::GMAX && nE / static_cast<uint32_t>(4 * g) >= 2u * k) g *= 4;
             }
             for (;;) {
-                if (tid < 4) s.ctr[tid] = tid == CTR_SMAX ? 0u : (tid == CTR_BUFMAX ? s.ctr[tid] : 0u);
+                if (tid == 0) {
+                    s.v_ngt = 0u;
+                    s.v_neq = 0u;
+                    s.v_smax = 0u;
+                }
                 if (tid < 16) s.sub[tid] = 0u;
-                dispatch_g(g, [&]<int G>() { reps_hist<G>(raw, ek, tile_v0, nv); });
+                with_g(g, [&]<int G>() {
+                    for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
+                        if (key) atomicAdd(&s.hist[key >> 4], 1u);
+                    });
+                });
                 __syncthreads();
                 const uint32_t NR = find_cut4096(k);
                 if (NR < k) {
                     if (g > 1) {  // the representatives cannot bound the tile: exact path
-                        count_event(p, TOPK_CNT_TILE_OVERSHOT);
+                        count_event(p, TOPK_CNT_TILE_UNBOUNDED);
                         g = 1;
                         continue;
                     }
-                    count_event(p, TOPK_CNT_TILE_TAKE_ALL);  // at most k candidates
-                    break;
+                    break;  // at most k candidates: take them all
                 }
                 const uint32_t bin = s.bc[0], above = s.bc[1], cnt = s.bc[2];
-                uint32_t c, c_above = above;
+                uint32_t c;
                 if (g == 1 || cnt > SUB_EXACT) {
-                    dispatch_g(g, [&]<int G>() { reps_sub<G>(raw, ek, tile_v0, nv, bin); });
+                    with_g(g, [&]<int G>() {
+                        for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
+                            if (key && (key >> 4) == bin) atomicAdd(&s.sub[key & 15u], 1u);
+                        });
+                    });
                     __syncthreads();
                     uint32_t acc = above, sb = 0;
                     bool done = false;
@@ -847,7 +903,6 @@ struct Cta {
                         const uint32_t v = s.sub[i];
                         if (!done && acc + v >= k) {
                             sb = static_cast<uint32_t>(i);
-                            c_above = acc;
                             done = true;
                         }
                         acc += v;
@@ -856,95 +911,130 @@ struct Cta {
                 } else {
                     c = max(bin << 4, thr - 1u);  // a lower bound on the k-th representative
                 }
-                if (g == 1) {
-                    // Every key is a representative: c is the k-th key itself.
-                    T = c;
-                    take = k - c_above;
-                    found = true;
-                    break;
-                }
-                survivors(raw, ek, stg, tile_v0, nv, c);
-                const uint32_t ngt = s.ctr[CTR_NGT], smax = s.ctr[CTR_SMAX];
-                if (ngt > static_cast<uint32_t>(SURV)) {
+                survivors(raw, ek, stg, tile_v0, nv, c, first, room);
+                const uint32_t ngt = s.v_ngt, neq = s.v_neq, smax = s.v_smax;
+                if (ngt > room) {
+                    // Too many survivors to hold: every key becomes its own
+                    // representative (then fewer than k keys exceed c).
                     count_event(p, TOPK_CNT_TILE_OVERFLOW);
-                    g = 1;
                     __syncthreads();
+                    if (g == 1) {  // cannot happen: record it rather than loop
+                        if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+                        break;
+                    }
+                    g = 1;
                     continue;
                 }
-                count_event(p, TOPK_CNT_TILE_SAMPLED);
+                count_event(p, g == 1 ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+                uint32_t T, take;
                 if (ngt >= k) {
                     uint32_t a2;
-                    window_select(s.surv, ngt, c + 1u, smax, k, T, a2);
+                    window_select(first, ngt, c + 1u, smax, k, T, a2);
                     take = k - a2;
+                    if (tid == 0) s.v_count = first + ngt;
+                    if (tid == 0 && smax > s.v_bufmax) s.v_bufmax = smax;
+                    buf_lo = min(buf_lo, c + 1u);
                 } else {
+                    // The cut is c itself: the survivors and the take
+                    // lowest-index ties at c.
                     T = c;
                     take = k - ngt;
+                    if (neq <= static_cast<uint32_t>(TIECAP)) {
+                        if (static_cast<uint32_t>(tid) < neq) {
+                            const uint32_t mine = s.tie_idx[tid];
+                            uint32_t r = 0;
+                            for (uint32_t u = 0; u < neq; ++u) r += s.tie_idx[u] < mine;
+                            if (r < take) {
+                                s.buf_key[first + ngt + r] = static_cast<uint16_t>(c);
+                                s.buf_idx[first + ngt + r] = mine;
+                            }
+                        }
+                    } else {
+                        ordered_ties(stg, tile_v0, nv, c, take, first + ngt);
+                    }
+                    __syncthreads();
+                    if (tid == 0) {
+                        s.v_count = first + ngt + take;
+                        s.v_bufmax = max(s.v_bufmax, max(smax, c));
+                    }
+                    buf_lo = min(buf_lo, c);
                 }
-                found = true;
-                break;
+                known_T = first == 0 ? T : 0u;
+                last_take = take;
+                // The buffer holds the tile's top-k, all >= T, ahead of any
+                // later key: a later key equal to T can no longer be selected.
+                thr = max(thr, T + 1u);
+                publish(T);
+                __syncthreads();
+                return;
             }
         }
-        const uint32_t room = static_cast<uint32_t>(CAP) - count;
-        const uint32_t added = append_pass(raw, ek, stg, tile_v0, nv, T, take, room);
-        count += added == NO_ROOM ? 0u : added;
-        buf_lo = min(buf_lo, found ? T : thr);
-        if (found) {
-            // The buffer holds this tile's top-k, all >= T, ahead of any later
-            // key: a later key equal to T can no longer be selected.
-            thr = max(thr, T + 1u);
-            publish(T);
-        }
+        // At most k candidates: all of them.
+        count_event(p, TOPK_CNT_TILE_TAKE_ALL);
+        const uint32_t Q = build_queue(raw, ek, nv, thr);
+        append_keys(stg, tile_v0, Q, 0, thr);
+        buf_lo = min(buf_lo, thr);
         __syncthreads();
     }
 
-    // Reduce the candidate buffer to its exact top-k, keeping index order.
-    __device__ void compact() {
+    // Keep (compact = true) or write out (compact = false) the buffer entries
+    // [0, n) that are selected: key > T, or key == T with index <= cut. Kept
+    // entries go to the front of the buffer; written ones to out[row, offset +
+    // slot]. Returns how many were selected.
+    __device__ uint32_t select_entries(uint32_t n, uint32_t T, uint32_t cut, bool compact,
+                                       uint32_t offset) {
         const int tid = threadIdx.x;
-        count_event(p, TOPK_CNT_COMPACTIONS);
-        __syncthreads();
-        const uint32_t hi = s.ctr[CTR_BUFMAX];
-        uint32_t T, above;
-        window_select(s.buf_key, count, buf_lo, max(hi, buf_lo), k, T, above);
-        const uint32_t take = k - above;
-        uint32_t gt_run = 0, eq_run = 0;
+        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
         constexpr int PER = 8;
-        for (uint32_t base = 0; base < count; base += THREADS * PER) {
-            const uint32_t first = base + static_cast<uint32_t>(tid) * PER;
-            uint32_t key[PER], idx[PER], gt = 0, eq = 0;
+        __syncthreads();
+        if (tid == 0) s.v_emit = 0u;
+        __syncthreads();
+        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        for (uint32_t base = 0; base < n; base += THREADS * PER) {
+            uint32_t key[PER], idx[PER];
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
-                const uint32_t i = first + e;
-                key[e] = i < count ? s.buf_key[i] : 0u;
-                idx[e] = i < count ? s.buf_idx[i] : 0u;
-                gt += key[e] > T;
-                eq += key[e] == T;
+                const uint32_t i = base + static_cast<uint32_t>(e) * THREADS + tid;
+                key[e] = i < n ? s.buf_key[i] : 0u;
+                idx[e] = i < n ? s.buf_idx[i] : 0u;
             }
-            uint32_t total;
-            const uint32_t incl = block_incl_scan(gt | (eq << 16), total);
-            const uint32_t ex = incl - (gt | (eq << 16));
-            uint32_t gt_before = gt_run + (ex & 0xFFFFu), eq_before = eq_run + (ex >> 16);
+            if (compact) __syncthreads();  // this chunk is read before it is overwritten
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
-                if (key[e] > T) {
-                    const uint32_t slot = gt_before + min(eq_before, take);
-                    s.buf_key[slot] = static_cast<uint16_t>(key[e]);
-                    s.buf_idx[slot] = idx[e];
-                    ++gt_before;
-                } else if (key[e] == T) {
-                    if (eq_before < take) {
-                        const uint32_t slot = gt_before + eq_before;
+                const bool sel = key[e] != 0u && (key[e] > T || (key[e] == T && idx[e] <= cut));
+                const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
+                const uint32_t slot = warp_reserve(&s.v_emit, __popc(b)) + __popc(b & lt);
+                if (sel) {
+                    if (compact) {
                         s.buf_key[slot] = static_cast<uint16_t>(key[e]);
                         s.buf_idx[slot] = idx[e];
+                    } else {
+                        orow[offset + slot] = transform(p, row, static_cast<int32_t>(idx[e]));
                     }
-                    ++eq_before;
                 }
             }
-            gt_run += total & 0xFFFFu;
-            eq_run += total >> 16;
         }
-        count = gt_run + min(eq_run, take);
+        __syncthreads();
+        return s.v_emit;
+    }
+
+    // Reduce the buffer to its exact top-k. strict: every buffered key precedes
+    // every key still to come, so later keys equal to the cut are dropped too.
+    __device__ void compact(bool strict) {
+        const int tid = threadIdx.x;
+        __syncthreads();
+        const uint32_t n = s.v_count;
+        if (n <= k) return;
+        count_event(p, TOPK_CNT_COMPACTIONS);
+        uint32_t T, above;
+        window_select(0, n, buf_lo, max(s.v_bufmax, buf_lo), k, T, above);
+        const uint32_t take = k - above;
+        const uint32_t cut = tie_cut(n, T, take);
+        const uint32_t kept = select_entries(n, T, cut, true, 0);
+        if (tid == 0) s.v_count = kept;
         buf_lo = T;
-        thr = max(thr, T + 1u);
+        known_T = 0;
+        thr = max(thr, strict ? T + 1u : T);
         publish(T);
         __syncthreads();
     }
@@ -952,39 +1042,62 @@ struct Cta {
     // A later tile: append every key >= the threshold.
     __device__ void filter_tile(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
                                 int64_t tile_v0, int nv) {
-        uint32_t t = effective_thr();
-        uint32_t added = append_pass(raw, ek, stg, tile_v0, nv, t - 1u, 0u, static_cast<uint32_t>(CAP) - count);
-        if (added == NO_ROOM && count > k) {
-            compact();
-            t = effective_thr();
-            added = append_pass(raw, ek, stg, tile_v0, nv, t - 1u, 0u, static_cast<uint32_t>(CAP) - count);
+        const int tid = threadIdx.x;
+        known_T = 0;
+        if (s.v_count > static_cast<uint32_t>(CAP / 2) && s.v_count > 2u * k) compact(true);
+        uint32_t lim = effective_thr();
+        const uint32_t Q = build_queue(raw, ek, nv, lim);
+        uint32_t next = append_keys(stg, tile_v0, Q, 0, lim);
+        buf_lo = min(buf_lo, lim);
+        for (int refill = 0;; ++refill) {
+            if (tid == 0) s.v_flag = 0u;
+            __syncthreads();
+            if (next < Q && lane_id() == 0) s.v_flag = 1u;
+            __syncthreads();
+            if (s.v_flag == 0u) break;  // uniform
+            if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
+                if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+                break;
+            }
+            // The buffer filled up mid-tile: compact it (the rest of this tile
+            // may still tie with it) and carry on.
+            count_event(p, TOPK_CNT_REFILLS);
+            compact(false);
+            next = append_keys(stg, tile_v0, Q, next, lim);
         }
-        if (added == NO_ROOM) {
-            // This tile alone holds more than the buffer's room: select its
-            // top-k exactly instead.
-            count_event(p, TOPK_CNT_OVERFLOW_ROUNDS);
-            thr = max(thr, t);
-            tile_select(raw, ek, stg, tile_v0, nv);
-            return;
-        }
-        count += added;
-        buf_lo = min(buf_lo, t);
     }
 
+    // C == 1: the buffer holds the row's candidates; write its top-k.
     __device__ void emit_single() {
         __syncthreads();
-        for (uint32_t i = threadIdx.x; i < k; i += THREADS)
-            p.out[static_cast<int64_t>(row) * k + i] =
-                i < count ? transform(p, row, static_cast<int32_t>(s.buf_idx[i])) : -1;
+        const uint32_t n = s.v_count;
+        uint32_t T = 0, cut = ALL;
+        if (n > k) {
+            uint32_t take;
+            if (known_T) {
+                T = known_T;
+                take = last_take;
+            } else {
+                uint32_t above;
+                window_select(0, n, buf_lo, max(s.v_bufmax, buf_lo), k, T, above);
+                take = k - above;
+            }
+            cut = tie_cut(n, T, take);
+        }
+        const uint32_t written = select_entries(n, T, cut, false, 0);
+        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        for (uint32_t i = written + threadIdx.x; i < k; i += THREADS) orow[i] = -1;
     }
 
-    // Cluster merge of the C buffers (each its CTA's top-k, in index order).
+    // Cluster merge: the C buffers (each its CTA's top-k) give the row's k-th
+    // key; ties at it go to the lowest indices, lower-ranked CTAs first.
     __device__ void merge_and_emit() {
         const int tid = threadIdx.x;
         count_event(p, TOPK_CNT_CLUSTER_MERGES);
+        compact(false);
         __syncthreads();
-        // Every CTA learns the row's best lower bound and its largest key.
-        const uint32_t my_max = count ? s.ctr[CTR_BUFMAX] : 0u;
+        const uint32_t n = s.v_count;
+        const uint32_t my_max = n ? s.v_bufmax : 0u;
         if (tid == 0) {
             atomicMax(&s.shared_thr, best_T);
             atomicMax(&s.shared_max, my_max);
@@ -995,20 +1108,13 @@ struct Cta {
         }
         cluster_arrive();
         cluster_wait();
-        const uint32_t LB = max(*reinterpret_cast<volatile uint32_t *>(&s.shared_thr), 1u);
-        const uint32_t HI = *reinterpret_cast<volatile uint32_t *>(&s.shared_max);
+        const uint32_t LB = max(volatile_load(&s.shared_thr), 1u);
+        const uint32_t HI = volatile_load(&s.shared_max);
         const uint32_t range = HI > LB ? HI - LB : 0u;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
-        constexpr int PER = (TOPK_MAX_K + THREADS - 1) / THREADS;
-        const uint32_t first = static_cast<uint32_t>(tid) * PER;
-        uint32_t key[PER], idx[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            const uint32_t i = first + e;
-            key[e] = i < count ? s.buf_key[i] : 0u;
-            idx[e] = i < count ? s.buf_idx[i] : 0u;
-            if (key[e] < LB || HI < LB) key[e] = 0u;  // cannot be selected
-            if (key[e]) atomicAdd(&s.h_merge[0][window_bin(key[e], LB, shift)], 1u);
+        for (uint32_t i = tid; i < n; i += THREADS) {
+            const uint32_t key = s.buf_key[i];
+            if (key >= LB && HI >= LB) atomicAdd(&s.h_merge[0][window_bin(key, LB, shift)], 1u);
         }
         cluster_arrive();
         cluster_wait();
@@ -1028,7 +1134,7 @@ struct Cta {
         uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0, b2 = 0;
         const uint32_t lane = lane_id();
         if (!enough) {
-            // Fewer than k candidates in the row: all of them.
+            // Fewer than k candidates in the row: all of them (all are >= LB).
             uint32_t x = 0;
             for (uint32_t b = lane; b < 256u; b += 32u) x += s.m_pre[0][b];
             gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
@@ -1041,10 +1147,10 @@ struct Cta {
             eq_prev = s.m_pre[0][b1];
         } else {
             const uint32_t mask = (1u << shift) - 1u;
-#pragma unroll
-            for (int e = 0; e < PER; ++e)
-                if (key[e] && ((key[e] - LB) >> shift) == b1) atomicAdd(&s.h_merge[1][(key[e] - LB) & mask], 1u);
-            __syncthreads();
+            for (uint32_t i = tid; i < n; i += THREADS) {
+                const uint32_t key = s.buf_key[i];
+                if (key >= LB && ((key - LB) >> shift) == b1) atomicAdd(&s.h_merge[1][(key - LB) & mask], 1u);
+            }
             cluster_arrive();
             cluster_wait();
             uint32_t all = 0, pre = 0;
@@ -1067,36 +1173,18 @@ struct Cta {
             eq_prev = s.m_pre[1][b2];
         }
         cluster_arrive();  // done reading the peers' shared memory
-        // Ordered emission: keys > T, then ties while the row-wide tie rank < take.
-        uint32_t gt = 0, eq = 0;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            gt += key[e] != 0u && key[e] > T;
-            eq += key[e] != 0u && key[e] == T;
-        }
-        uint32_t totals;
-        const uint32_t incl = block_incl_scan(gt | (eq << 16), totals);
-        const uint32_t ex = incl - (gt | (eq << 16));
+        // This CTA's selected: keys > T, and its quota of the lowest-index ties.
         const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
-        const uint32_t mine = (totals & 0xFFFFu) + min(totals >> 16, quota);
         const uint32_t offset = gt_prev + min(eq_prev, take);
-        uint32_t lgt = ex & 0xFFFFu, leq = ex >> 16;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            if (key[e] == 0u) continue;
-            if (key[e] > T) {
-                s.buf_idx[lgt + min(leq, quota)] = idx[e];
-                ++lgt;
-            } else if (key[e] == T) {
-                if (leq < quota) s.buf_idx[lgt + leq] = idx[e];
-                ++leq;
-            }
+        if (!enough) {
+            select_entries(n, LB, ALL, false, offset);        // every key >= LB
+        } else if (quota == 0) {
+            select_entries(n, T + 1u, ALL, false, offset);    // keys > T
+        } else {
+            select_entries(n, T, tie_cut(n, T, quota), false, offset);
         }
-        __syncthreads();
         const uint32_t selected_total = enough ? k : total;
         int32_t *orow = p.out + static_cast<int64_t>(row) * k;
-        for (uint32_t i = tid; i < mine; i += THREADS)
-            orow[offset + i] = transform(p, row, static_cast<int32_t>(s.buf_idx[i]));
         for (uint32_t i = selected_total + rank + static_cast<uint32_t>(tid) * C; i < k; i += THREADS * C)
             orow[i] = -1;
         cluster_wait();
@@ -1158,10 +1246,10 @@ __device__ __forceinline__ void feed_issue(Feed &f, S &s, int st, const Params &
     if (++f.tile == f.ntiles) feed_seek(f, p, block, f.row + step, step, C, rank);
 }
 
-template <class M, int NSTAGE, int CAP, int SURV>
+template <class M, int NSTAGE, int CAP>
 __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    using S = Smem<NSTAGE, CAP, SURV>;
+    using S = Smem<NSTAGE, CAP>;
     S &s = *reinterpret_cast<S *>(smem_raw);
     const int tid = threadIdx.x;
     const uint32_t C = cluster_size();
@@ -1193,7 +1281,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cluster_wait();
     }
 
-    Cta<M, NSTAGE, CAP, SURV> cta(s, p);
+    Cta<M, NSTAGE, CAP> cta(s, p);
     cta.C = C;
     cta.rank = rank;
     cta.k = static_cast<uint32_t>(p.k);
@@ -1214,11 +1302,15 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cta.row = row;
         cta.L = L;
         cta.V = V;
-        cta.count = 0;
         cta.thr = M::KMIN;
         cta.buf_lo = 0xFFFFu;
         cta.best_T = 0;
-        if (tid == 0) s.ctr[CTR_BUFMAX] = 0u;
+        cta.known_T = 0;
+        if (tid == 0) {
+            s.v_count = 0u;
+            s.v_bufmax = 0u;
+        }
+        __syncthreads();
         const int ntiles = static_cast<int>((v1 - v0 + TILE_VEC - 1) / TILE_VEC);
         for (int i = 0; i < ntiles; ++i, ++seq) {
             const int st = static_cast<int>(seq % NSTAGE);
@@ -1259,7 +1351,6 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
                 feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);
             }
         }
-        if (cta.count > cta.k) cta.compact();
         if (C == 1) {
             cta.emit_single();
         } else {
@@ -1276,21 +1367,19 @@ struct Variant {
     int smem;
 };
 
-constexpr int NARROW_NSTAGE = 2, NARROW_CAP = 2048, NARROW_SURV = 4096;
-constexpr int WIDE_NSTAGE = 4, WIDE_CAP = 8192, WIDE_SURV = 4096;
+constexpr int NARROW_NSTAGE = 2, NARROW_CAP = 3072;
+constexpr int WIDE_NSTAGE = 4, WIDE_CAP = 8192;
 
-template <class M, int NSTAGE, int CAP, int SURV>
+template <class M, int NSTAGE, int CAP>
 Variant variant() {
-    return Variant{reinterpret_cast<const void *>(&topk_kernel<M, NSTAGE, CAP, SURV>),
-                   static_cast<int>(sizeof(Smem<NSTAGE, CAP, SURV>))};
+    return Variant{reinterpret_cast<const void *>(&topk_kernel<M, NSTAGE, CAP>),
+                   static_cast<int>(sizeof(Smem<NSTAGE, CAP>))};
 }
 
 Variant pick(bool block, bool wide) {
     if (block)
-        return wide ? variant<BlockMode, WIDE_NSTAGE, WIDE_CAP, WIDE_SURV>()
-                    : variant<BlockMode, NARROW_NSTAGE, NARROW_CAP, NARROW_SURV>();
-    return wide ? variant<TokenMode, WIDE_NSTAGE, WIDE_CAP, WIDE_SURV>()
-                : variant<TokenMode, NARROW_NSTAGE, NARROW_CAP, NARROW_SURV>();
+        return wide ? variant<BlockMode, WIDE_NSTAGE, WIDE_CAP>() : variant<BlockMode, NARROW_NSTAGE, NARROW_CAP>();
+    return wide ? variant<TokenMode, WIDE_NSTAGE, WIDE_CAP>() : variant<TokenMode, NARROW_NSTAGE, NARROW_CAP>();
 }
 
 struct DeviceInit {

@@ -95,8 +95,8 @@ const char *topk_bf16_status_string(topk_status_t status);
  * internal path computes the result, never the result itself.
  */
 typedef struct {
-    int32_t force_direct;   /* 1: skip the sampled cutoff; every tile takes the exact
-                               whole-tile radix path (the fallback) */
+    int32_t force_direct;   /* 1: skip the group-representative cutoff; every first
+                               tile takes the exact whole-tile radix path (the fallback) */
     int32_t cluster;        /* 0: automatic; else CTAs per row: 1, 2, 4, 8 or 16 */
     uint32_t *counters;     /* NULL, or device uint32 [TOPK_NUM_COUNTERS] that each
                                launch adds its path counts to */
@@ -105,15 +105,16 @@ typedef struct {
 /* Indices into topk_bf16_options_t.counters. */
 enum {
     TOPK_CNT_BYPASS_ROWS = 0,    /* rows with n <= k */
-    TOPK_CNT_TILE_SAMPLED = 1,   /* tiles solved by the sampled cutoff */
-    TOPK_CNT_TILE_FORCED = 2,    /* tiles solved by the exact path because forced */
-    TOPK_CNT_TILE_OVERSHOT = 3,  /* sample cutoff above the k-th: exact path taken */
-    TOPK_CNT_TILE_OVERFLOW = 4,  /* too many survivors: exact path taken */
-    TOPK_CNT_TILE_TAKE_ALL = 5,  /* tiles with at most k candidates */
+    TOPK_CNT_TILE_SAMPLED = 1,   /* first tiles cut by the k-th largest group representative */
+    TOPK_CNT_TILE_EXACT = 2,     /* first tiles cut by the exact path (every key its own
+                                    representative): forced, fallen back to, or k-sized groups */
+    TOPK_CNT_TILE_UNBOUNDED = 3, /* fewer than k usable representatives: exact path taken */
+    TOPK_CNT_TILE_OVERFLOW = 4,  /* more survivors than buffer room: exact path taken */
+    TOPK_CNT_TILE_TAKE_ALL = 5,  /* first tiles with at most k candidates */
     TOPK_CNT_COMPACTIONS = 6,    /* candidate-buffer compactions */
-    TOPK_CNT_OVERFLOW_ROUNDS = 7,/* streamed rounds that needed their own selection */
+    TOPK_CNT_REFILLS = 7,        /* tiles that filled the buffer and resumed after a compaction */
     TOPK_CNT_CLUSTER_MERGES = 8, /* rows merged across a cluster of CTAs */
-    TOPK_CNT_ROUNDS = 9,         /* streamed rounds (tiles) in total */
+    TOPK_CNT_ROUNDS = 9,         /* tiles streamed in total */
     TOPK_NUM_COUNTERS = 16
 };
 
@@ -136,8 +137,9 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
 
 /*
  * Device-side status word of the current device: nonzero bits record a bounded
- * wait that gave up (bit 0) or an internal bound check that failed (bit 1, debug
- * builds). Synchronises the device. clear != 0 resets the word afterwards.
+ * wait that gave up (bit 0) or an internal capacity or range check that failed
+ * (bit 1); neither happens in correct operation, and the kernels never trap.
+ * Synchronises the device. clear != 0 resets the word afterwards.
  */
 topk_status_t topk_bf16_device_status(uint32_t *flags, int32_t clear);
 

@@ -110,7 +110,7 @@ def test_path_counters_cover_every_path():
         run_gpu(case, counters=counters, cluster=4)
     run_gpu(W.edge_cases(0)[0], counters=counters, force_direct=True)
     c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
-    for name in ("bypass_rows", "tile_sampled", "tile_forced", "tile_take_all", "compactions",
+    for name in ("bypass_rows", "tile_sampled", "tile_exact", "tile_take_all", "compactions",
                  "cluster_merges", "rounds"):
         assert c[name] > 0, (name, c)
 

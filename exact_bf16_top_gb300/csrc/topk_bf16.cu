@@ -99,8 +99,9 @@ struct alignas(128) Smem {
     uint32_t v_bufmax;                       // largest buffer key
     uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
     uint32_t v_ntie, v_emit, v_flag;
-    uint32_t shared_thr;                     // lower bound on the row's k-th key (max)
-    uint32_t shared_max;                     // largest candidate key of the cluster (max)
+    uint32_t shared_thr[2];                  // lower bound on the row's k-th key (max), by row parity
+    uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
+    uint32_t thr_snap;                       // shared_thr as every thread sees it this tile
     uint32_t abort_flag;                     // a bounded wait gave up
     uint8_t queue[WARPS][QCAP];              // per-warp vector queues
     unsigned long long full[NSTAGE];         // stage mbarriers
@@ -428,6 +429,7 @@ struct Cta {
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
     uint32_t known_T = 0;    // nonzero: the buffer's top-k cut is known (last_take ties at it)
     uint32_t last_take = 0;
+    uint32_t slot = 0;       // parity of this cluster's row: which shared words it uses
 
     __device__ Cta(S &s_, const Params &p_) : s(s_), p(p_) {}
 
@@ -435,15 +437,21 @@ struct Cta {
         return *reinterpret_cast<const volatile uint32_t *>(x);
     }
 
-    __device__ __forceinline__ uint32_t effective_thr() {
-        return C > 1 ? max(thr, volatile_load(&s.shared_thr)) : thr;
+    // The threshold with the peers' bound as of the last snapshot (the same in
+    // every thread: the snapshot is taken by one thread before a barrier).
+    __device__ __forceinline__ uint32_t effective_thr() { return C > 1 ? max(thr, s.thr_snap) : thr; }
+
+    // Thread 0 records the peers' current bound; a __syncthreads must follow
+    // before effective_thr() reads it.
+    __device__ __forceinline__ void snapshot_shared() {
+        if (C > 1 && threadIdx.x == 0) s.thr_snap = volatile_load(&s.shared_thr[slot]);
     }
 
     // Every CTA of the row learns that the row's k-th key is at least `bound`.
     __device__ __forceinline__ void publish(uint32_t bound) {
         best_T = max(best_T, bound);
         if (C > 1 && threadIdx.x < C && threadIdx.x != rank)
-            red_max_peer(peer_addr(&s.shared_thr, threadIdx.x), bound);
+            red_max_peer(peer_addr(&s.shared_thr[slot], threadIdx.x), bound);
     }
 
     // Inclusive scan over the CTA's threads (one __syncthreads).
@@ -1099,17 +1107,19 @@ struct Cta {
         const uint32_t n = s.v_count;
         const uint32_t my_max = n ? s.v_bufmax : 0u;
         if (tid == 0) {
-            atomicMax(&s.shared_thr, best_T);
-            atomicMax(&s.shared_max, my_max);
+            atomicMax(&s.shared_thr[slot], best_T);
+            atomicMax(&s.shared_max[slot], my_max);
         }
         if (tid < static_cast<int>(C) && tid != static_cast<int>(rank)) {
-            red_max_peer(peer_addr(&s.shared_thr, tid), best_T);
-            red_max_peer(peer_addr(&s.shared_max, tid), my_max);
+            red_max_peer(peer_addr(&s.shared_thr[slot], tid), best_T);
+            red_max_peer(peer_addr(&s.shared_max[slot], tid), my_max);
         }
         cluster_arrive();
         cluster_wait();
-        const uint32_t LB = max(volatile_load(&s.shared_thr), 1u);
-        const uint32_t HI = volatile_load(&s.shared_max);
+        // Every publication for this row came before the barrier: all threads
+        // read the same words.
+        const uint32_t LB = max(volatile_load(&s.shared_thr[slot]), 1u);
+        const uint32_t HI = volatile_load(&s.shared_max[slot]);
         const uint32_t range = HI > LB ? HI - LB : 0u;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         for (uint32_t i = tid; i < n; i += THREADS) {
@@ -1188,12 +1198,13 @@ struct Cta {
         for (uint32_t i = selected_total + rank + static_cast<uint32_t>(tid) * C; i < k; i += THREADS * C)
             orow[i] = -1;
         cluster_wait();
-        // Every peer is done with this row's shared words: reset them.
+        // Every peer is done with this row's shared words: reset them for the
+        // row after next (the next row uses the other parity).
         s.h_merge[0][tid] = 0u;
         s.h_merge[1][tid] = 0u;
         if (tid == 0) {
-            s.shared_thr = 0u;
-            s.shared_max = 0u;
+            s.shared_thr[slot] = 0u;
+            s.shared_max[slot] = 0u;
         }
     }
 };
@@ -1261,8 +1272,9 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
-        s.shared_thr = 0u;
-        s.shared_max = 0u;
+        s.shared_thr[0] = s.shared_thr[1] = 0u;
+        s.shared_max[0] = s.shared_max[1] = 0u;
+        s.thr_snap = 0u;
         s.abort_flag = 0u;
     }
     for (int i = tid; i < HBINS; i += THREADS) s.hist[i] = 0u;
@@ -1285,8 +1297,8 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     cta.C = C;
     cta.rank = rank;
     cta.k = static_cast<uint32_t>(p.k);
-    uint32_t seq = 0;
-    for (int32_t row = cid; row < p.rows; row += ncl) {
+    uint32_t seq = 0, it = 0;
+    for (int32_t row = cid; row < p.rows; row += ncl, ++it) {
         int32_t L;
         int64_t V, v0, v1;
         if (!row_share(p, M::BLOCK, row, C, rank, L, V, v0, v1)) {
@@ -1306,10 +1318,12 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cta.buf_lo = 0xFFFFu;
         cta.best_T = 0;
         cta.known_T = 0;
+        cta.slot = it & 1u;
         if (tid == 0) {
             s.v_count = 0u;
             s.v_bufmax = 0u;
         }
+        cta.snapshot_shared();
         __syncthreads();
         const int ntiles = static_cast<int>((v1 - v0 + TILE_VEC - 1) / TILE_VEC);
         for (int i = 0; i < ntiles; ++i, ++seq) {
@@ -1345,6 +1359,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             } else {
                 cta.filter_tile(raw, ek, stg, tile_v0, nv);
             }
+            cta.snapshot_shared();
             __syncthreads();  // every thread is done with this stage
             if (tid == 0 && feed.row < p.rows) {
                 fence_proxy_async();

@@ -23,6 +23,11 @@ def _setup():
     oracle.build()
     tk.device_status(clear=True)
     yield
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean():
+    yield
     assert tk.device_status(clear=True) == 0, "device status flags set"
 
 

@@ -1071,6 +1071,7 @@ struct Cta {
             // may still tie with it) and carry on.
             count_event(p, TOPK_CNT_REFILLS);
             compact(false);
+            lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
             next = append_keys(stg, tile_v0, Q, next, lim);
         }
     }

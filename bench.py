@@ -300,6 +300,30 @@ def profile(args):
                       "plan": tk.plan(case.rows, case.width, case.k, case.mode)}))
 
 
+def diag(args):
+    """Path counters and cycle split (thread 0 of each CTA) of chosen workloads."""
+    import torch
+    import exact_bf16_top_gb300 as tk
+    tk._build.build()
+    dev = torch.device("cuda", 0)
+    for want in args.diag.split(","):
+        for name, make in sweep_cases(True):
+            if want not in name:
+                continue
+            case = make()
+            gc = GpuCase(case, torch, dev, min_copies=1)
+            gc.launch(0, tk)
+            ctr = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device=dev)
+            c = case
+            tk.select(gc.logits[0], gc.valid, c.k, c.mode, gc.table, c.page_size, out=gc.out,
+                      width=c.width, counters=ctr)
+            torch.cuda.synchronize()
+            vals = ctr.cpu().numpy().view(np.uint32).tolist()
+            print(json.dumps({"workload": name, "plan": tk.plan(c.rows, c.width, c.k, c.mode),
+                              **dict(zip(tk.COUNTER_NAMES, vals))}))
+            break
+
+
 # -------------------------------------------------------------------- main
 
 def main():
@@ -311,12 +335,17 @@ def main():
     ap.add_argument("--sweep", choices=("none", "k512", "full"), default="k512")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--diag", default=None,
+                    help="comma-separated substrings of sweep workloads: print their path "
+                         "counters and the per-phase cycle split, then exit")
     ap.add_argument("--profile", default=None,
                     help="launch one sweep workload (a substring of its name) --steps times "
                          "after --warmup launches, eagerly, and exit (for ncu)")
     args = ap.parse_args()
     if args.profile:
         return profile(args)
+    if args.diag:
+        return diag(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

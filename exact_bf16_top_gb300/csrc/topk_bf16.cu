@@ -396,6 +396,18 @@ __device__ __forceinline__ void count_event(const Params &p, int which) {
     if (p.counters && threadIdx.x == 0) atomicAdd(p.counters + which, 1u);
 }
 
+// Cycle accounting for the diagnosis counters (thread 0, only when enabled).
+struct PhaseClock {
+    long long t = 0;
+    __device__ __forceinline__ void start(const Params &p) {
+        if (p.counters && threadIdx.x == 0) t = clock64();
+    }
+    __device__ __forceinline__ void stop(const Params &p, int which) {
+        if (p.counters && threadIdx.x == 0)
+            atomicAdd(p.counters + which, static_cast<uint32_t>(clock64() - t));
+    }
+};
+
 __device__ __forceinline__ int32_t transform(const Params &p, int32_t row, int32_t i) {
     if (!p.table) return i;
     const int32_t page = p.table[static_cast<int64_t>(row) * p.table_stride + (i >> p.page_shift)];
@@ -1034,6 +1046,8 @@ struct Cta {
         const uint32_t n = s.v_count;
         if (n <= k) return;
         count_event(p, TOPK_CNT_COMPACTIONS);
+        PhaseClock clk;
+        clk.start(p);
         uint32_t T, above;
         window_select(0, n, buf_lo, max(s.v_bufmax, buf_lo), k, T, above);
         const uint32_t take = k - above;
@@ -1045,6 +1059,7 @@ struct Cta {
         thr = max(thr, strict ? T + 1u : T);
         publish(T);
         __syncthreads();
+        clk.stop(p, TOPK_CNT_CYC_COMPACT);
     }
 
     // A later tile: append every key >= the threshold.
@@ -1331,8 +1346,12 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             const int st = static_cast<int>(seq % NSTAGE);
             const int64_t tile_v0 = v0 + static_cast<int64_t>(i) * TILE_VEC;
             const int nv = static_cast<int>(v1 - tile_v0 < TILE_VEC ? v1 - tile_v0 : TILE_VEC);
+            PhaseClock clk;
+            clk.start(p);
             mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+            clk.stop(p, TOPK_CNT_CYC_WAIT);
             count_event(p, TOPK_CNT_ROUNDS);
+            clk.start(p);
             const uint4 *stg = s.stage[st];
             uint4 raw[VPT];
             uint32_t ek[VPT];
@@ -1357,8 +1376,10 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             if (i == 0) {
                 cta.thr = max(cta.thr, cta.effective_thr());
                 cta.tile_select(raw, ek, stg, tile_v0, nv);
+                clk.stop(p, TOPK_CNT_CYC_SELECT);
             } else {
                 cta.filter_tile(raw, ek, stg, tile_v0, nv);
+                clk.stop(p, TOPK_CNT_CYC_FILTER);
             }
             cta.snapshot_shared();
             __syncthreads();  // every thread is done with this stage
@@ -1367,12 +1388,15 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
                 feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);
             }
         }
+        PhaseClock fin;
+        fin.start(p);
         if (C == 1) {
             cta.emit_single();
         } else {
             cta.merge_and_emit();
         }
         __syncthreads();
+        fin.stop(p, TOPK_CNT_CYC_FINISH);
     }
 }
 

@@ -115,6 +115,12 @@ enum {
     TOPK_CNT_REFILLS = 7,        /* tiles that filled the buffer and resumed after a compaction */
     TOPK_CNT_CLUSTER_MERGES = 8, /* rows merged across a cluster of CTAs */
     TOPK_CNT_ROUNDS = 9,         /* tiles streamed in total */
+    /* SM clock cycles thread 0 of each CTA spent, summed over CTAs: */
+    TOPK_CNT_CYC_WAIT = 10,      /* waiting for a stage */
+    TOPK_CNT_CYC_SELECT = 11,    /* first-tile selects */
+    TOPK_CNT_CYC_FILTER = 12,    /* later tiles (compactions included) */
+    TOPK_CNT_CYC_FINISH = 13,    /* the row's final select, merge and write */
+    TOPK_CNT_CYC_COMPACT = 14,   /* buffer compactions */
     TOPK_NUM_COUNTERS = 16
 };
 

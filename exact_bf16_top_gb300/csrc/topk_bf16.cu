@@ -87,7 +87,7 @@ struct alignas(128) Smem {
     uint32_t buf_idx[CAP];                   // candidate buffer (any order)
     uint16_t buf_key[CAP];
     uint32_t hist[HBINS];                    // 12-bit histogram (zero between uses)
-    uint32_t hwin[2][256];                   // window histograms (zero between uses)
+    uint32_t hwin[4][256];                   // window histograms (zero between uses)
     uint32_t h_merge[2][256];                // this CTA's merge histograms (peers read them)
     uint32_t m_all[256];                     // merge: counts over the cluster
     uint32_t m_pre[2][256];                  // merge: counts over lower-ranked CTAs
@@ -422,101 +422,65 @@ __device__ __forceinline__ uint32_t warp_reserve(uint32_t *ctr, uint32_t n) {
 }
 
 // --------------------------------------------------------- the CTA's machinery
+//
+// The per-row state is uniform across the CTA. The larger routines are kept out
+// of line: a row's selection walks many phases once each, and inlining them all
+// made the code far larger than the SM's instruction cache.
 
 template <class M, int NSTAGE, int CAP>
 struct Cta {
     static constexpr int KPV = M::KPV;
     using S = Smem<NSTAGE, CAP>;
 
-    S &s;
-    const Params &p;
-    uint32_t C, rank;
+    S *s;
+    const Params *p;
+    uint32_t C = 1, rank = 0;
     uint32_t parity = 0;     // alternates double-buffered scan scratch
-    // per row
+    uint32_t slot = 0;       // parity of this cluster's row: which shared words it uses
     int32_t row = 0, L = 0;
     int64_t V = 0;
     uint32_t k = 0;
     uint32_t thr = 0;        // keep keys >= thr
     uint32_t buf_lo = 0;     // every buffer key is >= buf_lo
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
-    uint32_t known_T = 0;    // nonzero: the buffer's top-k cut is known (last_take ties at it)
+    uint32_t known_T = 0;    // nonzero: the buffer's top-k cut (last_take ties at it)
     uint32_t last_take = 0;
-    uint32_t slot = 0;       // parity of this cluster's row: which shared words it uses
 
-    __device__ Cta(S &s_, const Params &p_) : s(s_), p(p_) {}
-
-    __device__ __forceinline__ uint32_t volatile_load(const uint32_t *x) {
+    __device__ __forceinline__ static uint32_t volatile_load(const uint32_t *x) {
         return *reinterpret_cast<const volatile uint32_t *>(x);
     }
 
     // The threshold with the peers' bound as of the last snapshot (the same in
-    // every thread: the snapshot is taken by one thread before a barrier).
-    __device__ __forceinline__ uint32_t effective_thr() { return C > 1 ? max(thr, s.thr_snap) : thr; }
+    // every thread: thread 0 takes the snapshot before a barrier).
+    __device__ __forceinline__ uint32_t effective_thr() const { return C > 1 ? max(thr, s->thr_snap) : thr; }
 
-    // Thread 0 records the peers' current bound; a __syncthreads must follow
-    // before effective_thr() reads it.
     __device__ __forceinline__ void snapshot_shared() {
-        if (C > 1 && threadIdx.x == 0) s.thr_snap = volatile_load(&s.shared_thr[slot]);
+        if (C > 1 && threadIdx.x == 0) s->thr_snap = volatile_load(&s->shared_thr[slot]);
     }
 
     // Every CTA of the row learns that the row's k-th key is at least `bound`.
     __device__ __forceinline__ void publish(uint32_t bound) {
         best_T = max(best_T, bound);
         if (C > 1 && threadIdx.x < C && threadIdx.x != rank)
-            red_max_peer(peer_addr(&s.shared_thr[slot], threadIdx.x), bound);
+            red_max_peer(peer_addr(&s->shared_thr[slot], threadIdx.x), bound);
+    }
+
+    __device__ __forceinline__ void clean_at(const uint4 *stg, int64_t tile_v0, int pos, uint32_t (&ck)[4]) const {
+        M::clean(stg[pos], tile_v0 + pos, V, L, ck);
     }
 
     // Inclusive scan over the CTA's threads (one __syncthreads).
     __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t &total) {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
         const uint32_t inc = warp_incl_scan(x);
-        if (lane == 31) s.red[parity][warp] = inc;
+        if (lane == 31) s->red[parity][warp] = inc;
         __syncthreads();
-        const uint32_t w = lane < WARPS ? s.red[parity][lane] : 0u;
+        const uint32_t w = lane < WARPS ? s->red[parity][lane] : 0u;
         const uint32_t wi = warp_incl_scan(w);
         total = __shfl_sync(0xFFFFFFFFu, wi, 31);
         const uint32_t pre = __shfl_sync(0xFFFFFFFFu, wi - w, warp);
         parity ^= 1u;
         return pre + inc;
-    }
-
-    // The 12-bit bin of s.hist holding the q-th largest key: writes s.bc =
-    // {bin, above, count(bin)} and returns the histogram total (every thread).
-    // Zeroes s.hist. Two __syncthreads.
-    __device__ uint32_t find_cut4096(uint32_t q) {
-        const int t = threadIdx.x;
-        const int base = HBINS - 16 * (t + 1);  // thread 0 owns the highest 16 bins
-        uint4 *h4 = reinterpret_cast<uint4 *>(s.hist + base);
-        const uint4 a = h4[0], b = h4[1], c = h4[2], d = h4[3];
-        const uint32_t v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
-                                c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        h4[0] = z;
-        h4[1] = z;
-        h4[2] = z;
-        h4[3] = z;
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sum += v[i];
-        uint32_t total;
-        const uint32_t incl = block_incl_scan(sum, total);
-        const uint32_t excl = incl - sum;
-        if (excl < q && q <= incl) {
-            uint32_t acc = excl;
-            bool done = false;
-#pragma unroll
-            for (int i = 15; i >= 0; --i) {
-                if (!done && acc + v[i] >= q) {
-                    s.bc[0] = static_cast<uint32_t>(base + i);
-                    s.bc[1] = acc;
-                    s.bc[2] = v[i];
-                    done = true;
-                }
-                acc += v[i];
-            }
-        }
-        __syncthreads();
-        return total;
     }
 
     // Bin of `key` in a window [lo, lo + (256 << shift)); a key outside it would
@@ -530,153 +494,191 @@ struct Cta {
         return o;
     }
 
+    // The 12-bit bin of s->hist holding the q-th largest key: s->bc = {bin,
+    // above, count(bin)}; returns the histogram total. Zeroes s->hist.
+    __device__ __noinline__ uint32_t find_cut4096(uint32_t q) {
+        const int t = threadIdx.x;
+        const int base = HBINS - 16 * (t + 1);  // thread 0 owns the highest 16 bins
+        uint4 *h4 = reinterpret_cast<uint4 *>(s->hist + base);
+        const uint4 a = h4[0], b = h4[1], c = h4[2], d = h4[3];
+        const uint32_t v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
+                                c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        h4[0] = z;
+        h4[1] = z;
+        h4[2] = z;
+        h4[3] = z;
+        uint32_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sum += v[i];
+        uint32_t total;
+        const uint32_t incl = block_incl_scan(sum, total);
+        uint32_t acc = incl - sum;
+        if (acc < q && q <= incl) {
+            bool done = false;
+#pragma unroll
+            for (int i = 15; i >= 0; --i) {
+                if (!done && acc + v[i] >= q) {
+                    s->bc[0] = static_cast<uint32_t>(base + i);
+                    s->bc[1] = acc;
+                    s->bc[2] = v[i];
+                    done = true;
+                }
+                acc += v[i];
+            }
+        }
+        __syncthreads();
+        return total;
+    }
+
     // The q-th largest of buf_key[first .. first + n), all within [lo, hi]
-    // (q <= n): a radix select over bins relative to lo, one pass when
-    // hi - lo < 256, else two. T = that key, above = keys greater than it.
-    // s.hwin is zero on entry and on exit.
-    __device__ void window_select(uint32_t first, uint32_t n, uint32_t lo, uint32_t hi, uint32_t q,
-                                  uint32_t &T, uint32_t &above) {
+    // (q <= n): radix select over bins relative to lo, one pass when hi - lo <
+    // 256, else two. T = that key, above = keys greater than it. Uses
+    // s->hwin[2] and s->hwin[3] (zero on entry and on exit).
+    __device__ __noinline__ void window_select(uint32_t first, uint32_t n, uint32_t lo, uint32_t hi,
+                                               uint32_t q, uint32_t *T_out, uint32_t *above_out) {
         const int tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         for (uint32_t i = tid; i < n; i += THREADS)
-            atomicAdd(&s.hwin[0][window_bin(s.buf_key[first + i], lo, shift)], 1u);
+            atomicAdd(&s->hwin[2][window_bin(s->buf_key[first + i], lo, shift)], 1u);
         __syncthreads();
-        uint32_t b1, above1, tot;
-        find_bin256(s.hwin[0], q, b1, above1, tot);
+        uint32_t b1, above1, tot, T, above;
+        find_bin256(s->hwin[2], q, b1, above1, tot);
         if (shift == 0) {
             T = lo + b1;
             above = above1;
         } else {
             const uint32_t mask = (1u << shift) - 1u;
             for (uint32_t i = tid; i < n; i += THREADS) {
-                const uint32_t o = static_cast<uint32_t>(s.buf_key[first + i]) - lo;
-                if ((o >> shift) == b1) atomicAdd(&s.hwin[1][o & mask], 1u);
+                const uint32_t o = static_cast<uint32_t>(s->buf_key[first + i]) - lo;
+                if ((o >> shift) == b1) atomicAdd(&s->hwin[3][o & mask], 1u);
             }
             __syncthreads();
             uint32_t b2, above2;
-            find_bin256(s.hwin[1], q - above1, b2, above2, tot);
+            find_bin256(s->hwin[3], q - above1, b2, above2, tot);
             T = lo + (b1 << shift) + b2;
             above = above1 + above2;
         }
         __syncthreads();
-        s.hwin[0][tid] = 0u;
-        s.hwin[1][tid] = 0u;
+        s->hwin[2][tid] = 0u;
+        s->hwin[3][tid] = 0u;
+        *T_out = T;
+        *above_out = above;
     }
 
-    // Rank the indices in s.tie_idx[0 .. e) (e <= TIECAP, distinct): the index
-    // with exactly q - 1 smaller ones. One __syncthreads.
-    __device__ uint32_t rank_cut(uint32_t e, uint32_t q) {
-        const uint32_t t = threadIdx.x;
-        if (t < e) {
-            const uint32_t mine = s.tie_idx[t];
-            uint32_t r = 0;
-            for (uint32_t u = 0; u < e; ++u) r += s.tie_idx[u] < mine;
-            if (r == q - 1) s.bc[3] = mine;
-        }
-        __syncthreads();
-        return s.bc[3];
-    }
-
-    // Among buffer entries [0, n) with key == T (e of them, all distinct
-    // indices), the cut such that exactly q have an index <= cut: ALL when
-    // q >= e. Few ties are ranked directly; many by a two-pass radix select over
-    // 10-bit index digits (indices are below 2^20).
-    __device__ uint32_t tie_cut(uint32_t n, uint32_t T, uint32_t q) {
+    // The q-th smallest index among buffer entries [0, n) whose key is T, when
+    // there are more than TIECAP of them: a two-pass radix select over 10-bit
+    // digits (indices are below 2^20), in s->hist (zero on entry and exit).
+    __device__ __noinline__ uint32_t tie_radix(uint32_t n, uint32_t T, uint32_t q) {
         const int tid = threadIdx.x;
-        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
-        __syncthreads();
-        if (tid == 0) s.v_ntie = 0u;
-        __syncthreads();
-        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
-            const uint32_t i = i0 + tid;
-            const bool tie = i < n && s.buf_key[i] == T;
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, tie);
-            const uint32_t base = warp_reserve(&s.v_ntie, __popc(b));
-            const uint32_t slot = base + __popc(b & lt);
-            if (tie && slot < static_cast<uint32_t>(TIECAP)) s.tie_idx[slot] = s.buf_idx[i];
-        }
-        __syncthreads();
-        const uint32_t e = s.v_ntie;
-        if (q >= e) return ALL;
-        if (e <= static_cast<uint32_t>(TIECAP)) return rank_cut(e, q);
-        // Many ties: q-th smallest index, digit by digit.
         uint32_t cut = 0, need = q;
         for (int pass = 0; pass < 2; ++pass) {
             const int sh = pass == 0 ? 10 : 0;
             for (uint32_t i = tid; i < n; i += THREADS) {
-                if (s.buf_key[i] != T) continue;
-                const uint32_t x = s.buf_idx[i];
+                if (s->buf_key[i] != T) continue;
+                const uint32_t x = s->buf_idx[i];
                 if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
-                atomicAdd(&s.hist[(x >> sh) & 1023u], 1u);
+                atomicAdd(&s->hist[(x >> sh) & 1023u], 1u);
             }
             __syncthreads();
-            // Ascending: thread t owns bins [4t, 4t + 4).
-            uint4 *h4 = reinterpret_cast<uint4 *>(s.hist) + tid;
+            uint4 *h4 = reinterpret_cast<uint4 *>(s->hist) + tid;  // bins [4t, 4t + 4), ascending
             const uint4 hv = *h4;
             *h4 = make_uint4(0, 0, 0, 0);
             const uint32_t v[4] = {hv.x, hv.y, hv.z, hv.w};
+            const uint32_t sum = v[0] + v[1] + v[2] + v[3];
             uint32_t total;
-            const uint32_t incl = block_incl_scan(v[0] + v[1] + v[2] + v[3], total);
-            uint32_t acc = incl - (v[0] + v[1] + v[2] + v[3]);
+            const uint32_t incl = block_incl_scan(sum, total);
+            uint32_t acc = incl - sum;
             if (acc < need && need <= incl) {
                 bool done = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (!done && acc + v[i] >= need) {
-                        s.bc[0] = static_cast<uint32_t>(4 * tid + i);
-                        s.bc[1] = acc;
+                        s->bc[0] = static_cast<uint32_t>(4 * tid + i);
+                        s->bc[1] = acc;
                         done = true;
                     }
                     acc += v[i];
                 }
             }
             __syncthreads();
-            cut |= s.bc[0] << sh;
-            need -= s.bc[1];
+            cut |= s->bc[0] << sh;
+            need -= s->bc[1];
         }
         return cut;
     }
 
+    // Among buffer entries [0, n) with key T (distinct indices), the cut with
+    // exactly q of them at or below it; ALL when q covers them all.
+    __device__ __noinline__ uint32_t tie_cut(uint32_t n, uint32_t T, uint32_t q) {
+        const int tid = threadIdx.x;
+        const uint32_t lt = (1u << lane_id()) - 1u;
+        __syncthreads();
+        if (tid == 0) s->v_ntie = 0u;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
+            const uint32_t i = i0 + tid;
+            const bool tie = i < n && s->buf_key[i] == T;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, tie);
+            const uint32_t at = warp_reserve(&s->v_ntie, __popc(b)) + __popc(b & lt);
+            if (tie && at < static_cast<uint32_t>(TIECAP)) s->tie_idx[at] = s->buf_idx[i];
+        }
+        __syncthreads();
+        const uint32_t e = s->v_ntie;
+        if (q >= e) return ALL;
+        if (e > static_cast<uint32_t>(TIECAP)) return tie_radix(n, T, q);
+        if (static_cast<uint32_t>(tid) < e) {
+            const uint32_t mine = s->tie_idx[tid];
+            uint32_t r = 0;
+            for (uint32_t u = 0; u < e; ++u) r += s->tie_idx[u] < mine;
+            if (r == q - 1) s->bc[3] = mine;
+        }
+        __syncthreads();
+        return s->bc[3];
+    }
+
     // Queue, per warp and in index order, the tile's vectors that may hold a
     // key >= lim. Returns the queue length.
-    __device__ __forceinline__ uint32_t build_queue(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                                    int nv, uint32_t lim) {
+    __device__ __noinline__ uint32_t build_queue(const uint4 *stg, int64_t tile_v0, int nv, uint32_t lim) {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
         uint32_t q = 0;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int pos = j * THREADS + static_cast<int>(threadIdx.x);
-            const bool pass = pos < nv && M::may_reach(raw[j], ek[j], lim);
+            bool pass = false;
+            if (pos < nv) {
+                const uint4 raw = stg[pos];
+                pass = M::may_reach(raw, M::BLOCK ? BlockMode::key(raw, tile_v0 + pos, V) : 0u, lim);
+            }
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s.queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
+            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
             q += __popc(b);
         }
         __syncwarp();
         return q;
     }
 
-    // Clean keys of queued entry e of this warp (zeros past the queue).
-    __device__ __forceinline__ int queued_keys(const uint4 *stg, int64_t tile_v0, uint32_t e, uint32_t Q,
-                                               uint32_t (&ck)[4]) {
-        ck[0] = ck[1] = ck[2] = ck[3] = 0u;
-        if (e >= Q) return 0;
-        const uint32_t q = s.queue[threadIdx.x >> 5][e];
-        const int pos = static_cast<int>(q >> 5) * THREADS + static_cast<int>((threadIdx.x >> 5) * 32 + (q & 31u));
-        M::clean(stg[pos], tile_v0 + pos, V, L, ck);
-        return pos;
+    __device__ __forceinline__ int queued_pos(uint32_t e) const {
+        const uint32_t q = s->queue[threadIdx.x >> 5][e];
+        return static_cast<int>(q >> 5) * THREADS + static_cast<int>((threadIdx.x >> 5) * 32 + (q & 31u));
     }
 
     // Append every key >= lim of this warp's queued vectors, from queue entry
     // `from` on, to the buffer (any order). Slots are reserved a warp at a time
     // and only while they fit. Returns the first entry not appended (Q: all).
-    __device__ uint32_t append_keys(const uint4 *stg, int64_t tile_v0, uint32_t Q, uint32_t from,
-                                    uint32_t lim) {
+    __device__ __noinline__ uint32_t append_keys(const uint4 *stg, int64_t tile_v0, uint32_t Q,
+                                                 uint32_t from, uint32_t lim) {
         const uint32_t lane = lane_id();
         for (uint32_t e0 = from; e0 < Q; e0 += 32) {
-            uint32_t ck[4];
-            const int pos = queued_keys(stg, tile_v0, e0 + lane, Q, ck);
+            const uint32_t e = e0 + lane;
+            uint32_t ck[4] = {0u, 0u, 0u, 0u};
+            int pos = 0;
+            if (e < Q) {
+                pos = queued_pos(e);
+                clean_at(stg, tile_v0, pos, ck);
+            }
             uint32_t cnt = 0, kmax = 0;
 #pragma unroll
             for (int h = 0; h < KPV; ++h) {
@@ -688,13 +690,13 @@ struct Cta {
             const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
             uint32_t base = 0, ok = 1;
             if (lane == 0 && total) {
-                uint32_t old = volatile_load(&s.v_count);
+                uint32_t old = volatile_load(&s->v_count);
                 for (;;) {
                     if (old + total > static_cast<uint32_t>(CAP)) {
                         ok = 0;
                         break;
                     }
-                    const uint32_t prev = atomicCAS(&s.v_count, old, old + total);
+                    const uint32_t prev = atomicCAS(&s->v_count, old, old + total);
                     if (prev == old) {
                         base = old;
                         break;
@@ -706,16 +708,16 @@ struct Cta {
             if (!ok) return e0;  // full: the caller compacts and resumes here
             base = __shfl_sync(0xFFFFFFFFu, base, 0);
             kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0 && kmax) atomicMax(&s.v_bufmax, kmax);
+            if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
             if (cnt) {
-                uint32_t slot = base + incl - cnt;
+                uint32_t at = base + incl - cnt;
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
                     const uint32_t key = key_at<M>(ck, h);
                     if (key >= lim) {
-                        s.buf_key[slot] = static_cast<uint16_t>(key);
-                        s.buf_idx[slot] = M::elem(tile_v0 + pos, h);
-                        ++slot;
+                        s->buf_key[at] = static_cast<uint16_t>(key);
+                        s->buf_idx[at] = M::elem(tile_v0 + pos, h);
+                        ++at;
                     }
                 }
             }
@@ -723,207 +725,194 @@ struct Cta {
         return Q;
     }
 
-    // Group representatives of this thread's tile, fed to f(key) (0 = none).
-    template <int G, class F>
-    __device__ __forceinline__ void for_reps(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT],
-                                             int64_t tile_v0, int nv, F &&f) {
-        if constexpr (M::BLOCK) {
+    // Feed the tile's group representatives to the 12-bit histogram (bin ==
+    // ALL) or to the 16 sub-bins of one 12-bit bin. A representative is one
+    // element of a group of g logits (token) or g blocks (block), with key >=
+    // thr, or nothing; g = 1 feeds every candidate key.
+    __device__ __noinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t bin) {
+        uint32_t *hist = s->hist;
+        uint32_t *sub = s->sub;
+        auto feed = [&](uint32_t key) {
+            if (key == 0u) return;
+            if (bin == ALL) atomicAdd(&hist[key >> 4], 1u);
+            else if ((key >> 4) == bin) atomicAdd(&sub[key & 15u], 1u);
+        };
+        uint32_t acc = 0x80008000u;   // token: packed running maximum of a group
+        uint32_t bacc = 0u;           // block: running maximum key of a group
+        const uint32_t per = g >= 8u ? g >> 3 : 1u;  // vectors per token group
+        for (int j = 0; j < VPT; ++j) {
+            const int pos = j * THREADS + static_cast<int>(threadIdx.x);
+            const int64_t v = tile_v0 + pos;
+            if constexpr (M::BLOCK) {
+                const uint32_t key = pos < nv ? BlockMode::key(stg[pos], v, V) : 0u;
+                bacc = max(bacc, key);
+                if (((j + 1) & (g - 1u)) == 0u) {
+                    feed(bacc >= thr ? bacc : 0u);
+                    bacc = 0u;
+                }
+            } else {
+                const bool usable = pos < nv && !(v == V - 1 && (L & 7));
+                if (g == 1u) {
+                    if (pos < nv) {
+                        uint32_t ck[4];
+                        clean_at(stg, tile_v0, pos, ck);
 #pragma unroll
-            for (int j = 0; j < VPT; j += G) {
-                uint32_t r = 0;
-#pragma unroll
-                for (int i = 0; i < G; ++i) r = max(r, ek[j + i]);
-                f(r >= thr ? r : 0u);
-            }
-        } else if constexpr (G == 1) {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int pos = j * THREADS + static_cast<int>(threadIdx.x);
-                uint32_t ck[4] = {0u, 0u, 0u, 0u};
-                if (pos < nv) M::clean(raw[j], tile_v0 + pos, V, L, ck);
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    const uint32_t key = key_at<M>(ck, h);
-                    f(key >= thr ? key : 0u);
+                        for (int h = 0; h < 8; ++h) {
+                            const uint32_t key = key_at<M>(ck, h);
+                            feed(key >= thr ? key : 0u);
+                        }
+                    }
+                } else if (g == 4u) {
+                    if (usable) {
+                        const uint4 r = stg[pos];
+                        feed(rep_key(smax_halves(smax2(r.x, r.y)), thr));
+                        feed(rep_key(smax_halves(smax2(r.z, r.w)), thr));
+                    }
+                } else {
+                    if (usable) acc = smax2(acc, vec_smax(stg[pos]));
+                    if ((static_cast<uint32_t>(j) + 1u) % per == 0u) {
+                        feed(rep_key(smax_halves(acc), thr));
+                        acc = 0x80008000u;
+                    }
                 }
             }
-        } else if constexpr (G == 4) {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                f(rep_key(smax_halves(smax2(raw[j].x, raw[j].y)), thr));
-                f(rep_key(smax_halves(smax2(raw[j].z, raw[j].w)), thr));
-            }
-        } else {
-            constexpr int NV = G / 8;  // vectors per group
-#pragma unroll
-            for (int j = 0; j < VPT; j += NV) {
-                uint32_t m = vec_smax(raw[j]);
-#pragma unroll
-                for (int i = 1; i < NV; ++i) m = smax2(m, vec_smax(raw[j + i]));
-                f(rep_key(smax_halves(m), thr));
-            }
-        }
-    }
-
-    template <class F>
-    __device__ __forceinline__ void with_g(int g, F &&f) {
-        if constexpr (M::BLOCK) {
-            if (g == 4) f.template operator()<4>();
-            else f.template operator()<1>();
-        } else {
-            if (g == 64) f.template operator()<64>();
-            else if (g == 16) f.template operator()<16>();
-            else if (g == 4) f.template operator()<4>();
-            else f.template operator()<1>();
         }
     }
 
     // Keys > c of the tile (and >= thr) appended to the buffer at `first` on (any
-    // order; slot overflow past `room` is counted but not written); keys == c
-    // counted, their indices kept in s.tie_idx while they fit. Counts in s.v_ngt,
-    // s.v_neq and the largest survivor in s.v_smax after the closing
-    // __syncthreads (all three zero on entry).
-    __device__ void survivors(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
-                              int64_t tile_v0, int nv, uint32_t c, uint32_t first, uint32_t room) {
-        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
-        const uint32_t Q = build_queue(raw, ek, nv, max(c, thr));
+    // order; past `room` they are counted, not written), and counted into the
+    // window histogram s->hwin[0] over [c + 1, c + 256) whose top bin also
+    // holds every larger key; keys == c counted, their indices kept in
+    // s->tie_idx while they fit. Counts in s->v_ngt / v_neq, the largest
+    // survivor in s->v_smax, after the closing __syncthreads (zero on entry).
+    __device__ __noinline__ void survivors(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
+                                           uint32_t first, uint32_t room) {
+        const uint32_t lane = lane_id();
+        const uint32_t Q = build_queue(stg, tile_v0, nv, max(c, thr));
         for (uint32_t e0 = 0; e0 < Q; e0 += 32) {
-            uint32_t ck[4];
-            const int pos = queued_keys(stg, tile_v0, e0 + lane, Q, ck);
-            uint32_t ngt = 0, kmax = 0, eqmask = 0;
+            const uint32_t e = e0 + lane;
+            uint32_t ck[4] = {0u, 0u, 0u, 0u};
+            int pos = 0;
+            if (e < Q) {
+                pos = queued_pos(e);
+                clean_at(stg, tile_v0, pos, ck);
+            }
+            uint32_t ngt = 0, neq = 0, kmax = 0;
 #pragma unroll
             for (int h = 0; h < KPV; ++h) {
                 const uint32_t key = key_at<M>(ck, h);
                 const bool ok = key >= thr;
                 ngt += ok && key > c;
-                eqmask |= (ok && key == c) ? (1u << h) : 0u;
+                neq += ok && key == c;
                 kmax = (ok && key > c) ? max(kmax, key) : kmax;
             }
-            const uint32_t incl = warp_incl_scan(ngt);
-            uint32_t base = 0;
-            if (lane == 31 && incl) base = atomicAdd(&s.v_ngt, incl);
-            base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - ngt;
+            const uint32_t incl = warp_incl_scan(ngt | (neq << 16));
+            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t base = 0, ebase = 0;
+            if (lane == 31) {
+                if (tot & 0xFFFFu) base = atomicAdd(&s->v_ngt, tot & 0xFFFFu);
+                if (tot >> 16) ebase = atomicAdd(&s->v_neq, tot >> 16);
+            }
+            const uint32_t ex = incl - (ngt | (neq << 16));
+            base = __shfl_sync(0xFFFFFFFFu, base, 31) + (ex & 0xFFFFu);
+            ebase = __shfl_sync(0xFFFFFFFFu, ebase, 31) + (ex >> 16);
             const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0 && mx) atomicMax(&s.v_smax, mx);
-            if (ngt) {
+            if (lane == 0 && mx) atomicMax(&s->v_smax, mx);
+            if (ngt | neq) {
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
                     const uint32_t key = key_at<M>(ck, h);
-                    if (key >= thr && key > c) {
+                    if (key < thr) continue;
+                    if (key > c) {
+                        atomicAdd(&s->hwin[0][min(key - c - 1u, 255u)], 1u);
                         if (base < room) {
-                            s.buf_key[first + base] = static_cast<uint16_t>(key);
-                            s.buf_idx[first + base] = M::elem(tile_v0 + pos, h);
+                            s->buf_key[first + base] = static_cast<uint16_t>(key);
+                            s->buf_idx[first + base] = M::elem(tile_v0 + pos, h);
                         }
                         ++base;
-                    }
-                }
-            }
-            const uint32_t neq = __popc(eqmask);
-            const uint32_t any = __ballot_sync(0xFFFFFFFFu, neq != 0);
-            if (any) {
-                const uint32_t einc = warp_incl_scan(neq);
-                uint32_t ebase = 0;
-                if (lane == 31) ebase = atomicAdd(&s.v_neq, einc);
-                ebase = __shfl_sync(0xFFFFFFFFu, ebase, 31) + einc - neq;
-#pragma unroll
-                for (int h = 0; h < KPV; ++h) {
-                    if (eqmask & (1u << h)) {
-                        if (ebase < static_cast<uint32_t>(TIECAP)) s.tie_idx[ebase] = M::elem(tile_v0 + pos, h);
+                    } else if (key == c) {
+                        if (ebase < static_cast<uint32_t>(TIECAP)) s->tie_idx[ebase] = M::elem(tile_v0 + pos, h);
                         ++ebase;
                     }
                 }
-                (void)lt;
             }
         }
         __syncthreads();
     }
 
     // The `take` lowest-index keys equal to c in the tile, appended at
-    // first .. first + take in index order (tile order (j, thread, lane)), found
-    // with ordered scans of per-vector tie counts. For rows whose cutoff sits
-    // in a crowded bin.
-    __device__ void ordered_ties(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c, uint32_t take,
-                                 uint32_t first) {
+    // first .. first + take, found with ordered scans of per-vector tie counts
+    // (tile order is index order: vector j * THREADS + thread, then lane). For
+    // tiles whose cut sits in a crowded bin.
+    __device__ __noinline__ void ordered_ties(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
+                                              uint32_t take, uint32_t first) {
         uint32_t before = 0;
-        for (int j = 0; j < VPT; ++j) {
+        for (int j = 0; j < VPT && before < take; ++j) {
             const int pos = j * THREADS + static_cast<int>(threadIdx.x);
             uint32_t ck[4] = {0u, 0u, 0u, 0u};
-            if (pos < nv) M::clean(stg[pos], tile_v0 + pos, V, L, ck);
+            if (pos < nv) clean_at(stg, tile_v0, pos, ck);
             uint32_t eq = 0;
 #pragma unroll
-            for (int h = 0; h < KPV; ++h) eq += key_at<M>(ck, h) == c && c >= thr;
+            for (int h = 0; h < KPV; ++h) eq += key_at<M>(ck, h) == c;
             uint32_t total;
             const uint32_t incl = block_incl_scan(eq, total);
             uint32_t r = before + incl - eq;
 #pragma unroll
             for (int h = 0; h < KPV; ++h) {
-                if (key_at<M>(ck, h) == c && c >= thr) {
+                if (key_at<M>(ck, h) == c) {
                     if (r < take) {
-                        s.buf_key[first + r] = static_cast<uint16_t>(c);
-                        s.buf_idx[first + r] = M::elem(tile_v0 + pos, h);
+                        s->buf_key[first + r] = static_cast<uint16_t>(c);
+                        s->buf_idx[first + r] = M::elem(tile_v0 + pos, h);
                     }
                     ++r;
                 }
             }
             before += total;
-            if (before >= take) break;  // uniform
         }
     }
 
     // Exact top-k of the tile's keys >= thr into the buffer (see the file
     // comment). Raises thr when the tile held more than k candidates.
-    __device__ void tile_select(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
-                                int64_t tile_v0, int nv) {
+    __device__ __noinline__ void tile_select(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
-        const uint32_t first = s.v_count;
+        const uint32_t first = s->v_count;
         const uint32_t room = static_cast<uint32_t>(CAP) - first;
         const uint32_t nE = static_cast<uint32_t>(
             M::BLOCK ? nv : min(static_cast<int64_t>(nv) * 8, static_cast<int64_t>(L) - 8 * tile_v0));
         known_T = 0;
         if (nE > k) {
-            int g = 1;
-            if (!p.force_direct) {
-                while (g < M::GMAX && nE / static_cast<uint32_t>(4 * g) >= 2u * k) g *= 4;
-            }
+            uint32_t g = 1;
+            if (!p->force_direct)
+                while (g < static_cast<uint32_t>(M::GMAX) && nE / (4u * g) >= 2u * k) g *= 4u;
             for (;;) {
                 if (tid == 0) {
-                    s.v_ngt = 0u;
-                    s.v_neq = 0u;
-                    s.v_smax = 0u;
+                    s->v_ngt = 0u;
+                    s->v_neq = 0u;
+                    s->v_smax = 0u;
                 }
-                if (tid < 16) s.sub[tid] = 0u;
-                with_g(g, [&]<int G>() {
-                    for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
-                        if (key) atomicAdd(&s.hist[key >> 4], 1u);
-                    });
-                });
+                if (tid < 16) s->sub[tid] = 0u;
+                rep_pass(stg, tile_v0, nv, g, ALL);
                 __syncthreads();
                 const uint32_t NR = find_cut4096(k);
                 if (NR < k) {
-                    if (g > 1) {  // the representatives cannot bound the tile: exact path
-                        count_event(p, TOPK_CNT_TILE_UNBOUNDED);
-                        g = 1;
+                    if (g > 1u) {  // the representatives cannot bound the tile: exact path
+                        count_event(*p, TOPK_CNT_TILE_UNBOUNDED);
+                        g = 1u;
                         continue;
                     }
                     break;  // at most k candidates: take them all
                 }
-                const uint32_t bin = s.bc[0], above = s.bc[1], cnt = s.bc[2];
+                const uint32_t bin = s->bc[0], above = s->bc[1], cnt = s->bc[2];
                 uint32_t c;
-                if (g == 1 || cnt > SUB_EXACT) {
-                    with_g(g, [&]<int G>() {
-                        for_reps<G>(raw, ek, tile_v0, nv, [&](uint32_t key) {
-                            if (key && (key >> 4) == bin) atomicAdd(&s.sub[key & 15u], 1u);
-                        });
-                    });
+                if (g == 1u || cnt > SUB_EXACT) {
+                    rep_pass(stg, tile_v0, nv, g, bin);
                     __syncthreads();
                     uint32_t acc = above, sb = 0;
-                    bool done = false;
-#pragma unroll
                     for (int i = 15; i >= 0; --i) {
-                        const uint32_t v = s.sub[i];
-                        if (!done && acc + v >= k) {
+                        const uint32_t v = s->sub[i];
+                        if (acc + v >= k) {
                             sb = static_cast<uint32_t>(i);
-                            done = true;
+                            break;
                         }
                         acc += v;
                     }
@@ -931,42 +920,57 @@ struct Cta {
                 } else {
                     c = max(bin << 4, thr - 1u);  // a lower bound on the k-th representative
                 }
-                survivors(raw, ek, stg, tile_v0, nv, c, first, room);
-                const uint32_t ngt = s.v_ngt, neq = s.v_neq, smax = s.v_smax;
+                survivors(stg, tile_v0, nv, c, first, room);
+                const uint32_t ngt = s->v_ngt, neq = s->v_neq, smax = s->v_smax;
+                uint32_t T, take;
                 if (ngt > room) {
                     // Too many survivors to hold: every key becomes its own
                     // representative (then fewer than k keys exceed c).
-                    count_event(p, TOPK_CNT_TILE_OVERFLOW);
+                    count_event(*p, TOPK_CNT_TILE_OVERFLOW);
                     __syncthreads();
-                    if (g == 1) {  // cannot happen: record it rather than loop
+                    s->hwin[0][tid] = 0u;
+                    if (g == 1u) {  // cannot happen: record it rather than loop
                         if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
                         break;
                     }
-                    g = 1;
+                    g = 1u;
                     continue;
                 }
-                count_event(p, g == 1 ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
-                uint32_t T, take;
+                count_event(*p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
                 if (ngt >= k) {
-                    uint32_t a2;
-                    window_select(first, ngt, c + 1u, smax, k, T, a2);
-                    take = k - a2;
-                    if (tid == 0) s.v_count = first + ngt;
-                    if (tid == 0 && smax > s.v_bufmax) s.v_bufmax = smax;
+                    // The k-th survivor from the window histogram; a second look
+                    // only when it lies in the top bin (keys >= c + 256).
+                    uint32_t b1, above1, tot;
+                    find_bin256(s->hwin[0], k, b1, above1, tot);
+                    if (b1 < 255u) {
+                        T = c + 1u + b1;
+                        take = k - above1;
+                    } else {
+                        uint32_t a2;
+                        window_select(first, ngt, c + 1u, smax, k, &T, &a2);
+                        take = k - a2;
+                    }
+                    __syncthreads();
+                    s->hwin[0][tid] = 0u;
+                    if (tid == 0) {
+                        s->v_count = first + ngt;
+                        s->v_bufmax = max(s->v_bufmax, smax);
+                    }
                     buf_lo = min(buf_lo, c + 1u);
                 } else {
                     // The cut is c itself: the survivors and the take
                     // lowest-index ties at c.
                     T = c;
                     take = k - ngt;
+                    s->hwin[0][tid] = 0u;
                     if (neq <= static_cast<uint32_t>(TIECAP)) {
                         if (static_cast<uint32_t>(tid) < neq) {
-                            const uint32_t mine = s.tie_idx[tid];
+                            const uint32_t mine = s->tie_idx[tid];
                             uint32_t r = 0;
-                            for (uint32_t u = 0; u < neq; ++u) r += s.tie_idx[u] < mine;
+                            for (uint32_t u = 0; u < neq; ++u) r += s->tie_idx[u] < mine;
                             if (r < take) {
-                                s.buf_key[first + ngt + r] = static_cast<uint16_t>(c);
-                                s.buf_idx[first + ngt + r] = mine;
+                                s->buf_key[first + ngt + r] = static_cast<uint16_t>(c);
+                                s->buf_idx[first + ngt + r] = mine;
                             }
                         }
                     } else {
@@ -974,8 +978,8 @@ struct Cta {
                     }
                     __syncthreads();
                     if (tid == 0) {
-                        s.v_count = first + ngt + take;
-                        s.v_bufmax = max(s.v_bufmax, max(smax, c));
+                        s->v_count = first + ngt + take;
+                        s->v_bufmax = max(s->v_bufmax, max(smax, c));
                     }
                     buf_lo = min(buf_lo, c);
                 }
@@ -990,101 +994,145 @@ struct Cta {
             }
         }
         // At most k candidates: all of them.
-        count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-        const uint32_t Q = build_queue(raw, ek, nv, thr);
+        count_event(*p, TOPK_CNT_TILE_TAKE_ALL);
+        const uint32_t Q = build_queue(stg, tile_v0, nv, thr);
         append_keys(stg, tile_v0, Q, 0, thr);
         buf_lo = min(buf_lo, thr);
         __syncthreads();
     }
 
-    // Keep (compact = true) or write out (compact = false) the buffer entries
-    // [0, n) that are selected: key > T, or key == T with index <= cut. Kept
-    // entries go to the front of the buffer; written ones to out[row, offset +
-    // slot]. Returns how many were selected.
-    __device__ uint32_t select_entries(uint32_t n, uint32_t T, uint32_t cut, bool compact,
-                                       uint32_t offset) {
+    // Keep the buffer entries [0, n) that are selected (key > T, or key == T
+    // with index <= cut) at the front of the buffer, in any order. Returns how
+    // many were kept.
+    __device__ __noinline__ uint32_t keep_selected(uint32_t n, uint32_t T, uint32_t cut) {
         const int tid = threadIdx.x;
-        const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
+        const uint32_t lt = (1u << lane_id()) - 1u;
         constexpr int PER = 8;
         __syncthreads();
-        if (tid == 0) s.v_emit = 0u;
+        if (tid == 0) s->v_emit = 0u;
         __syncthreads();
-        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
         for (uint32_t base = 0; base < n; base += THREADS * PER) {
             uint32_t key[PER], idx[PER];
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
                 const uint32_t i = base + static_cast<uint32_t>(e) * THREADS + tid;
-                key[e] = i < n ? s.buf_key[i] : 0u;
-                idx[e] = i < n ? s.buf_idx[i] : 0u;
+                key[e] = i < n ? s->buf_key[i] : 0u;
+                idx[e] = i < n ? s->buf_idx[i] : 0u;
             }
-            if (compact) __syncthreads();  // this chunk is read before it is overwritten
+            __syncthreads();  // this chunk is read before it is overwritten
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
                 const bool sel = key[e] != 0u && (key[e] > T || (key[e] == T && idx[e] <= cut));
                 const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
-                const uint32_t slot = warp_reserve(&s.v_emit, __popc(b)) + __popc(b & lt);
+                const uint32_t at = warp_reserve(&s->v_emit, __popc(b)) + __popc(b & lt);
                 if (sel) {
-                    if (compact) {
-                        s.buf_key[slot] = static_cast<uint16_t>(key[e]);
-                        s.buf_idx[slot] = idx[e];
-                    } else {
-                        orow[offset + slot] = transform(p, row, static_cast<int32_t>(idx[e]));
-                    }
+                    s->buf_key[at] = static_cast<uint16_t>(key[e]);
+                    s->buf_idx[at] = idx[e];
                 }
             }
         }
         __syncthreads();
-        return s.v_emit;
+        return s->v_emit;
+    }
+
+    // Write the selected buffer entries [0, n) to out[row, offset + slot]: every
+    // key > T, and the `take` lowest-index keys == T (ties beyond TIECAP go
+    // through the index radix). Returns the number written.
+    __device__ __noinline__ uint32_t emit_selected(uint32_t n, uint32_t T, uint32_t take, uint32_t offset) {
+        const int tid = threadIdx.x;
+        const uint32_t lt = (1u << lane_id()) - 1u;
+        int32_t *orow = p->out + static_cast<int64_t>(row) * k + offset;
+        __syncthreads();
+        if (tid == 0) {
+            s->v_emit = 0u;
+            s->v_ntie = 0u;
+        }
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
+            const uint32_t i = i0 + tid;
+            const uint32_t key = i < n ? s->buf_key[i] : 0u;
+            const bool gt = key > T, tie = take && key == T;
+            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
+            const uint32_t ag = warp_reserve(&s->v_emit, __popc(bg)) + __popc(bg & lt);
+            const uint32_t at = warp_reserve(&s->v_ntie, __popc(bt)) + __popc(bt & lt);
+            if (gt) orow[ag] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
+            if (tie && at < static_cast<uint32_t>(TIECAP)) s->tie_idx[at] = s->buf_idx[i];
+        }
+        __syncthreads();
+        const uint32_t ngt = s->v_emit, e = s->v_ntie;
+        if (take == 0u) return ngt;
+        if (e <= static_cast<uint32_t>(TIECAP)) {
+            if (static_cast<uint32_t>(tid) < e) {
+                const uint32_t mine = s->tie_idx[tid];
+                uint32_t r = 0;
+                if (take < e)
+                    for (uint32_t u = 0; u < e; ++u) r += s->tie_idx[u] < mine;
+                else
+                    r = static_cast<uint32_t>(tid);
+                if (r < take) orow[ngt + r] = transform(*p, row, static_cast<int32_t>(mine));
+            }
+            return ngt + min(take, e);
+        }
+        // Many ties: cut by index, then write the ties at or below the cut.
+        const uint32_t cut = take >= e ? ALL : tie_radix(n, T, take);
+        if (tid == 0) s->v_ntie = 0u;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
+            const uint32_t i = i0 + tid;
+            const bool sel = i < n && s->buf_key[i] == T && s->buf_idx[i] <= cut;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
+            const uint32_t at = warp_reserve(&s->v_ntie, __popc(b)) + __popc(b & lt);
+            if (sel) orow[ngt + at] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
+        }
+        return ngt + min(take, e);
     }
 
     // Reduce the buffer to its exact top-k. strict: every buffered key precedes
     // every key still to come, so later keys equal to the cut are dropped too.
-    __device__ void compact(bool strict) {
+    __device__ __noinline__ void compact(bool strict) {
         const int tid = threadIdx.x;
         __syncthreads();
-        const uint32_t n = s.v_count;
+        const uint32_t n = s->v_count;
         if (n <= k) return;
-        count_event(p, TOPK_CNT_COMPACTIONS);
+        count_event(*p, TOPK_CNT_COMPACTIONS);
         PhaseClock clk;
-        clk.start(p);
+        clk.start(*p);
         uint32_t T, above;
-        window_select(0, n, buf_lo, max(s.v_bufmax, buf_lo), k, T, above);
+        window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
         const uint32_t take = k - above;
         const uint32_t cut = tie_cut(n, T, take);
-        const uint32_t kept = select_entries(n, T, cut, true, 0);
-        if (tid == 0) s.v_count = kept;
+        const uint32_t kept = keep_selected(n, T, cut);
+        if (tid == 0) s->v_count = kept;
         buf_lo = T;
         known_T = 0;
         thr = max(thr, strict ? T + 1u : T);
         publish(T);
         __syncthreads();
-        clk.stop(p, TOPK_CNT_CYC_COMPACT);
+        clk.stop(*p, TOPK_CNT_CYC_COMPACT);
     }
 
     // A later tile: append every key >= the threshold.
-    __device__ void filter_tile(const uint4 (&raw)[VPT], const uint32_t (&ek)[VPT], const uint4 *stg,
-                                int64_t tile_v0, int nv) {
+    __device__ __noinline__ void filter_tile(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
         known_T = 0;
-        if (s.v_count > static_cast<uint32_t>(CAP / 2) && s.v_count > 2u * k) compact(true);
+        if (s->v_count > static_cast<uint32_t>(CAP / 2) && s->v_count > 2u * k) compact(true);
         uint32_t lim = effective_thr();
-        const uint32_t Q = build_queue(raw, ek, nv, lim);
+        const uint32_t Q = build_queue(stg, tile_v0, nv, lim);
         uint32_t next = append_keys(stg, tile_v0, Q, 0, lim);
         buf_lo = min(buf_lo, lim);
         for (int refill = 0;; ++refill) {
-            if (tid == 0) s.v_flag = 0u;
+            if (tid == 0) s->v_flag = 0u;
             __syncthreads();
-            if (next < Q && lane_id() == 0) s.v_flag = 1u;
+            if (next < Q && lane_id() == 0) s->v_flag = 1u;
             __syncthreads();
-            if (s.v_flag == 0u) break;  // uniform
+            if (s->v_flag == 0u) break;  // uniform
             if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
                 if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
                 break;
             }
             // The buffer filled up mid-tile: compact it (the rest of this tile
             // may still tie with it) and carry on.
-            count_event(p, TOPK_CNT_REFILLS);
+            count_event(*p, TOPK_CNT_REFILLS);
             compact(false);
             lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
             next = append_keys(stg, tile_v0, Q, next, lim);
@@ -1092,135 +1140,131 @@ struct Cta {
     }
 
     // C == 1: the buffer holds the row's candidates; write its top-k.
-    __device__ void emit_single() {
+    __device__ __noinline__ void emit_single() {
         __syncthreads();
-        const uint32_t n = s.v_count;
-        uint32_t T = 0, cut = ALL;
+        const uint32_t n = s->v_count;
+        uint32_t T = 0, take = 0;
         if (n > k) {
-            uint32_t take;
             if (known_T) {
                 T = known_T;
                 take = last_take;
             } else {
                 uint32_t above;
-                window_select(0, n, buf_lo, max(s.v_bufmax, buf_lo), k, T, above);
+                window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
                 take = k - above;
             }
-            cut = tie_cut(n, T, take);
         }
-        const uint32_t written = select_entries(n, T, cut, false, 0);
-        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        const uint32_t written = emit_selected(n, T, take, 0);
+        int32_t *orow = p->out + static_cast<int64_t>(row) * k;
         for (uint32_t i = written + threadIdx.x; i < k; i += THREADS) orow[i] = -1;
     }
 
     // Cluster merge: the C buffers (each its CTA's top-k) give the row's k-th
     // key; ties at it go to the lowest indices, lower-ranked CTAs first.
-    __device__ void merge_and_emit() {
+    __device__ __noinline__ void merge_and_emit() {
         const int tid = threadIdx.x;
-        count_event(p, TOPK_CNT_CLUSTER_MERGES);
+        count_event(*p, TOPK_CNT_CLUSTER_MERGES);
         compact(false);
         __syncthreads();
-        const uint32_t n = s.v_count;
-        const uint32_t my_max = n ? s.v_bufmax : 0u;
+        const uint32_t n = s->v_count;
+        const uint32_t my_max = n ? s->v_bufmax : 0u;
         if (tid == 0) {
-            atomicMax(&s.shared_thr[slot], best_T);
-            atomicMax(&s.shared_max[slot], my_max);
+            atomicMax(&s->shared_thr[slot], best_T);
+            atomicMax(&s->shared_max[slot], my_max);
         }
         if (tid < static_cast<int>(C) && tid != static_cast<int>(rank)) {
-            red_max_peer(peer_addr(&s.shared_thr[slot], tid), best_T);
-            red_max_peer(peer_addr(&s.shared_max[slot], tid), my_max);
+            red_max_peer(peer_addr(&s->shared_thr[slot], tid), best_T);
+            red_max_peer(peer_addr(&s->shared_max[slot], tid), my_max);
         }
         cluster_arrive();
         cluster_wait();
         // Every publication for this row came before the barrier: all threads
         // read the same words.
-        const uint32_t LB = max(volatile_load(&s.shared_thr[slot]), 1u);
-        const uint32_t HI = volatile_load(&s.shared_max[slot]);
+        const uint32_t LB = max(volatile_load(&s->shared_thr[slot]), 1u);
+        const uint32_t HI = volatile_load(&s->shared_max[slot]);
         const uint32_t range = HI > LB ? HI - LB : 0u;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         for (uint32_t i = tid; i < n; i += THREADS) {
-            const uint32_t key = s.buf_key[i];
-            if (key >= LB && HI >= LB) atomicAdd(&s.h_merge[0][window_bin(key, LB, shift)], 1u);
+            const uint32_t key = s->buf_key[i];
+            if (key >= LB && HI >= LB) atomicAdd(&s->h_merge[0][window_bin(key, LB, shift)], 1u);
         }
         cluster_arrive();
         cluster_wait();
         {
             uint32_t all = 0, pre = 0;
             for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t x = ld_peer(peer_addr(&s.h_merge[0][tid], r));
+                const uint32_t x = ld_peer(peer_addr(&s->h_merge[0][tid], r));
                 all += x;
                 pre += r < rank ? x : 0u;
             }
-            s.m_all[tid] = all;
-            s.m_pre[0][tid] = pre;
+            s->m_all[tid] = all;
+            s->m_pre[0][tid] = pre;
         }
         __syncthreads();
         uint32_t b1, above1, total;
-        const bool enough = find_bin256(s.m_all, k, b1, above1, total);
+        const bool enough = find_bin256(s->m_all, k, b1, above1, total);
         uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0, b2 = 0;
         const uint32_t lane = lane_id();
         if (!enough) {
-            // Fewer than k candidates in the row: all of them (all are >= LB).
+            // Fewer than k candidates in the row: all of them.
             uint32_t x = 0;
-            for (uint32_t b = lane; b < 256u; b += 32u) x += s.m_pre[0][b];
+            for (uint32_t b = lane; b < 256u; b += 32u) x += s->m_pre[0][b];
             gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
         } else if (shift == 0) {
             T = LB + b1;
             take = k - above1;
             uint32_t x = 0;
-            for (uint32_t b = lane; b < 256u; b += 32u) x += b > b1 ? s.m_pre[0][b] : 0u;
+            for (uint32_t b = lane; b < 256u; b += 32u) x += b > b1 ? s->m_pre[0][b] : 0u;
             gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
-            eq_prev = s.m_pre[0][b1];
+            eq_prev = s->m_pre[0][b1];
         } else {
             const uint32_t mask = (1u << shift) - 1u;
             for (uint32_t i = tid; i < n; i += THREADS) {
-                const uint32_t key = s.buf_key[i];
-                if (key >= LB && ((key - LB) >> shift) == b1) atomicAdd(&s.h_merge[1][(key - LB) & mask], 1u);
+                const uint32_t key = s->buf_key[i];
+                if (key >= LB && ((key - LB) >> shift) == b1) atomicAdd(&s->h_merge[1][(key - LB) & mask], 1u);
             }
             cluster_arrive();
             cluster_wait();
             uint32_t all = 0, pre = 0;
             for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t x = ld_peer(peer_addr(&s.h_merge[1][tid], r));
+                const uint32_t x = ld_peer(peer_addr(&s->h_merge[1][tid], r));
                 all += x;
                 pre += r < rank ? x : 0u;
             }
-            s.m_all[tid] = all;
-            s.m_pre[1][tid] = pre;
+            s->m_all[tid] = all;
+            s->m_pre[1][tid] = pre;
             __syncthreads();
             uint32_t above2, tot2;
-            find_bin256(s.m_all, k - above1, b2, above2, tot2);
+            find_bin256(s->m_all, k - above1, b2, above2, tot2);
             T = LB + (b1 << shift) + b2;
             take = k - above1 - above2;
             uint32_t x = 0;
             for (uint32_t b = lane; b < 256u; b += 32u)
-                x += (b > b1 ? s.m_pre[0][b] : 0u) + (b > b2 ? s.m_pre[1][b] : 0u);
+                x += (b > b1 ? s->m_pre[0][b] : 0u) + (b > b2 ? s->m_pre[1][b] : 0u);
             gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
-            eq_prev = s.m_pre[1][b2];
+            eq_prev = s->m_pre[1][b2];
         }
         cluster_arrive();  // done reading the peers' shared memory
-        // This CTA's selected: keys > T, and its quota of the lowest-index ties.
+        // This CTA's part: keys > T, and its quota of the lowest-index ties.
         const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
         const uint32_t offset = gt_prev + min(eq_prev, take);
         if (!enough) {
-            select_entries(n, LB, ALL, false, offset);        // every key >= LB
-        } else if (quota == 0) {
-            select_entries(n, T + 1u, ALL, false, offset);    // keys > T
+            emit_selected(n, LB - 1u, 0u, offset);  // every key >= LB
         } else {
-            select_entries(n, T, tie_cut(n, T, quota), false, offset);
+            emit_selected(n, T, quota, offset);
         }
         const uint32_t selected_total = enough ? k : total;
-        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        int32_t *orow = p->out + static_cast<int64_t>(row) * k;
         for (uint32_t i = selected_total + rank + static_cast<uint32_t>(tid) * C; i < k; i += THREADS * C)
             orow[i] = -1;
         cluster_wait();
         // Every peer is done with this row's shared words: reset them for the
         // row after next (the next row uses the other parity).
-        s.h_merge[0][tid] = 0u;
-        s.h_merge[1][tid] = 0u;
+        s->h_merge[0][tid] = 0u;
+        s->h_merge[1][tid] = 0u;
         if (tid == 0) {
-            s.shared_thr[slot] = 0u;
-            s.shared_max[slot] = 0u;
+            s->shared_thr[slot] = 0u;
+            s->shared_max[slot] = 0u;
         }
     }
 };
@@ -1294,7 +1338,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         s.abort_flag = 0u;
     }
     for (int i = tid; i < HBINS; i += THREADS) s.hist[i] = 0u;
-    s.hwin[0][tid] = s.hwin[1][tid] = 0u;
+    for (int i = 0; i < 4; ++i) s.hwin[i][tid] = 0u;
     s.h_merge[0][tid] = s.h_merge[1][tid] = 0u;
     __syncthreads();
     Feed feed;
@@ -1309,7 +1353,10 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cluster_wait();
     }
 
-    Cta<M, NSTAGE, CAP> cta(s, p);
+    const Params prm = p;
+    Cta<M, NSTAGE, CAP> cta;
+    cta.s = &s;
+    cta.p = &prm;
     cta.C = C;
     cta.rank = rank;
     cta.k = static_cast<uint32_t>(p.k);
@@ -1353,32 +1400,12 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             count_event(p, TOPK_CNT_ROUNDS);
             clk.start(p);
             const uint4 *stg = s.stage[st];
-            uint4 raw[VPT];
-            uint32_t ek[VPT];
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int pos = j * THREADS + tid;
-                const int64_t v = tile_v0 + pos;
-                raw[j] = pos < nv ? stg[pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
-                if (!M::BLOCK && pos < nv && v == V - 1 && (L & 7)) {
-                    // Lanes past the valid length carry no element.
-                    uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-                    const int lanes = L & 7;
-#pragma unroll
-                    for (int h = 0; h < 8; ++h)
-                        if (h >= lanes)
-                            w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
-                                        ((h & 1) ? 0x80000000u : 0x00008000u);
-                    raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                ek[j] = (M::BLOCK && pos < nv) ? BlockMode::key(raw[j], v, V) : 0u;
-            }
             if (i == 0) {
                 cta.thr = max(cta.thr, cta.effective_thr());
-                cta.tile_select(raw, ek, stg, tile_v0, nv);
+                cta.tile_select(stg, tile_v0, nv);
                 clk.stop(p, TOPK_CNT_CYC_SELECT);
             } else {
-                cta.filter_tile(raw, ek, stg, tile_v0, nv);
+                cta.filter_tile(stg, tile_v0, nv);
                 clk.stop(p, TOPK_CNT_CYC_FILTER);
             }
             cta.snapshot_shared();

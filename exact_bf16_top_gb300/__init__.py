@@ -25,10 +25,11 @@ TOKEN = 0
 BLOCK8 = 1
 MAX_K = 2048
 MAX_WIDTH = 1 << 20
-NUM_COUNTERS = 16
+NUM_COUNTERS = 32
 COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", "tile_overflow",
                  "tile_take_all", "compactions", "refills", "cluster_merges", "rounds",
-                 "cyc_wait", "cyc_select", "cyc_filter", "cyc_finish", "cyc_compact")
+                 "cyc_wait", "cyc_select", "cyc_filter", "cyc_finish", "cyc_compact",
+                 "cyc_reps", "cyc_cut", "cyc_survivors", "cyc_exact")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
            5: "CUDA error"}

@@ -891,8 +891,12 @@ struct Cta {
                     s->v_smax = 0u;
                 }
                 if (tid < 16) s->sub[tid] = 0u;
+                PhaseClock clk;
+                clk.start(*p);
                 rep_pass(stg, tile_v0, nv, g, ALL);
                 __syncthreads();
+                clk.stop(*p, TOPK_CNT_CYC_REPS);
+                clk.start(*p);
                 const uint32_t NR = find_cut4096(k);
                 if (NR < k) {
                     if (g > 1u) {  // the representatives cannot bound the tile: exact path
@@ -920,7 +924,11 @@ struct Cta {
                 } else {
                     c = max(bin << 4, thr - 1u);  // a lower bound on the k-th representative
                 }
+                clk.stop(*p, TOPK_CNT_CYC_CUT);
+                clk.start(*p);
                 survivors(stg, tile_v0, nv, c, first, room);
+                clk.stop(*p, TOPK_CNT_CYC_SURVIVORS);
+                clk.start(*p);
                 const uint32_t ngt = s->v_ngt, neq = s->v_neq, smax = s->v_smax;
                 uint32_t T, take;
                 if (ngt > room) {
@@ -983,6 +991,7 @@ struct Cta {
                     }
                     buf_lo = min(buf_lo, c);
                 }
+                clk.stop(*p, TOPK_CNT_CYC_EXACT);
                 known_T = first == 0 ? T : 0u;
                 last_take = take;
                 // The buffer holds the tile's top-k, all >= T, ahead of any

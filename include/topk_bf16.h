@@ -99,7 +99,7 @@ typedef struct {
                                tile takes the exact whole-tile radix path (the fallback) */
     int32_t cluster;        /* 0: automatic; else CTAs per row: 1, 2, 4, 8 or 16 */
     uint32_t *counters;     /* NULL, or device uint32 [TOPK_NUM_COUNTERS] that each
-                               launch adds its path counts to */
+                               launch adds its path counts and cycle split to */
 } topk_bf16_options_t;
 
 /* Indices into topk_bf16_options_t.counters. */
@@ -121,7 +121,11 @@ enum {
     TOPK_CNT_CYC_FILTER = 12,    /* later tiles (compactions included) */
     TOPK_CNT_CYC_FINISH = 13,    /* the row's final select, merge and write */
     TOPK_CNT_CYC_COMPACT = 14,   /* buffer compactions */
-    TOPK_NUM_COUNTERS = 16
+    TOPK_CNT_CYC_REPS = 15,      /* first-tile select, split: representatives histogram */
+    TOPK_CNT_CYC_CUT = 16,       /*   the representatives' cut */
+    TOPK_CNT_CYC_SURVIVORS = 17, /*   the survivor pass */
+    TOPK_CNT_CYC_EXACT = 18,     /*   the exact cut among survivors and the tie appends */
+    TOPK_NUM_COUNTERS = 32
 };
 
 /* topk_bf16_select with options (NULL = defaults). Same arguments and errors,

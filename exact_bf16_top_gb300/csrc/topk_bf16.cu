@@ -423,9 +423,9 @@ __device__ __forceinline__ uint32_t warp_reserve(uint32_t *ctr, uint32_t n) {
 
 // --------------------------------------------------------- the CTA's machinery
 //
-// The per-row state is uniform across the CTA. The larger routines are kept out
-// of line: a row's selection walks many phases once each, and inlining them all
-// made the code far larger than the SM's instruction cache.
+// The per-row state is uniform across the CTA and lives in registers; every
+// routine is inlined so that the compiler sees shared-memory accesses as such
+// (out of line, they would go through generic addresses).
 
 template <class M, int NSTAGE, int CAP>
 struct Cta {
@@ -496,7 +496,7 @@ struct Cta {
 
     // The 12-bit bin of s->hist holding the q-th largest key: s->bc = {bin,
     // above, count(bin)}; returns the histogram total. Zeroes s->hist.
-    __device__ __noinline__ uint32_t find_cut4096(uint32_t q) {
+    __device__ __forceinline__ uint32_t find_cut4096(uint32_t q) {
         const int t = threadIdx.x;
         const int base = HBINS - 16 * (t + 1);  // thread 0 owns the highest 16 bins
         uint4 *h4 = reinterpret_cast<uint4 *>(s->hist + base);
@@ -535,7 +535,7 @@ struct Cta {
     // (q <= n): radix select over bins relative to lo, one pass when hi - lo <
     // 256, else two. T = that key, above = keys greater than it. Uses
     // s->hwin[2] and s->hwin[3] (zero on entry and on exit).
-    __device__ __noinline__ void window_select(uint32_t first, uint32_t n, uint32_t lo, uint32_t hi,
+    __device__ __forceinline__ void window_select(uint32_t first, uint32_t n, uint32_t lo, uint32_t hi,
                                                uint32_t q, uint32_t *T_out, uint32_t *above_out) {
         const int tid = threadIdx.x;
         const uint32_t range = hi - lo;
@@ -570,7 +570,7 @@ struct Cta {
     // The q-th smallest index among buffer entries [0, n) whose key is T, when
     // there are more than TIECAP of them: a two-pass radix select over 10-bit
     // digits (indices are below 2^20), in s->hist (zero on entry and exit).
-    __device__ __noinline__ uint32_t tie_radix(uint32_t n, uint32_t T, uint32_t q) {
+    __device__ __forceinline__ uint32_t tie_radix(uint32_t n, uint32_t T, uint32_t q) {
         const int tid = threadIdx.x;
         uint32_t cut = 0, need = q;
         for (int pass = 0; pass < 2; ++pass) {
@@ -611,7 +611,7 @@ struct Cta {
 
     // Among buffer entries [0, n) with key T (distinct indices), the cut with
     // exactly q of them at or below it; ALL when q covers them all.
-    __device__ __noinline__ uint32_t tie_cut(uint32_t n, uint32_t T, uint32_t q) {
+    __device__ __forceinline__ uint32_t tie_cut(uint32_t n, uint32_t T, uint32_t q) {
         const int tid = threadIdx.x;
         const uint32_t lt = (1u << lane_id()) - 1u;
         __syncthreads();
@@ -640,7 +640,7 @@ struct Cta {
 
     // Queue, per warp and in index order, the tile's vectors that may hold a
     // key >= lim. Returns the queue length.
-    __device__ __noinline__ uint32_t build_queue(const uint4 *stg, int64_t tile_v0, int nv, uint32_t lim) {
+    __device__ __forceinline__ uint32_t build_queue(const uint4 *stg, int64_t tile_v0, int nv, uint32_t lim) {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
         uint32_t q = 0;
@@ -668,7 +668,7 @@ struct Cta {
     // Append every key >= lim of this warp's queued vectors, from queue entry
     // `from` on, to the buffer (any order). Slots are reserved a warp at a time
     // and only while they fit. Returns the first entry not appended (Q: all).
-    __device__ __noinline__ uint32_t append_keys(const uint4 *stg, int64_t tile_v0, uint32_t Q,
+    __device__ __forceinline__ uint32_t append_keys(const uint4 *stg, int64_t tile_v0, uint32_t Q,
                                                  uint32_t from, uint32_t lim) {
         const uint32_t lane = lane_id();
         for (uint32_t e0 = from; e0 < Q; e0 += 32) {
@@ -729,7 +729,7 @@ struct Cta {
     // ALL) or to the 16 sub-bins of one 12-bit bin. A representative is one
     // element of a group of g logits (token) or g blocks (block), with key >=
     // thr, or nothing; g = 1 feeds every candidate key.
-    __device__ __noinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t bin) {
+    __device__ __forceinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t bin) {
         uint32_t *hist = s->hist;
         uint32_t *sub = s->sub;
         auto feed = [&](uint32_t key) {
@@ -785,7 +785,7 @@ struct Cta {
     // holds every larger key; keys == c counted, their indices kept in
     // s->tie_idx while they fit. Counts in s->v_ngt / v_neq, the largest
     // survivor in s->v_smax, after the closing __syncthreads (zero on entry).
-    __device__ __noinline__ void survivors(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
+    __device__ __forceinline__ void survivors(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
                                            uint32_t first, uint32_t room) {
         const uint32_t lane = lane_id();
         const uint32_t Q = build_queue(stg, tile_v0, nv, max(c, thr));
@@ -844,7 +844,7 @@ struct Cta {
     // first .. first + take, found with ordered scans of per-vector tie counts
     // (tile order is index order: vector j * THREADS + thread, then lane). For
     // tiles whose cut sits in a crowded bin.
-    __device__ __noinline__ void ordered_ties(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
+    __device__ __forceinline__ void ordered_ties(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
                                               uint32_t take, uint32_t first) {
         uint32_t before = 0;
         for (int j = 0; j < VPT && before < take; ++j) {
@@ -873,7 +873,7 @@ struct Cta {
 
     // Exact top-k of the tile's keys >= thr into the buffer (see the file
     // comment). Raises thr when the tile held more than k candidates.
-    __device__ __noinline__ void tile_select(const uint4 *stg, int64_t tile_v0, int nv) {
+    __device__ __forceinline__ void tile_select(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
         const uint32_t first = s->v_count;
         const uint32_t room = static_cast<uint32_t>(CAP) - first;
@@ -1013,7 +1013,7 @@ struct Cta {
     // Keep the buffer entries [0, n) that are selected (key > T, or key == T
     // with index <= cut) at the front of the buffer, in any order. Returns how
     // many were kept.
-    __device__ __noinline__ uint32_t keep_selected(uint32_t n, uint32_t T, uint32_t cut) {
+    __device__ __forceinline__ uint32_t keep_selected(uint32_t n, uint32_t T, uint32_t cut) {
         const int tid = threadIdx.x;
         const uint32_t lt = (1u << lane_id()) - 1u;
         constexpr int PER = 8;
@@ -1047,7 +1047,7 @@ struct Cta {
     // Write the selected buffer entries [0, n) to out[row, offset + slot]: every
     // key > T, and the `take` lowest-index keys == T (ties beyond TIECAP go
     // through the index radix). Returns the number written.
-    __device__ __noinline__ uint32_t emit_selected(uint32_t n, uint32_t T, uint32_t take, uint32_t offset) {
+    __device__ __forceinline__ uint32_t emit_selected(uint32_t n, uint32_t T, uint32_t take, uint32_t offset) {
         const int tid = threadIdx.x;
         const uint32_t lt = (1u << lane_id()) - 1u;
         int32_t *orow = p->out + static_cast<int64_t>(row) * k + offset;
@@ -1098,7 +1098,7 @@ struct Cta {
 
     // Reduce the buffer to its exact top-k. strict: every buffered key precedes
     // every key still to come, so later keys equal to the cut are dropped too.
-    __device__ __noinline__ void compact(bool strict) {
+    __device__ __forceinline__ void compact(bool strict) {
         const int tid = threadIdx.x;
         __syncthreads();
         const uint32_t n = s->v_count;
@@ -1121,7 +1121,7 @@ struct Cta {
     }
 
     // A later tile: append every key >= the threshold.
-    __device__ __noinline__ void filter_tile(const uint4 *stg, int64_t tile_v0, int nv) {
+    __device__ __forceinline__ void filter_tile(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
         known_T = 0;
         if (s->v_count > static_cast<uint32_t>(CAP / 2) && s->v_count > 2u * k) compact(true);
@@ -1149,7 +1149,7 @@ struct Cta {
     }
 
     // C == 1: the buffer holds the row's candidates; write its top-k.
-    __device__ __noinline__ void emit_single() {
+    __device__ __forceinline__ void emit_single() {
         __syncthreads();
         const uint32_t n = s->v_count;
         uint32_t T = 0, take = 0;
@@ -1170,7 +1170,7 @@ struct Cta {
 
     // Cluster merge: the C buffers (each its CTA's top-k) give the row's k-th
     // key; ties at it go to the lowest indices, lower-ranked CTAs first.
-    __device__ __noinline__ void merge_and_emit() {
+    __device__ __forceinline__ void merge_and_emit() {
         const int tid = threadIdx.x;
         count_event(*p, TOPK_CNT_CLUSTER_MERGES);
         compact(false);

@@ -1436,6 +1436,581 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     }
 }
 
+// ------------------------------------------------------- one-tile rows kernel
+//
+// Rows whose valid prefix fits one tile (at most 2048 vectors) take a leaner
+// path: 512 threads hold the row in registers (4 vectors each), the stage it
+// came through is handed back to the copy ring at once, and the selection runs
+// in a handful of barrier phases: representatives -> cut -> survivors -> exact
+// cut -> write. Same cutoff argument as the streamed kernel.
+namespace one {
+
+constexpr int NT = 512;
+constexpr int NW = NT / 32;
+constexpr int NV = 4;                        // vectors per thread
+constexpr int NTILE = NT * NV;               // 2048 vectors
+constexpr int NSTAGE = 2;
+constexpr int SURV_CAP = 4096;
+
+struct alignas(128) Smem {
+    uint4 stage[NSTAGE][NTILE];
+    uint32_t surv_idx[SURV_CAP];
+    uint16_t surv_key[SURV_CAP];
+    uint32_t hist[HBINS];                    // 12-bit histogram (zero between uses)
+    uint32_t hwin[2][256];                   // window histograms (zero between uses)
+    uint32_t tie_idx[TIECAP];
+    uint32_t sub[16];
+    uint32_t red[2][NW];
+    uint32_t bc[4];
+    uint32_t v_ngt, v_neq, v_smax, v_emit, v_ntie;
+    uint32_t abort_flag;
+    unsigned long long full[NSTAGE];
+};
+
+// Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
+// warp (crowded bins would otherwise serialise the atomics of the whole warp).
+__device__ __forceinline__ void agg_add(uint32_t *hist, uint32_t bin, bool valid) {
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
+    if (valid && lane_id() == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+}
+
+__device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    const uint32_t inc = warp_incl_scan(x);
+    if (lane == 31) s.red[par][warp] = inc;
+    __syncthreads();
+    const uint32_t w = lane < NW ? s.red[par][lane] : 0u;
+    const uint32_t wi = warp_incl_scan(w);
+    total = __shfl_sync(0xFFFFFFFFu, wi, 31);
+    const uint32_t pre = __shfl_sync(0xFFFFFFFFu, wi - w, warp);
+    par ^= 1u;
+    return pre + inc;
+}
+
+// Warp-aggregated slot for this lane's `n` items (one atomic per warp).
+__device__ __forceinline__ uint32_t warp_slots(uint32_t *ctr, uint32_t n) {
+    const uint32_t incl = warp_incl_scan(n);
+    uint32_t base = 0;
+    if (lane_id() == 31 && incl) base = atomicAdd(ctr, incl);
+    return __shfl_sync(0xFFFFFFFFu, base, 31) + incl - n;
+}
+
+template <class M>
+struct Row {
+    Smem &s;
+    const Params &p;
+    uint32_t par = 0;
+    int32_t row = 0, L = 0;
+    int64_t V = 0;
+    uint32_t k = 0;
+    uint4 raw[NV];     // the row, this thread's vectors j * NT + threadIdx.x
+    uint32_t ek[NV];   // block mode: the vectors' element keys
+
+    __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
+
+    __device__ __forceinline__ int pos_of(int j) const { return j * NT + static_cast<int>(threadIdx.x); }
+
+    __device__ __forceinline__ void clean(int j, uint32_t (&ck)[4]) const {
+        if (pos_of(j) < V) M::clean(raw[j], pos_of(j), V, L, ck);
+        else ck[0] = ck[1] = ck[2] = ck[3] = 0u;
+    }
+
+    __device__ __forceinline__ int32_t *orow() const { return p.out + static_cast<int64_t>(row) * k; }
+
+    __device__ __forceinline__ void put(uint32_t slot, uint32_t idx) const {
+        orow()[slot] = transform(p, row, static_cast<int32_t>(idx));
+    }
+
+    // Representatives of groups of g (token: logits of this thread's vectors;
+    // block: its blocks), each fed to f (0 = none).
+    template <class F>
+    __device__ __forceinline__ void reps(uint32_t g, F &&f) const {
+        if constexpr (M::BLOCK) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                acc = max(acc, ek[j]);
+                if (((j + 1) & (g - 1u)) == 0u) {
+                    f(acc);
+                    acc = 0;
+                }
+            }
+        } else if (g == 1u) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                uint32_t ck[4];
+                clean(j, ck);
+#pragma unroll
+                for (int h = 0; h < 8; ++h) f(key_at<M>(ck, h));
+            }
+        } else if (g == 2u) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                f(rep_key(smax_halves(raw[j].x), 1u));
+                f(rep_key(smax_halves(raw[j].y), 1u));
+                f(rep_key(smax_halves(raw[j].z), 1u));
+                f(rep_key(smax_halves(raw[j].w), 1u));
+            }
+        } else if (g == 4u) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                f(rep_key(smax_halves(smax2(raw[j].x, raw[j].y)), 1u));
+                f(rep_key(smax_halves(smax2(raw[j].z, raw[j].w)), 1u));
+            }
+        } else {
+            const uint32_t per = g >> 3;  // 1, 2 or 4 vectors
+            uint32_t acc = 0x80008000u;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                acc = smax2(acc, vec_smax(raw[j]));
+                if ((static_cast<uint32_t>(j) + 1u) % per == 0u) {
+                    f(rep_key(smax_halves(acc), 1u));
+                    acc = 0x80008000u;
+                }
+            }
+        }
+    }
+
+    // The 12-bit bin of s.hist holding the q-th largest: s.bc = {bin, above,
+    // count}; returns the total. Zeroes s.hist. Thread t owns 8 bins from the top.
+    __device__ __forceinline__ uint32_t find_cut(uint32_t q) {
+        const int t = threadIdx.x;
+        const int base = HBINS - 8 * (t + 1);
+        uint4 *h4 = reinterpret_cast<uint4 *>(s.hist + base);
+        const uint4 a = h4[0], b = h4[1];
+        const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        h4[0] = make_uint4(0, 0, 0, 0);
+        h4[1] = make_uint4(0, 0, 0, 0);
+        uint32_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum += v[i];
+        uint32_t total;
+        const uint32_t incl = block_scan(s, par, sum, total);
+        uint32_t acc = incl - sum;
+        if (acc < q && q <= incl) {
+            bool done = false;
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                if (!done && acc + v[i] >= q) {
+                    s.bc[0] = static_cast<uint32_t>(base + i);
+                    s.bc[1] = acc;
+                    s.bc[2] = v[i];
+                    done = true;
+                }
+                acc += v[i];
+            }
+        }
+        __syncthreads();
+        return total;
+    }
+
+    // Every candidate of the row (at most k of them): written in index order.
+    __device__ void take_all() {
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) cnt += key_at<M>(ck, h) != 0u;
+        }
+        uint32_t total;
+        uint32_t at = block_scan(s, par, cnt, total) - cnt;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h)
+                if (key_at<M>(ck, h) != 0u) put(at++, M::elem(pos_of(j), h));
+        }
+        for (uint32_t i = total + threadIdx.x; i < k; i += NT) orow()[i] = -1;
+    }
+
+    // Ties at c among the row's keys: the `take` lowest indices, written at
+    // out[first + rank]. Few ties are in s.tie_idx and ranked there; many are
+    // found again in index order with scans of per-vector tie counts.
+    __device__ void write_ties(uint32_t c, uint32_t take, uint32_t first, uint32_t e) {
+        const uint32_t tid = threadIdx.x;
+        if (e <= static_cast<uint32_t>(TIECAP)) {
+            if (tid < e) {
+                const uint32_t mine = s.tie_idx[tid];
+                uint32_t r = tid;
+                if (take < e) {
+                    r = 0;
+                    for (uint32_t u = 0; u < e; ++u) r += s.tie_idx[u] < mine;
+                }
+                if (r < take) put(first + r, mine);
+            }
+            return;
+        }
+        uint32_t before = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (before >= take) break;  // uniform
+            uint32_t ck[4];
+            clean(j, ck);
+            uint32_t eq = 0;
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) eq += key_at<M>(ck, h) == c;
+            uint32_t total;
+            uint32_t r = before + block_scan(s, par, eq, total) - eq;
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) {
+                if (key_at<M>(ck, h) == c) {
+                    if (r < take) put(first + r, M::elem(pos_of(j), h));
+                    ++r;
+                }
+            }
+            before += total;
+        }
+    }
+
+    // The q-th largest survivor key, when it is not in the window histogram's
+    // range: a two-pass radix select over s.surv_key[0 .. n) in [lo, hi].
+    __device__ uint32_t survivor_select(uint32_t n, uint32_t lo, uint32_t hi, uint32_t q, uint32_t &above) {
+        const uint32_t tid = threadIdx.x;
+        const uint32_t range = hi - lo;
+        const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
+        const uint32_t mask = (1u << shift) - 1u;
+        for (uint32_t i = tid; i < n; i += NT)
+            atomicAdd(&s.hwin[1][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
+        __syncthreads();
+        uint32_t b1, a1, tot;
+        find_bin256(s.hwin[1], q, b1, a1, tot);
+        __syncthreads();
+        if (tid < 256) s.hwin[1][tid] = 0u;
+        __syncthreads();
+        if (shift == 0) {
+            above = a1;
+            return lo + b1;
+        }
+        for (uint32_t i = tid; i < n; i += NT) {
+            const uint32_t o = static_cast<uint32_t>(s.surv_key[i]) - lo;
+            if ((o >> shift) == b1) atomicAdd(&s.hwin[1][o & mask], 1u);
+        }
+        __syncthreads();
+        uint32_t b2, a2;
+        find_bin256(s.hwin[1], q - a1, b2, a2, tot);
+        __syncthreads();
+        if (tid < 256) s.hwin[1][tid] = 0u;
+        above = a1 + a2;
+        return lo + (b1 << shift) + b2;
+    }
+
+    // The q-th smallest index among survivors with key T (more than TIECAP of
+    // them): radix select over 10-bit digits in s.hist (zero on entry, exit).
+    __device__ uint32_t survivor_tie_cut(uint32_t n, uint32_t T, uint32_t q) {
+        const uint32_t tid = threadIdx.x;
+        uint32_t cut = 0, need = q;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int sh = pass == 0 ? 10 : 0;
+            for (uint32_t i = tid; i < n; i += NT) {
+                if (s.surv_key[i] != T) continue;
+                const uint32_t x = s.surv_idx[i];
+                if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
+                atomicAdd(&s.hist[(x >> sh) & 1023u], 1u);
+            }
+            __syncthreads();
+            // Ascending: threads 0..255 own bins [4t, 4t + 4).
+            uint32_t v[4] = {0u, 0u, 0u, 0u};
+            if (tid < 256) {
+                uint4 *h4 = reinterpret_cast<uint4 *>(s.hist) + tid;
+                const uint4 hv = *h4;
+                *h4 = make_uint4(0, 0, 0, 0);
+                v[0] = hv.x;
+                v[1] = hv.y;
+                v[2] = hv.z;
+                v[3] = hv.w;
+            }
+            const uint32_t sum = v[0] + v[1] + v[2] + v[3];
+            uint32_t total;
+            const uint32_t incl = block_scan(s, par, sum, total);
+            uint32_t acc = incl - sum;
+            if (acc < need && need <= incl) {
+                bool done = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (!done && acc + v[i] >= need) {
+                        s.bc[0] = 4 * tid + i;
+                        s.bc[1] = acc;
+                        done = true;
+                    }
+                    acc += v[i];
+                }
+            }
+            __syncthreads();
+            cut |= s.bc[0] << sh;
+            need -= s.bc[1];
+        }
+        return cut;
+    }
+
+    __device__ void select() {
+        const uint32_t tid = threadIdx.x;
+        const uint32_t nE = M::BLOCK ? static_cast<uint32_t>(V) : static_cast<uint32_t>(L);
+        if (nE <= k) {
+            count_event(p, TOPK_CNT_TILE_TAKE_ALL);
+            take_all();
+            return;
+        }
+        uint32_t g = 1;
+        if (!p.force_direct)
+            while (g < static_cast<uint32_t>(M::BLOCK ? 4 : 32) && nE / (2u * g) >= 2u * k) g *= 2u;
+        for (;;) {
+            if (tid == 0) {
+                s.v_ngt = 0u;
+                s.v_neq = 0u;
+                s.v_smax = 0u;
+            }
+            if (tid < 16) s.sub[tid] = 0u;
+            reps(g, [&](uint32_t key) { agg_add(s.hist, key >> 4, key != 0u); });
+            __syncthreads();
+            const uint32_t NR = find_cut(k);
+            if (NR < k) {
+                if (g > 1u) {
+                    count_event(p, TOPK_CNT_TILE_UNBOUNDED);
+                    g = 1u;
+                    continue;
+                }
+                count_event(p, TOPK_CNT_TILE_TAKE_ALL);
+                take_all();
+                return;
+            }
+            const uint32_t bin = s.bc[0], above = s.bc[1], cnt = s.bc[2];
+            uint32_t c;
+            if (g == 1u || cnt > SUB_EXACT) {
+                reps(g, [&](uint32_t key) { agg_add(s.sub, key & 15u, key != 0u && (key >> 4) == bin); });
+                __syncthreads();
+                uint32_t acc = above, sb = 0;
+                for (int i = 15; i >= 0; --i) {
+                    const uint32_t v = s.sub[i];
+                    if (acc + v >= k) {
+                        sb = static_cast<uint32_t>(i);
+                        break;
+                    }
+                    acc += v;
+                }
+                c = (bin << 4) | sb;
+            } else {
+                c = bin << 4;  // a lower bound on the k-th representative
+            }
+            // Survivors: keys > c into the list (and the window histogram over
+            // [c + 1, c + 256), its top bin holding every larger key); ties at c
+            // counted, their indices kept while they fit.
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                uint32_t ck[4] = {0u, 0u, 0u, 0u};
+                if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) clean(j, ck);
+                uint32_t ngt = 0, neq = 0, kmax = 0;
+#pragma unroll
+                for (int h = 0; h < M::KPV; ++h) {
+                    const uint32_t key = key_at<M>(ck, h);
+                    ngt += key > c;
+                    neq += key == c;
+                    kmax = key > c ? max(kmax, key) : kmax;
+                }
+                const uint32_t any = __ballot_sync(0xFFFFFFFFu, (ngt | neq) != 0u);
+                if (any == 0u) continue;
+                uint32_t at = warp_slots(&s.v_ngt, ngt);
+                uint32_t et = warp_slots(&s.v_neq, neq);
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, kmax);
+                if (lane_id() == 0 && mx) atomicMax(&s.v_smax, mx);
+#pragma unroll
+                for (int h = 0; h < M::KPV; ++h) {
+                    const uint32_t key = key_at<M>(ck, h);
+                    if (key > c) {
+                        atomicAdd(&s.hwin[0][min(key - c - 1u, 255u)], 1u);
+                        if (at < static_cast<uint32_t>(SURV_CAP)) {
+                            s.surv_key[at] = static_cast<uint16_t>(key);
+                            s.surv_idx[at] = M::elem(pos_of(j), h);
+                        }
+                        ++at;
+                    } else if (key == c) {
+                        if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos_of(j), h);
+                        ++et;
+                    }
+                }
+            }
+            __syncthreads();
+            const uint32_t ngt = s.v_ngt, neq = s.v_neq, smax = s.v_smax;
+            if (ngt > static_cast<uint32_t>(SURV_CAP)) {
+                count_event(p, TOPK_CNT_TILE_OVERFLOW);
+                if (tid < 256) s.hwin[0][tid] = 0u;
+                __syncthreads();
+                if (g == 1u) {  // cannot happen: fewer than k keys exceed an exact cut
+                    if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+                    return;
+                }
+                g = 1u;
+                continue;
+            }
+            count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+            uint32_t T, take;
+            if (ngt >= k) {
+                uint32_t b1, above1, tot;
+                find_bin256(s.hwin[0], k, b1, above1, tot);
+                __syncthreads();
+                if (tid < 256) s.hwin[0][tid] = 0u;
+                if (b1 < 255u) {
+                    T = c + 1u + b1;
+                    take = k - above1;
+                } else {
+                    __syncthreads();
+                    uint32_t a2;
+                    T = survivor_select(ngt, c + 1u, smax, k, a2);
+                    take = k - a2;
+                }
+                // Keys > T, then the take lowest-index ties at T.
+                if (tid == 0) {
+                    s.v_emit = 0u;
+                    s.v_ntie = 0u;
+                }
+                __syncthreads();
+                const uint32_t lt = (1u << lane_id()) - 1u;
+                for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
+                    const uint32_t i = i0 + tid;
+                    const uint32_t key = i < ngt ? s.surv_key[i] : 0u;
+                    const bool gt = key > T, tie = key == T;
+                    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
+                    const uint32_t ag = warp_reserve(&s.v_emit, __popc(bg)) + __popc(bg & lt);
+                    const uint32_t at = warp_reserve(&s.v_ntie, __popc(bt)) + __popc(bt & lt);
+                    if (gt) put(ag, s.surv_idx[i]);
+                    if (tie && at < static_cast<uint32_t>(TIECAP)) s.tie_idx[at] = s.surv_idx[i];
+                }
+                __syncthreads();
+                const uint32_t e = s.v_ntie;
+                if (e <= static_cast<uint32_t>(TIECAP)) {
+                    write_ties(T, take, k - take, e);
+                } else {
+                    const uint32_t cut = survivor_tie_cut(ngt, T, take);
+                    if (tid == 0) s.v_ntie = 0u;
+                    __syncthreads();
+                    for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
+                        const uint32_t i = i0 + tid;
+                        const bool sel = i < ngt && s.surv_key[i] == T && s.surv_idx[i] <= cut;
+                        const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
+                        const uint32_t at = warp_reserve(&s.v_ntie, __popc(b)) + __popc(b & lt);
+                        if (sel) put(k - take + at, s.surv_idx[i]);
+                    }
+                }
+            } else {
+                // The cut is c itself: every survivor, then the lowest-index ties.
+                T = c;
+                take = k - ngt;
+                if (tid < 256) s.hwin[0][tid] = 0u;
+                for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
+                write_ties(c, take, ngt, neq);
+            }
+            return;
+        }
+    }
+};
+
+__device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int64_t V) {
+    const uint32_t bytes = static_cast<uint32_t>(V * 16);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
+    mbar_expect_tx(&s.full[st], bytes);
+    bulk_load(&s.stage[st][0], src, bytes, &s.full[st]);
+}
+
+// The next row of this CTA (from `row` on, step `step`) that reads logits, or
+// rows; V = its valid vectors.
+__device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, int32_t row, int32_t step,
+                                                    int64_t &V) {
+    for (; row < p.rows; row += step) {
+        const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
+        const int32_t n = block ? (L + 7) >> 3 : L;
+        if (n > p.k) {
+            V = (static_cast<int64_t>(L) + 7) >> 3;
+            return row;
+        }
+    }
+    return p.rows;
+}
+
+template <class M>
+__global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int32_t step = static_cast<int32_t>(gridDim.x);
+
+    grid_dependency_wait();
+    if (tid == 0) {
+        for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
+        fence_mbar_init();
+        s.abort_flag = 0u;
+    }
+    for (int i = tid; i < HBINS; i += NT) s.hist[i] = 0u;
+    if (tid < 256) s.hwin[0][tid] = s.hwin[1][tid] = 0u;
+    __syncthreads();
+    int32_t feed_row = 0;
+    if (tid == 0) {
+        int64_t V;
+        feed_row = next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
+        for (int i = 0; i < NSTAGE && feed_row < p.rows; ++i) {
+            issue_row(s, i, p, feed_row, V);
+            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+        }
+    }
+
+    Row<M> r(s, p);
+    r.k = static_cast<uint32_t>(p.k);
+    uint32_t seq = 0;
+    for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += step) {
+        const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
+        const int32_t n = M::BLOCK ? (L + 7) >> 3 : L;
+        if (n <= p.k) {
+            if (tid == 0) count_event(p, TOPK_CNT_BYPASS_ROWS);
+            for (int32_t i = tid; i < p.k; i += NT)
+                p.out[static_cast<int64_t>(row) * p.k + i] = i < n ? transform(p, row, i) : -1;
+            continue;
+        }
+        r.row = row;
+        r.L = L;
+        r.V = (static_cast<int64_t>(L) + 7) >> 3;
+        const int st = static_cast<int>(seq & (NSTAGE - 1));
+        PhaseClock clk;
+        clk.start(p);
+        mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+        clk.stop(p, TOPK_CNT_CYC_WAIT);
+        count_event(p, TOPK_CNT_ROUNDS);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int pos = j * NT + tid;
+            const int64_t v = pos;
+            r.raw[j] = pos < r.V ? s.stage[st][pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+            if (!M::BLOCK && v == r.V - 1 && (L & 7)) {
+                // Lanes past the valid length carry no element.
+                uint32_t w[4] = {r.raw[j].x, r.raw[j].y, r.raw[j].z, r.raw[j].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if (h >= (L & 7))
+                        w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
+                                    ((h & 1) ? 0x80000000u : 0x00008000u);
+                r.raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            r.ek[j] = (M::BLOCK && pos < r.V) ? BlockMode::key(r.raw[j], v, r.V) : 0u;
+        }
+        ++seq;
+        __syncthreads();  // the stage is in registers: hand it back to the ring
+        if (tid == 0 && feed_row < p.rows) {
+            int64_t V;
+            next_loaded_row(p, M::BLOCK, feed_row, step, V);
+            fence_proxy_async();
+            issue_row(s, st, p, feed_row, V);
+            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+        }
+        clk.start(p);
+        r.select();
+        __syncthreads();
+        clk.stop(p, TOPK_CNT_CYC_SELECT);
+    }
+}
+
+}  // namespace one
+
 // ------------------------------------------------------------------ host side
 
 struct Variant {
@@ -1443,7 +2018,6 @@ struct Variant {
     int smem;
 };
 
-constexpr int NARROW_NSTAGE = 2, NARROW_CAP = 3072;
 constexpr int WIDE_NSTAGE = 4, WIDE_CAP = 8192;
 
 template <class M, int NSTAGE, int CAP>
@@ -1452,10 +2026,16 @@ Variant variant() {
                    static_cast<int>(sizeof(Smem<NSTAGE, CAP>))};
 }
 
-Variant pick(bool block, bool wide) {
-    if (block)
-        return wide ? variant<BlockMode, WIDE_NSTAGE, WIDE_CAP>() : variant<BlockMode, NARROW_NSTAGE, NARROW_CAP>();
-    return wide ? variant<TokenMode, WIDE_NSTAGE, WIDE_CAP>() : variant<TokenMode, NARROW_NSTAGE, NARROW_CAP>();
+Variant pick_one(bool block) {
+    return block ? Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<BlockMode>),
+                           static_cast<int>(sizeof(one::Smem))}
+                 : Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<TokenMode>),
+                           static_cast<int>(sizeof(one::Smem))};
+}
+
+// The streamed kernel (rows wider than one tile, or split over a cluster).
+Variant pick(bool block, bool) {
+    return block ? variant<BlockMode, WIDE_NSTAGE, WIDE_CAP>() : variant<TokenMode, WIDE_NSTAGE, WIDE_CAP>();
 }
 
 struct DeviceInit {
@@ -1463,6 +2043,7 @@ struct DeviceInit {
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int per_sm[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [block][wide]
+    int per_sm_one[2] = {0, 0};            // the one-tile kernel, [block]
 };
 DeviceInit g_init[64];
 
@@ -1472,8 +2053,8 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
     std::call_once(d.once, [&]() {
         cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         for (int b = 0; b < 2 && e == cudaSuccess; ++b)
-            for (int w = 0; w < 2 && e == cudaSuccess; ++w) {
-                const Variant v = pick(b != 0, w != 0);
+            for (int w = 1; w < 2 && e == cudaSuccess; ++w) {
+                const Variant v = pick(b != 0, true);
                 e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1482,6 +2063,14 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                                                                       static_cast<size_t>(v.smem));
                 if (e == cudaSuccess && d.per_sm[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            const Variant v = pick_one(b != 0);
+            e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b], v.fn, one::NT,
+                                                                  static_cast<size_t>(v.smem));
+            if (e == cudaSuccess && d.per_sm_one[b] < 1) e = cudaErrorInvalidConfiguration;
+        }
         d.err = e;
     });
     out = &d;
@@ -1511,7 +2100,8 @@ Plan make_plan(int rows, int width, const DeviceInit &d, bool block, int forced)
         while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages) c *= 2;
         pl.cluster = c;
     }
-    const int64_t slots = static_cast<int64_t>(d.sms) * d.per_sm[block][pl.wide ? 1 : 0];
+    const int64_t slots = pl.wide ? static_cast<int64_t>(d.sms) * d.per_sm[block][1]
+                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block];
     const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
     return pl;
@@ -1556,7 +2146,8 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
 
     const bool block = mode == TOPK_BLOCK8;
     const Plan pl = make_plan(rows, width, *d, block, forced);
-    const Variant v = pick(block, pl.wide);
+    const Variant v = pl.wide ? pick(block, true) : pick_one(block);
+    const int threads = pl.wide ? THREADS : one::NT;
 
     Params prm;
     prm.logits = logits;
@@ -1577,7 +2168,7 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     const int64_t blocks = pl.clusters * pl.cluster;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -1637,9 +2228,9 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
     if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
     if (topk::init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
     const topk::Plan pl = topk::make_plan(rows, width, *d, mode == TOPK_BLOCK8, 0);
-    const topk::Variant v = topk::pick(mode == TOPK_BLOCK8, pl.wide);
+    const topk::Variant v = pl.wide ? topk::pick(mode == TOPK_BLOCK8, true) : topk::pick_one(mode == TOPK_BLOCK8);
     if (cluster) *cluster = pl.cluster;
-    if (threads) *threads = topk::THREADS;
+    if (threads) *threads = pl.wide ? topk::THREADS : topk::one::NT;
     if (smem_bytes) *smem_bytes = v.smem;
     if (variant) *variant = pl.wide ? 1 : 0;
     return TOPK_OK;

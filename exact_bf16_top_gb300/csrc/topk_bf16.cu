@@ -1764,8 +1764,12 @@ struct Row {
                 s.v_smax = 0u;
             }
             if (tid < 16) s.sub[tid] = 0u;
+            PhaseClock clk;
+            clk.start(p);
             reps(g, [&](uint32_t key) { agg_add(s.hist, key >> 4, key != 0u); });
             __syncthreads();
+            clk.stop(p, TOPK_CNT_CYC_REPS);
+            clk.start(p);
             const uint32_t NR = find_cut(k);
             if (NR < k) {
                 if (g > 1u) {
@@ -1795,6 +1799,8 @@ struct Row {
             } else {
                 c = bin << 4;  // a lower bound on the k-th representative
             }
+            clk.stop(p, TOPK_CNT_CYC_CUT);
+            clk.start(p);
             // Survivors: keys > c into the list (and the window histogram over
             // [c + 1, c + 256), its top bin holding every larger key); ties at c
             // counted, their indices kept while they fit.
@@ -1833,6 +1839,8 @@ struct Row {
                 }
             }
             __syncthreads();
+            clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
+            clk.start(p);
             const uint32_t ngt = s.v_ngt, neq = s.v_neq, smax = s.v_smax;
             if (ngt > static_cast<uint32_t>(SURV_CAP)) {
                 count_event(p, TOPK_CNT_TILE_OVERFLOW);
@@ -1861,6 +1869,8 @@ struct Row {
                     T = survivor_select(ngt, c + 1u, smax, k, a2);
                     take = k - a2;
                 }
+                clk.stop(p, TOPK_CNT_CYC_EXACT);
+                clk.start(p);
                 // Keys > T, then the take lowest-index ties at T.
                 if (tid == 0) {
                     s.v_emit = 0u;
@@ -1894,6 +1904,8 @@ struct Row {
                         if (sel) put(k - take + at, s.surv_idx[i]);
                     }
                 }
+                __syncthreads();
+                clk.stop(p, TOPK_CNT_CYC_FINISH);
             } else {
                 // The cut is c itself: every survivor, then the lowest-index ties.
                 T = c;

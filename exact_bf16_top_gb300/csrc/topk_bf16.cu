@@ -1801,38 +1801,52 @@ struct Row {
             }
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
-            // Survivors: keys > c into the list (and the window histogram over
-            // [c + 1, c + 256), its top bin holding every larger key); ties at c
-            // counted, their indices kept while they fit.
+            // Survivors: keys > c into the list; ties at c counted, their
+            // indices kept while they fit. Per vector a bit mask of each kind,
+            // one warp scan for the thread's totals, one atomic per warp.
+            uint32_t gtm[NV], eqm[NV], my_gt = 0, my_eq = 0;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                uint32_t ck[4] = {0u, 0u, 0u, 0u};
-                if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) clean(j, ck);
-                uint32_t ngt = 0, neq = 0, kmax = 0;
+                gtm[j] = eqm[j] = 0u;
+                if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) {
+                    uint32_t ck[4];
+                    clean(j, ck);
 #pragma unroll
-                for (int h = 0; h < M::KPV; ++h) {
-                    const uint32_t key = key_at<M>(ck, h);
-                    ngt += key > c;
-                    neq += key == c;
-                    kmax = key > c ? max(kmax, key) : kmax;
+                    for (int h = 0; h < M::KPV; ++h) {
+                        const uint32_t key = key_at<M>(ck, h);
+                        gtm[j] |= (key > c ? 1u : 0u) << h;
+                        eqm[j] |= (key == c ? 1u : 0u) << h;
+                    }
                 }
-                const uint32_t any = __ballot_sync(0xFFFFFFFFu, (ngt | neq) != 0u);
-                if (any == 0u) continue;
-                uint32_t at = warp_slots(&s.v_ngt, ngt);
-                uint32_t et = warp_slots(&s.v_neq, neq);
-                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, kmax);
-                if (lane_id() == 0 && mx) atomicMax(&s.v_smax, mx);
+                my_gt += __popc(gtm[j]);
+                my_eq += __popc(eqm[j]);
+            }
+            {
+                const uint32_t incl = warp_incl_scan(my_gt | (my_eq << 16));
+                const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                uint32_t b0 = 0, b1 = 0;
+                if (lane_id() == 31) {
+                    if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
+                    if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
+                }
+                const uint32_t ex = incl - (my_gt | (my_eq << 16));
+                uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
+                uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
 #pragma unroll
-                for (int h = 0; h < M::KPV; ++h) {
-                    const uint32_t key = key_at<M>(ck, h);
-                    if (key > c) {
-                        atomicAdd(&s.hwin[0][min(key - c - 1u, 255u)], 1u);
+                for (int j = 0; j < NV; ++j) {
+                    if ((gtm[j] | eqm[j]) == 0u) continue;
+                    uint32_t ck[4];
+                    clean(j, ck);
+                    for (uint32_t m = gtm[j]; m; m &= m - 1u) {
+                        const int h = __ffs(m) - 1;
                         if (at < static_cast<uint32_t>(SURV_CAP)) {
-                            s.surv_key[at] = static_cast<uint16_t>(key);
+                            s.surv_key[at] = static_cast<uint16_t>(M::BLOCK ? ck[0] : (ck[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu);
                             s.surv_idx[at] = M::elem(pos_of(j), h);
                         }
                         ++at;
-                    } else if (key == c) {
+                    }
+                    for (uint32_t m = eqm[j]; m; m &= m - 1u) {
+                        const int h = __ffs(m) - 1;
                         if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos_of(j), h);
                         ++et;
                     }
@@ -1841,10 +1855,9 @@ struct Row {
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
             clk.start(p);
-            const uint32_t ngt = s.v_ngt, neq = s.v_neq, smax = s.v_smax;
-            if (ngt > static_cast<uint32_t>(SURV_CAP)) {
+            const uint32_t ngt_all = s.v_ngt, neq_all = s.v_neq;
+            if (ngt_all > static_cast<uint32_t>(SURV_CAP)) {
                 count_event(p, TOPK_CNT_TILE_OVERFLOW);
-                if (tid < 256) s.hwin[0][tid] = 0u;
                 __syncthreads();
                 if (g == 1u) {  // cannot happen: fewer than k keys exceed an exact cut
                     if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
@@ -1854,19 +1867,37 @@ struct Row {
                 continue;
             }
             count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+            const uint32_t ngt = ngt_all, neq = neq_all;
             uint32_t T, take;
             if (ngt >= k) {
-                uint32_t b1, above1, tot;
-                find_bin256(s.hwin[0], k, b1, above1, tot);
+                // The k-th survivor: a histogram of the list over [c + 1, c + 256)
+                // (its top bin also holding every larger key), searched by one
+                // warp; a full radix select only if it lies in that top bin.
+                for (uint32_t i = tid; i < ngt; i += NT)
+                    atomicAdd(&s.hwin[0][min(static_cast<uint32_t>(s.surv_key[i]) - c - 1u, 255u)], 1u);
                 __syncthreads();
+                if (tid < 32) {
+                    uint32_t b1, above1, tot;
+                    find_bin256(s.hwin[0], k, b1, above1, tot);
+                    if (tid == 0) {
+                        s.bc[0] = b1;
+                        s.bc[1] = above1;
+                    }
+                }
+                __syncthreads();
+                const uint32_t b1 = s.bc[0], above1 = s.bc[1];
                 if (tid < 256) s.hwin[0][tid] = 0u;
                 if (b1 < 255u) {
                     T = c + 1u + b1;
                     take = k - above1;
                 } else {
+                    uint32_t smax = 0;
+                    for (uint32_t i = tid; i < ngt; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
+                    smax = __reduce_max_sync(0xFFFFFFFFu, smax);
+                    if (lane_id() == 0) atomicMax(&s.v_smax, smax);
                     __syncthreads();
                     uint32_t a2;
-                    T = survivor_select(ngt, c + 1u, smax, k, a2);
+                    T = survivor_select(ngt, c + 1u, s.v_smax, k, a2);
                     take = k - a2;
                 }
                 clk.stop(p, TOPK_CNT_CYC_EXACT);
@@ -1910,7 +1941,6 @@ struct Row {
                 // The cut is c itself: every survivor, then the lowest-index ties.
                 T = c;
                 take = k - ngt;
-                if (tid < 256) s.hwin[0][tid] = 0u;
                 for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
                 write_ties(c, take, ngt, neq);
             }

@@ -1445,30 +1445,28 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
 // cut -> write. Same cutoff argument as the streamed kernel.
 namespace one {
 
-constexpr int NT = 512;
+constexpr int NT = 256;
 constexpr int NW = NT / 32;
-constexpr int NV = 4;                        // vectors per thread
+constexpr int NV = 8;                        // vectors per thread
 constexpr int NTILE = NT * NV;               // 2048 vectors
-constexpr int NSTAGE = 2;
 constexpr int SURV_CAP = 4096;
 
 struct alignas(128) Smem {
-    uint4 stage[NSTAGE][NTILE];
+    uint4 stage[NTILE];                      // the row, until it is in registers
     uint32_t surv_idx[SURV_CAP];
     uint16_t surv_key[SURV_CAP];
-    uint32_t hist[HBINS];                    // 12-bit histogram (zero between uses)
-    uint32_t hwin[2][256];                   // window histograms (zero between uses)
+    uint32_t hs[4][256];                     // [0], [1]: the cut's two passes; [2], [3]: windows
+                                             // (zero between uses; also index-radix scratch)
     uint32_t tie_idx[TIECAP];
-    uint32_t sub[16];
     uint32_t red[2][NW];
     uint32_t bc[4];
     uint32_t v_ngt, v_neq, v_smax, v_emit, v_ntie;
     uint32_t abort_flag;
-    unsigned long long full[NSTAGE];
+    unsigned long long full;
 };
 
 // Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
-// warp (crowded bins would otherwise serialise the atomics of the whole warp).
+// warp (a crowded bin would otherwise serialise the atomics of the whole warp).
 __device__ __forceinline__ void agg_add(uint32_t *hist, uint32_t bin, bool valid) {
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
     if (valid && lane_id() == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
@@ -1487,12 +1485,26 @@ __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t 
     return pre + inc;
 }
 
-// Warp-aggregated slot for this lane's `n` items (one atomic per warp).
-__device__ __forceinline__ uint32_t warp_slots(uint32_t *ctr, uint32_t n) {
-    const uint32_t incl = warp_incl_scan(n);
-    uint32_t base = 0;
-    if (lane_id() == 31 && incl) base = atomicAdd(ctr, incl);
-    return __shfl_sync(0xFFFFFFFFu, base, 31) + incl - n;
+// Warp 0 finds the bin of `hist` holding the q-th largest and zeroes the
+// histogram; the caller's __syncthreads then publishes s.bc = {bin, above, total}.
+__device__ __forceinline__ void warp0_find(Smem &s, uint32_t *hist, uint32_t q) {
+    if (threadIdx.x < 32) {
+        uint32_t b, above, total;
+        find_bin256(hist, q, b, above, total);
+        reinterpret_cast<uint4 *>(hist)[2 * threadIdx.x] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(hist)[2 * threadIdx.x + 1] = make_uint4(0, 0, 0, 0);
+        if (threadIdx.x == 0) {
+            s.bc[0] = b;
+            s.bc[1] = above;
+            s.bc[2] = total;
+        }
+    }
+}
+
+// The half h (0..7) of a vector as a 16-bit value.
+__device__ __forceinline__ uint32_t half_of(const uint4 &r, int h) {
+    const uint32_t w = (h & 4) ? ((h & 2) ? r.w : r.z) : ((h & 2) ? r.y : r.x);
+    return (h & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
 
 template <class M>
@@ -1500,11 +1512,10 @@ struct Row {
     Smem &s;
     const Params &p;
     uint32_t par = 0;
-    int32_t row = 0, L = 0;
-    int64_t V = 0;
+    int32_t row = 0, L = 0, V = 0;
     uint32_t k = 0;
-    uint4 raw[NV];     // the row, this thread's vectors j * NT + threadIdx.x
-    uint32_t ek[NV];   // block mode: the vectors' element keys
+    uint4 raw[NV];     // this thread's vectors j * NT + threadIdx.x (lanes without an element: 0x8000)
+    uint32_t ek[NV];   // block mode: their element keys
 
     __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
@@ -1515,14 +1526,13 @@ struct Row {
         else ck[0] = ck[1] = ck[2] = ck[3] = 0u;
     }
 
-    __device__ __forceinline__ int32_t *orow() const { return p.out + static_cast<int64_t>(row) * k; }
-
     __device__ __forceinline__ void put(uint32_t slot, uint32_t idx) const {
-        orow()[slot] = transform(p, row, static_cast<int32_t>(idx));
+        p.out[static_cast<int64_t>(row) * k + slot] = transform(p, row, static_cast<int32_t>(idx));
     }
 
-    // Representatives of groups of g (token: logits of this thread's vectors;
-    // block: its blocks), each fed to f (0 = none).
+    // Representatives of groups of g elements of this thread (token: g
+    // logits, within a vector for g <= 8, else whole vectors; block: g blocks),
+    // each fed to f (0 = none).
     template <class F>
     __device__ __forceinline__ void reps(uint32_t g, F &&f) const {
         if constexpr (M::BLOCK) {
@@ -1558,7 +1568,7 @@ struct Row {
                 f(rep_key(smax_halves(smax2(raw[j].z, raw[j].w)), 1u));
             }
         } else {
-            const uint32_t per = g >> 3;  // 1, 2 or 4 vectors
+            const uint32_t per = g >> 3;  // whole vectors per group: 1, 2, 4 or 8
             uint32_t acc = 0x80008000u;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
@@ -1571,40 +1581,7 @@ struct Row {
         }
     }
 
-    // The 12-bit bin of s.hist holding the q-th largest: s.bc = {bin, above,
-    // count}; returns the total. Zeroes s.hist. Thread t owns 8 bins from the top.
-    __device__ __forceinline__ uint32_t find_cut(uint32_t q) {
-        const int t = threadIdx.x;
-        const int base = HBINS - 8 * (t + 1);
-        uint4 *h4 = reinterpret_cast<uint4 *>(s.hist + base);
-        const uint4 a = h4[0], b = h4[1];
-        const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        h4[0] = make_uint4(0, 0, 0, 0);
-        h4[1] = make_uint4(0, 0, 0, 0);
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sum += v[i];
-        uint32_t total;
-        const uint32_t incl = block_scan(s, par, sum, total);
-        uint32_t acc = incl - sum;
-        if (acc < q && q <= incl) {
-            bool done = false;
-#pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                if (!done && acc + v[i] >= q) {
-                    s.bc[0] = static_cast<uint32_t>(base + i);
-                    s.bc[1] = acc;
-                    s.bc[2] = v[i];
-                    done = true;
-                }
-                acc += v[i];
-            }
-        }
-        __syncthreads();
-        return total;
-    }
-
-    // Every candidate of the row (at most k of them): written in index order.
+    // Every candidate of the row (at most k of them), in index order.
     __device__ void take_all() {
         uint32_t cnt = 0;
 #pragma unroll
@@ -1624,12 +1601,13 @@ struct Row {
             for (int h = 0; h < M::KPV; ++h)
                 if (key_at<M>(ck, h) != 0u) put(at++, M::elem(pos_of(j), h));
         }
-        for (uint32_t i = total + threadIdx.x; i < k; i += NT) orow()[i] = -1;
+        for (uint32_t i = total + threadIdx.x; i < k; i += NT)
+            p.out[static_cast<int64_t>(row) * k + i] = -1;
     }
 
-    // Ties at c among the row's keys: the `take` lowest indices, written at
-    // out[first + rank]. Few ties are in s.tie_idx and ranked there; many are
-    // found again in index order with scans of per-vector tie counts.
+    // The take lowest-index elements equal to c, written at out[first + rank].
+    // Up to TIECAP of them are in s.tie_idx and ranked there; more are found
+    // again in index order with scans of per-vector tie counts.
     __device__ void write_ties(uint32_t c, uint32_t take, uint32_t first, uint32_t e) {
         const uint32_t tid = threadIdx.x;
         if (e <= static_cast<uint32_t>(TIECAP)) {
@@ -1666,20 +1644,19 @@ struct Row {
         }
     }
 
-    // The q-th largest survivor key, when it is not in the window histogram's
-    // range: a two-pass radix select over s.surv_key[0 .. n) in [lo, hi].
+    // The q-th largest survivor when the window histogram cannot place it: a
+    // two-pass radix select over s.surv_key[0 .. n), all in [lo, hi].
     __device__ uint32_t survivor_select(uint32_t n, uint32_t lo, uint32_t hi, uint32_t q, uint32_t &above) {
         const uint32_t tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         const uint32_t mask = (1u << shift) - 1u;
         for (uint32_t i = tid; i < n; i += NT)
-            atomicAdd(&s.hwin[1][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
+            atomicAdd(&s.hs[3][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
         __syncthreads();
-        uint32_t b1, a1, tot;
-        find_bin256(s.hwin[1], q, b1, a1, tot);
+        warp0_find(s, s.hs[3], q);
         __syncthreads();
-        if (tid < 256) s.hwin[1][tid] = 0u;
+        const uint32_t b1 = s.bc[0], a1 = s.bc[1];
         __syncthreads();
         if (shift == 0) {
             above = a1;
@@ -1687,21 +1664,22 @@ struct Row {
         }
         for (uint32_t i = tid; i < n; i += NT) {
             const uint32_t o = static_cast<uint32_t>(s.surv_key[i]) - lo;
-            if ((o >> shift) == b1) atomicAdd(&s.hwin[1][o & mask], 1u);
+            if ((o >> shift) == b1) atomicAdd(&s.hs[3][o & mask], 1u);
         }
         __syncthreads();
-        uint32_t b2, a2;
-        find_bin256(s.hwin[1], q - a1, b2, a2, tot);
+        warp0_find(s, s.hs[3], q - a1);
         __syncthreads();
-        if (tid < 256) s.hwin[1][tid] = 0u;
+        const uint32_t b2 = s.bc[0], a2 = s.bc[1];
+        __syncthreads();
         above = a1 + a2;
         return lo + (b1 << shift) + b2;
     }
 
     // The q-th smallest index among survivors with key T (more than TIECAP of
-    // them): radix select over 10-bit digits in s.hist (zero on entry, exit).
+    // them): radix select over 10-bit digits, in the 1024 words of s.hs.
     __device__ uint32_t survivor_tie_cut(uint32_t n, uint32_t T, uint32_t q) {
         const uint32_t tid = threadIdx.x;
+        uint32_t *h = &s.hs[0][0];
         uint32_t cut = 0, need = q;
         for (int pass = 0; pass < 2; ++pass) {
             const int sh = pass == 0 ? 10 : 0;
@@ -1709,20 +1687,13 @@ struct Row {
                 if (s.surv_key[i] != T) continue;
                 const uint32_t x = s.surv_idx[i];
                 if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
-                atomicAdd(&s.hist[(x >> sh) & 1023u], 1u);
+                atomicAdd(&h[(x >> sh) & 1023u], 1u);
             }
             __syncthreads();
-            // Ascending: threads 0..255 own bins [4t, 4t + 4).
-            uint32_t v[4] = {0u, 0u, 0u, 0u};
-            if (tid < 256) {
-                uint4 *h4 = reinterpret_cast<uint4 *>(s.hist) + tid;
-                const uint4 hv = *h4;
-                *h4 = make_uint4(0, 0, 0, 0);
-                v[0] = hv.x;
-                v[1] = hv.y;
-                v[2] = hv.z;
-                v[3] = hv.w;
-            }
+            uint4 *h4 = reinterpret_cast<uint4 *>(h) + tid;  // ascending: bins [4t, 4t + 4)
+            const uint4 hv = *h4;
+            *h4 = make_uint4(0, 0, 0, 0);
+            const uint32_t v[4] = {hv.x, hv.y, hv.z, hv.w};
             const uint32_t sum = v[0] + v[1] + v[2] + v[3];
             uint32_t total;
             const uint32_t incl = block_scan(s, par, sum, total);
@@ -1742,8 +1713,86 @@ struct Row {
             __syncthreads();
             cut |= s.bc[0] << sh;
             need -= s.bc[1];
+            __syncthreads();
         }
         return cut;
+    }
+
+    // Survivors of cut c: keys > c to the list, keys == c counted and (while
+    // they fit) their indices kept. Per vector a bit mask of each kind, one warp
+    // scan of the thread's totals, one shared atomic per warp.
+    __device__ void survivors(uint32_t c) {
+        uint32_t gtm[NV], eqm[NV], my_gt = 0, my_eq = 0;
+        // Non-negative cut (the usual case): the surviving keys are exactly the
+        // BF16 bits in (c - 0x8000, 0x7F80] read as signed 16-bit integers, and
+        // the ties are the bits c - 0x8000; masked lanes hold 0x8000 (negative).
+        const bool fast = !M::BLOCK && c >= 0x8000u;
+        const int32_t cs = static_cast<int32_t>(c) - 0x8000;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            uint32_t gm = 0, em = 0;
+            if (fast) {
+                if (smax_halves(vec_smax(raw[j])) >= cs) {
+                    const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int32_t lo = static_cast<int16_t>(w[i] & 0xFFFFu);
+                        const int32_t hi = static_cast<int32_t>(w[i]) >> 16;
+                        gm |= ((lo > cs && lo <= 0x7F80) ? 1u : 0u) << (2 * i);
+                        gm |= ((hi > cs && hi <= 0x7F80) ? 2u : 0u) << (2 * i);
+                        em |= (lo == cs ? 1u : 0u) << (2 * i);
+                        em |= (hi == cs ? 2u : 0u) << (2 * i);
+                    }
+                }
+            } else if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) {
+                uint32_t ck[4];
+                clean(j, ck);
+#pragma unroll
+                for (int h = 0; h < M::KPV; ++h) {
+                    const uint32_t key = key_at<M>(ck, h);
+                    gm |= (key > c ? 1u : 0u) << h;
+                    em |= (key == c ? 1u : 0u) << h;
+                }
+            }
+            gtm[j] = gm;
+            eqm[j] = em;
+            my_gt += __popc(gm);
+            my_eq += __popc(em);
+        }
+        const uint32_t packed = my_gt | (my_eq << 16);
+        const uint32_t incl = warp_incl_scan(packed);
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t b0 = 0, b1 = 0;
+        if (lane_id() == 31) {
+            if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
+            if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
+        }
+        const uint32_t ex = incl - packed;
+        uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
+        uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if ((gtm[j] | eqm[j]) == 0u) continue;
+            uint32_t ck[4] = {0u, 0u, 0u, 0u};
+            if (!fast) clean(j, ck);
+            for (uint32_t m = gtm[j]; m; m &= m - 1u) {
+                const int h = __ffs(m) - 1;
+                if (at < static_cast<uint32_t>(SURV_CAP)) {
+                    uint32_t key;
+                    if (fast) key = half_of(raw[j], h) + 0x8000u;
+                    else if (M::BLOCK) key = ck[0];
+                    else key = (ck[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu;
+                    s.surv_key[at] = static_cast<uint16_t>(key);
+                    s.surv_idx[at] = M::elem(pos_of(j), h);
+                }
+                ++at;
+            }
+            for (uint32_t m = eqm[j]; m; m &= m - 1u) {
+                const int h = __ffs(m) - 1;
+                if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos_of(j), h);
+                ++et;
+            }
+        }
     }
 
     __device__ void select() {
@@ -1754,112 +1803,50 @@ struct Row {
             take_all();
             return;
         }
+        // Group size: at least 2k representatives.
         uint32_t g = 1;
         if (!p.force_direct)
-            while (g < static_cast<uint32_t>(M::BLOCK ? 4 : 32) && nE / (2u * g) >= 2u * k) g *= 2u;
+            while (g < static_cast<uint32_t>(M::BLOCK ? 8 : 64) && nE / (2u * g) >= 2u * k) g *= 2u;
         for (;;) {
+            PhaseClock clk;
+            clk.start(p);
             if (tid == 0) {
                 s.v_ngt = 0u;
                 s.v_neq = 0u;
-                s.v_smax = 0u;
             }
-            if (tid < 16) s.sub[tid] = 0u;
-            PhaseClock clk;
-            clk.start(p);
-            reps(g, [&](uint32_t key) { agg_add(s.hist, key >> 4, key != 0u); });
+            // The k-th largest representative, exactly: high byte, then low byte.
+            reps(g, [&](uint32_t key) { agg_add(s.hs[0], key >> 8, key != 0u); });
             __syncthreads();
-            clk.stop(p, TOPK_CNT_CYC_REPS);
-            clk.start(p);
-            const uint32_t NR = find_cut(k);
-            if (NR < k) {
-                if (g > 1u) {
+            warp0_find(s, s.hs[0], k);
+            __syncthreads();
+            const uint32_t hb = s.bc[0], habove = s.bc[1], nreps = s.bc[2];
+            if (nreps < k) {
+                if (g > 1u) {  // the representatives cannot bound the row: exact path
                     count_event(p, TOPK_CNT_TILE_UNBOUNDED);
                     g = 1u;
+                    __syncthreads();
                     continue;
                 }
                 count_event(p, TOPK_CNT_TILE_TAKE_ALL);
                 take_all();
                 return;
             }
-            const uint32_t bin = s.bc[0], above = s.bc[1], cnt = s.bc[2];
-            uint32_t c;
-            if (g == 1u || cnt > SUB_EXACT) {
-                reps(g, [&](uint32_t key) { agg_add(s.sub, key & 15u, key != 0u && (key >> 4) == bin); });
-                __syncthreads();
-                uint32_t acc = above, sb = 0;
-                for (int i = 15; i >= 0; --i) {
-                    const uint32_t v = s.sub[i];
-                    if (acc + v >= k) {
-                        sb = static_cast<uint32_t>(i);
-                        break;
-                    }
-                    acc += v;
-                }
-                c = (bin << 4) | sb;
-            } else {
-                c = bin << 4;  // a lower bound on the k-th representative
-            }
+            reps(g, [&](uint32_t key) { agg_add(s.hs[1], key & 0xFFu, key != 0u && (key >> 8) == hb); });
+            __syncthreads();
+            warp0_find(s, s.hs[1], k - habove);
+            __syncthreads();
+            const uint32_t c = (hb << 8) | s.bc[0];
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
-            // Survivors: keys > c into the list; ties at c counted, their
-            // indices kept while they fit. Per vector a bit mask of each kind,
-            // one warp scan for the thread's totals, one atomic per warp.
-            uint32_t gtm[NV], eqm[NV], my_gt = 0, my_eq = 0;
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                gtm[j] = eqm[j] = 0u;
-                if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) {
-                    uint32_t ck[4];
-                    clean(j, ck);
-#pragma unroll
-                    for (int h = 0; h < M::KPV; ++h) {
-                        const uint32_t key = key_at<M>(ck, h);
-                        gtm[j] |= (key > c ? 1u : 0u) << h;
-                        eqm[j] |= (key == c ? 1u : 0u) << h;
-                    }
-                }
-                my_gt += __popc(gtm[j]);
-                my_eq += __popc(eqm[j]);
-            }
-            {
-                const uint32_t incl = warp_incl_scan(my_gt | (my_eq << 16));
-                const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-                uint32_t b0 = 0, b1 = 0;
-                if (lane_id() == 31) {
-                    if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
-                    if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
-                }
-                const uint32_t ex = incl - (my_gt | (my_eq << 16));
-                uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
-                uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
-#pragma unroll
-                for (int j = 0; j < NV; ++j) {
-                    if ((gtm[j] | eqm[j]) == 0u) continue;
-                    uint32_t ck[4];
-                    clean(j, ck);
-                    for (uint32_t m = gtm[j]; m; m &= m - 1u) {
-                        const int h = __ffs(m) - 1;
-                        if (at < static_cast<uint32_t>(SURV_CAP)) {
-                            s.surv_key[at] = static_cast<uint16_t>(M::BLOCK ? ck[0] : (ck[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu);
-                            s.surv_idx[at] = M::elem(pos_of(j), h);
-                        }
-                        ++at;
-                    }
-                    for (uint32_t m = eqm[j]; m; m &= m - 1u) {
-                        const int h = __ffs(m) - 1;
-                        if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos_of(j), h);
-                        ++et;
-                    }
-                }
-            }
+            survivors(c);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
             clk.start(p);
-            const uint32_t ngt_all = s.v_ngt, neq_all = s.v_neq;
-            if (ngt_all > static_cast<uint32_t>(SURV_CAP)) {
+            const uint32_t ngt = s.v_ngt, neq = s.v_neq;
+            if (ngt > static_cast<uint32_t>(SURV_CAP)) {
                 count_event(p, TOPK_CNT_TILE_OVERFLOW);
                 __syncthreads();
-                if (g == 1u) {  // cannot happen: fewer than k keys exceed an exact cut
+                if (g == 1u) {  // cannot happen: fewer than k keys exceed the exact k-th key
                     if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
                     return;
                 }
@@ -1867,104 +1854,92 @@ struct Row {
                 continue;
             }
             count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
-            const uint32_t ngt = ngt_all, neq = neq_all;
+            if (ngt < k) {
+                // The cut is c itself: every survivor, then the lowest-index ties.
+                for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
+                write_ties(c, k - ngt, ngt, neq);
+                clk.stop(p, TOPK_CNT_CYC_FINISH);
+                return;
+            }
+            // The k-th survivor: a histogram of the list over [c + 1, c + 256),
+            // its top bin also holding every larger key; a full radix select only
+            // when the k-th lies in that top bin.
+            for (uint32_t i = tid; i < ngt; i += NT)
+                atomicAdd(&s.hs[2][min(static_cast<uint32_t>(s.surv_key[i]) - c - 1u, 255u)], 1u);
+            __syncthreads();
+            warp0_find(s, s.hs[2], k);
+            if (tid == 0) {
+                s.v_emit = 0u;
+                s.v_ntie = 0u;
+            }
+            __syncthreads();
             uint32_t T, take;
-            if (ngt >= k) {
-                // The k-th survivor: a histogram of the list over [c + 1, c + 256)
-                // (its top bin also holding every larger key), searched by one
-                // warp; a full radix select only if it lies in that top bin.
-                for (uint32_t i = tid; i < ngt; i += NT)
-                    atomicAdd(&s.hwin[0][min(static_cast<uint32_t>(s.surv_key[i]) - c - 1u, 255u)], 1u);
+            if (s.bc[0] < 255u) {
+                T = c + 1u + s.bc[0];
+                take = k - s.bc[1];
+            } else {
+                uint32_t smax = 0;
+                for (uint32_t i = tid; i < ngt; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
+                smax = __reduce_max_sync(0xFFFFFFFFu, smax);
+                if (lane_id() == 0) atomicMax(&s.v_smax, smax);
                 __syncthreads();
-                if (tid < 32) {
-                    uint32_t b1, above1, tot;
-                    find_bin256(s.hwin[0], k, b1, above1, tot);
-                    if (tid == 0) {
-                        s.bc[0] = b1;
-                        s.bc[1] = above1;
-                    }
-                }
+                uint32_t a2;
+                T = survivor_select(ngt, c + 1u, s.v_smax, k, a2);
+                take = k - a2;
+                if (tid == 0) s.v_smax = 0u;
+            }
+            clk.stop(p, TOPK_CNT_CYC_EXACT);
+            clk.start(p);
+            // Keys > T, then the take lowest-index ties at T.
+            const uint32_t lt = (1u << lane_id()) - 1u;
+            for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
+                const uint32_t i = i0 + tid;
+                const uint32_t key = i < ngt ? s.surv_key[i] : 0u;
+                const bool gt = key > T, tie = key == T;
+                const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
+                const uint32_t ag = warp_reserve(&s.v_emit, __popc(bg)) + __popc(bg & lt);
+                const uint32_t at = warp_reserve(&s.v_ntie, __popc(bt)) + __popc(bt & lt);
+                if (gt) put(ag, s.surv_idx[i]);
+                if (tie && at < static_cast<uint32_t>(TIECAP)) s.tie_idx[at] = s.surv_idx[i];
+            }
+            __syncthreads();
+            const uint32_t e = s.v_ntie;
+            if (e <= static_cast<uint32_t>(TIECAP)) {
+                write_ties(T, take, k - take, e);
+            } else {
+                const uint32_t cut = survivor_tie_cut(ngt, T, take);
+                if (tid == 0) s.v_ntie = 0u;
                 __syncthreads();
-                const uint32_t b1 = s.bc[0], above1 = s.bc[1];
-                if (tid < 256) s.hwin[0][tid] = 0u;
-                if (b1 < 255u) {
-                    T = c + 1u + b1;
-                    take = k - above1;
-                } else {
-                    uint32_t smax = 0;
-                    for (uint32_t i = tid; i < ngt; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
-                    smax = __reduce_max_sync(0xFFFFFFFFu, smax);
-                    if (lane_id() == 0) atomicMax(&s.v_smax, smax);
-                    __syncthreads();
-                    uint32_t a2;
-                    T = survivor_select(ngt, c + 1u, s.v_smax, k, a2);
-                    take = k - a2;
-                }
-                clk.stop(p, TOPK_CNT_CYC_EXACT);
-                clk.start(p);
-                // Keys > T, then the take lowest-index ties at T.
-                if (tid == 0) {
-                    s.v_emit = 0u;
-                    s.v_ntie = 0u;
-                }
-                __syncthreads();
-                const uint32_t lt = (1u << lane_id()) - 1u;
                 for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
                     const uint32_t i = i0 + tid;
-                    const uint32_t key = i < ngt ? s.surv_key[i] : 0u;
-                    const bool gt = key > T, tie = key == T;
-                    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
-                    const uint32_t ag = warp_reserve(&s.v_emit, __popc(bg)) + __popc(bg & lt);
-                    const uint32_t at = warp_reserve(&s.v_ntie, __popc(bt)) + __popc(bt & lt);
-                    if (gt) put(ag, s.surv_idx[i]);
-                    if (tie && at < static_cast<uint32_t>(TIECAP)) s.tie_idx[at] = s.surv_idx[i];
+                    const bool sel = i < ngt && s.surv_key[i] == T && s.surv_idx[i] <= cut;
+                    const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
+                    const uint32_t at = warp_reserve(&s.v_ntie, __popc(b)) + __popc(b & lt);
+                    if (sel) put(k - take + at, s.surv_idx[i]);
                 }
-                __syncthreads();
-                const uint32_t e = s.v_ntie;
-                if (e <= static_cast<uint32_t>(TIECAP)) {
-                    write_ties(T, take, k - take, e);
-                } else {
-                    const uint32_t cut = survivor_tie_cut(ngt, T, take);
-                    if (tid == 0) s.v_ntie = 0u;
-                    __syncthreads();
-                    for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
-                        const uint32_t i = i0 + tid;
-                        const bool sel = i < ngt && s.surv_key[i] == T && s.surv_idx[i] <= cut;
-                        const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
-                        const uint32_t at = warp_reserve(&s.v_ntie, __popc(b)) + __popc(b & lt);
-                        if (sel) put(k - take + at, s.surv_idx[i]);
-                    }
-                }
-                __syncthreads();
-                clk.stop(p, TOPK_CNT_CYC_FINISH);
-            } else {
-                // The cut is c itself: every survivor, then the lowest-index ties.
-                T = c;
-                take = k - ngt;
-                for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
-                write_ties(c, take, ngt, neq);
             }
+            clk.stop(p, TOPK_CNT_CYC_FINISH);
             return;
         }
     }
 };
 
-__device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int64_t V) {
-    const uint32_t bytes = static_cast<uint32_t>(V * 16);
+__device__ __forceinline__ void issue_row(Smem &s, const Params &p, int32_t row, int32_t V) {
+    const uint32_t bytes = static_cast<uint32_t>(V) * 16u;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
-    mbar_expect_tx(&s.full[st], bytes);
-    bulk_load(&s.stage[st][0], src, bytes, &s.full[st]);
+    mbar_expect_tx(&s.full, bytes);
+    bulk_load(&s.stage[0], src, bytes, &s.full);
 }
 
-// The next row of this CTA (from `row` on, step `step`) that reads logits, or
-// rows; V = its valid vectors.
+// The next row of this CTA, from `row` on in steps of `step`, that reads
+// logits (p.rows when none is left); V = its valid vectors.
 __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, int32_t row, int32_t step,
-                                                    int64_t &V) {
+                                                    int32_t &V) {
     for (; row < p.rows; row += step) {
         const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
         const int32_t n = block ? (L + 7) >> 3 : L;
         if (n > p.k) {
-            V = (static_cast<int64_t>(L) + 7) >> 3;
+            V = (L + 7) >> 3;
             return row;
         }
     }
@@ -1980,21 +1955,18 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
 
     grid_dependency_wait();
     if (tid == 0) {
-        for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
+        mbar_init(&s.full, 1);
         fence_mbar_init();
         s.abort_flag = 0u;
+        s.v_smax = 0u;
     }
-    for (int i = tid; i < HBINS; i += NT) s.hist[i] = 0u;
-    if (tid < 256) s.hwin[0][tid] = s.hwin[1][tid] = 0u;
+    for (int i = tid; i < 4 * 256; i += NT) (&s.hs[0][0])[i] = 0u;
     __syncthreads();
-    int32_t feed_row = 0;
+    int32_t feed_row = p.rows;
     if (tid == 0) {
-        int64_t V;
+        int32_t V;
         feed_row = next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
-        for (int i = 0; i < NSTAGE && feed_row < p.rows; ++i) {
-            issue_row(s, i, p, feed_row, V);
-            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
-        }
+        if (feed_row < p.rows) issue_row(s, p, feed_row, V);
     }
 
     Row<M> r(s, p);
@@ -2011,38 +1983,38 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
         }
         r.row = row;
         r.L = L;
-        r.V = (static_cast<int64_t>(L) + 7) >> 3;
-        const int st = static_cast<int>(seq & (NSTAGE - 1));
+        r.V = (L + 7) >> 3;
         PhaseClock clk;
         clk.start(p);
-        mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+        mbar_wait(&s.full, seq & 1u, &s.abort_flag);
         clk.stop(p, TOPK_CNT_CYC_WAIT);
         count_event(p, TOPK_CNT_ROUNDS);
+        const int lanes = L & 7;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int pos = j * NT + tid;
-            const int64_t v = pos;
-            r.raw[j] = pos < r.V ? s.stage[st][pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
-            if (!M::BLOCK && v == r.V - 1 && (L & 7)) {
+            r.raw[j] = pos < r.V ? s.stage[pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+            if (!M::BLOCK && pos == r.V - 1 && lanes) {
                 // Lanes past the valid length carry no element.
                 uint32_t w[4] = {r.raw[j].x, r.raw[j].y, r.raw[j].z, r.raw[j].w};
 #pragma unroll
                 for (int h = 0; h < 8; ++h)
-                    if (h >= (L & 7))
+                    if (h >= lanes)
                         w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
                                     ((h & 1) ? 0x80000000u : 0x00008000u);
                 r.raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            r.ek[j] = (M::BLOCK && pos < r.V) ? BlockMode::key(r.raw[j], v, r.V) : 0u;
+            r.ek[j] = (M::BLOCK && pos < r.V) ? BlockMode::key(r.raw[j], pos, r.V) : 0u;
         }
         ++seq;
-        __syncthreads();  // the stage is in registers: hand it back to the ring
+        __syncthreads();  // the row is in registers: the stage takes the next row
         if (tid == 0 && feed_row < p.rows) {
-            int64_t V;
-            next_loaded_row(p, M::BLOCK, feed_row, step, V);
-            fence_proxy_async();
-            issue_row(s, st, p, feed_row, V);
+            int32_t V;
             feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+            if (feed_row < p.rows) {
+                fence_proxy_async();
+                issue_row(s, p, feed_row, V);
+            }
         }
         clk.start(p);
         r.select();

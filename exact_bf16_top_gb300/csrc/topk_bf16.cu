@@ -1449,20 +1449,25 @@ constexpr int NT = 256;
 constexpr int NW = NT / 32;
 constexpr int NV = 8;                        // vectors per thread
 constexpr int NTILE = NT * NV;               // 2048 vectors
+constexpr int NSTAGE = 2;
 constexpr int SURV_CAP = 4096;
+constexpr int REP_CAP = 4096;                // stored representatives (groups of >= 4 logits)
+constexpr int QN = 32 * NV;                  // queue entries of one warp
 
 struct alignas(128) Smem {
-    uint4 stage[NTILE];                      // the row, until it is in registers
+    uint4 stage[NSTAGE][NTILE];
     uint32_t surv_idx[SURV_CAP];
     uint16_t surv_key[SURV_CAP];
-    uint32_t hs[4][256];                     // [0], [1]: the cut's two passes; [2], [3]: windows
+    uint16_t rep[REP_CAP];                   // the row's representatives (0 = none)
+    uint32_t hs[4][256];                     // [0], [1]: the cut's byte passes; [2], [3]: windows
                                              // (zero between uses; also index-radix scratch)
     uint32_t tie_idx[TIECAP];
+    uint16_t queue[NW][QN];
     uint32_t red[2][NW];
     uint32_t bc[4];
     uint32_t v_ngt, v_neq, v_smax, v_emit, v_ntie;
     uint32_t abort_flag;
-    unsigned long long full;
+    unsigned long long full[NSTAGE];
 };
 
 // Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
@@ -1511,18 +1516,37 @@ template <class M>
 struct Row {
     Smem &s;
     const Params &p;
+    const uint4 *stg = nullptr;   // the row's vectors, in shared memory
     uint32_t par = 0;
     int32_t row = 0, L = 0, V = 0;
     uint32_t k = 0;
-    uint4 raw[NV];     // this thread's vectors j * NT + threadIdx.x (lanes without an element: 0x8000)
-    uint32_t ek[NV];   // block mode: their element keys
 
     __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
-    __device__ __forceinline__ int pos_of(int j) const { return j * NT + static_cast<int>(threadIdx.x); }
+    // Vector at position pos: lanes without an element read as 0x8000 (a
+    // negative value no cut can select and no group maximum prefers).
+    __device__ __forceinline__ uint4 vec(int pos) const {
+        if (pos >= V) return make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+        uint4 r = stg[pos];
+        if (!M::BLOCK && pos == V - 1 && (L & 7)) {
+            const int lanes = L & 7;
+            uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h >= lanes)
+                    w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
+                                ((h & 1) ? 0x80000000u : 0x00008000u);
+            r = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        return r;
+    }
 
-    __device__ __forceinline__ void clean(int j, uint32_t (&ck)[4]) const {
-        if (pos_of(j) < V) M::clean(raw[j], pos_of(j), V, L, ck);
+    __device__ __forceinline__ uint32_t bkey(int pos) const {
+        return pos < V ? BlockMode::key(stg[pos], pos, V) : 0u;
+    }
+
+    __device__ __forceinline__ void clean(int pos, uint32_t (&ck)[4]) const {
+        if (pos < V) M::clean(stg[pos], pos, V, L, ck);
         else ck[0] = ck[1] = ck[2] = ck[3] = 0u;
     }
 
@@ -1530,76 +1554,138 @@ struct Row {
         p.out[static_cast<int64_t>(row) * k + slot] = transform(p, row, static_cast<int32_t>(idx));
     }
 
-    // Representatives of groups of g elements of this thread (token: g
-    // logits, within a vector for g <= 8, else whole vectors; block: g blocks),
-    // each fed to f (0 = none).
-    template <class F>
-    __device__ __forceinline__ void reps(uint32_t g, F &&f) const {
+    // Representatives of groups of G elements of this thread's vectors
+    // j * NT + tid (token: G logits, within a vector for G <= 8, else whole
+    // vectors; block: G blocks), fed to f(slot, key) in a fixed slot order.
+    template <int G, class F>
+    __device__ __forceinline__ void reps(F &&f) const {
+        const int tid = threadIdx.x;
         if constexpr (M::BLOCK) {
-            uint32_t acc = 0;
 #pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                acc = max(acc, ek[j]);
-                if (((j + 1) & (g - 1u)) == 0u) {
-                    f(acc);
-                    acc = 0;
-                }
+            for (int j = 0; j < NV; j += G) {
+                uint32_t acc = 0;
+#pragma unroll
+                for (int i = 0; i < G; ++i) acc = max(acc, bkey((j + i) * NT + tid));
+                f((j / G) * NT + tid, acc);
             }
-        } else if (g == 1u) {
+        } else if constexpr (G == 4) {
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                uint32_t ck[4];
-                clean(j, ck);
-#pragma unroll
-                for (int h = 0; h < 8; ++h) f(key_at<M>(ck, h));
-            }
-        } else if (g == 2u) {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                f(rep_key(smax_halves(raw[j].x), 1u));
-                f(rep_key(smax_halves(raw[j].y), 1u));
-                f(rep_key(smax_halves(raw[j].z), 1u));
-                f(rep_key(smax_halves(raw[j].w), 1u));
-            }
-        } else if (g == 4u) {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                f(rep_key(smax_halves(smax2(raw[j].x, raw[j].y)), 1u));
-                f(rep_key(smax_halves(smax2(raw[j].z, raw[j].w)), 1u));
+                const uint4 r = vec(j * NT + tid);
+                f((2 * j) * NT + tid, rep_key(smax_halves(smax2(r.x, r.y)), 1u));
+                f((2 * j + 1) * NT + tid, rep_key(smax_halves(smax2(r.z, r.w)), 1u));
             }
         } else {
-            const uint32_t per = g >> 3;  // whole vectors per group: 1, 2, 4 or 8
-            uint32_t acc = 0x80008000u;
+            constexpr int PER = G / 8;  // whole vectors per group
 #pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                acc = smax2(acc, vec_smax(raw[j]));
-                if ((static_cast<uint32_t>(j) + 1u) % per == 0u) {
-                    f(rep_key(smax_halves(acc), 1u));
-                    acc = 0x80008000u;
-                }
+            for (int j = 0; j < NV; j += PER) {
+                uint32_t acc = vec_smax(vec(j * NT + tid));
+#pragma unroll
+                for (int i = 1; i < PER; ++i) acc = smax2(acc, vec_smax(vec((j + i) * NT + tid)));
+                f((j / PER) * NT + tid, rep_key(smax_halves(acc), 1u));
+            }
+        }
+    }
+
+    // The exact k-th largest representative of groups of G: high byte over the
+    // representatives as they are formed (and stored), low byte over the
+    // stored ones. False when there are fewer than k representatives.
+    template <int G>
+    __device__ __forceinline__ bool rep_cut(uint32_t &c) {
+        constexpr int NREP = (M::BLOCK ? NV / G : (G >= 8 ? NV * 8 / G : NV * 2)) * NT;
+        static_assert(NREP <= REP_CAP, "representatives do not fit");
+        reps<G>([&](int slot, uint32_t key) {
+            s.rep[slot] = static_cast<uint16_t>(key);
+            agg_add(s.hs[0], key >> 8, key != 0u);
+        });
+        __syncthreads();
+        warp0_find(s, s.hs[0], k);
+        __syncthreads();
+        const uint32_t hb = s.bc[0], habove = s.bc[1], nreps = s.bc[2];
+        if (nreps < k) return false;
+#pragma unroll
+        for (int i = threadIdx.x; i < NREP; i += NT) {
+            const uint32_t key = s.rep[i];
+            agg_add(s.hs[1], key & 0xFFu, key != 0u && (key >> 8) == hb);
+        }
+        __syncthreads();
+        warp0_find(s, s.hs[1], k - habove);
+        __syncthreads();
+        c = (hb << 8) | s.bc[0];
+        return true;
+    }
+
+    // The exact path's cut: every candidate key is its own representative.
+    __device__ bool exact_cut(uint32_t &c) {
+        const int tid = threadIdx.x;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) {
+                const uint32_t key = key_at<M>(ck, h);
+                agg_add(s.hs[0], key >> 8, key != 0u);
+            }
+        }
+        __syncthreads();
+        warp0_find(s, s.hs[0], k);
+        __syncthreads();
+        const uint32_t hb = s.bc[0], habove = s.bc[1], nkeys = s.bc[2];
+        if (nkeys < k) return false;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) {
+                const uint32_t key = key_at<M>(ck, h);
+                agg_add(s.hs[1], key & 0xFFu, key != 0u && (key >> 8) == hb);
+            }
+        }
+        __syncthreads();
+        warp0_find(s, s.hs[1], k - habove);
+        __syncthreads();
+        c = (hb << 8) | s.bc[0];
+        return true;
+    }
+
+    __device__ __forceinline__ bool cut_for(uint32_t g, uint32_t &c) {
+        if constexpr (M::BLOCK) {
+            switch (g) {
+                case 8: return rep_cut<8>(c);
+                case 4: return rep_cut<4>(c);
+                case 2: return rep_cut<2>(c);
+                default: return exact_cut(c);
+            }
+        } else {
+            switch (g) {
+                case 64: return rep_cut<64>(c);
+                case 32: return rep_cut<32>(c);
+                case 16: return rep_cut<16>(c);
+                case 8: return rep_cut<8>(c);
+                case 4: return rep_cut<4>(c);
+                default: return exact_cut(c);
             }
         }
     }
 
     // Every candidate of the row (at most k of them), in index order.
     __device__ void take_all() {
+        const int tid = threadIdx.x;
         uint32_t cnt = 0;
-#pragma unroll
         for (int j = 0; j < NV; ++j) {
             uint32_t ck[4];
-            clean(j, ck);
+            clean(j * NT + tid, ck);
 #pragma unroll
             for (int h = 0; h < M::KPV; ++h) cnt += key_at<M>(ck, h) != 0u;
         }
         uint32_t total;
         uint32_t at = block_scan(s, par, cnt, total) - cnt;
-#pragma unroll
         for (int j = 0; j < NV; ++j) {
             uint32_t ck[4];
-            clean(j, ck);
+            clean(j * NT + tid, ck);
 #pragma unroll
             for (int h = 0; h < M::KPV; ++h)
-                if (key_at<M>(ck, h) != 0u) put(at++, M::elem(pos_of(j), h));
+                if (key_at<M>(ck, h) != 0u) put(at++, M::elem(j * NT + tid, h));
         }
         for (uint32_t i = total + threadIdx.x; i < k; i += NT)
             p.out[static_cast<int64_t>(row) * k + i] = -1;
@@ -1623,11 +1709,9 @@ struct Row {
             return;
         }
         uint32_t before = 0;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if (before >= take) break;  // uniform
+        for (int j = 0; j < NV && before < take; ++j) {
             uint32_t ck[4];
-            clean(j, ck);
+            clean(j * NT + static_cast<int>(tid), ck);
             uint32_t eq = 0;
 #pragma unroll
             for (int h = 0; h < M::KPV; ++h) eq += key_at<M>(ck, h) == c;
@@ -1636,7 +1720,7 @@ struct Row {
 #pragma unroll
             for (int h = 0; h < M::KPV; ++h) {
                 if (key_at<M>(ck, h) == c) {
-                    if (r < take) put(first + r, M::elem(pos_of(j), h));
+                    if (r < take) put(first + r, M::elem(j * NT + static_cast<int>(tid), h));
                     ++r;
                 }
             }
@@ -1719,21 +1803,40 @@ struct Row {
     }
 
     // Survivors of cut c: keys > c to the list, keys == c counted and (while
-    // they fit) their indices kept. Per vector a bit mask of each kind, one warp
-    // scan of the thread's totals, one shared atomic per warp.
-    __device__ void survivors(uint32_t c) {
-        uint32_t gtm[NV], eqm[NV], my_gt = 0, my_eq = 0;
-        // Non-negative cut (the usual case): the surviving keys are exactly the
-        // BF16 bits in (c - 0x8000, 0x7F80] read as signed 16-bit integers, and
-        // the ties are the bits c - 0x8000; masked lanes hold 0x8000 (negative).
-        const bool fast = !M::BLOCK && c >= 0x8000u;
+    // they fit) their indices kept. Each thread tests its vectors' maxima; the
+    // vectors that may reach c are queued per warp and worked through by all
+    // its lanes; slots come from one warp scan and one shared atomic per round.
+    template <bool FAST>
+    __device__ __forceinline__ void survivors_t(uint32_t c) {
+        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
         const int32_t cs = static_cast<int32_t>(c) - 0x8000;
+        uint32_t q = 0;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
+            const int pos = j * NT + static_cast<int>(threadIdx.x);
+            bool pass;
+            if constexpr (FAST) pass = pos < V && smax_halves(vec_smax(stg[pos])) >= cs;
+            else if constexpr (M::BLOCK) pass = bkey(pos) >= c && bkey(pos) != 0u;
+            else pass = pos < V && M::may_reach(stg[pos], 0u, c);
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
+            if (pass) s.queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(pos);
+            q += __popc(b);
+        }
+        __syncwarp();
+        for (uint32_t e0 = 0; e0 < q; e0 += 32) {
+            const uint32_t e = e0 + lane;
             uint32_t gm = 0, em = 0;
-            if (fast) {
-                if (smax_halves(vec_smax(raw[j])) >= cs) {
-                    const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+            int pos = 0;
+            uint4 r = make_uint4(0, 0, 0, 0);
+            uint32_t ck[4] = {0u, 0u, 0u, 0u};
+            if (e < q) {
+                pos = s.queue[warp][e];
+                if constexpr (FAST) {
+                    // Non-negative cut: the surviving keys are the BF16 bits in
+                    // (c - 0x8000, 0x7F80] as signed 16-bit integers, the ties
+                    // the bits c - 0x8000.
+                    r = vec(pos);
+                    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int32_t lo = static_cast<int16_t>(w[i] & 0xFFFFu);
@@ -1743,56 +1846,50 @@ struct Row {
                         em |= (lo == cs ? 1u : 0u) << (2 * i);
                         em |= (hi == cs ? 2u : 0u) << (2 * i);
                     }
-                }
-            } else if (pos_of(j) < V && M::may_reach(raw[j], ek[j], c)) {
-                uint32_t ck[4];
-                clean(j, ck);
+                } else {
+                    clean(pos, ck);
 #pragma unroll
-                for (int h = 0; h < M::KPV; ++h) {
-                    const uint32_t key = key_at<M>(ck, h);
-                    gm |= (key > c ? 1u : 0u) << h;
-                    em |= (key == c ? 1u : 0u) << h;
+                    for (int h = 0; h < M::KPV; ++h) {
+                        const uint32_t key = key_at<M>(ck, h);
+                        gm |= (key > c ? 1u : 0u) << h;
+                        em |= (key == c ? 1u : 0u) << h;
+                    }
                 }
             }
-            gtm[j] = gm;
-            eqm[j] = em;
-            my_gt += __popc(gm);
-            my_eq += __popc(em);
-        }
-        const uint32_t packed = my_gt | (my_eq << 16);
-        const uint32_t incl = warp_incl_scan(packed);
-        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-        uint32_t b0 = 0, b1 = 0;
-        if (lane_id() == 31) {
-            if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
-            if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
-        }
-        const uint32_t ex = incl - packed;
-        uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
-        uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if ((gtm[j] | eqm[j]) == 0u) continue;
-            uint32_t ck[4] = {0u, 0u, 0u, 0u};
-            if (!fast) clean(j, ck);
-            for (uint32_t m = gtm[j]; m; m &= m - 1u) {
+            const uint32_t packed = __popc(gm) | (__popc(em) << 16);
+            const uint32_t incl = warp_incl_scan(packed);
+            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t b0 = 0, b1 = 0;
+            if (lane == 31) {
+                if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
+                if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
+            }
+            const uint32_t ex = incl - packed;
+            uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
+            uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
+            for (uint32_t m = gm; m; m &= m - 1u) {
                 const int h = __ffs(m) - 1;
                 if (at < static_cast<uint32_t>(SURV_CAP)) {
                     uint32_t key;
-                    if (fast) key = half_of(raw[j], h) + 0x8000u;
-                    else if (M::BLOCK) key = ck[0];
+                    if constexpr (FAST) key = half_of(r, h) + 0x8000u;
+                    else if constexpr (M::BLOCK) key = ck[0];
                     else key = (ck[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu;
                     s.surv_key[at] = static_cast<uint16_t>(key);
-                    s.surv_idx[at] = M::elem(pos_of(j), h);
+                    s.surv_idx[at] = M::elem(pos, h);
                 }
                 ++at;
             }
-            for (uint32_t m = eqm[j]; m; m &= m - 1u) {
+            for (uint32_t m = em; m; m &= m - 1u) {
                 const int h = __ffs(m) - 1;
-                if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos_of(j), h);
+                if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos, h);
                 ++et;
             }
         }
+    }
+
+    __device__ __forceinline__ void survivors(uint32_t c) {
+        if (!M::BLOCK && c >= 0x8000u) survivors_t<!M::BLOCK>(c);
+        else survivors_t<false>(c);
     }
 
     __device__ void select() {
@@ -1803,10 +1900,17 @@ struct Row {
             take_all();
             return;
         }
-        // Group size: at least 2k representatives.
+        // Group size: at least 2k representatives (and at least 4 logits).
         uint32_t g = 1;
-        if (!p.force_direct)
-            while (g < static_cast<uint32_t>(M::BLOCK ? 8 : 64) && nE / (2u * g) >= 2u * k) g *= 2u;
+        if (!p.force_direct) {
+            if constexpr (M::BLOCK) {
+                while (g < 8u && nE / (2u * g) >= 2u * k) g *= 2u;
+            } else {
+                g = 4;
+                while (g < 64u && nE / (2u * g) >= 2u * k) g *= 2u;
+                if (nE / g < 2u * k) g = 1;  // too few groups of 4: exact path
+            }
+        }
         for (;;) {
             PhaseClock clk;
             clk.start(p);
@@ -1814,13 +1918,8 @@ struct Row {
                 s.v_ngt = 0u;
                 s.v_neq = 0u;
             }
-            // The k-th largest representative, exactly: high byte, then low byte.
-            reps(g, [&](uint32_t key) { agg_add(s.hs[0], key >> 8, key != 0u); });
-            __syncthreads();
-            warp0_find(s, s.hs[0], k);
-            __syncthreads();
-            const uint32_t hb = s.bc[0], habove = s.bc[1], nreps = s.bc[2];
-            if (nreps < k) {
+            uint32_t c = 0;
+            if (!cut_for(g, c)) {
                 if (g > 1u) {  // the representatives cannot bound the row: exact path
                     count_event(p, TOPK_CNT_TILE_UNBOUNDED);
                     g = 1u;
@@ -1831,11 +1930,6 @@ struct Row {
                 take_all();
                 return;
             }
-            reps(g, [&](uint32_t key) { agg_add(s.hs[1], key & 0xFFu, key != 0u && (key >> 8) == hb); });
-            __syncthreads();
-            warp0_find(s, s.hs[1], k - habove);
-            __syncthreads();
-            const uint32_t c = (hb << 8) | s.bc[0];
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
             survivors(c);
@@ -1924,11 +2018,11 @@ struct Row {
     }
 };
 
-__device__ __forceinline__ void issue_row(Smem &s, const Params &p, int32_t row, int32_t V) {
+__device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int32_t V) {
     const uint32_t bytes = static_cast<uint32_t>(V) * 16u;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
-    mbar_expect_tx(&s.full, bytes);
-    bulk_load(&s.stage[0], src, bytes, &s.full);
+    mbar_expect_tx(&s.full[st], bytes);
+    bulk_load(&s.stage[st][0], src, bytes, &s.full[st]);
 }
 
 // The next row of this CTA, from `row` on in steps of `step`, that reads
@@ -1955,7 +2049,7 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
 
     grid_dependency_wait();
     if (tid == 0) {
-        mbar_init(&s.full, 1);
+        for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
         s.abort_flag = 0u;
         s.v_smax = 0u;
@@ -1966,7 +2060,10 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
     if (tid == 0) {
         int32_t V;
         feed_row = next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
-        if (feed_row < p.rows) issue_row(s, p, feed_row, V);
+        for (int i = 0; i < NSTAGE && feed_row < p.rows; ++i) {
+            issue_row(s, i, p, feed_row, V);
+            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+        }
     }
 
     Row<M> r(s, p);
@@ -1981,45 +2078,28 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
                 p.out[static_cast<int64_t>(row) * p.k + i] = i < n ? transform(p, row, i) : -1;
             continue;
         }
+        const int st = static_cast<int>(seq & (NSTAGE - 1));
         r.row = row;
         r.L = L;
         r.V = (L + 7) >> 3;
+        r.stg = s.stage[st];
         PhaseClock clk;
         clk.start(p);
-        mbar_wait(&s.full, seq & 1u, &s.abort_flag);
+        mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
         clk.stop(p, TOPK_CNT_CYC_WAIT);
         count_event(p, TOPK_CNT_ROUNDS);
-        const int lanes = L & 7;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int pos = j * NT + tid;
-            r.raw[j] = pos < r.V ? s.stage[pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
-            if (!M::BLOCK && pos == r.V - 1 && lanes) {
-                // Lanes past the valid length carry no element.
-                uint32_t w[4] = {r.raw[j].x, r.raw[j].y, r.raw[j].z, r.raw[j].w};
-#pragma unroll
-                for (int h = 0; h < 8; ++h)
-                    if (h >= lanes)
-                        w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
-                                    ((h & 1) ? 0x80000000u : 0x00008000u);
-                r.raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            r.ek[j] = (M::BLOCK && pos < r.V) ? BlockMode::key(r.raw[j], pos, r.V) : 0u;
-        }
         ++seq;
-        __syncthreads();  // the row is in registers: the stage takes the next row
-        if (tid == 0 && feed_row < p.rows) {
-            int32_t V;
-            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
-            if (feed_row < p.rows) {
-                fence_proxy_async();
-                issue_row(s, p, feed_row, V);
-            }
-        }
         clk.start(p);
         r.select();
-        __syncthreads();
+        __syncthreads();  // every thread is done with this stage
         clk.stop(p, TOPK_CNT_CYC_SELECT);
+        if (tid == 0 && feed_row < p.rows) {
+            int32_t V;
+            next_loaded_row(p, M::BLOCK, feed_row, step, V);
+            fence_proxy_async();
+            issue_row(s, st, p, feed_row, V);
+            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+        }
     }
 }
 

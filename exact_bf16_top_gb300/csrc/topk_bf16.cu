@@ -1453,6 +1453,7 @@ constexpr int NSTAGE = 2;
 constexpr int SURV_CAP = 4096;
 constexpr int REP_CAP = 4096;                // stored representatives (groups of >= 4 logits)
 constexpr int QN = 32 * NV;                  // queue entries of one warp
+constexpr int TAB_CAP = 2 * NT;              // page ids of a row staged in shared memory
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
@@ -1463,9 +1464,11 @@ struct alignas(128) Smem {
                                              // (zero between uses; also index-radix scratch)
     uint32_t tie_idx[TIECAP];
     uint16_t queue[NW][QN];
+    int32_t tab[TAB_CAP];
     uint32_t red[2][NW];
     uint32_t bc[4];
-    uint32_t v_ngt, v_neq, v_smax, v_emit, v_ntie;
+    uint32_t v_cnt[2][2];                    // survivor counts {> cut, == cut}, by row parity
+    uint32_t v_smax, v_emit, v_ntie;
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
 };
@@ -1520,6 +1523,9 @@ struct Row {
     uint32_t par = 0;
     int32_t row = 0, L = 0, V = 0;
     uint32_t k = 0;
+    uint32_t guess = 0;   // the cut carried over from this CTA's previous row (0: none)
+    uint32_t rp = 0;      // parity of the rows this CTA has selected: picks s.v_cnt[rp]
+    bool tab = false;     // the row's page ids are in s.tab
 
     __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
@@ -1551,7 +1557,10 @@ struct Row {
     }
 
     __device__ __forceinline__ void put(uint32_t slot, uint32_t idx) const {
-        p.out[static_cast<int64_t>(row) * k + slot] = transform(p, row, static_cast<int32_t>(idx));
+        int32_t v = static_cast<int32_t>(idx);
+        if (tab) v = (s.tab[idx >> p.page_shift] << p.page_shift) | (v & ((1 << p.page_shift) - 1));
+        else v = transform(p, row, v);
+        p.out[static_cast<int64_t>(row) * k + slot] = v;
     }
 
     // Representatives of groups of G elements of this thread's vectors
@@ -1669,8 +1678,9 @@ struct Row {
     }
 
     // Every candidate of the row (at most k of them), in index order.
-    __device__ void take_all() {
+    __device__ void take_all(int32_t t0, int32_t t1) {
         const int tid = threadIdx.x;
+        stage_table(t0, t1);
         uint32_t cnt = 0;
         for (int j = 0; j < NV; ++j) {
             uint32_t ck[4];
@@ -1861,8 +1871,8 @@ struct Row {
             const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
             uint32_t b0 = 0, b1 = 0;
             if (lane == 31) {
-                if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_ngt, tot & 0xFFFFu);
-                if (tot >> 16) b1 = atomicAdd(&s.v_neq, tot >> 16);
+                if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_cnt[rp][0], tot & 0xFFFFu);
+                if (tot >> 16) b1 = atomicAdd(&s.v_cnt[rp][1], tot >> 16);
             }
             const uint32_t ex = incl - packed;
             uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
@@ -1887,17 +1897,48 @@ struct Row {
         }
     }
 
+    // The cut for the next row: below the k-th key T by the distance that held
+    // (ngt - k) extra survivors over [c, T], scaled to aim at about
+    // min(2k, (k + SURV_CAP) / 2) survivors on a row like this one.
+    __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t ngt) {
+        const uint32_t want = min(k, (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
+        const uint32_t d = (want * (T - c)) / (ngt - k + 1u);
+        guess = T > d + 1u ? T - max(d, 1u) : 1u;
+    }
+
     __device__ __forceinline__ void survivors(uint32_t c) {
         if (!M::BLOCK && c >= 0x8000u) survivors_t<!M::BLOCK>(c);
         else survivors_t<false>(c);
     }
 
+    // Store the page ids loaded by load_table (the caller synchronises before
+    // the first put).
+    __device__ __forceinline__ void stage_table(int32_t t0, int32_t t1) const {
+        if (tab) {
+            s.tab[threadIdx.x] = t0;
+            s.tab[threadIdx.x + NT] = t1;
+        }
+    }
+
     __device__ void select() {
         const uint32_t tid = threadIdx.x;
         const uint32_t nE = M::BLOCK ? static_cast<uint32_t>(V) : static_cast<uint32_t>(L);
+        // The row's page ids, loaded now and staged in shared memory before the
+        // first write (their latency hides behind the survivor pass).
+        int32_t t0 = 0, t1 = 0;
+        tab = false;
+        if (p.table) {
+            const uint32_t npages = (nE + (1u << p.page_shift) - 1u) >> p.page_shift;
+            if (npages <= static_cast<uint32_t>(TAB_CAP)) {
+                tab = true;
+                const int32_t *trow = p.table + static_cast<int64_t>(row) * p.table_stride;
+                if (tid < npages) t0 = __ldg(trow + tid);
+                if (tid + NT < npages) t1 = __ldg(trow + tid + NT);
+            }
+        }
         if (nE <= k) {
             count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-            take_all();
+            take_all(t0, t1);
             return;
         }
         // Group size: at least 2k representatives (and at least 4 logits).
@@ -1911,15 +1952,25 @@ struct Row {
                 if (nE / g < 2u * k) g = 1;  // too few groups of 4: exact path
             }
         }
+        // First try the previous row's cut: any c with at least k keys >= c
+        // bounds the k-th largest key from below, and the survivor pass counts
+        // exactly that; a cut that is too high or leaves too many survivors is
+        // dropped for the representatives' cut.
+        bool guessed = guess != 0u && !p.force_direct;
+        // This row counts in s.v_cnt[rp], zeroed while the previous row ran; the
+        // other pair, last read before the barrier that ended the previous row,
+        // is zeroed now for the next one. A retry zeroes its own pair, ordered
+        // before the new counts by the barriers of the representatives' cut.
+        rp ^= 1u;
+        if (tid == 0) s.v_cnt[rp ^ 1u][0] = s.v_cnt[rp ^ 1u][1] = 0u;
+        bool retry = false;
         for (;;) {
             PhaseClock clk;
             clk.start(p);
-            if (tid == 0) {
-                s.v_ngt = 0u;
-                s.v_neq = 0u;
-            }
-            uint32_t c = 0;
-            if (!cut_for(g, c)) {
+            if (tid == 0 && retry) s.v_cnt[rp][0] = s.v_cnt[rp][1] = 0u;
+            retry = true;
+            uint32_t c = guess;
+            if (!guessed && !cut_for(g, c)) {
                 if (g > 1u) {  // the representatives cannot bound the row: exact path
                     count_event(p, TOPK_CNT_TILE_UNBOUNDED);
                     g = 1u;
@@ -1927,16 +1978,26 @@ struct Row {
                     continue;
                 }
                 count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-                take_all();
+                take_all(t0, t1);
                 return;
             }
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
             survivors(c);
+            stage_table(t0, t1);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
             clk.start(p);
-            const uint32_t ngt = s.v_ngt, neq = s.v_neq;
+            const uint32_t ngt = s.v_cnt[rp][0], neq = s.v_cnt[rp][1];
+            if (guessed) {
+                if (ngt + neq < k || ngt > static_cast<uint32_t>(SURV_CAP)) {
+                    count_event(p, TOPK_CNT_GUESS_MISS);
+                    guessed = false;
+                    __syncthreads();
+                    continue;
+                }
+                count_event(p, TOPK_CNT_GUESS_HIT);
+            }
             if (ngt > static_cast<uint32_t>(SURV_CAP)) {
                 count_event(p, TOPK_CNT_TILE_OVERFLOW);
                 __syncthreads();
@@ -1947,11 +2008,12 @@ struct Row {
                 g = 1u;
                 continue;
             }
-            count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+            if (!guessed) count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
             if (ngt < k) {
                 // The cut is c itself: every survivor, then the lowest-index ties.
                 for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
                 write_ties(c, k - ngt, ngt, neq);
+                guess = c > 8u ? c - 8u : 1u;
                 clk.stop(p, TOPK_CNT_CYC_FINISH);
                 return;
             }
@@ -1984,6 +2046,7 @@ struct Row {
             }
             clk.stop(p, TOPK_CNT_CYC_EXACT);
             clk.start(p);
+            next_guess(c, T, ngt);
             // Keys > T, then the take lowest-index ties at T.
             const uint32_t lt = (1u << lane_id()) - 1u;
             for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
@@ -2053,6 +2116,7 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
         fence_mbar_init();
         s.abort_flag = 0u;
         s.v_smax = 0u;
+        s.v_cnt[0][0] = s.v_cnt[0][1] = s.v_cnt[1][0] = s.v_cnt[1][1] = 0u;
     }
     for (int i = tid; i < 4 * 256; i += NT) (&s.hs[0][0])[i] = 0u;
     __syncthreads();

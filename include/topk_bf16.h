@@ -125,6 +125,10 @@ enum {
     TOPK_CNT_CYC_CUT = 16,       /*   the representatives' cut */
     TOPK_CNT_CYC_SURVIVORS = 17, /*   the survivor pass */
     TOPK_CNT_CYC_EXACT = 18,     /*   the exact cut among survivors and the tie appends */
+    TOPK_CNT_GUESS_HIT = 19,     /* one-tile rows cut by the cut of the CTA's previous row
+                                    (checked by the exact survivor counts) */
+    TOPK_CNT_GUESS_MISS = 20,    /* carried-over cuts dropped: fewer than k keys at or above
+                                    it, or more survivors than buffer room */
     TOPK_NUM_COUNTERS = 32
 };
 

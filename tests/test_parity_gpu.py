@@ -140,3 +140,16 @@ def test_strided_logits_and_nondefault_stream():
         out = tk.select(logits[:, :30000], valid, case.k, width=case.width)
     s.synchronize()
     assert_same_sets(out.cpu().numpy(), run_oracle(case))
+
+
+@pytest.mark.parametrize("mode,width,k", [(W.TOKEN, 8192, 512), (W.BLOCK8, 16384, 128)])
+def test_carried_cut_hits_and_misses(mode, width, k):
+    """Rows whose distribution shifts between runs: the cut a CTA carries from
+    one row to the next is kept on alike rows and dropped on the others, and
+    every row is still exact."""
+    case = W.shifting_rows(5, width=width, k=k, mode=mode)
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    assert_same_sets(run_gpu(case, counters=counters), run_oracle(case), case.name)
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["guess_hit"] > 0 and c["guess_miss"] > 0, c
+    assert tk.plan(case.rows, case.width, case.k, case.mode)["variant"] == "one-tile"

@@ -272,3 +272,24 @@ def ragged_case(seed: int, rows: int, width: int, row_stride: int, k: int, mode:
         table = permuted_table(rng, rows, n_width)
     return Case(f"ragged {rows}x{width}/{row_stride} k{k} mode{mode}", logits, width, valid, k,
                 mode, table)
+
+
+def shifting_rows(seed: int, rows: int = 3000, width: int = 8192, k: int = 512,
+                  mode: int = TOKEN, run: int = 700) -> Case:
+    """Runs of `run` rows that share a value distribution, the distribution
+    changing from run to run: N(0,1); 4 N(0,1) - 20 (every value negative);
+    N(0,1) / 4; N(0,1) with every 13th row a short one (valid length k / 2 in
+    token mode, 4k logits in block mode); then around again. A CTA that walks
+    rows in a fixed stride meets long runs of alike rows and the changes
+    between them."""
+    rng = rng_for(seed)
+    x = rng.standard_normal(size=(rows, width), dtype=np.float32)
+    kind = (np.arange(rows) // run) % 4
+    x[kind == 1] = 4.0 * x[kind == 1] - 20.0
+    x[kind == 2] *= 0.25
+    valid = np.full(rows, width, np.int32)
+    short = (kind == 3) & (np.arange(rows) % 13 == 0)
+    valid[short] = k // 2 if mode == TOKEN else 4 * k
+    n_width = width if mode == TOKEN else -(-width // 8)
+    return Case(f"shifting {rows}x{width} k{k} mode{mode}", to_bf16_bits(x), width, valid, k,
+                mode, permuted_table(rng, rows, n_width))

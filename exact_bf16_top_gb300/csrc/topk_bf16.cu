@@ -44,6 +44,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -86,8 +87,8 @@ struct alignas(128) Smem {
     uint4 stage[NSTAGE][TILE_VEC];           // streamed logits
     uint32_t buf_idx[CAP];                   // candidate buffer (any order)
     uint16_t buf_key[CAP];
-    uint32_t hist[HBINS];                    // 12-bit histogram (zero between uses)
-    uint32_t hwin[4][256];                   // window histograms (zero between uses)
+    alignas(16) uint32_t hist[HBINS];        // 12-bit histogram (zero between uses)
+    alignas(16) uint32_t hwin[4][256];       // window histograms (zero between uses)
     uint32_t h_merge[2][256];                // this CTA's merge histograms (peers read them)
     uint32_t m_all[256];                     // merge: counts over the cluster
     uint32_t m_pre[2][256];                  // merge: counts over lower-ranked CTAs
@@ -1457,21 +1458,24 @@ constexpr int TAB_CAP = 2 * NT;              // page ids of a row staged in shar
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
-    uint32_t surv_idx[SURV_CAP];
-    uint16_t surv_key[SURV_CAP];
+    uint32_t surv_idx[SURV_CAP + 4];         // + a spare slot for writes past the end
+    uint16_t surv_key[SURV_CAP + 8];
     uint16_t rep[REP_CAP];                   // the row's representatives (0 = none)
-    uint32_t hs[4][256];                     // [0], [1]: the cut's byte passes; [2], [3]: windows
-                                             // (zero between uses; also index-radix scratch)
+    alignas(16) uint32_t hs[4][256];         // [0], [1]: the cut's byte passes (zero between
+                                             // uses); [2 + row parity]: the row's window
     uint32_t tie_idx[TIECAP];
     uint16_t queue[NW][QN];
     int32_t tab[TAB_CAP];
     uint32_t red[2][NW];
     uint32_t bc[4];
-    uint32_t v_cnt[2][2];                    // survivor counts {> cut, == cut}, by row parity
-    uint32_t v_smax, v_emit, v_ntie;
+    uint32_t v_cnt[2];                       // survivor counts, by row parity
+    uint32_t v_smax, v_ntie;
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
 };
+
+// Histograms are read and written as 16-byte vectors; stages are bulk-copy targets.
+static_assert(offsetof(Smem, hs) % 16 == 0 && offsetof(Smem, stage) % 128 == 0, "shared layout");
 
 // Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
 // warp (a crowded bin would otherwise serialise the atomics of the whole warp).
@@ -1519,32 +1523,39 @@ template <class M>
 struct Row {
     Smem &s;
     const Params &p;
-    const uint4 *stg = nullptr;   // the row's vectors, in shared memory
+    uint4 *stg = nullptr;         // the row's vectors, in shared memory
     uint32_t par = 0;
     int32_t row = 0, L = 0, V = 0;
+    int32_t *orow = nullptr;      // the row's k output slots
     uint32_t k = 0;
     uint32_t guess = 0;   // the cut carried over from this CTA's previous row (0: none)
-    uint32_t rp = 0;      // parity of the rows this CTA has selected: picks s.v_cnt[rp]
+    uint32_t rp = 0;      // parity of the rows this CTA has selected
     bool tab = false;     // the row's page ids are in s.tab
 
     __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
     // Vector at position pos: lanes without an element read as 0x8000 (a
-    // negative value no cut can select and no group maximum prefers).
+    // negative value no cut can select and no group maximum prefers). The
+    // row's last vector is masked in place by mask_tail.
     __device__ __forceinline__ uint4 vec(int pos) const {
         if (pos >= V) return make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
-        uint4 r = stg[pos];
-        if (!M::BLOCK && pos == V - 1 && (L & 7)) {
-            const int lanes = L & 7;
-            uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        return stg[pos];
+    }
+
+    // Token mode: overwrite the lanes of the last vector past the valid length
+    // with 0x8000, by the thread that owns that position (every later reader of
+    // it is that thread or, after a warp barrier, its warp).
+    __device__ __forceinline__ void mask_tail() const {
+        if (M::BLOCK || (L & 7) == 0 || static_cast<int>(threadIdx.x) != (V - 1) % NT) return;
+        const int lanes = L & 7;
+        const uint4 r = stg[V - 1];
+        uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-                if (h >= lanes)
-                    w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
-                                ((h & 1) ? 0x80000000u : 0x00008000u);
-            r = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        return r;
+        for (int h = 0; h < 8; ++h)
+            if (h >= lanes)
+                w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
+                            ((h & 1) ? 0x80000000u : 0x00008000u);
+        stg[V - 1] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 
     __device__ __forceinline__ uint32_t bkey(int pos) const {
@@ -1560,7 +1571,7 @@ struct Row {
         int32_t v = static_cast<int32_t>(idx);
         if (tab) v = (s.tab[idx >> p.page_shift] << p.page_shift) | (v & ((1 << p.page_shift) - 1));
         else v = transform(p, row, v);
-        p.out[static_cast<int64_t>(row) * k + slot] = v;
+        orow[slot] = v;
     }
 
     // Representatives of groups of G elements of this thread's vectors
@@ -1698,7 +1709,7 @@ struct Row {
                 if (key_at<M>(ck, h) != 0u) put(at++, M::elem(j * NT + tid, h));
         }
         for (uint32_t i = total + threadIdx.x; i < k; i += NT)
-            p.out[static_cast<int64_t>(row) * k + i] = -1;
+            orow[i] = -1;
     }
 
     // The take lowest-index elements equal to c, written at out[first + rank].
@@ -1746,9 +1757,9 @@ struct Row {
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         const uint32_t mask = (1u << shift) - 1u;
         for (uint32_t i = tid; i < n; i += NT)
-            atomicAdd(&s.hs[3][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
+            atomicAdd(&s.hs[0][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
         __syncthreads();
-        warp0_find(s, s.hs[3], q);
+        warp0_find(s, s.hs[0], q);
         __syncthreads();
         const uint32_t b1 = s.bc[0], a1 = s.bc[1];
         __syncthreads();
@@ -1758,10 +1769,10 @@ struct Row {
         }
         for (uint32_t i = tid; i < n; i += NT) {
             const uint32_t o = static_cast<uint32_t>(s.surv_key[i]) - lo;
-            if ((o >> shift) == b1) atomicAdd(&s.hs[3][o & mask], 1u);
+            if ((o >> shift) == b1) atomicAdd(&s.hs[0][o & mask], 1u);
         }
         __syncthreads();
-        warp0_find(s, s.hs[3], q - a1);
+        warp0_find(s, s.hs[0], q - a1);
         __syncthreads();
         const uint32_t b2 = s.bc[0], a2 = s.bc[1];
         __syncthreads();
@@ -1769,150 +1780,185 @@ struct Row {
         return lo + (b1 << shift) + b2;
     }
 
-    // The q-th smallest index among survivors with key T (more than TIECAP of
-    // them): radix select over 10-bit digits, in the 1024 words of s.hs.
-    __device__ uint32_t survivor_tie_cut(uint32_t n, uint32_t T, uint32_t q) {
-        const uint32_t tid = threadIdx.x;
-        uint32_t *h = &s.hs[0][0];
-        uint32_t cut = 0, need = q;
-        for (int pass = 0; pass < 2; ++pass) {
-            const int sh = pass == 0 ? 10 : 0;
-            for (uint32_t i = tid; i < n; i += NT) {
-                if (s.surv_key[i] != T) continue;
-                const uint32_t x = s.surv_idx[i];
-                if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
-                atomicAdd(&h[(x >> sh) & 1023u], 1u);
-            }
-            __syncthreads();
-            uint4 *h4 = reinterpret_cast<uint4 *>(h) + tid;  // ascending: bins [4t, 4t + 4)
-            const uint4 hv = *h4;
-            *h4 = make_uint4(0, 0, 0, 0);
-            const uint32_t v[4] = {hv.x, hv.y, hv.z, hv.w};
-            const uint32_t sum = v[0] + v[1] + v[2] + v[3];
-            uint32_t total;
-            const uint32_t incl = block_scan(s, par, sum, total);
-            uint32_t acc = incl - sum;
-            if (acc < need && need <= incl) {
-                bool done = false;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (!done && acc + v[i] >= need) {
-                        s.bc[0] = 4 * tid + i;
-                        s.bc[1] = acc;
-                        done = true;
-                    }
-                    acc += v[i];
-                }
-            }
-            __syncthreads();
-            cut |= s.bc[0] << sh;
-            need -= s.bc[1];
-            __syncthreads();
-        }
-        return cut;
-    }
-
-    // Survivors of cut c: keys > c to the list, keys == c counted and (while
-    // they fit) their indices kept. Each thread tests its vectors' maxima; the
-    // vectors that may reach c are queued per warp and worked through by all
-    // its lanes; slots come from one warp scan and one shared atomic per round.
+    // Survivors of cut c: every key >= c goes to the list, and to the window
+    // histogram hw (bin key - c, the top bin holding every key >= c + 255).
+    // Each thread tests its vectors' maxima; the vectors that may reach c are
+    // queued per warp and worked through by all its lanes; slots come from one
+    // warp scan and one shared atomic per round.
     template <bool FAST>
-    __device__ __forceinline__ void survivors_t(uint32_t c) {
+    __device__ __forceinline__ void survivors_t(uint32_t c, uint32_t *hw) {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
         const int32_t cs = static_cast<int32_t>(c) - 0x8000;
         uint32_t q = 0;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
+            if (j * NT >= V) break;
             const int pos = j * NT + static_cast<int>(threadIdx.x);
             bool pass;
             if constexpr (FAST) pass = pos < V && smax_halves(vec_smax(stg[pos])) >= cs;
-            else if constexpr (M::BLOCK) pass = bkey(pos) >= c && bkey(pos) != 0u;
+            else if constexpr (M::BLOCK) pass = bkey(pos) >= c;
             else pass = pos < V && M::may_reach(stg[pos], 0u, c);
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
             if (pass) s.queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(pos);
             q += __popc(b);
         }
         __syncwarp();
+        // Non-negative cut (FAST): the keys >= c are the BF16 bits >= c - 0x8000
+        // as signed 16-bit integers, NaN excluded (its sign bit is set first).
+        const uint32_t csm = (static_cast<uint32_t>(cs - 1) & 0xFFFFu) * 0x10001u;
         for (uint32_t e0 = 0; e0 < q; e0 += 32) {
             const uint32_t e = e0 + lane;
-            uint32_t gm = 0, em = 0;
+            uint32_t m = 0;
             int pos = 0;
             uint4 r = make_uint4(0, 0, 0, 0);
             uint32_t ck[4] = {0u, 0u, 0u, 0u};
             if (e < q) {
                 pos = s.queue[warp][e];
                 if constexpr (FAST) {
-                    // Non-negative cut: the surviving keys are the BF16 bits in
-                    // (c - 0x8000, 0x7F80] as signed 16-bit integers, the ties
-                    // the bits c - 0x8000.
-                    r = vec(pos);
+                    // Bit i (i < 4): low half of word i; bit 4 + i: its high half.
+                    r = stg[pos];
                     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+                    uint32_t u = 0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int32_t lo = static_cast<int16_t>(w[i] & 0xFFFFu);
-                        const int32_t hi = static_cast<int32_t>(w[i]) >> 16;
-                        gm |= ((lo > cs && lo <= 0x7F80) ? 1u : 0u) << (2 * i);
-                        gm |= ((hi > cs && hi <= 0x7F80) ? 2u : 0u) << (2 * i);
-                        em |= (lo == cs ? 1u : 0u) << (2 * i);
-                        em |= (hi == cs ? 2u : 0u) << (2 * i);
+                        const uint32_t x = w[i] | nan2(w[i]);
+                        const uint32_t g = smax2(x, csm) ^ csm;  // nonzero halves: x >= cs
+                        u |= ((((g & 0x7FFF7FFFu) + 0x7FFF7FFFu) | g) & 0x80008000u) >> (15 - i);
                     }
+                    m = (u & 0xFu) | ((u >> 12) & 0xF0u);
                 } else {
                     clean(pos, ck);
 #pragma unroll
-                    for (int h = 0; h < M::KPV; ++h) {
-                        const uint32_t key = key_at<M>(ck, h);
-                        gm |= (key > c ? 1u : 0u) << h;
-                        em |= (key == c ? 1u : 0u) << h;
-                    }
+                    for (int h = 0; h < M::KPV; ++h) m |= (key_at<M>(ck, h) >= c ? 1u : 0u) << h;
                 }
             }
-            const uint32_t packed = __popc(gm) | (__popc(em) << 16);
-            const uint32_t incl = warp_incl_scan(packed);
+            const uint32_t cnt = __popc(m);
+            const uint32_t incl = warp_incl_scan(cnt);
             const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t b0 = 0, b1 = 0;
-            if (lane == 31) {
-                if (tot & 0xFFFFu) b0 = atomicAdd(&s.v_cnt[rp][0], tot & 0xFFFFu);
-                if (tot >> 16) b1 = atomicAdd(&s.v_cnt[rp][1], tot >> 16);
-            }
-            const uint32_t ex = incl - packed;
-            uint32_t at = __shfl_sync(0xFFFFFFFFu, b0, 31) + (ex & 0xFFFFu);
-            uint32_t et = __shfl_sync(0xFFFFFFFFu, b1, 31) + (ex >> 16);
-            for (uint32_t m = gm; m; m &= m - 1u) {
-                const int h = __ffs(m) - 1;
-                if (at < static_cast<uint32_t>(SURV_CAP)) {
-                    uint32_t key;
-                    if constexpr (FAST) key = half_of(r, h) + 0x8000u;
-                    else if constexpr (M::BLOCK) key = ck[0];
-                    else key = (ck[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu;
-                    s.surv_key[at] = static_cast<uint16_t>(key);
-                    s.surv_idx[at] = M::elem(pos, h);
+            uint32_t base = 0;
+            if (lane == 31 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
+            uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll 1
+            for (; m; m &= m - 1u) {
+                const int bit = __ffs(m) - 1;
+                uint32_t key, idx;
+                if constexpr (FAST) {
+                    const int i = bit & 3, hi = bit >> 2;
+                    const uint32_t w = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+                    key = ((hi ? w >> 16 : w) & 0xFFFFu) + 0x8000u;
+                    idx = static_cast<uint32_t>(pos) * 8u + static_cast<uint32_t>(2 * i + hi);
+                } else if constexpr (M::BLOCK) {
+                    key = ck[0];
+                    idx = static_cast<uint32_t>(pos);
+                } else {
+                    const int i = bit >> 1;
+                    const uint32_t w = i == 0 ? ck[0] : i == 1 ? ck[1] : i == 2 ? ck[2] : ck[3];
+                    key = (bit & 1) ? (w >> 16) : (w & 0xFFFFu);
+                    idx = static_cast<uint32_t>(pos) * 8u + static_cast<uint32_t>(bit);
                 }
+                // Past the list's end (the count then exceeds it and the pass is
+                // redone or replaced) writes go to the spare slot.
+                const uint32_t slot = min(at, static_cast<uint32_t>(SURV_CAP));
+                s.surv_key[slot] = static_cast<uint16_t>(key);
+                s.surv_idx[slot] = idx;
+                atomicAdd(&hw[min(key - c, 255u)], 1u);
                 ++at;
-            }
-            for (uint32_t m = em; m; m &= m - 1u) {
-                const int h = __ffs(m) - 1;
-                if (et < static_cast<uint32_t>(TIECAP)) s.tie_idx[et] = M::elem(pos, h);
-                ++et;
             }
         }
     }
 
+    __device__ __forceinline__ void survivors(uint32_t c, uint32_t *hw) {
+        if (!M::BLOCK && c >= 0x8000u) survivors_t<!M::BLOCK>(c, hw);
+        else survivors_t<false>(c, hw);
+    }
+
+    // Warp 0: the bin b of window histogram h that holds the q-th largest key,
+    // the count above it and the count in it, to s.bc; every bin from b up
+    // becomes a cursor, the count of the bins above it (the output slot of its
+    // first key). The caller's __syncthreads publishes both.
+    __device__ __forceinline__ void warp0_cursors(uint32_t *h, uint32_t q) {
+        if (threadIdx.x >= 32) return;
+        const uint32_t lane = lane_id();
+        uint4 *h4 = reinterpret_cast<uint4 *>(h + 248 - 8 * static_cast<int>(lane));
+        const uint4 a = h4[0], b = h4[1];
+        const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum += v[i];
+        const uint32_t incl = warp_incl_scan(sum);
+        uint32_t acc = incl - sum, cur[8], bin = 0, above = 0, cnt = 0;
+        bool mine = false;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            cur[i] = acc;
+            if (!mine && acc < q && acc + v[i] >= q) {
+                mine = true;
+                bin = 248u - 8u * lane + static_cast<uint32_t>(i);
+                above = acc;
+                cnt = v[i];
+            }
+            acc += v[i];
+        }
+        h4[0] = make_uint4(cur[0], cur[1], cur[2], cur[3]);
+        h4[1] = make_uint4(cur[4], cur[5], cur[6], cur[7]);
+        if (mine) {
+            s.bc[0] = bin;
+            s.bc[1] = above;
+            s.bc[2] = cnt;
+        }
+        if (lane == 0) s.v_ntie = 0u;
+    }
+
+    // Output of the list against window h based at `base` (bins key - base)
+    // whose bin b holds the k-th key: keys in higher bins take their bin's
+    // next slot; keys in bin b too when every one of them is taken, otherwise
+    // their indices go to s.tie_idx (while they fit) to be ranked.
+    __device__ __forceinline__ void emit(uint32_t n, uint32_t *h, uint32_t base, uint32_t b, bool all_ties) {
+        for (uint32_t i = threadIdx.x; i < n; i += NT) {
+            const uint32_t key = s.surv_key[i];
+            if (key < base) continue;
+            const uint32_t bin = min(key - base, 255u);
+            if (bin > b || (bin == b && all_ties)) {
+                put(atomicAdd(&h[bin], 1u), s.surv_idx[i]);
+            } else if (bin == b) {
+                const uint32_t t = atomicAdd(&s.v_ntie, 1u);
+                if (t < static_cast<uint32_t>(TIECAP)) s.tie_idx[t] = s.surv_idx[i];
+            }
+        }
+    }
+
+    // The exact cut c with more keys at or above it than the list holds (a
+    // crowd of ties at c): keys > c in index order, then the lowest-index ties.
+    __device__ void emit_rescan(uint32_t c) {
+        const int tid = threadIdx.x;
+        uint32_t before = 0;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+            uint32_t gt = 0;
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) gt += key_at<M>(ck, h) > c;
+            uint32_t total;
+            uint32_t r = before + block_scan(s, par, gt, total) - gt;
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h)
+                if (key_at<M>(ck, h) > c) put(r++, M::elem(j * NT + tid, h));
+            before += total;
+        }
+        write_ties(c, k - before, before, 0xFFFFFFFFu);
+    }
+
     // The cut for the next row: below the k-th key T by the distance that held
-    // (ngt - k) extra survivors over [c, T], scaled to aim at about
-    // min(2k, (k + SURV_CAP) / 2) survivors on a row like this one.
-    __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t ngt) {
-        const uint32_t want = min(k, (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
-        const uint32_t d = (want * (T - c)) / (ngt - k + 1u);
-        guess = T > d + 1u ? T - max(d, 1u) : 1u;
+    // the n - k extra keys over [c, T], scaled to aim at about
+    // k + min(k, SURV_CAP - k) / 2 keys at or above it on a row like this one.
+    __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t n) {
+        const uint32_t want = min(k / 2u, (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
+        const uint32_t d = T > c ? max((want * (T - c)) / (n - k + 1u), 1u) : 16u;
+        guess = T > d ? T - d : 1u;
     }
 
-    __device__ __forceinline__ void survivors(uint32_t c) {
-        if (!M::BLOCK && c >= 0x8000u) survivors_t<!M::BLOCK>(c);
-        else survivors_t<false>(c);
-    }
-
-    // Store the page ids loaded by load_table (the caller synchronises before
-    // the first put).
+    // Store the page ids loaded at the start of select() (the caller
+    // synchronises before the first put).
     __device__ __forceinline__ void stage_table(int32_t t0, int32_t t1) const {
         if (tab) {
             s.tab[threadIdx.x] = t0;
@@ -1936,6 +1982,7 @@ struct Row {
                 if (tid + NT < npages) t1 = __ldg(trow + tid + NT);
             }
         }
+        mask_tail();
         if (nE <= k) {
             count_event(p, TOPK_CNT_TILE_TAKE_ALL);
             take_all(t0, t1);
@@ -1954,20 +2001,26 @@ struct Row {
         }
         // First try the previous row's cut: any c with at least k keys >= c
         // bounds the k-th largest key from below, and the survivor pass counts
-        // exactly that; a cut that is too high or leaves too many survivors is
-        // dropped for the representatives' cut.
+        // exactly those keys; a cut with too few of them or more than the list
+        // holds is dropped for the representatives' cut.
         bool guessed = guess != 0u && !p.force_direct;
-        // This row counts in s.v_cnt[rp], zeroed while the previous row ran; the
-        // other pair, last read before the barrier that ended the previous row,
-        // is zeroed now for the next one. A retry zeroes its own pair, ordered
-        // before the new counts by the barriers of the representatives' cut.
+        // This row counts in s.v_cnt[rp] and s.hs[2 + rp], zeroed while the
+        // previous row ran; the other pair, last used before the barrier that
+        // ended the previous row, is zeroed now for the next one. A retry
+        // zeroes its own pair, ordered before the new counts by the barriers of
+        // the representatives' cut.
         rp ^= 1u;
-        if (tid == 0) s.v_cnt[rp ^ 1u][0] = s.v_cnt[rp ^ 1u][1] = 0u;
+        uint32_t *hw = s.hs[2 + rp];
+        s.hs[3 - rp][tid] = 0u;
+        if (tid == 0) s.v_cnt[rp ^ 1u] = 0u;
         bool retry = false;
         for (;;) {
             PhaseClock clk;
             clk.start(p);
-            if (tid == 0 && retry) s.v_cnt[rp][0] = s.v_cnt[rp][1] = 0u;
+            if (retry) {
+                hw[tid] = 0u;
+                if (tid == 0) s.v_cnt[rp] = 0u;
+            }
             retry = true;
             uint32_t c = guess;
             if (!guessed && !cut_for(g, c)) {
@@ -1983,97 +2036,75 @@ struct Row {
             }
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
-            survivors(c);
+            survivors(c, hw);
             stage_table(t0, t1);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
             clk.start(p);
-            const uint32_t ngt = s.v_cnt[rp][0], neq = s.v_cnt[rp][1];
-            if (guessed) {
-                if (ngt + neq < k || ngt > static_cast<uint32_t>(SURV_CAP)) {
+            const uint32_t n = s.v_cnt[rp];
+            if (n < k || n > static_cast<uint32_t>(SURV_CAP)) {
+                __syncthreads();
+                if (guessed) {
                     count_event(p, TOPK_CNT_GUESS_MISS);
                     guessed = false;
-                    __syncthreads();
                     continue;
                 }
-                count_event(p, TOPK_CNT_GUESS_HIT);
-            }
-            if (ngt > static_cast<uint32_t>(SURV_CAP)) {
-                count_event(p, TOPK_CNT_TILE_OVERFLOW);
-                __syncthreads();
-                if (g == 1u) {  // cannot happen: fewer than k keys exceed the exact k-th key
+                if (n < k) {  // cannot happen: the cut is at most the k-th largest key
                     if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
                     return;
                 }
-                g = 1u;
-                continue;
-            }
-            if (!guessed) count_event(p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
-            if (ngt < k) {
-                // The cut is c itself: every survivor, then the lowest-index ties.
-                for (uint32_t i = tid; i < ngt; i += NT) put(i, s.surv_idx[i]);
-                write_ties(c, k - ngt, ngt, neq);
-                guess = c > 8u ? c - 8u : 1u;
+                count_event(p, TOPK_CNT_TILE_OVERFLOW);
+                if (g > 1u) {
+                    g = 1u;
+                    continue;
+                }
+                emit_rescan(c);  // the exact cut, with a crowd of ties at it
+                guess = c > 16u ? c - 16u : 1u;
                 clk.stop(p, TOPK_CNT_CYC_FINISH);
                 return;
             }
-            // The k-th survivor: a histogram of the list over [c + 1, c + 256),
-            // its top bin also holding every larger key; a full radix select only
-            // when the k-th lies in that top bin.
-            for (uint32_t i = tid; i < ngt; i += NT)
-                atomicAdd(&s.hs[2][min(static_cast<uint32_t>(s.surv_key[i]) - c - 1u, 255u)], 1u);
+            count_event(p, guessed ? TOPK_CNT_GUESS_HIT : g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+            warp0_cursors(hw, k);
             __syncthreads();
-            warp0_find(s, s.hs[2], k);
-            if (tid == 0) {
-                s.v_emit = 0u;
-                s.v_ntie = 0u;
-            }
-            __syncthreads();
-            uint32_t T, take;
-            if (s.bc[0] < 255u) {
-                T = c + 1u + s.bc[0];
-                take = k - s.bc[1];
-            } else {
+            uint32_t b = s.bc[0], above = s.bc[1], e = s.bc[2];
+            uint32_t T = c + b, base = c;
+            uint32_t *h = hw;
+            if (b == 255u) {
+                // The k-th key is at least c + 255: find it by radix select over
+                // the list, then emit against a window based at it.
                 uint32_t smax = 0;
-                for (uint32_t i = tid; i < ngt; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
+                for (uint32_t i = tid; i < n; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
                 smax = __reduce_max_sync(0xFFFFFFFFu, smax);
                 if (lane_id() == 0) atomicMax(&s.v_smax, smax);
                 __syncthreads();
                 uint32_t a2;
-                T = survivor_select(ngt, c + 1u, s.v_smax, k, a2);
-                take = k - a2;
+                T = survivor_select(n, c, s.v_smax, k, a2);
                 if (tid == 0) s.v_smax = 0u;
+                h = s.hs[1];
+                base = T;
+                for (uint32_t i = tid; i < n; i += NT) {
+                    const uint32_t key = s.surv_key[i];
+                    if (key >= T) atomicAdd(&h[min(key - T, 255u)], 1u);
+                }
+                __syncthreads();
+                warp0_cursors(h, k);
+                __syncthreads();
+                b = s.bc[0];
+                above = s.bc[1];
+                e = s.bc[2];
             }
             clk.stop(p, TOPK_CNT_CYC_EXACT);
             clk.start(p);
-            next_guess(c, T, ngt);
-            // Keys > T, then the take lowest-index ties at T.
-            const uint32_t lt = (1u << lane_id()) - 1u;
-            for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
-                const uint32_t i = i0 + tid;
-                const uint32_t key = i < ngt ? s.surv_key[i] : 0u;
-                const bool gt = key > T, tie = key == T;
-                const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
-                const uint32_t ag = warp_reserve(&s.v_emit, __popc(bg)) + __popc(bg & lt);
-                const uint32_t at = warp_reserve(&s.v_ntie, __popc(bt)) + __popc(bt & lt);
-                if (gt) put(ag, s.surv_idx[i]);
-                if (tie && at < static_cast<uint32_t>(TIECAP)) s.tie_idx[at] = s.surv_idx[i];
-            }
-            __syncthreads();
-            const uint32_t e = s.v_ntie;
-            if (e <= static_cast<uint32_t>(TIECAP)) {
-                write_ties(T, take, k - take, e);
-            } else {
-                const uint32_t cut = survivor_tie_cut(ngt, T, take);
-                if (tid == 0) s.v_ntie = 0u;
+            const uint32_t take = k - above;
+            next_guess(c, T, n);
+            emit(n, h, base, b, take == e);
+            if (take != e) {
                 __syncthreads();
-                for (uint32_t i0 = 0; i0 < ngt; i0 += NT) {
-                    const uint32_t i = i0 + tid;
-                    const bool sel = i < ngt && s.surv_key[i] == T && s.surv_idx[i] <= cut;
-                    const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
-                    const uint32_t at = warp_reserve(&s.v_ntie, __popc(b)) + __popc(b & lt);
-                    if (sel) put(k - take + at, s.surv_idx[i]);
-                }
+                write_ties(T, take, above, e);
+            }
+            if (h != hw) {  // the cut's histogram back to zero
+                __syncthreads();
+                h[tid] = 0u;
             }
             clk.stop(p, TOPK_CNT_CYC_FINISH);
             return;
@@ -2116,7 +2147,7 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
         fence_mbar_init();
         s.abort_flag = 0u;
         s.v_smax = 0u;
-        s.v_cnt[0][0] = s.v_cnt[0][1] = s.v_cnt[1][0] = s.v_cnt[1][1] = 0u;
+        s.v_cnt[0] = s.v_cnt[1] = 0u;
     }
     for (int i = tid; i < 4 * 256; i += NT) (&s.hs[0][0])[i] = 0u;
     __syncthreads();
@@ -2147,6 +2178,7 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
         r.L = L;
         r.V = (L + 7) >> 3;
         r.stg = s.stage[st];
+        r.orow = p.out + static_cast<int64_t>(row) * p.k;
         PhaseClock clk;
         clk.start(p);
         mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);

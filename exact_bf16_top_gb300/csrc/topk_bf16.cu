@@ -88,7 +88,8 @@ struct alignas(128) Smem {
     uint32_t buf_idx[CAP];                   // candidate buffer (any order)
     uint16_t buf_key[CAP];
     alignas(16) uint32_t hist[HBINS];        // 12-bit histogram (zero between uses)
-    alignas(16) uint32_t hwin[4][256];       // window histograms (zero between uses)
+    alignas(16) uint32_t hwin[4][256];       // window histograms (zero between uses); [1]: the
+                                             // running histogram of the buffer (see filter_tile)
     uint32_t h_merge[2][256];                // this CTA's merge histograms (peers read them)
     uint32_t m_all[256];                     // merge: counts over the cluster
     uint32_t m_pre[2][256];                  // merge: counts over lower-ranked CTAs
@@ -100,6 +101,7 @@ struct alignas(128) Smem {
     uint32_t v_bufmax;                       // largest buffer key
     uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
     uint32_t v_ntie, v_emit, v_flag;
+    uint32_t v_newthr;                       // a raised threshold for the next tile (0: none)
     uint32_t shared_thr[2];                  // lower bound on the row's k-th key (max), by row parity
     uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
     uint32_t thr_snap;                       // shared_thr as every thread sees it this tile
@@ -446,6 +448,8 @@ struct Cta {
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
     uint32_t known_T = 0;    // nonzero: the buffer's top-k cut (last_take ties at it)
     uint32_t last_take = 0;
+    bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
+    uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
 
     __device__ __forceinline__ static uint32_t volatile_load(const uint32_t *x) {
         return *reinterpret_cast<const volatile uint32_t *>(x);
@@ -718,6 +722,7 @@ struct Cta {
                     if (key >= lim) {
                         s->buf_key[at] = static_cast<uint16_t>(key);
                         s->buf_idx[at] = M::elem(tile_v0 + pos, h);
+                        if (run_ok) atomicAdd(&s->hwin[1][min(key - run_lo, 255u)], 1u);
                         ++at;
                     }
                 }
@@ -1117,15 +1122,45 @@ struct Cta {
         known_T = 0;
         thr = max(thr, strict ? T + 1u : T);
         publish(T);
+        s->hwin[1][tid] = 0u;  // the running histogram is rebuilt from the kept entries
+        run_ok = false;
         __syncthreads();
         clk.stop(*p, TOPK_CNT_CYC_COMPACT);
     }
 
     // A later tile: append every key >= the threshold.
+    //
+    // The threshold also rises after every tile: the running histogram of the
+    // buffer gives its k-th largest key F, and k keys >= F precede every later
+    // key of this CTA's share, so a later key equal to F can no longer be
+    // selected (ties go to the lowest index): keep keys >= F + 1 from now on,
+    // and tell the peers that the row's k-th key is at least F.
     __device__ __forceinline__ void filter_tile(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
         known_T = 0;
+        const uint32_t raised = s->v_newthr;  // written before the barrier that ended the last tile
+        if (raised > thr) {
+            thr = raised;
+            best_T = max(best_T, raised - 1u);
+            if (raised - 1u >= run_lo + 255u) {  // past the histogram's window: rebuild it
+                s->hwin[1][tid] = 0u;
+                run_ok = false;
+                __syncthreads();
+            }
+        }
         if (s->v_count > static_cast<uint32_t>(CAP / 2) && s->v_count > 2u * k) compact(true);
+        if (!run_ok) {
+            // Every buffer key >= thr - 1 into the (zero) running histogram,
+            // before any append of this tile changes the count.
+            run_lo = thr - 1u;
+            const uint32_t n = s->v_count;
+            for (uint32_t i = tid; i < n; i += THREADS) {
+                const uint32_t key = s->buf_key[i];
+                if (key >= run_lo) atomicAdd(&s->hwin[1][min(key - run_lo, 255u)], 1u);
+            }
+            run_ok = true;
+            __syncthreads();
+        }
         uint32_t lim = effective_thr();
         const uint32_t Q = build_queue(stg, tile_v0, nv, lim);
         uint32_t next = append_keys(stg, tile_v0, Q, 0, lim);
@@ -1146,6 +1181,16 @@ struct Cta {
             compact(false);
             lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
             next = append_keys(stg, tile_v0, Q, next, lim);
+        }
+        // Every append of the tile is done (the loop ended on a barrier): warp 0
+        // finds the buffer's k-th key for the next tile's threshold.
+        if (run_ok && tid < 32) {
+            uint32_t b, above, total;
+            if (find_bin256(s->hwin[1], k, b, above, total)) {
+                const uint32_t F = run_lo + b;
+                if (tid == 0) s->v_newthr = F + 1u;
+                publish(F);
+            }
         }
     }
 
@@ -1392,10 +1437,13 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cta.best_T = 0;
         cta.known_T = 0;
         cta.slot = it & 1u;
+        cta.run_ok = false;
         if (tid == 0) {
             s.v_count = 0u;
             s.v_bufmax = 0u;
+            s.v_newthr = 0u;
         }
+        s.hwin[1][tid] = 0u;
         cta.snapshot_shared();
         __syncthreads();
         const int ntiles = static_cast<int>((v1 - v0 + TILE_VEC - 1) / TILE_VEC);

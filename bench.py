@@ -42,6 +42,12 @@ import workloads as W  # noqa: E402
 HEADLINE = dict(rows=2048, valid=16384, k=512)
 METRIC = "exact BF16 top-k rows/s (us/launch, HBM GB/s vs measured peak)"
 L2_BYTES = 129 * 1024 * 1024
+# The pages' own figure for this workload: 36 us for 2048 full 16384-wide rows,
+# k = 512, page transform included, CUDA graph with L2-rotated inputs, on a
+# B200 (sglang PR #39305, Benchmark). Another machine's number: context only.
+PAGES_US_2048 = 36.0
+KERNEL_SRC = os.path.join(ROOT, "exact_bf16_top_gb300", "csrc", "topk_bf16.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "one_tile_kernel_2048x16384_k512.md")
 
 
 def peaks():
@@ -56,13 +62,37 @@ def peaks():
 
 def algorithmic_bytes(case) -> int:
     """Bytes a launch must move: every valid logit of rows with n > k, the valid
-    lengths, the output, and one table entry per selected index when a table is
-    given."""
+    lengths, the output, and, with a table, one entry per page that can hold a
+    selected index: min(selected, pages of the row's n elements) per row."""
     rows = case.rows
     b = case.logit_bytes() + 4 * rows + 4 * rows * case.k
     if case.block_table is not None:
-        b += 4 * rows * case.k
+        L = np.clip(case.valid_len.astype(np.int64), 0, case.width)
+        n = L if case.mode == W.TOKEN else (L + 7) // 8
+        pages = -(-n // case.page_size)
+        b += int(4 * np.minimum(np.minimum(n, case.k), pages).sum())
     return int(b)
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the one-tile kernel on the headline workload,
+    from the committed ncu summary, when it was taken on the current kernel
+    source (else None)."""
+    import hashlib
+    try:
+        with open(KERNEL_SRC, "rb") as fh:
+            digest = hashlib.sha256(fh.read()).hexdigest()
+        fields = {}
+        with open(TRAFFIC_SUMMARY) as fh:
+            for line in fh:
+                if line.startswith("- ") and ":" in line:
+                    key, val = line[2:].split(":", 1)
+                    fields[key.strip()] = val.strip().strip("`")
+        if fields.get("kernel source sha256") != digest:
+            return None
+        return int(fields["dram bytes per launch"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -405,6 +435,7 @@ def main():
         t = torch.tensor([e2e_v], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MIN)
         e2e_v = float(t.item()) * world
+    copies = gc.copies
     del gc
     torch.cuda.empty_cache()
 
@@ -412,14 +443,15 @@ def main():
         "metric": METRIC, "value": round(rows_per_s, 1), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
         "us_per_launch": round(us, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u16 keys (bf16 bits), int32 indices", "data": "synthetic",
+        "vs_baseline": round(rows_per_s / (case.rows / (PAGES_US_2048 * 1e-6)), 4),
+        "dtype": "u16 keys (bf16 bits), int32 indices", "data": "synthetic",
         "config": {"workload": workload, "rows": case.rows, "width": case.width,
                    "valid_len": HEADLINE["valid"], "k": case.k, "parallelism": f"rows x{world}",
-                   "l2": f"inputs rotated over {max(4, -(-2 * L2_BYTES // (case.rows * case.width * 2)))} "
-                         f"copies (> 2x the 129 MB L2 between reuses)",
+                   "l2": f"inputs rotated over {copies} copies (> 2x the 129 MB L2 read "
+                         f"between reuses of a copy)",
                    "timing": "CUDA graph of `steps` launches, events on the replay stream"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab},
         "e2e": {"value": round(e2e_v, 1), "unit": "rows/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},

@@ -57,9 +57,7 @@ constexpr int WARPS = THREADS / 32;
 constexpr int VPT = 8;                       // 16-byte vectors per thread per tile
 constexpr int TILE_VEC = THREADS * VPT;      // 2048 vectors = 32 KiB per stage
 constexpr int QCAP = 32 * VPT;               // queue entries of one warp
-constexpr int HBINS = 4096;                  // 12-bit key bins
 constexpr int TIECAP = 256;                  // ties ranked directly
-constexpr uint32_t SUB_EXACT = 32;           // a bin fuller than this is resolved to the key
 constexpr uint32_t KEY_POS_INF = 0xFF80u;    // key of +inf
 constexpr uint32_t KEY_NEG_INF = 0x007Fu;    // key of -inf
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a stage wait gives up after 1 s
@@ -87,14 +85,12 @@ struct alignas(128) Smem {
     uint4 stage[NSTAGE][TILE_VEC];           // streamed logits
     uint32_t buf_idx[CAP];                   // candidate buffer (any order)
     uint16_t buf_key[CAP];
-    alignas(16) uint32_t hist[HBINS];        // 12-bit histogram (zero between uses)
     alignas(16) uint32_t hwin[4][256];       // window histograms (zero between uses); [1]: the
                                              // running histogram of the buffer (see filter_tile)
     uint32_t h_merge[2][256];                // this CTA's merge histograms (peers read them)
     uint32_t m_all[256];                     // merge: counts over the cluster
     uint32_t m_pre[2][256];                  // merge: counts over lower-ranked CTAs
     uint32_t tie_idx[TIECAP];                // indices of ties being ranked
-    uint32_t sub[16];                        // sub-bins of one 12-bit bin
     uint32_t red[2][WARPS];                  // block-scan warp totals
     uint32_t bc[4];                          // broadcast words
     uint32_t v_count;                        // buffer entries
@@ -430,6 +426,13 @@ __device__ __forceinline__ uint32_t warp_reserve(uint32_t *ctr, uint32_t n) {
 // routine is inlined so that the compiler sees shared-memory accesses as such
 // (out of line, they would go through generic addresses).
 
+// Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
+// warp (a crowded bin would otherwise serialise the atomics of the whole warp).
+__device__ __forceinline__ void agg_add(uint32_t *hist, uint32_t bin, bool valid) {
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
+    if (valid && lane_id() == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+}
+
 template <class M, int NSTAGE, int CAP>
 struct Cta {
     static constexpr int KPV = M::KPV;
@@ -499,43 +502,6 @@ struct Cta {
         return o;
     }
 
-    // The 12-bit bin of s->hist holding the q-th largest key: s->bc = {bin,
-    // above, count(bin)}; returns the histogram total. Zeroes s->hist.
-    __device__ __forceinline__ uint32_t find_cut4096(uint32_t q) {
-        const int t = threadIdx.x;
-        const int base = HBINS - 16 * (t + 1);  // thread 0 owns the highest 16 bins
-        uint4 *h4 = reinterpret_cast<uint4 *>(s->hist + base);
-        const uint4 a = h4[0], b = h4[1], c = h4[2], d = h4[3];
-        const uint32_t v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
-                                c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        h4[0] = z;
-        h4[1] = z;
-        h4[2] = z;
-        h4[3] = z;
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sum += v[i];
-        uint32_t total;
-        const uint32_t incl = block_incl_scan(sum, total);
-        uint32_t acc = incl - sum;
-        if (acc < q && q <= incl) {
-            bool done = false;
-#pragma unroll
-            for (int i = 15; i >= 0; --i) {
-                if (!done && acc + v[i] >= q) {
-                    s->bc[0] = static_cast<uint32_t>(base + i);
-                    s->bc[1] = acc;
-                    s->bc[2] = v[i];
-                    done = true;
-                }
-                acc += v[i];
-            }
-        }
-        __syncthreads();
-        return total;
-    }
-
     // The q-th largest of buf_key[first .. first + n), all within [lo, hi]
     // (q <= n): radix select over bins relative to lo, one pass when hi - lo <
     // 256, else two. T = that key, above = keys greater than it. Uses
@@ -574,7 +540,8 @@ struct Cta {
 
     // The q-th smallest index among buffer entries [0, n) whose key is T, when
     // there are more than TIECAP of them: a two-pass radix select over 10-bit
-    // digits (indices are below 2^20), in s->hist (zero on entry and exit).
+    // digits (indices are below 2^20), in the 1024 words of s->hwin (zero on
+    // entry and on exit).
     __device__ __forceinline__ uint32_t tie_radix(uint32_t n, uint32_t T, uint32_t q) {
         const int tid = threadIdx.x;
         uint32_t cut = 0, need = q;
@@ -584,10 +551,10 @@ struct Cta {
                 if (s->buf_key[i] != T) continue;
                 const uint32_t x = s->buf_idx[i];
                 if (pass == 1 && (x >> 10) != (cut >> 10)) continue;
-                atomicAdd(&s->hist[(x >> sh) & 1023u], 1u);
+                atomicAdd(&s->hwin[0][(x >> sh) & 1023u], 1u);
             }
             __syncthreads();
-            uint4 *h4 = reinterpret_cast<uint4 *>(s->hist) + tid;  // bins [4t, 4t + 4), ascending
+            uint4 *h4 = reinterpret_cast<uint4 *>(&s->hwin[0][0]) + tid;  // bins [4t, 4t + 4), ascending
             const uint4 hv = *h4;
             *h4 = make_uint4(0, 0, 0, 0);
             const uint32_t v[4] = {hv.x, hv.y, hv.z, hv.w};
@@ -731,17 +698,15 @@ struct Cta {
         return Q;
     }
 
-    // Feed the tile's group representatives to the 12-bit histogram (bin ==
-    // ALL) or to the 16 sub-bins of one 12-bit bin. A representative is one
-    // element of a group of g logits (token) or g blocks (block), with key >=
-    // thr, or nothing; g = 1 feeds every candidate key.
-    __device__ __forceinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t bin) {
-        uint32_t *hist = s->hist;
-        uint32_t *sub = s->sub;
+    // Feed the tile's group representatives, as keys, to the high-byte
+    // histogram s->hwin[2] (hb == ALL), or those whose high byte is hb to the
+    // low-byte histogram s->hwin[3]. A representative is one element of a group
+    // of g logits (token) or g blocks (block), with key >= thr, or nothing;
+    // g = 1 feeds every candidate key. Every lane of a warp feeds together.
+    __device__ __forceinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t hb) {
         auto feed = [&](uint32_t key) {
-            if (key == 0u) return;
-            if (bin == ALL) atomicAdd(&hist[key >> 4], 1u);
-            else if ((key >> 4) == bin) atomicAdd(&sub[key & 15u], 1u);
+            if (hb == ALL) agg_add(s->hwin[2], key >> 8, key != 0u);
+            else agg_add(s->hwin[3], key & 0xFFu, key != 0u && (key >> 8) == hb);
         };
         uint32_t acc = 0x80008000u;   // token: packed running maximum of a group
         uint32_t bacc = 0u;           // block: running maximum key of a group
@@ -759,21 +724,17 @@ struct Cta {
             } else {
                 const bool usable = pos < nv && !(v == V - 1 && (L & 7));
                 if (g == 1u) {
-                    if (pos < nv) {
-                        uint32_t ck[4];
-                        clean_at(stg, tile_v0, pos, ck);
+                    uint32_t ck[4] = {0u, 0u, 0u, 0u};
+                    if (pos < nv) clean_at(stg, tile_v0, pos, ck);
 #pragma unroll
-                        for (int h = 0; h < 8; ++h) {
-                            const uint32_t key = key_at<M>(ck, h);
-                            feed(key >= thr ? key : 0u);
-                        }
+                    for (int h = 0; h < 8; ++h) {
+                        const uint32_t key = key_at<M>(ck, h);
+                        feed(key >= thr ? key : 0u);
                     }
                 } else if (g == 4u) {
-                    if (usable) {
-                        const uint4 r = stg[pos];
-                        feed(rep_key(smax_halves(smax2(r.x, r.y)), thr));
-                        feed(rep_key(smax_halves(smax2(r.z, r.w)), thr));
-                    }
+                    const uint4 r = usable ? stg[pos] : make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+                    feed(rep_key(smax_halves(smax2(r.x, r.y)), thr));
+                    feed(rep_key(smax_halves(smax2(r.z, r.w)), thr));
                 } else {
                     if (usable) acc = smax2(acc, vec_smax(stg[pos]));
                     if ((static_cast<uint32_t>(j) + 1u) % per == 0u) {
@@ -896,15 +857,19 @@ struct Cta {
                     s->v_neq = 0u;
                     s->v_smax = 0u;
                 }
-                if (tid < 16) s->sub[tid] = 0u;
                 PhaseClock clk;
                 clk.start(*p);
                 rep_pass(stg, tile_v0, nv, g, ALL);
                 __syncthreads();
                 clk.stop(*p, TOPK_CNT_CYC_REPS);
                 clk.start(*p);
-                const uint32_t NR = find_cut4096(k);
-                if (NR < k) {
+                // The k-th largest representative, a byte at a time (every warp
+                // reads the same histograms and finds the same bins).
+                uint32_t hb, habove, NR;
+                if (!find_bin256(s->hwin[2], k, hb, habove, NR)) {
+                    __syncthreads();
+                    s->hwin[2][tid] = 0u;
+                    __syncthreads();
                     if (g > 1u) {  // the representatives cannot bound the tile: exact path
                         count_event(*p, TOPK_CNT_TILE_UNBOUNDED);
                         g = 1u;
@@ -912,24 +877,14 @@ struct Cta {
                     }
                     break;  // at most k candidates: take them all
                 }
-                const uint32_t bin = s->bc[0], above = s->bc[1], cnt = s->bc[2];
-                uint32_t c;
-                if (g == 1u || cnt > SUB_EXACT) {
-                    rep_pass(stg, tile_v0, nv, g, bin);
-                    __syncthreads();
-                    uint32_t acc = above, sb = 0;
-                    for (int i = 15; i >= 0; --i) {
-                        const uint32_t v = s->sub[i];
-                        if (acc + v >= k) {
-                            sb = static_cast<uint32_t>(i);
-                            break;
-                        }
-                        acc += v;
-                    }
-                    c = (bin << 4) | sb;
-                } else {
-                    c = max(bin << 4, thr - 1u);  // a lower bound on the k-th representative
-                }
+                rep_pass(stg, tile_v0, nv, g, hb);
+                __syncthreads();
+                uint32_t lb, labove, ltotal;
+                find_bin256(s->hwin[3], k - habove, lb, labove, ltotal);
+                const uint32_t c = (hb << 8) | lb;
+                __syncthreads();  // both histograms read: zero them (survivors ends on a barrier)
+                s->hwin[2][tid] = 0u;
+                s->hwin[3][tid] = 0u;
                 clk.stop(*p, TOPK_CNT_CYC_CUT);
                 clk.start(*p);
                 survivors(stg, tile_v0, nv, c, first, room);
@@ -1109,6 +1064,10 @@ struct Cta {
         __syncthreads();
         const uint32_t n = s->v_count;
         if (n <= k) return;
+        // The buffer is about to change: the running histogram is dropped (its
+        // words are also the index radix's scratch), rebuilt by the next tile.
+        s->hwin[1][tid] = 0u;
+        run_ok = false;
         count_event(*p, TOPK_CNT_COMPACTIONS);
         PhaseClock clk;
         clk.start(*p);
@@ -1122,8 +1081,6 @@ struct Cta {
         known_T = 0;
         thr = max(thr, strict ? T + 1u : T);
         publish(T);
-        s->hwin[1][tid] = 0u;  // the running histogram is rebuilt from the kept entries
-        run_ok = false;
         __syncthreads();
         clk.stop(*p, TOPK_CNT_CYC_COMPACT);
     }
@@ -1196,6 +1153,8 @@ struct Cta {
 
     // C == 1: the buffer holds the row's candidates; write its top-k.
     __device__ __forceinline__ void emit_single() {
+        s->hwin[1][threadIdx.x] = 0u;  // the index radix's scratch (ordered by the barriers below)
+        run_ok = false;
         __syncthreads();
         const uint32_t n = s->v_count;
         uint32_t T = 0, take = 0;
@@ -1219,6 +1178,8 @@ struct Cta {
     __device__ __forceinline__ void merge_and_emit() {
         const int tid = threadIdx.x;
         count_event(*p, TOPK_CNT_CLUSTER_MERGES);
+        s->hwin[1][tid] = 0u;  // the index radix's scratch (compact starts on a barrier)
+        run_ok = false;
         compact(false);
         __syncthreads();
         const uint32_t n = s->v_count;
@@ -1392,7 +1353,6 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         s.thr_snap = 0u;
         s.abort_flag = 0u;
     }
-    for (int i = tid; i < HBINS; i += THREADS) s.hist[i] = 0u;
     for (int i = 0; i < 4; ++i) s.hwin[i][tid] = 0u;
     s.h_merge[0][tid] = s.h_merge[1][tid] = 0u;
     __syncthreads();
@@ -1525,12 +1485,6 @@ struct alignas(128) Smem {
 // Histograms are read and written as 16-byte vectors; stages are bulk-copy targets.
 static_assert(offsetof(Smem, hs) % 16 == 0 && offsetof(Smem, stage) % 128 == 0, "shared layout");
 
-// Add 1 for every lane with `valid`, one shared atomic per distinct bin in the
-// warp (a crowded bin would otherwise serialise the atomics of the whole warp).
-__device__ __forceinline__ void agg_add(uint32_t *hist, uint32_t bin, bool valid) {
-    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
-    if (valid && lane_id() == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
-}
 
 __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -2256,7 +2210,7 @@ struct Variant {
     int smem;
 };
 
-constexpr int WIDE_NSTAGE = 4, WIDE_CAP = 8192;
+constexpr int WIDE_NSTAGE = 2, WIDE_CAP = 4096;
 
 template <class M, int NSTAGE, int CAP>
 Variant variant() {

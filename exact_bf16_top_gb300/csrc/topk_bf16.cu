@@ -97,6 +97,7 @@ struct alignas(128) Smem {
     uint32_t v_bufmax;                       // largest buffer key
     uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
     uint32_t v_ntie, v_emit, v_flag;
+    uint32_t v_full[2];                      // a warp found the buffer full, by tile parity
     uint32_t v_newthr;                       // a raised threshold for the next tile (0: none)
     uint32_t shared_thr[2];                  // lower bound on the row's k-th key (max), by row parity
     uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
@@ -451,6 +452,7 @@ struct Cta {
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
     uint32_t known_T = 0;    // nonzero: the buffer's top-k cut (last_take ties at it)
     uint32_t last_take = 0;
+    uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full
     bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
     uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
 
@@ -696,6 +698,111 @@ struct Cta {
             }
         }
         return Q;
+    }
+
+    // Token mode, lim >= 0x8000: the keys >= lim are the non-negative values
+    // whose BF16 bits, as signed 16-bit integers, are >= lim - 0x8000 (NaN is
+    // excluded by setting its sign bit first). These are build_queue and
+    // append_keys for that case, on raw bits: no key conversion per element.
+    __device__ __forceinline__ uint32_t build_queue_fast(const uint4 *stg, int nv, int32_t cs) {
+        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+        const uint32_t lt = (1u << lane) - 1u;
+        uint32_t q = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int pos = j * THREADS + static_cast<int>(threadIdx.x);
+            const bool pass = pos < nv && smax_halves(vec_smax(stg[pos])) >= cs;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
+            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
+            q += __popc(b);
+        }
+        __syncwarp();
+        return q;
+    }
+
+    __device__ __forceinline__ uint32_t append_fast(const uint4 *stg, int64_t tile_v0, uint32_t Q,
+                                                 uint32_t from, uint32_t lim) {
+        const uint32_t lane = lane_id();
+        const int32_t cs = static_cast<int32_t>(lim) - 0x8000;
+        const uint32_t csm = (static_cast<uint32_t>(cs - 1) & 0xFFFFu) * 0x10001u;
+        for (uint32_t e0 = from; e0 < Q; e0 += 32) {
+            const uint32_t e = e0 + lane;
+            uint32_t m = 0, kmax = 0;
+            int pos = 0;
+            uint4 r = make_uint4(0, 0, 0, 0);
+            if (e < Q) {
+                pos = queued_pos(e);
+                r = stg[pos];
+                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+                uint32_t u = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t x = w[i] | nan2(w[i]);
+                    const uint32_t g = smax2(x, csm) ^ csm;  // nonzero halves: x >= cs
+                    u |= ((((g & 0x7FFF7FFFu) + 0x7FFF7FFFu) | g) & 0x80008000u) >> (15 - i);
+                }
+                m = (u & 0xFu) | ((u >> 12) & 0xF0u);  // bit i: low half of word i; bit 4 + i: high half
+                if (m) kmax = min(static_cast<uint32_t>(smax_halves(vec_smax(r)) + 0x8000), KEY_POS_INF);
+            }
+            const uint32_t cnt = __popc(m);
+            const uint32_t incl = warp_incl_scan(cnt);
+            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t base = 0, ok = 1;
+            if (lane == 0 && total) {
+                uint32_t old = volatile_load(&s->v_count);
+                for (;;) {
+                    if (old + total > static_cast<uint32_t>(CAP)) {
+                        ok = 0;
+                        break;
+                    }
+                    const uint32_t prev = atomicCAS(&s->v_count, old, old + total);
+                    if (prev == old) {
+                        base = old;
+                        break;
+                    }
+                    old = prev;
+                }
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) return e0;  // full: the caller compacts and resumes here
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+            if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
+            uint32_t at = base + incl - cnt;
+            const uint32_t idx0 = static_cast<uint32_t>(tile_v0 + pos) * 8u;
+#pragma unroll 1
+            for (; m; m &= m - 1u) {
+                const int bit = __ffs(m) - 1;
+                const int i = bit & 3, hi = bit >> 2;
+                const uint32_t w = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+                const uint32_t key = ((hi ? w >> 16 : w) & 0xFFFFu) + 0x8000u;
+                s->buf_key[at] = static_cast<uint16_t>(key);
+                s->buf_idx[at] = idx0 + static_cast<uint32_t>(2 * i + hi);
+                if (run_ok) atomicAdd(&s->hwin[1][min(key - run_lo, 255u)], 1u);
+                ++at;
+            }
+        }
+        return Q;
+    }
+
+    // Token mode: the row's last vector, when partial, gets 0x8000 (a negative
+    // value no cut selects) in the lanes past the valid length, by the thread
+    // that owns its position in this tile (its warp reads it after a warp
+    // barrier).
+    __device__ __forceinline__ void mask_tail(const uint4 *stg, int64_t tile_v0, int nv) const {
+        if (M::BLOCK || (L & 7) == 0) return;
+        const int64_t pos = V - 1 - tile_v0;
+        if (pos < 0 || pos >= nv || static_cast<int>(pos % THREADS) != static_cast<int>(threadIdx.x)) return;
+        uint4 *v = const_cast<uint4 *>(stg) + pos;
+        const int lanes = L & 7;
+        const uint4 r = *v;
+        uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+            if (h >= lanes)
+                w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
+                            ((h & 1) ? 0x80000000u : 0x00008000u);
+        *v = make_uint4(w[0], w[1], w[2], w[3]);
     }
 
     // Feed the tile's group representatives, as keys, to the high-byte
@@ -1119,25 +1226,36 @@ struct Cta {
             __syncthreads();
         }
         uint32_t lim = effective_thr();
-        const uint32_t Q = build_queue(stg, tile_v0, nv, lim);
-        uint32_t next = append_keys(stg, tile_v0, Q, 0, lim);
+        // v_full[tpar] was zeroed during the last tile; the other word, last
+        // read before the barrier that ended the last tile, is zeroed now.
+        tpar ^= 1u;
+        if (tid == 0) s->v_full[tpar ^ 1u] = 0u;
+        const bool fast = !M::BLOCK && lim >= 0x8000u && lim <= KEY_POS_INF;
+        mask_tail(stg, tile_v0, nv);
+        const uint32_t Q = fast ? build_queue_fast(stg, nv, static_cast<int32_t>(lim) - 0x8000)
+                                : build_queue(stg, tile_v0, nv, lim);
+        uint32_t next = fast ? append_fast(stg, tile_v0, Q, 0, lim) : append_keys(stg, tile_v0, Q, 0, lim);
         buf_lo = min(buf_lo, lim);
-        for (int refill = 0;; ++refill) {
-            if (tid == 0) s->v_flag = 0u;
-            __syncthreads();
-            if (next < Q && lane_id() == 0) s->v_flag = 1u;
-            __syncthreads();
-            if (s->v_flag == 0u) break;  // uniform
-            if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
-                if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
-                break;
+        if (next < Q && lane_id() == 0) s->v_full[tpar] = 1u;
+        __syncthreads();
+        if (s->v_full[tpar] != 0u) {  // uniform; rare
+            for (int refill = 0;; ++refill) {
+                if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
+                    if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+                    break;
+                }
+                // The buffer filled up mid-tile: compact it (the rest of this
+                // tile may still tie with it) and carry on.
+                count_event(*p, TOPK_CNT_REFILLS);
+                compact(false);
+                lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
+                next = fast ? append_fast(stg, tile_v0, Q, next, lim) : append_keys(stg, tile_v0, Q, next, lim);
+                if (tid == 0) s->v_flag = 0u;
+                __syncthreads();
+                if (next < Q && lane_id() == 0) s->v_flag = 1u;
+                __syncthreads();
+                if (s->v_flag == 0u) break;  // uniform
             }
-            // The buffer filled up mid-tile: compact it (the rest of this tile
-            // may still tie with it) and carry on.
-            count_event(*p, TOPK_CNT_REFILLS);
-            compact(false);
-            lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
-            next = append_keys(stg, tile_v0, Q, next, lim);
         }
         // Every append of the tile is done (the loop ended on a barrier): warp 0
         // finds the buffer's k-th key for the next tile's threshold.
@@ -1402,6 +1520,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             s.v_count = 0u;
             s.v_bufmax = 0u;
             s.v_newthr = 0u;
+            s.v_full[0] = s.v_full[1] = 0u;
         }
         s.hwin[1][tid] = 0u;
         cta.snapshot_shared();

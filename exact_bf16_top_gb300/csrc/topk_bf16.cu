@@ -98,6 +98,7 @@ struct alignas(128) Smem {
     uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
     uint32_t v_ntie, v_emit, v_flag;
     uint32_t v_full[2];                      // a warp found the buffer full, by tile parity
+    uint32_t v_arrive[2];                    // warps done appending, by tile parity
     uint32_t v_newthr;                       // a raised threshold for the next tile (0: none)
     uint32_t shared_thr[2];                  // lower bound on the row's k-th key (max), by row parity
     uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
@@ -341,6 +342,16 @@ __device__ __forceinline__ uint32_t key_at(const uint32_t (&ck)[4], int h) {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Exclusive prefix over the warp of counts in [0, 15], and their total: four
+// ballots of the count's bits instead of a shuffle scan.
+__device__ __forceinline__ uint32_t warp_excl_small(uint32_t cnt, uint32_t &total) {
+    const uint32_t lt = (1u << lane_id()) - 1u;
+    const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, cnt & 1u), b1 = __ballot_sync(0xFFFFFFFFu, cnt & 2u);
+    const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, cnt & 4u), b3 = __ballot_sync(0xFFFFFFFFu, cnt & 8u);
+    total = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2) + 8u * __popc(b3);
+    return __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt) + 8u * __popc(b3 & lt);
+}
+
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
     const uint32_t lane = lane_id();
 #pragma unroll
@@ -452,7 +463,9 @@ struct Cta {
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
     uint32_t known_T = 0;    // nonzero: the buffer's top-k cut (last_take ties at it)
     uint32_t last_take = 0;
-    uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full
+    uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full, s->v_arrive
+    uint32_t f_Q = 0, f_next = 0, f_lim = 0;  // this warp's queue, where its appends stopped, the limit
+    bool f_fast = false;
     bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
     uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
 
@@ -513,8 +526,10 @@ struct Cta {
         const int tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
-        for (uint32_t i = tid; i < n; i += THREADS)
-            atomicAdd(&s->hwin[2][window_bin(s->buf_key[first + i], lo, shift)], 1u);
+        for (uint32_t i = tid; i < n; i += THREADS) {
+            const uint32_t key = s->buf_key[first + i];
+            if (key != 0u) atomicAdd(&s->hwin[2][window_bin(key, lo, shift)], 1u);  // 0: a dead entry
+        }
         __syncthreads();
         uint32_t b1, above1, tot, T, above;
         find_bin256(s->hwin[2], q, b1, above1, tot);
@@ -524,8 +539,9 @@ struct Cta {
         } else {
             const uint32_t mask = (1u << shift) - 1u;
             for (uint32_t i = tid; i < n; i += THREADS) {
-                const uint32_t o = static_cast<uint32_t>(s->buf_key[first + i]) - lo;
-                if ((o >> shift) == b1) atomicAdd(&s->hwin[3][o & mask], 1u);
+                const uint32_t key = s->buf_key[first + i];
+                const uint32_t o = key - lo;
+                if (key != 0u && (o >> shift) == b1) atomicAdd(&s->hwin[3][o & mask], 1u);
             }
             __syncthreads();
             uint32_t b2, above2;
@@ -660,31 +676,12 @@ struct Cta {
                 cnt += key >= lim;
                 kmax = key >= lim ? max(kmax, key) : kmax;
             }
-            const uint32_t incl = warp_incl_scan(cnt);
-            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t base = 0, ok = 1;
-            if (lane == 0 && total) {
-                uint32_t old = volatile_load(&s->v_count);
-                for (;;) {
-                    if (old + total > static_cast<uint32_t>(CAP)) {
-                        ok = 0;
-                        break;
-                    }
-                    const uint32_t prev = atomicCAS(&s->v_count, old, old + total);
-                    if (prev == old) {
-                        base = old;
-                        break;
-                    }
-                    old = prev;
-                }
-            }
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) return e0;  // full: the caller compacts and resumes here
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            uint32_t total, at;
+            const uint32_t before = warp_excl_small(cnt, total);
+            if (!reserve(total, before, cnt, at)) return e0;  // full: the caller compacts and resumes here
             kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
             if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
             if (cnt) {
-                uint32_t at = base + incl - cnt;
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
                     const uint32_t key = key_at<M>(ck, h);
@@ -700,6 +697,29 @@ struct Cta {
         return Q;
     }
 
+    // Slots for a warp's `total` new entries (lane 0 adds; every lane learns
+    // the base); `at` = this lane's first slot, `before` entries of lower lanes
+    // precede it. When the buffer cannot hold them all, the warp's slots below
+    // CAP get key 0 (an entry nothing counts or selects) and false is returned:
+    // the caller compacts and resumes. Reservations only grow, so every later
+    // one fails too.
+    __device__ __forceinline__ bool reserve(uint32_t total, uint32_t before, uint32_t cnt, uint32_t &at) {
+        uint32_t base = 0;
+        if (lane_id() == 0 && total) base = atomicAdd(&s->v_count, total);
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        at = base + before;
+        if (base + total <= static_cast<uint32_t>(CAP)) return true;
+        for (uint32_t i = at; i < at + cnt && i < static_cast<uint32_t>(CAP); ++i) s->buf_key[i] = 0u;
+        return false;
+    }
+
+    // publish() from any one warp: lane r tells peer r.
+    __device__ __forceinline__ void publish_lane(uint32_t bound) {
+        const uint32_t lane = lane_id();
+        best_T = max(best_T, bound);
+        if (C > 1 && lane < C && lane != rank) red_max_peer(peer_addr(&s->shared_thr[slot], lane), bound);
+    }
+
     // Token mode, lim >= 0x8000: the keys >= lim are the non-negative values
     // whose BF16 bits, as signed 16-bit integers, are >= lim - 0x8000 (NaN is
     // excluded by setting its sign bit first). These are build_queue and
@@ -708,10 +728,15 @@ struct Cta {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
         uint32_t q = 0;
+        int32_t mx[VPT];  // every vector's maximum first: the loads issue together
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int pos = j * THREADS + static_cast<int>(threadIdx.x);
-            const bool pass = pos < nv && smax_halves(vec_smax(stg[pos])) >= cs;
+            mx[j] = pos < nv ? smax_halves(vec_smax(stg[pos])) : -32768;
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const bool pass = mx[j] >= cs;
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
             if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
             q += __popc(b);
@@ -745,30 +770,11 @@ struct Cta {
                 if (m) kmax = min(static_cast<uint32_t>(smax_halves(vec_smax(r)) + 0x8000), KEY_POS_INF);
             }
             const uint32_t cnt = __popc(m);
-            const uint32_t incl = warp_incl_scan(cnt);
-            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t base = 0, ok = 1;
-            if (lane == 0 && total) {
-                uint32_t old = volatile_load(&s->v_count);
-                for (;;) {
-                    if (old + total > static_cast<uint32_t>(CAP)) {
-                        ok = 0;
-                        break;
-                    }
-                    const uint32_t prev = atomicCAS(&s->v_count, old, old + total);
-                    if (prev == old) {
-                        base = old;
-                        break;
-                    }
-                    old = prev;
-                }
-            }
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) return e0;  // full: the caller compacts and resumes here
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            uint32_t total, at;
+            const uint32_t before = warp_excl_small(cnt, total);
+            if (!reserve(total, before, cnt, at)) return e0;  // full: the caller compacts and resumes here
             kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
             if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
-            uint32_t at = base + incl - cnt;
             const uint32_t idx0 = static_cast<uint32_t>(tile_v0 + pos) * 8u;
 #pragma unroll 1
             for (; m; m &= m - 1u) {
@@ -1169,7 +1175,7 @@ struct Cta {
     __device__ __forceinline__ void compact(bool strict) {
         const int tid = threadIdx.x;
         __syncthreads();
-        const uint32_t n = s->v_count;
+        const uint32_t n = min(s->v_count, static_cast<uint32_t>(CAP));
         if (n <= k) return;
         // The buffer is about to change: the running histogram is dropped (its
         // words are also the index radix's scratch), rebuilt by the next tile.
@@ -1201,6 +1207,8 @@ struct Cta {
     // and tell the peers that the row's k-th key is at least F.
     __device__ __forceinline__ void filter_tile(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
+        PhaseClock clk;
+        clk.start(*p);
         known_T = 0;
         const uint32_t raised = s->v_newthr;  // written before the barrier that ended the last tile
         if (raised > thr) {
@@ -1225,47 +1233,72 @@ struct Cta {
             run_ok = true;
             __syncthreads();
         }
-        uint32_t lim = effective_thr();
-        // v_full[tpar] was zeroed during the last tile; the other word, last
-        // read before the barrier that ended the last tile, is zeroed now.
+        const uint32_t lim = effective_thr();
+        // v_full[tpar] and v_arrive[tpar] were zeroed during the last tile; the
+        // other words, last read before the barrier that ended the last tile,
+        // are zeroed now for the next one.
         tpar ^= 1u;
-        if (tid == 0) s->v_full[tpar ^ 1u] = 0u;
+        if (tid == 0) {
+            s->v_full[tpar ^ 1u] = 0u;
+            s->v_arrive[tpar ^ 1u] = 0u;
+        }
         const bool fast = !M::BLOCK && lim >= 0x8000u && lim <= KEY_POS_INF;
         mask_tail(stg, tile_v0, nv);
+        clk.stop(*p, TOPK_CNT_CYC_F_PREP);
+        clk.start(*p);
         const uint32_t Q = fast ? build_queue_fast(stg, nv, static_cast<int32_t>(lim) - 0x8000)
                                 : build_queue(stg, tile_v0, nv, lim);
-        uint32_t next = fast ? append_fast(stg, tile_v0, Q, 0, lim) : append_keys(stg, tile_v0, Q, 0, lim);
+        clk.stop(*p, TOPK_CNT_CYC_F_QUEUE);
+        clk.start(*p);
+        const uint32_t next = fast ? append_fast(stg, tile_v0, Q, 0, lim) : append_keys(stg, tile_v0, Q, 0, lim);
         buf_lo = min(buf_lo, lim);
+        f_Q = Q;
+        f_next = next;
+        f_lim = lim;
+        f_fast = fast;
         if (next < Q && lane_id() == 0) s->v_full[tpar] = 1u;
-        __syncthreads();
-        if (s->v_full[tpar] != 0u) {  // uniform; rare
-            for (int refill = 0;; ++refill) {
-                if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
-                    if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
-                    break;
-                }
-                // The buffer filled up mid-tile: compact it (the rest of this
-                // tile may still tie with it) and carry on.
-                count_event(*p, TOPK_CNT_REFILLS);
-                compact(false);
-                lim = max(lim, thr);  // the buffer now holds k keys >= thr (== its lower bound)
-                next = fast ? append_fast(stg, tile_v0, Q, next, lim) : append_keys(stg, tile_v0, Q, next, lim);
-                if (tid == 0) s->v_flag = 0u;
-                __syncthreads();
-                if (next < Q && lane_id() == 0) s->v_flag = 1u;
-                __syncthreads();
-                if (s->v_flag == 0u) break;  // uniform
-            }
-        }
-        // Every append of the tile is done (the loop ended on a barrier): warp 0
-        // finds the buffer's k-th key for the next tile's threshold.
-        if (run_ok && tid < 32) {
+        clk.stop(*p, TOPK_CNT_CYC_F_APPEND);
+        clk.start(*p);
+        // The first warp done appending finds the buffer's k-th key F for the
+        // next tiles while the others still append: each count it reads is at
+        // most the number of buffer keys in its bin, so at least k buffer keys
+        // are >= F whatever it reads. (The next tile's threshold is raised to
+        // F + 1; see above.)
+        uint32_t order = 0;
+        if (lane_id() == 0) order = atomicAdd(&s->v_arrive[tpar], 1u);
+        order = __shfl_sync(0xFFFFFFFFu, order, 0);
+        if (order == 0u && run_ok) {
             uint32_t b, above, total;
             if (find_bin256(s->hwin[1], k, b, above, total)) {
                 const uint32_t F = run_lo + b;
-                if (tid == 0) s->v_newthr = F + 1u;
-                publish(F);
+                if (lane_id() == 0) s->v_newthr = F + 1u;
+                publish_lane(F);
             }
+        }
+        clk.stop(*p, TOPK_CNT_CYC_F_FIND);
+    }
+
+    // After the barrier that ends a filter tile: if a warp found the buffer
+    // full, compact it and append the rest of the tile (the rest may still tie
+    // with the buffer, so the compaction keeps keys equal to its cut).
+    __device__ __forceinline__ void finish_tile(const uint4 *stg, int64_t tile_v0) {
+        if (s->v_full[tpar] == 0u) return;  // uniform; rare
+        const int tid = threadIdx.x;
+        uint32_t next = f_next;
+        for (int refill = 0;; ++refill) {
+            if (refill == 64) {  // each refill frees >= CAP - k slots: cannot happen
+                if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+                break;
+            }
+            count_event(*p, TOPK_CNT_REFILLS);
+            compact(false);
+            const uint32_t lim = max(f_lim, thr);  // the buffer now holds k keys >= thr
+            next = f_fast ? append_fast(stg, tile_v0, f_Q, next, lim) : append_keys(stg, tile_v0, f_Q, next, lim);
+            if (tid == 0) s->v_flag = 0u;
+            __syncthreads();
+            if (next < f_Q && lane_id() == 0) s->v_flag = 1u;
+            __syncthreads();
+            if (s->v_flag == 0u) break;  // uniform
         }
     }
 
@@ -1296,6 +1329,7 @@ struct Cta {
     __device__ __forceinline__ void merge_and_emit() {
         const int tid = threadIdx.x;
         count_event(*p, TOPK_CNT_CLUSTER_MERGES);
+        if (s->v_newthr) best_T = max(best_T, s->v_newthr - 1u);  // the last tile's find
         s->hwin[1][tid] = 0u;  // the index radix's scratch (compact starts on a barrier)
         run_ok = false;
         compact(false);
@@ -1521,6 +1555,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             s.v_bufmax = 0u;
             s.v_newthr = 0u;
             s.v_full[0] = s.v_full[1] = 0u;
+            s.v_arrive[0] = s.v_arrive[1] = 0u;
         }
         s.hwin[1][tid] = 0u;
         cta.snapshot_shared();
@@ -1545,12 +1580,15 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
                 cta.filter_tile(stg, tile_v0, nv);
                 clk.stop(p, TOPK_CNT_CYC_FILTER);
             }
+            clk.start(p);
             cta.snapshot_shared();
-            __syncthreads();  // every thread is done with this stage
+            __syncthreads();  // every warp is done with this stage (but for a refill)
+            if (i > 0) cta.finish_tile(stg, tile_v0);
             if (tid == 0 && feed.row < p.rows) {
                 fence_proxy_async();
                 feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);
             }
+            clk.stop(p, TOPK_CNT_CYC_F_LOOP);
         }
         PhaseClock fin;
         fin.start(p);

@@ -129,6 +129,13 @@ enum {
                                     (checked by the exact survivor counts) */
     TOPK_CNT_GUESS_MISS = 20,    /* carried-over cuts dropped: fewer than k keys at or above
                                     it, or more survivors than buffer room */
+    /* streamed rows, later tiles, split (thread 0 of each CTA): */
+    TOPK_CNT_CYC_F_PREP = 21,    /*   threshold update, compaction, running-histogram rebuild */
+    TOPK_CNT_CYC_F_QUEUE = 22,   /*   candidate-vector queue */
+    TOPK_CNT_CYC_F_APPEND = 23,  /*   appends to the buffer */
+    TOPK_CNT_CYC_F_SYNC = 24,    /*   the tile's barrier (and any refill) */
+    TOPK_CNT_CYC_F_FIND = 25,    /*   the buffer's k-th key for the next threshold */
+    TOPK_CNT_CYC_F_LOOP = 26,    /*   end of tile: barrier and the next copy's issue */
     TOPK_NUM_COUNTERS = 32
 };
 

@@ -1611,15 +1611,20 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
 // cut -> write. Same cutoff argument as the streamed kernel.
 namespace one {
 
-constexpr int NT = 256;
-constexpr int NW = NT / 32;
-constexpr int NV = 8;                        // vectors per thread
-constexpr int NTILE = NT * NV;               // 2048 vectors
-constexpr int NSTAGE = 2;
-constexpr int SURV_CAP = 4096;
-constexpr int REP_CAP = 4096;                // stored representatives (groups of >= 4 logits)
-constexpr int QN = 32 * NV;                  // queue entries of one warp
-constexpr int TAB_CAP = 2 * NT;              // page ids of a row staged in shared memory
+// Everything of the one-tile path for a CTA of NT_ threads (256: two CTAs per
+// SM for many rows; 512: one, for rows that do not fill the SMs, where a row's
+// latency is what counts).
+template <int NT_>
+struct Tile {
+static constexpr int NT = NT_;
+static constexpr int NW = NT / 32;
+static constexpr int NV = 2048 / NT;         // vectors per thread
+static constexpr int NTILE = NT * NV;        // 2048 vectors
+static constexpr int NSTAGE = 2;
+static constexpr int SURV_CAP = 4096;
+static constexpr int REP_CAP = 4096;         // stored representatives (groups of >= 4 logits)
+static constexpr int QN = 32 * NV;           // queue entries of one warp
+static constexpr int TAB_CAP = 2 * NT;       // page ids of a row staged in shared memory
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
@@ -1643,7 +1648,7 @@ struct alignas(128) Smem {
 static_assert(offsetof(Smem, hs) % 16 == 0 && offsetof(Smem, stage) % 128 == 0, "shared layout");
 
 
-__device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
+static __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t inc = warp_incl_scan(x);
     if (lane == 31) s.red[par][warp] = inc;
@@ -1658,7 +1663,7 @@ __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t 
 
 // Warp 0 finds the bin of `hist` holding the q-th largest and zeroes the
 // histogram; the caller's __syncthreads then publishes s.bc = {bin, above, total}.
-__device__ __forceinline__ void warp0_find(Smem &s, uint32_t *hist, uint32_t q) {
+static __device__ __forceinline__ void warp0_find(Smem &s, uint32_t *hist, uint32_t q) {
     if (threadIdx.x < 32) {
         uint32_t b, above, total;
         find_bin256(hist, q, b, above, total);
@@ -1673,7 +1678,7 @@ __device__ __forceinline__ void warp0_find(Smem &s, uint32_t *hist, uint32_t q) 
 }
 
 // The half h (0..7) of a vector as a 16-bit value.
-__device__ __forceinline__ uint32_t half_of(const uint4 &r, int h) {
+static __device__ __forceinline__ uint32_t half_of(const uint4 &r, int h) {
     const uint32_t w = (h & 4) ? ((h & 2) ? r.w : r.z) : ((h & 2) ? r.y : r.x);
     return (h & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
@@ -1828,22 +1833,19 @@ struct Row {
     }
 
     __device__ __forceinline__ bool cut_for(uint32_t g, uint32_t &c) {
+        // (a group is at most a thread's NV vectors)
         if constexpr (M::BLOCK) {
-            switch (g) {
-                case 8: return rep_cut<8>(c);
-                case 4: return rep_cut<4>(c);
-                case 2: return rep_cut<2>(c);
-                default: return exact_cut(c);
-            }
+            if constexpr (NV >= 8) if (g == 8u) return rep_cut<8>(c);
+            if constexpr (NV >= 4) if (g == 4u) return rep_cut<4>(c);
+            if (g == 2u) return rep_cut<2>(c);
+            return exact_cut(c);
         } else {
-            switch (g) {
-                case 64: return rep_cut<64>(c);
-                case 32: return rep_cut<32>(c);
-                case 16: return rep_cut<16>(c);
-                case 8: return rep_cut<8>(c);
-                case 4: return rep_cut<4>(c);
-                default: return exact_cut(c);
-            }
+            if constexpr (NV >= 8) if (g == 64u) return rep_cut<64>(c);
+            if constexpr (NV >= 4) if (g == 32u) return rep_cut<32>(c);
+            if (g == 16u) return rep_cut<16>(c);
+            if (g == 8u) return rep_cut<8>(c);
+            if (g == 4u) return rep_cut<4>(c);
+            return exact_cut(c);
         }
     }
 
@@ -1949,16 +1951,20 @@ struct Row {
         const uint32_t lane = lane_id(), warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
         const int32_t cs = static_cast<int32_t>(c) - 0x8000;
         uint32_t q = 0;
+        bool pass[NV];  // every vector's test first: the loads issue together
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int pos = j * NT + static_cast<int>(threadIdx.x);
+            if constexpr (FAST) pass[j] = pos < V && smax_halves(vec_smax(stg[pos])) >= cs;
+            else if constexpr (M::BLOCK) pass[j] = bkey(pos) >= c;
+            else pass[j] = pos < V && M::may_reach(stg[pos], 0u, c);
+        }
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             if (j * NT >= V) break;
             const int pos = j * NT + static_cast<int>(threadIdx.x);
-            bool pass;
-            if constexpr (FAST) pass = pos < V && smax_halves(vec_smax(stg[pos])) >= cs;
-            else if constexpr (M::BLOCK) pass = bkey(pos) >= c;
-            else pass = pos < V && M::may_reach(stg[pos], 0u, c);
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s.queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(pos);
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass[j]);
+            if (pass[j]) s.queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(pos);
             q += __popc(b);
         }
         __syncwarp();
@@ -1992,11 +1998,11 @@ struct Row {
                 }
             }
             const uint32_t cnt = __popc(m);
-            const uint32_t incl = warp_incl_scan(cnt);
-            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t tot;
+            const uint32_t before = warp_excl_small(cnt, tot);
             uint32_t base = 0;
-            if (lane == 31 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
-            uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+            if (lane == 0 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
+            uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + before;
 #pragma unroll 1
             for (; m; m &= m - 1u) {
                 const int bit = __ffs(m) - 1;
@@ -2150,11 +2156,12 @@ struct Row {
         // Group size: at least 2k representatives (and at least 4 logits).
         uint32_t g = 1;
         if (!p.force_direct) {
+            // (groups are a thread's own vectors: at most NV blocks, 8 NV logits)
             if constexpr (M::BLOCK) {
-                while (g < 8u && nE / (2u * g) >= 2u * k) g *= 2u;
+                while (g < min(8u, static_cast<uint32_t>(NV)) && nE / (2u * g) >= 2u * k) g *= 2u;
             } else {
                 g = 4;
-                while (g < 64u && nE / (2u * g) >= 2u * k) g *= 2u;
+                while (g < min(64u, 8u * NV) && nE / (2u * g) >= 2u * k) g *= 2u;
                 if (nE / g < 2u * k) g = 1;  // too few groups of 4: exact path
             }
         }
@@ -2170,14 +2177,14 @@ struct Row {
         // the representatives' cut.
         rp ^= 1u;
         uint32_t *hw = s.hs[2 + rp];
-        s.hs[3 - rp][tid] = 0u;
+        if (tid < 256u) s.hs[3 - rp][tid] = 0u;
         if (tid == 0) s.v_cnt[rp ^ 1u] = 0u;
         bool retry = false;
         for (;;) {
             PhaseClock clk;
             clk.start(p);
             if (retry) {
-                hw[tid] = 0u;
+                if (tid < 256u) hw[tid] = 0u;
                 if (tid == 0) s.v_cnt[rp] = 0u;
             }
             retry = true;
@@ -2263,7 +2270,7 @@ struct Row {
             }
             if (h != hw) {  // the cut's histogram back to zero
                 __syncthreads();
-                h[tid] = 0u;
+                if (tid < 256u) h[tid] = 0u;
             }
             clk.stop(p, TOPK_CNT_CYC_FINISH);
             return;
@@ -2271,7 +2278,7 @@ struct Row {
     }
 };
 
-__device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int32_t V) {
+static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int32_t V) {
     const uint32_t bytes = static_cast<uint32_t>(V) * 16u;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
     mbar_expect_tx(&s.full[st], bytes);
@@ -2280,7 +2287,7 @@ __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int3
 
 // The next row of this CTA, from `row` on in steps of `step`, that reads
 // logits (p.rows when none is left); V = its valid vectors.
-__device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, int32_t row, int32_t step,
+static __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, int32_t row, int32_t step,
                                                     int32_t &V) {
     for (; row < p.rows; row += step) {
         const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
@@ -2293,10 +2300,14 @@ __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, 
     return p.rows;
 }
 
-template <class M>
-__global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
+};  // struct Tile
+
+template <class M, int NT>
+__global__ void __launch_bounds__(NT, NT == 256 ? 2 : 1) topk_one_tile_kernel(const Params p) {
+    using O = Tile<NT>;
+    constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    typename O::Smem &s = *reinterpret_cast<typename O::Smem *>(smem_raw);
     const int tid = threadIdx.x;
     const int32_t step = static_cast<int32_t>(gridDim.x);
 
@@ -2313,14 +2324,14 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
     int32_t feed_row = p.rows;
     if (tid == 0) {
         int32_t V;
-        feed_row = next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
+        feed_row = O::next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
         for (int i = 0; i < NSTAGE && feed_row < p.rows; ++i) {
-            issue_row(s, i, p, feed_row, V);
-            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+            O::issue_row(s, i, p, feed_row, V);
+            feed_row = O::next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
         }
     }
 
-    Row<M> r(s, p);
+    typename O::template Row<M> r(s, p);
     r.k = static_cast<uint32_t>(p.k);
     uint32_t seq = 0;
     for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += step) {
@@ -2350,10 +2361,10 @@ __global__ void __launch_bounds__(NT, 2) topk_one_tile_kernel(const Params p) {
         clk.stop(p, TOPK_CNT_CYC_SELECT);
         if (tid == 0 && feed_row < p.rows) {
             int32_t V;
-            next_loaded_row(p, M::BLOCK, feed_row, step, V);
+            O::next_loaded_row(p, M::BLOCK, feed_row, step, V);
             fence_proxy_async();
-            issue_row(s, st, p, feed_row, V);
-            feed_row = next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
+            O::issue_row(s, st, p, feed_row, V);
+            feed_row = O::next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
         }
     }
 }
@@ -2375,11 +2386,16 @@ Variant variant() {
                    static_cast<int>(sizeof(Smem<NSTAGE, CAP>))};
 }
 
-Variant pick_one(bool block) {
-    return block ? Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<BlockMode>),
-                           static_cast<int>(sizeof(one::Smem))}
-                 : Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<TokenMode>),
-                           static_cast<int>(sizeof(one::Smem))};
+template <class M, int NT>
+Variant one_variant() {
+    return Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<M, NT>),
+                   static_cast<int>(sizeof(typename one::Tile<NT>::Smem))};
+}
+
+// wide: the 512-thread build (rows that do not fill the SMs).
+Variant pick_one(bool block, bool wide) {
+    if (wide) return block ? one_variant<BlockMode, 512>() : one_variant<TokenMode, 512>();
+    return block ? one_variant<BlockMode, 256>() : one_variant<TokenMode, 256>();
 }
 
 // The streamed kernel (rows wider than one tile, or split over a cluster).
@@ -2392,7 +2408,7 @@ struct DeviceInit {
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int per_sm[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [block][wide]
-    int per_sm_one[2] = {0, 0};            // the one-tile kernel, [block]
+    int per_sm_one[2][2] = {{0, 0}, {0, 0}};  // the one-tile kernel, [block][512 threads]
 };
 DeviceInit g_init[64];
 
@@ -2412,14 +2428,15 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                                                                       static_cast<size_t>(v.smem));
                 if (e == cudaSuccess && d.per_sm[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
-        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-            const Variant v = pick_one(b != 0);
-            e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
-            if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b], v.fn, one::NT,
-                                                                  static_cast<size_t>(v.smem));
-            if (e == cudaSuccess && d.per_sm_one[b] < 1) e = cudaErrorInvalidConfiguration;
-        }
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b)
+            for (int w = 0; w < 2 && e == cudaSuccess; ++w) {
+                const Variant v = pick_one(b != 0, w != 0);
+                e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+                if (e == cudaSuccess)
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b][w], v.fn, w ? 512 : 256,
+                                                                      static_cast<size_t>(v.smem));
+                if (e == cudaSuccess && d.per_sm_one[b][w] < 1) e = cudaErrorInvalidConfiguration;
+            }
         d.err = e;
     });
     out = &d;
@@ -2428,7 +2445,9 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
 
 struct Plan {
     int cluster;
-    bool wide;
+    bool wide;         // the streamed kernel
+    bool big;          // one-tile rows: the 512-thread build
+    int threads;
     int64_t clusters;  // persistent clusters launched
 };
 
@@ -2438,7 +2457,7 @@ struct Plan {
 // never exceeds what is resident at once.
 Plan make_plan(int rows, int width, const DeviceInit &d, bool block, int forced) {
     const int64_t vecs = (static_cast<int64_t>(width) + 7) / 8;
-    Plan pl{1, vecs > TILE_VEC, 1};
+    Plan pl{1, vecs > TILE_VEC, false, THREADS, 1};
     if (forced > 0) {
         pl.cluster = forced;
         pl.wide = pl.wide || forced > 1;
@@ -2449,8 +2468,14 @@ Plan make_plan(int rows, int width, const DeviceInit &d, bool block, int forced)
         while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages) c *= 2;
         pl.cluster = c;
     }
+    if (!pl.wide) {
+        // Rows that leave SMs idle at one 512-thread CTA each take that build:
+        // twice the threads on every row, so half the row's latency.
+        pl.big = rows <= d.sms * d.per_sm_one[block][1];
+        pl.threads = pl.big ? 512 : 256;
+    }
     const int64_t slots = pl.wide ? static_cast<int64_t>(d.sms) * d.per_sm[block][1]
-                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block];
+                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block][pl.big ? 1 : 0];
     const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
     return pl;
@@ -2495,8 +2520,8 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
 
     const bool block = mode == TOPK_BLOCK8;
     const Plan pl = make_plan(rows, width, *d, block, forced);
-    const Variant v = pl.wide ? pick(block, true) : pick_one(block);
-    const int threads = pl.wide ? THREADS : one::NT;
+    const Variant v = pl.wide ? pick(block, true) : pick_one(block, pl.big);
+    const int threads = pl.threads;
 
     Params prm;
     prm.logits = logits;
@@ -2577,9 +2602,10 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
     if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
     if (topk::init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
     const topk::Plan pl = topk::make_plan(rows, width, *d, mode == TOPK_BLOCK8, 0);
-    const topk::Variant v = pl.wide ? topk::pick(mode == TOPK_BLOCK8, true) : topk::pick_one(mode == TOPK_BLOCK8);
+    const topk::Variant v = pl.wide ? topk::pick(mode == TOPK_BLOCK8, true)
+                                    : topk::pick_one(mode == TOPK_BLOCK8, pl.big);
     if (cluster) *cluster = pl.cluster;
-    if (threads) *threads = pl.wide ? topk::THREADS : topk::one::NT;
+    if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = v.smem;
     if (variant) *variant = pl.wide ? 1 : 0;
     return TOPK_OK;

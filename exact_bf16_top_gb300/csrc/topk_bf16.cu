@@ -95,7 +95,6 @@ struct alignas(128) Smem {
     uint32_t bc[4];                          // broadcast words
     uint32_t v_count;                        // buffer entries
     uint32_t v_bufmax;                       // largest buffer key
-    uint32_t v_ngt, v_neq, v_smax;           // survivor counts and maximum
     uint32_t v_ntie, v_emit, v_flag;
     uint32_t v_full[2];                      // a warp found the buffer full, by tile parity
     uint32_t v_arrive[2];                    // warps done appending, by tile parity
@@ -461,10 +460,9 @@ struct Cta {
     uint32_t thr = 0;        // keep keys >= thr
     uint32_t buf_lo = 0;     // every buffer key is >= buf_lo
     uint32_t best_T = 0;     // largest lower bound on the row's k-th key found here
-    uint32_t known_T = 0;    // nonzero: the buffer's top-k cut (last_take ties at it)
-    uint32_t last_take = 0;
     uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full, s->v_arrive
     uint32_t f_Q = 0, f_next = 0, f_lim = 0;  // this warp's queue, where its appends stopped, the limit
+    uint32_t first_c = 0;    // the first tile's cut while its ties are pending (0: none)
     bool f_fast = false;
     bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
     uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
@@ -859,67 +857,6 @@ struct Cta {
         }
     }
 
-    // Keys > c of the tile (and >= thr) appended to the buffer at `first` on (any
-    // order; past `room` they are counted, not written), and counted into the
-    // window histogram s->hwin[0] over [c + 1, c + 256) whose top bin also
-    // holds every larger key; keys == c counted, their indices kept in
-    // s->tie_idx while they fit. Counts in s->v_ngt / v_neq, the largest
-    // survivor in s->v_smax, after the closing __syncthreads (zero on entry).
-    __device__ __forceinline__ void survivors(const uint4 *stg, int64_t tile_v0, int nv, uint32_t c,
-                                           uint32_t first, uint32_t room) {
-        const uint32_t lane = lane_id();
-        const uint32_t Q = build_queue(stg, tile_v0, nv, max(c, thr));
-        for (uint32_t e0 = 0; e0 < Q; e0 += 32) {
-            const uint32_t e = e0 + lane;
-            uint32_t ck[4] = {0u, 0u, 0u, 0u};
-            int pos = 0;
-            if (e < Q) {
-                pos = queued_pos(e);
-                clean_at(stg, tile_v0, pos, ck);
-            }
-            uint32_t ngt = 0, neq = 0, kmax = 0;
-#pragma unroll
-            for (int h = 0; h < KPV; ++h) {
-                const uint32_t key = key_at<M>(ck, h);
-                const bool ok = key >= thr;
-                ngt += ok && key > c;
-                neq += ok && key == c;
-                kmax = (ok && key > c) ? max(kmax, key) : kmax;
-            }
-            const uint32_t incl = warp_incl_scan(ngt | (neq << 16));
-            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t base = 0, ebase = 0;
-            if (lane == 31) {
-                if (tot & 0xFFFFu) base = atomicAdd(&s->v_ngt, tot & 0xFFFFu);
-                if (tot >> 16) ebase = atomicAdd(&s->v_neq, tot >> 16);
-            }
-            const uint32_t ex = incl - (ngt | (neq << 16));
-            base = __shfl_sync(0xFFFFFFFFu, base, 31) + (ex & 0xFFFFu);
-            ebase = __shfl_sync(0xFFFFFFFFu, ebase, 31) + (ex >> 16);
-            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0 && mx) atomicMax(&s->v_smax, mx);
-            if (ngt | neq) {
-#pragma unroll
-                for (int h = 0; h < KPV; ++h) {
-                    const uint32_t key = key_at<M>(ck, h);
-                    if (key < thr) continue;
-                    if (key > c) {
-                        atomicAdd(&s->hwin[0][min(key - c - 1u, 255u)], 1u);
-                        if (base < room) {
-                            s->buf_key[first + base] = static_cast<uint16_t>(key);
-                            s->buf_idx[first + base] = M::elem(tile_v0 + pos, h);
-                        }
-                        ++base;
-                    } else if (key == c) {
-                        if (ebase < static_cast<uint32_t>(TIECAP)) s->tie_idx[ebase] = M::elem(tile_v0 + pos, h);
-                        ++ebase;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-
     // The `take` lowest-index keys equal to c in the tile, appended at
     // first .. first + take, found with ordered scans of per-vector tie counts
     // (tile order is index order: vector j * THREADS + thread, then lane). For
@@ -951,137 +888,62 @@ struct Cta {
         }
     }
 
-    // Exact top-k of the tile's keys >= thr into the buffer (see the file
-    // comment). Raises thr when the tile held more than k candidates.
-    __device__ __forceinline__ void tile_select(const uint4 *stg, int64_t tile_v0, int nv) {
+    // The first tile of a CTA's share: a lower bound c on the row's k-th key
+    // from the tile's group representatives (one element per group of g, so k
+    // distinct elements reach the k-th largest representative), found a byte
+    // at a time; g = 1 makes every candidate its own representative (c = the
+    // tile's k-th key). The tile then appends its keys > c like any tile; if
+    // fewer than k, finish_tile adds its lowest-index keys == c up to k (a
+    // crowd of ties at c is never appended whole). Either way the buffer then
+    // holds k keys >= c that precede every later key, so later keys need to
+    // exceed c.
+    __device__ __forceinline__ void first_cut(const uint4 *stg, int64_t tile_v0, int nv) {
         const int tid = threadIdx.x;
-        const uint32_t first = s->v_count;
-        const uint32_t room = static_cast<uint32_t>(CAP) - first;
         const uint32_t nE = static_cast<uint32_t>(
             M::BLOCK ? nv : min(static_cast<int64_t>(nv) * 8, static_cast<int64_t>(L) - 8 * tile_v0));
-        known_T = 0;
-        if (nE > k) {
-            uint32_t g = 1;
-            if (!p->force_direct)
-                while (g < static_cast<uint32_t>(M::GMAX) && nE / (4u * g) >= 2u * k) g *= 4u;
-            for (;;) {
-                if (tid == 0) {
-                    s->v_ngt = 0u;
-                    s->v_neq = 0u;
-                    s->v_smax = 0u;
-                }
-                PhaseClock clk;
-                clk.start(*p);
-                rep_pass(stg, tile_v0, nv, g, ALL);
+        if (nE <= k) {
+            count_event(*p, TOPK_CNT_TILE_TAKE_ALL);
+            return;
+        }
+        uint32_t g = 1;
+        if (!p->force_direct)
+            while (g < static_cast<uint32_t>(M::GMAX) && nE / (4u * g) >= 2u * k) g *= 4u;
+        for (;;) {
+            PhaseClock clk;
+            clk.start(*p);
+            rep_pass(stg, tile_v0, nv, g, ALL);
+            __syncthreads();
+            clk.stop(*p, TOPK_CNT_CYC_REPS);
+            clk.start(*p);
+            // Every warp reads the same histograms and finds the same bins.
+            uint32_t hb, habove, NR;
+            if (!find_bin256(s->hwin[2], k, hb, habove, NR)) {
                 __syncthreads();
-                clk.stop(*p, TOPK_CNT_CYC_REPS);
-                clk.start(*p);
-                // The k-th largest representative, a byte at a time (every warp
-                // reads the same histograms and finds the same bins).
-                uint32_t hb, habove, NR;
-                if (!find_bin256(s->hwin[2], k, hb, habove, NR)) {
-                    __syncthreads();
-                    s->hwin[2][tid] = 0u;
-                    __syncthreads();
-                    if (g > 1u) {  // the representatives cannot bound the tile: exact path
-                        count_event(*p, TOPK_CNT_TILE_UNBOUNDED);
-                        g = 1u;
-                        continue;
-                    }
-                    break;  // at most k candidates: take them all
-                }
-                rep_pass(stg, tile_v0, nv, g, hb);
-                __syncthreads();
-                uint32_t lb, labove, ltotal;
-                find_bin256(s->hwin[3], k - habove, lb, labove, ltotal);
-                const uint32_t c = (hb << 8) | lb;
-                __syncthreads();  // both histograms read: zero them (survivors ends on a barrier)
                 s->hwin[2][tid] = 0u;
-                s->hwin[3][tid] = 0u;
-                clk.stop(*p, TOPK_CNT_CYC_CUT);
-                clk.start(*p);
-                survivors(stg, tile_v0, nv, c, first, room);
-                clk.stop(*p, TOPK_CNT_CYC_SURVIVORS);
-                clk.start(*p);
-                const uint32_t ngt = s->v_ngt, neq = s->v_neq, smax = s->v_smax;
-                uint32_t T, take;
-                if (ngt > room) {
-                    // Too many survivors to hold: every key becomes its own
-                    // representative (then fewer than k keys exceed c).
-                    count_event(*p, TOPK_CNT_TILE_OVERFLOW);
-                    __syncthreads();
-                    s->hwin[0][tid] = 0u;
-                    if (g == 1u) {  // cannot happen: record it rather than loop
-                        if (tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
-                        break;
-                    }
+                __syncthreads();
+                if (g > 1u) {  // the representatives cannot bound the row: every key its own
+                    count_event(*p, TOPK_CNT_TILE_UNBOUNDED);
                     g = 1u;
                     continue;
                 }
-                count_event(*p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
-                if (ngt >= k) {
-                    // The k-th survivor from the window histogram; a second look
-                    // only when it lies in the top bin (keys >= c + 256).
-                    uint32_t b1, above1, tot;
-                    find_bin256(s->hwin[0], k, b1, above1, tot);
-                    if (b1 < 255u) {
-                        T = c + 1u + b1;
-                        take = k - above1;
-                    } else {
-                        uint32_t a2;
-                        window_select(first, ngt, c + 1u, smax, k, &T, &a2);
-                        take = k - a2;
-                    }
-                    __syncthreads();
-                    s->hwin[0][tid] = 0u;
-                    if (tid == 0) {
-                        s->v_count = first + ngt;
-                        s->v_bufmax = max(s->v_bufmax, smax);
-                    }
-                    buf_lo = min(buf_lo, c + 1u);
-                } else {
-                    // The cut is c itself: the survivors and the take
-                    // lowest-index ties at c.
-                    T = c;
-                    take = k - ngt;
-                    s->hwin[0][tid] = 0u;
-                    if (neq <= static_cast<uint32_t>(TIECAP)) {
-                        if (static_cast<uint32_t>(tid) < neq) {
-                            const uint32_t mine = s->tie_idx[tid];
-                            uint32_t r = 0;
-                            for (uint32_t u = 0; u < neq; ++u) r += s->tie_idx[u] < mine;
-                            if (r < take) {
-                                s->buf_key[first + ngt + r] = static_cast<uint16_t>(c);
-                                s->buf_idx[first + ngt + r] = mine;
-                            }
-                        }
-                    } else {
-                        ordered_ties(stg, tile_v0, nv, c, take, first + ngt);
-                    }
-                    __syncthreads();
-                    if (tid == 0) {
-                        s->v_count = first + ngt + take;
-                        s->v_bufmax = max(s->v_bufmax, max(smax, c));
-                    }
-                    buf_lo = min(buf_lo, c);
-                }
-                clk.stop(*p, TOPK_CNT_CYC_EXACT);
-                known_T = first == 0 ? T : 0u;
-                last_take = take;
-                // The buffer holds the tile's top-k, all >= T, ahead of any
-                // later key: a later key equal to T can no longer be selected.
-                thr = max(thr, T + 1u);
-                publish(T);
-                __syncthreads();
+                count_event(*p, TOPK_CNT_TILE_TAKE_ALL);  // fewer than k candidates here
                 return;
             }
+            rep_pass(stg, tile_v0, nv, g, hb);
+            __syncthreads();
+            uint32_t lb, labove, ltotal;
+            find_bin256(s->hwin[3], k - habove, lb, labove, ltotal);
+            const uint32_t c = (hb << 8) | lb;
+            __syncthreads();  // both histograms read: zero them (filter_tile's barriers order it)
+            s->hwin[2][tid] = 0u;
+            s->hwin[3][tid] = 0u;
+            count_event(*p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+            first_c = c;
+            thr = max(thr, c + 1u);
+            publish(c);
+            clk.stop(*p, TOPK_CNT_CYC_CUT);
+            return;
         }
-        // At most k candidates: all of them.
-        count_event(*p, TOPK_CNT_TILE_TAKE_ALL);
-        const uint32_t Q = build_queue(stg, tile_v0, nv, thr);
-        append_keys(stg, tile_v0, Q, 0, thr);
-        buf_lo = min(buf_lo, thr);
-        __syncthreads();
     }
 
     // Keep the buffer entries [0, n) that are selected (key > T, or key == T
@@ -1191,7 +1053,6 @@ struct Cta {
         const uint32_t kept = keep_selected(n, T, cut);
         if (tid == 0) s->v_count = kept;
         buf_lo = T;
-        known_T = 0;
         thr = max(thr, strict ? T + 1u : T);
         publish(T);
         __syncthreads();
@@ -1209,7 +1070,6 @@ struct Cta {
         const int tid = threadIdx.x;
         PhaseClock clk;
         clk.start(*p);
-        known_T = 0;
         const uint32_t raised = s->v_newthr;  // written before the barrier that ended the last tile
         if (raised > thr) {
             thr = raised;
@@ -1281,7 +1141,26 @@ struct Cta {
     // After the barrier that ends a filter tile: if a warp found the buffer
     // full, compact it and append the rest of the tile (the rest may still tie
     // with the buffer, so the compaction keeps keys equal to its cut).
-    __device__ __forceinline__ void finish_tile(const uint4 *stg, int64_t tile_v0) {
+    __device__ __forceinline__ void finish_tile(const uint4 *stg, int64_t tile_v0, int nv) {
+        if (first_c) {
+            const uint32_t c = first_c;
+            first_c = 0;
+            const uint32_t n = s->v_count;  // the keys > c of the first tile (no refill: n <= CAP)
+            if (n < k && s->v_full[tpar] == 0u) {
+                count_event(*p, TOPK_CNT_TIE_FILLS);
+                ordered_ties(stg, tile_v0, nv, c, k - n, n);
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    s->v_count = k;
+                    s->v_bufmax = max(s->v_bufmax, c);
+                }
+                buf_lo = min(buf_lo, c);
+                s->hwin[1][threadIdx.x] = 0u;  // rebuilt by the next tile with the ties
+                run_ok = false;
+                __syncthreads();
+                return;
+            }
+        }
         if (s->v_full[tpar] == 0u) return;  // uniform; rare
         const int tid = threadIdx.x;
         uint32_t next = f_next;
@@ -1310,14 +1189,9 @@ struct Cta {
         const uint32_t n = s->v_count;
         uint32_t T = 0, take = 0;
         if (n > k) {
-            if (known_T) {
-                T = known_T;
-                take = last_take;
-            } else {
-                uint32_t above;
-                window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
-                take = k - above;
-            }
+            uint32_t above;
+            window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
+            take = k - above;
         }
         const uint32_t written = emit_selected(n, T, take, 0);
         int32_t *orow = p->out + static_cast<int64_t>(row) * k;
@@ -1547,7 +1421,6 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         cta.thr = M::KMIN;
         cta.buf_lo = 0xFFFFu;
         cta.best_T = 0;
-        cta.known_T = 0;
         cta.slot = it & 1u;
         cta.run_ok = false;
         if (tid == 0) {
@@ -1574,16 +1447,16 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             const uint4 *stg = s.stage[st];
             if (i == 0) {
                 cta.thr = max(cta.thr, cta.effective_thr());
-                cta.tile_select(stg, tile_v0, nv);
+                cta.first_cut(stg, tile_v0, nv);
                 clk.stop(p, TOPK_CNT_CYC_SELECT);
-            } else {
-                cta.filter_tile(stg, tile_v0, nv);
-                clk.stop(p, TOPK_CNT_CYC_FILTER);
+                clk.start(p);
             }
+            cta.filter_tile(stg, tile_v0, nv);
+            clk.stop(p, TOPK_CNT_CYC_FILTER);
             clk.start(p);
             cta.snapshot_shared();
             __syncthreads();  // every warp is done with this stage (but for a refill)
-            if (i > 0) cta.finish_tile(stg, tile_v0);
+            cta.finish_tile(stg, tile_v0, nv);
             if (tid == 0 && feed.row < p.rows) {
                 fence_proxy_async();
                 feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);

@@ -136,6 +136,7 @@ enum {
     TOPK_CNT_CYC_F_SYNC = 24,    /*   the tile's barrier (and any refill) */
     TOPK_CNT_CYC_F_FIND = 25,    /*   the buffer's k-th key for the next threshold */
     TOPK_CNT_CYC_F_LOOP = 26,    /*   end of tile: barrier and the next copy's issue */
+    TOPK_CNT_TIE_FILLS = 27,     /* streamed first tiles completed with lowest-index ties at their cut */
     TOPK_NUM_COUNTERS = 32
 };
 

@@ -94,7 +94,7 @@ struct alignas(128) Smem {
     uint32_t red[2][WARPS];                  // block-scan warp totals
     uint32_t bc[4];                          // broadcast words
     uint32_t v_count;                        // buffer entries
-    uint32_t v_bufmax;                       // largest buffer key
+    uint32_t v_bufmax;                       // largest buffer key (buffer_max's scratch)
     uint32_t v_ntie, v_emit, v_flag;
     uint32_t v_full[2];                      // a warp found the buffer full, by tile parity
     uint32_t v_arrive[2];                    // warps done appending, by tile parity
@@ -103,7 +103,7 @@ struct alignas(128) Smem {
     uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
     uint32_t thr_snap;                       // shared_thr as every thread sees it this tile
     uint32_t abort_flag;                     // a bounded wait gave up
-    uint8_t queue[WARPS][QCAP];              // per-warp vector queues
+    uint16_t queue[WARPS][QCAP];             // per-warp vector queues (tile positions)
     unsigned long long full[NSTAGE];         // stage mbarriers
 };
 
@@ -641,7 +641,7 @@ struct Cta {
                 pass = M::may_reach(raw, M::BLOCK ? BlockMode::key(raw, tile_v0 + pos, V) : 0u, lim);
             }
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
+            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
             q += __popc(b);
         }
         __syncwarp();
@@ -649,8 +649,7 @@ struct Cta {
     }
 
     __device__ __forceinline__ int queued_pos(uint32_t e) const {
-        const uint32_t q = s->queue[threadIdx.x >> 5][e];
-        return static_cast<int>(q >> 5) * THREADS + static_cast<int>((threadIdx.x >> 5) * 32 + (q & 31u));
+        return static_cast<int>(s->queue[threadIdx.x >> 5][e]);
     }
 
     // Append every key >= lim of this warp's queued vectors, from queue entry
@@ -667,18 +666,15 @@ struct Cta {
                 pos = queued_pos(e);
                 clean_at(stg, tile_v0, pos, ck);
             }
-            uint32_t cnt = 0, kmax = 0;
+            uint32_t cnt = 0;
 #pragma unroll
             for (int h = 0; h < KPV; ++h) {
                 const uint32_t key = key_at<M>(ck, h);
                 cnt += key >= lim;
-                kmax = key >= lim ? max(kmax, key) : kmax;
             }
             uint32_t total, at;
             const uint32_t before = warp_excl_small(cnt, total);
             if (!reserve(total, before, cnt, at)) return e0;  // full: the caller compacts and resumes here
-            kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
             if (cnt) {
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
@@ -736,7 +732,7 @@ struct Cta {
         for (int j = 0; j < VPT; ++j) {
             const bool pass = mx[j] >= cs;
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint8_t>((j << 5) | lane);
+            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
             q += __popc(b);
         }
         __syncwarp();
@@ -750,7 +746,7 @@ struct Cta {
         const uint32_t csm = (static_cast<uint32_t>(cs - 1) & 0xFFFFu) * 0x10001u;
         for (uint32_t e0 = from; e0 < Q; e0 += 32) {
             const uint32_t e = e0 + lane;
-            uint32_t m = 0, kmax = 0;
+            uint32_t m = 0;
             int pos = 0;
             uint4 r = make_uint4(0, 0, 0, 0);
             if (e < Q) {
@@ -765,14 +761,12 @@ struct Cta {
                     u |= ((((g & 0x7FFF7FFFu) + 0x7FFF7FFFu) | g) & 0x80008000u) >> (15 - i);
                 }
                 m = (u & 0xFu) | ((u >> 12) & 0xF0u);  // bit i: low half of word i; bit 4 + i: high half
-                if (m) kmax = min(static_cast<uint32_t>(smax_halves(vec_smax(r)) + 0x8000), KEY_POS_INF);
             }
             const uint32_t cnt = __popc(m);
             uint32_t total, at;
             const uint32_t before = warp_excl_small(cnt, total);
             if (!reserve(total, before, cnt, at)) return e0;  // full: the caller compacts and resumes here
-            kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-            if (lane == 0 && kmax) atomicMax(&s->v_bufmax, kmax);
+
             const uint32_t idx0 = static_cast<uint32_t>(tile_v0 + pos) * 8u;
 #pragma unroll 1
             for (; m; m &= m - 1u) {
@@ -1032,6 +1026,19 @@ struct Cta {
         return ngt + min(take, e);
     }
 
+    // The largest key of buffer entries [0, n) (0 for none), in every thread.
+    __device__ __forceinline__ uint32_t buffer_max(uint32_t n) {
+        uint32_t m = 0;
+        for (uint32_t i = threadIdx.x; i < n; i += THREADS) m = max(m, static_cast<uint32_t>(s->buf_key[i]));
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        __syncthreads();
+        if (threadIdx.x == 0) s->v_bufmax = 0u;
+        __syncthreads();
+        if (lane_id() == 0 && m) atomicMax(&s->v_bufmax, m);
+        __syncthreads();
+        return s->v_bufmax;
+    }
+
     // Reduce the buffer to its exact top-k. strict: every buffered key precedes
     // every key still to come, so later keys equal to the cut are dropped too.
     __device__ __forceinline__ void compact(bool strict) {
@@ -1047,7 +1054,7 @@ struct Cta {
         PhaseClock clk;
         clk.start(*p);
         uint32_t T, above;
-        window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
+        window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
         const uint32_t take = k - above;
         const uint32_t cut = tie_cut(n, T, take);
         const uint32_t kept = keep_selected(n, T, cut);
@@ -1080,7 +1087,8 @@ struct Cta {
                 __syncthreads();
             }
         }
-        if (s->v_count > static_cast<uint32_t>(CAP / 2) && s->v_count > 2u * k) compact(true);
+        // Compact ahead of a full buffer only (a refill covers the rest).
+        if (s->v_count > static_cast<uint32_t>(3 * CAP / 4) && s->v_count > 2u * k) compact(true);
         if (!run_ok) {
             // Every buffer key >= thr - 1 into the (zero) running histogram,
             // before any append of this tile changes the count.
@@ -1152,7 +1160,6 @@ struct Cta {
                 __syncthreads();
                 if (threadIdx.x == 0) {
                     s->v_count = k;
-                    s->v_bufmax = max(s->v_bufmax, c);
                 }
                 buf_lo = min(buf_lo, c);
                 s->hwin[1][threadIdx.x] = 0u;  // rebuilt by the next tile with the ties
@@ -1190,7 +1197,7 @@ struct Cta {
         uint32_t T = 0, take = 0;
         if (n > k) {
             uint32_t above;
-            window_select(0, n, buf_lo, max(s->v_bufmax, buf_lo), k, &T, &above);
+            window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
             take = k - above;
         }
         const uint32_t written = emit_selected(n, T, take, 0);
@@ -1209,7 +1216,7 @@ struct Cta {
         compact(false);
         __syncthreads();
         const uint32_t n = s->v_count;
-        const uint32_t my_max = n ? s->v_bufmax : 0u;
+        const uint32_t my_max = buffer_max(n);
         if (tid == 0) {
             atomicMax(&s->shared_thr[slot], best_T);
             atomicMax(&s->shared_max[slot], my_max);

@@ -728,12 +728,13 @@ struct Cta {
             const int pos = j * THREADS + static_cast<int>(threadIdx.x);
             mx[j] = pos < nv ? smax_halves(vec_smax(stg[pos])) : -32768;
         }
+        uint32_t b[VPT];  // every ballot first: the stores then only wait on popcounts
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) b[j] = __ballot_sync(0xFFFFFFFFu, mx[j] >= cs);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            const bool pass = mx[j] >= cs;
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
-            q += __popc(b);
+            if (mx[j] >= cs) s->queue[warp][q + __popc(b[j] & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
+            q += __popc(b[j]);
         }
         __syncwarp();
         return q;
@@ -1839,13 +1840,14 @@ struct Row {
             else if constexpr (M::BLOCK) pass[j] = bkey(pos) >= c;
             else pass[j] = pos < V && M::may_reach(stg[pos], 0u, c);
         }
+        uint32_t bal[NV];  // every ballot first: the stores then only wait on popcounts
+#pragma unroll
+        for (int j = 0; j < NV; ++j) bal[j] = __ballot_sync(0xFFFFFFFFu, pass[j]);
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            if (j * NT >= V) break;
             const int pos = j * NT + static_cast<int>(threadIdx.x);
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass[j]);
-            if (pass[j]) s.queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(pos);
-            q += __popc(b);
+            if (pass[j]) s.queue[warp][q + __popc(bal[j] & lt)] = static_cast<uint16_t>(pos);
+            q += __popc(bal[j]);
         }
         __syncwarp();
         // Non-negative cut (FAST): the keys >= c are the BF16 bits >= c - 0x8000

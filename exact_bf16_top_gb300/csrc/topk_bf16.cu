@@ -1501,7 +1501,7 @@ static constexpr int NT = NT_;
 static constexpr int NW = NT / 32;
 static constexpr int NV = 2048 / NT;         // vectors per thread
 static constexpr int NTILE = NT * NV;        // 2048 vectors
-static constexpr int NSTAGE = 2;
+static constexpr int NSTAGE = NT == 256 ? 1 : 2;  // 256: three CTAs per SM cover each other's copies
 static constexpr int SURV_CAP = 4096;
 static constexpr int REP_CAP = 4096;         // stored representatives (groups of >= 4 logits)
 static constexpr int QN = 32 * NV;           // queue entries of one warp
@@ -1509,9 +1509,13 @@ static constexpr int TAB_CAP = 2 * NT;       // page ids of a row staged in shar
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
-    uint32_t surv_idx[SURV_CAP + 4];         // + a spare slot for writes past the end
-    uint16_t surv_key[SURV_CAP + 8];
-    uint16_t rep[REP_CAP];                   // the row's representatives (0 = none)
+    union {                                  // the representatives are done before survivors start
+        struct {
+            uint32_t surv_idx[SURV_CAP + 4]; // + a spare slot for writes past the end
+            uint16_t surv_key[SURV_CAP + 8];
+        };
+        uint16_t rep[REP_CAP];               // the row's representatives (0 = none)
+    };
     alignas(16) uint32_t hs[4][256];         // [0], [1]: the cut's byte passes (zero between
                                              // uses); [2 + row parity]: the row's window
     uint32_t tie_idx[TIECAP];
@@ -2185,7 +2189,7 @@ static __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool 
 };  // struct Tile
 
 template <class M, int NT>
-__global__ void __launch_bounds__(NT, NT == 256 ? 2 : 1) topk_one_tile_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, NT == 256 ? 3 : 1) topk_one_tile_kernel(const Params p) {
     using O = Tile<NT>;
     constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];

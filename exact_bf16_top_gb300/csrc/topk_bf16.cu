@@ -1492,20 +1492,21 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
 // cut -> write. Same cutoff argument as the streamed kernel.
 namespace one {
 
-// Everything of the one-tile path for a CTA of NT_ threads (256: two CTAs per
-// SM for many rows; 512: one, for rows that do not fill the SMs, where a row's
-// latency is what counts).
-template <int NT_>
+// Everything of the one-tile path for a CTA of NT_ threads (256: several CTAs
+// per SM for many rows; 512: one, for rows that do not fill the SMs, where a
+// row's latency is what counts) with a survivor list of SURV_ entries (2048
+// for k <= 1024 fits four CTAs per SM; 4096 for larger k, three).
+template <int NT_, int SURV_>
 struct Tile {
 static constexpr int NT = NT_;
 static constexpr int NW = NT / 32;
 static constexpr int NV = 2048 / NT;         // vectors per thread
 static constexpr int NTILE = NT * NV;        // 2048 vectors
-static constexpr int NSTAGE = NT == 256 ? 1 : 2;  // 256: three CTAs per SM cover each other's copies
-static constexpr int SURV_CAP = 4096;
+static constexpr int NSTAGE = NT == 256 ? 1 : 2;  // 256: the other CTAs on the SM cover its copies
+static constexpr int SURV_CAP = SURV_;
 static constexpr int REP_CAP = 4096;         // stored representatives (groups of >= 4 logits)
 static constexpr int QN = 32 * NV;           // queue entries of one warp
-static constexpr int TAB_CAP = 2 * NT;       // page ids of a row staged in shared memory
+static constexpr int TAB_CAP = 256;         // page ids of a row staged in shared memory (<= NT)
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
@@ -1519,7 +1520,7 @@ struct alignas(128) Smem {
     alignas(16) uint32_t hs[4][256];         // [0], [1]: the cut's byte passes (zero between
                                              // uses); [2 + row parity]: the row's window
     uint32_t tie_idx[TIECAP];
-    uint16_t queue[NW][QN];
+    uint8_t queue[NW][QN];                   // (j << 5) | lane of queued vectors j * NT + thread
     int32_t tab[TAB_CAP];
     uint32_t red[2][NW];
     uint32_t bc[4];
@@ -1531,6 +1532,7 @@ struct alignas(128) Smem {
 
 // Histograms are read and written as 16-byte vectors; stages are bulk-copy targets.
 static_assert(offsetof(Smem, hs) % 16 == 0 && offsetof(Smem, stage) % 128 == 0, "shared layout");
+static_assert(TAB_CAP <= NT, "one page id per thread");
 
 
 static __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
@@ -1735,9 +1737,9 @@ struct Row {
     }
 
     // Every candidate of the row (at most k of them), in index order.
-    __device__ void take_all(int32_t t0, int32_t t1) {
+    __device__ void take_all(int32_t t0) {
         const int tid = threadIdx.x;
-        stage_table(t0, t1);
+        stage_table(t0);
         uint32_t cnt = 0;
         for (int j = 0; j < NV; ++j) {
             uint32_t ck[4];
@@ -1850,7 +1852,7 @@ struct Row {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int pos = j * NT + static_cast<int>(threadIdx.x);
-            if (pass[j]) s.queue[warp][q + __popc(bal[j] & lt)] = static_cast<uint16_t>(pos);
+            if (pass[j]) s.queue[warp][q + __popc(bal[j] & lt)] = static_cast<uint8_t>((j << 5) | lane);
             q += __popc(bal[j]);
         }
         __syncwarp();
@@ -1864,7 +1866,8 @@ struct Row {
             uint4 r = make_uint4(0, 0, 0, 0);
             uint32_t ck[4] = {0u, 0u, 0u, 0u};
             if (e < q) {
-                pos = s.queue[warp][e];
+                const uint32_t qe = s.queue[warp][e];
+                pos = static_cast<int>(qe >> 5) * NT + static_cast<int>(warp * 32u + (qe & 31u));
                 if constexpr (FAST) {
                     // Bit i (i < 4): low half of word i; bit 4 + i: its high half.
                     r = stg[pos];
@@ -2010,11 +2013,8 @@ struct Row {
 
     // Store the page ids loaded at the start of select() (the caller
     // synchronises before the first put).
-    __device__ __forceinline__ void stage_table(int32_t t0, int32_t t1) const {
-        if (tab) {
-            s.tab[threadIdx.x] = t0;
-            s.tab[threadIdx.x + NT] = t1;
-        }
+    __device__ __forceinline__ void stage_table(int32_t t0) const {
+        if (tab && threadIdx.x < static_cast<uint32_t>(TAB_CAP)) s.tab[threadIdx.x] = t0;
     }
 
     __device__ void select() {
@@ -2022,7 +2022,7 @@ struct Row {
         const uint32_t nE = M::BLOCK ? static_cast<uint32_t>(V) : static_cast<uint32_t>(L);
         // The row's page ids, loaded now and staged in shared memory before the
         // first write (their latency hides behind the survivor pass).
-        int32_t t0 = 0, t1 = 0;
+        int32_t t0 = 0;  // page id of this thread's entry (TAB_CAP <= NT)
         tab = false;
         if (p.table) {
             const uint32_t npages = (nE + (1u << p.page_shift) - 1u) >> p.page_shift;
@@ -2030,13 +2030,12 @@ struct Row {
                 tab = true;
                 const int32_t *trow = p.table + static_cast<int64_t>(row) * p.table_stride;
                 if (tid < npages) t0 = __ldg(trow + tid);
-                if (tid + NT < npages) t1 = __ldg(trow + tid + NT);
             }
         }
         mask_tail();
         if (nE <= k) {
             count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-            take_all(t0, t1);
+            take_all(t0);
             return;
         }
         // Group size: at least 2k representatives (and at least 4 logits).
@@ -2083,13 +2082,13 @@ struct Row {
                     continue;
                 }
                 count_event(p, TOPK_CNT_TILE_TAKE_ALL);
-                take_all(t0, t1);
+                take_all(t0);
                 return;
             }
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
             survivors(c, hw);
-            stage_table(t0, t1);
+            stage_table(t0);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
             clk.start(p);
@@ -2188,9 +2187,9 @@ static __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool 
 
 };  // struct Tile
 
-template <class M, int NT>
-__global__ void __launch_bounds__(NT, NT == 256 ? 3 : 1) topk_one_tile_kernel(const Params p) {
-    using O = Tile<NT>;
+template <class M, int NT, int SURV>
+__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) topk_one_tile_kernel(const Params p) {
+    using O = Tile<NT, SURV>;
     constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     typename O::Smem &s = *reinterpret_cast<typename O::Smem *>(smem_raw);
@@ -2272,16 +2271,21 @@ Variant variant() {
                    static_cast<int>(sizeof(Smem<NSTAGE, CAP>))};
 }
 
-template <class M, int NT>
+template <class M, int NT, int SURV>
 Variant one_variant() {
-    return Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<M, NT>),
-                   static_cast<int>(sizeof(typename one::Tile<NT>::Smem))};
+    return Variant{reinterpret_cast<const void *>(&one::topk_one_tile_kernel<M, NT, SURV>),
+                   static_cast<int>(sizeof(typename one::Tile<NT, SURV>::Smem))};
 }
 
-// wide: the 512-thread build (rows that do not fill the SMs).
-Variant pick_one(bool block, bool wide) {
-    if (wide) return block ? one_variant<BlockMode, 512>() : one_variant<TokenMode, 512>();
-    return block ? one_variant<BlockMode, 256>() : one_variant<TokenMode, 256>();
+// build 0: 256 threads, k <= 1024; 1: 256 threads, larger k; 2: 512 threads
+// (rows that do not fill the SMs).
+constexpr int ONE_BUILDS = 3;
+Variant pick_one(bool block, int build) {
+    switch (build) {
+        case 0: return block ? one_variant<BlockMode, 256, 2048>() : one_variant<TokenMode, 256, 2048>();
+        case 1: return block ? one_variant<BlockMode, 256, 4096>() : one_variant<TokenMode, 256, 4096>();
+        default: return block ? one_variant<BlockMode, 512, 4096>() : one_variant<TokenMode, 512, 4096>();
+    }
 }
 
 // The streamed kernel (rows wider than one tile, or split over a cluster).
@@ -2294,7 +2298,7 @@ struct DeviceInit {
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int per_sm[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [block][wide]
-    int per_sm_one[2][2] = {{0, 0}, {0, 0}};  // the one-tile kernel, [block][512 threads]
+    int per_sm_one[2][ONE_BUILDS] = {};    // the one-tile kernel, [block][build]
 };
 DeviceInit g_init[64];
 
@@ -2315,11 +2319,11 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                 if (e == cudaSuccess && d.per_sm[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
         for (int b = 0; b < 2 && e == cudaSuccess; ++b)
-            for (int w = 0; w < 2 && e == cudaSuccess; ++w) {
-                const Variant v = pick_one(b != 0, w != 0);
+            for (int w = 0; w < ONE_BUILDS && e == cudaSuccess; ++w) {
+                const Variant v = pick_one(b != 0, w);
                 e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
                 if (e == cudaSuccess)
-                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b][w], v.fn, w ? 512 : 256,
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b][w], v.fn, w == 2 ? 512 : 256,
                                                                       static_cast<size_t>(v.smem));
                 if (e == cudaSuccess && d.per_sm_one[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
@@ -2332,7 +2336,7 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
 struct Plan {
     int cluster;
     bool wide;         // the streamed kernel
-    bool big;          // one-tile rows: the 512-thread build
+    int build;         // one-tile rows: which build (see pick_one)
     int threads;
     int64_t clusters;  // persistent clusters launched
 };
@@ -2341,9 +2345,9 @@ struct Plan {
 // that puts about one CTA on every resident slot, at most 16, and never so many
 // CTAs that a share is below one stage. Clusters are persistent, so the grid
 // never exceeds what is resident at once.
-Plan make_plan(int rows, int width, const DeviceInit &d, bool block, int forced) {
+Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int forced) {
     const int64_t vecs = (static_cast<int64_t>(width) + 7) / 8;
-    Plan pl{1, vecs > TILE_VEC, false, THREADS, 1};
+    Plan pl{1, vecs > TILE_VEC, 0, THREADS, 1};
     if (forced > 0) {
         pl.cluster = forced;
         pl.wide = pl.wide || forced > 1;
@@ -2357,11 +2361,11 @@ Plan make_plan(int rows, int width, const DeviceInit &d, bool block, int forced)
     if (!pl.wide) {
         // Rows that leave SMs idle at one 512-thread CTA each take that build:
         // twice the threads on every row, so half the row's latency.
-        pl.big = rows <= d.sms * d.per_sm_one[block][1];
-        pl.threads = pl.big ? 512 : 256;
+        pl.build = rows <= d.sms * d.per_sm_one[block][2] ? 2 : (k <= 1024 ? 0 : 1);
+        pl.threads = pl.build == 2 ? 512 : 256;
     }
     const int64_t slots = pl.wide ? static_cast<int64_t>(d.sms) * d.per_sm[block][1]
-                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block][pl.big ? 1 : 0];
+                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block][pl.build];
     const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
     return pl;
@@ -2405,8 +2409,8 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     if (init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
 
     const bool block = mode == TOPK_BLOCK8;
-    const Plan pl = make_plan(rows, width, *d, block, forced);
-    const Variant v = pl.wide ? pick(block, true) : pick_one(block, pl.big);
+    const Plan pl = make_plan(rows, width, k, *d, block, forced);
+    const Variant v = pl.wide ? pick(block, true) : pick_one(block, pl.build);
     const int threads = pl.threads;
 
     Params prm;
@@ -2487,9 +2491,9 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
     topk::DeviceInit *d = nullptr;
     if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
     if (topk::init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
-    const topk::Plan pl = topk::make_plan(rows, width, *d, mode == TOPK_BLOCK8, 0);
+    const topk::Plan pl = topk::make_plan(rows, width, k, *d, mode == TOPK_BLOCK8, 0);
     const topk::Variant v = pl.wide ? topk::pick(mode == TOPK_BLOCK8, true)
-                                    : topk::pick_one(mode == TOPK_BLOCK8, pl.big);
+                                    : topk::pick_one(mode == TOPK_BLOCK8, pl.build);
     if (cluster) *cluster = pl.cluster;
     if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = v.smem;

@@ -214,8 +214,17 @@ __device__ __forceinline__ void red_max_peer(uint32_t addr, uint32_t v) {
                  : "memory");
 }
 
+// Programmatic dependent launch (the DecodeTopK page's synchronisation notes:
+// wait for the preceding grid before reading inputs, let the next one start
+// early): the wait returns once the preceding grid has completed and its writes
+// are visible; the release lets the next grid's CTAs start their prologue on
+// free SMs while this one runs (they wait the same way before reading).
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_release() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Packed 16-bit maxima (signed / unsigned).
@@ -1379,6 +1388,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     const int32_t ncl = static_cast<int32_t>(gridDim.x / C);
 
     grid_dependency_wait();
+    grid_dependents_release();
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
@@ -2197,6 +2207,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     const int32_t step = static_cast<int32_t>(gridDim.x);
 
     grid_dependency_wait();
+    grid_dependents_release();
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
@@ -2339,6 +2350,7 @@ struct Plan {
     int build;         // one-tile rows: which build (see pick_one)
     int threads;
     int64_t clusters;  // persistent clusters launched
+    bool spare;        // some resident slots stay free (the launch may overlap the previous one)
 };
 
 // One CTA per row when a row fits one stage. Wider rows: the smallest cluster
@@ -2347,7 +2359,7 @@ struct Plan {
 // never exceeds what is resident at once.
 Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int forced) {
     const int64_t vecs = (static_cast<int64_t>(width) + 7) / 8;
-    Plan pl{1, vecs > TILE_VEC, 0, THREADS, 1};
+    Plan pl{1, vecs > TILE_VEC, 0, THREADS, 1, false};
     if (forced > 0) {
         pl.cluster = forced;
         pl.wide = pl.wide || forced > 1;
@@ -2368,6 +2380,7 @@ Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int 
                                   : static_cast<int64_t>(d.sms) * d.per_sm_one[block][pl.build];
     const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
+    pl.spare = pl.clusters * pl.cluster < slots;
     return pl;
 }
 
@@ -2435,13 +2448,23 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // A grid that leaves resident slots free may start while the previous
+    // kernel on the stream finishes (see grid_dependency_wait); one that fills
+    // every slot would only crowd the previous one's tail.
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (pl.spare) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (pl.cluster > 1) {  // a lone CTA per row needs no cluster
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr++].val.clusterDim.z = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pl.cluster > 1 ? 1 : 0;  // a lone CTA per row needs no cluster
+    cfg.numAttrs = n_attr;
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, v.fn, args);
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;

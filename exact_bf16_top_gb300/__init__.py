@@ -31,7 +31,7 @@ COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", 
                  "cyc_wait", "cyc_select", "cyc_filter", "cyc_finish", "cyc_compact",
                  "cyc_reps", "cyc_cut", "cyc_survivors", "cyc_exact", "guess_hit", "guess_miss",
                  "cyc_f_prep", "cyc_f_queue", "cyc_f_append", "cyc_f_sync", "cyc_f_find", "cyc_f_loop",
-                 "tie_fills")
+                 "tie_fills", "direct_rows")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
            5: "CUDA error"}
@@ -45,7 +45,7 @@ class TopkError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("force_direct", ctypes.c_int32), ("cluster", ctypes.c_int32),
-                ("counters", ctypes.c_void_p)]
+                ("counters", ctypes.c_void_p), ("path", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -97,7 +97,7 @@ def _ptr(t) -> int | None:
 
 def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_size: int = 64,
            out=None, width: int | None = None, stream=None, *, force_direct: bool = False,
-           cluster: int = 0, counters=None):
+           cluster: int = 0, counters=None, path: int = 0):
     """Exact top-k of every row of ``logits`` -> int32 [rows, k] on the same device.
 
     logits: CUDA bfloat16 (or int16/uint16 holding BF16 bits) [rows, row_stride]
@@ -105,7 +105,7 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
     block_table: None or CUDA int32 [rows, pages] (unit inner stride);
     width: logits per row that may be valid (default: logits.shape[1]);
     stream: a torch.cuda.Stream (default: the current stream);
-    force_direct / cluster / counters: test hooks (see topk_bf16_select_ex).
+    force_direct / cluster / counters / path: test hooks (see topk_bf16_select_ex).
     """
     import torch
     if not (isinstance(logits, torch.Tensor) and logits.is_cuda):
@@ -144,9 +144,9 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
         args = (_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), int(mode),
                 _ptr(block_table), table_stride, int(page_size), _ptr(out),
                 ctypes.c_void_p(stream.cuda_stream))
-        if force_direct or cluster or counters is not None:
+        if force_direct or cluster or counters is not None or path:
             opt = _Options(1 if force_direct else 0, int(cluster),
-                           None if counters is None else counters.data_ptr())
+                           None if counters is None else counters.data_ptr(), int(path))
             st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
         else:
             st = lib.topk_bf16_select(*args)
@@ -169,7 +169,7 @@ def plan(rows: int, width: int, k: int, mode: int = TOKEN) -> dict:
     _check(load().topk_bf16_plan(rows, width, k, mode, ctypes.byref(c), ctypes.byref(t),
                                  ctypes.byref(s), ctypes.byref(v)))
     return {"cluster": c.value, "threads": t.value, "smem_bytes": s.value,
-            "variant": "streamed" if v.value else "one-tile"}
+            "variant": ("one-tile", "streamed", "direct")[v.value]}
 
 
 def device_status(clear: bool = True) -> int:

@@ -1493,6 +1493,247 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     }
 }
 
+// --------------------------------------------- resident-keys (direct) kernel
+//
+// Rows split over a cluster whose shares fit in shared memory as keys: the
+// DecodeTopK page's direct path (the exact k-th key from two cluster-wide 8-bit
+// radix histograms, then every CTA writes its own selected indices). Each CTA
+// streams its share through the stage ring once and keeps one 16-bit key per
+// element (0: not a candidate); no candidate buffer, no threshold, no
+// compaction. Used where a buffer would churn: block rows, whose k is large
+// next to a CTA's share.
+
+namespace direct {
+
+constexpr int NT = 256;
+constexpr int NSTAGE = 2;
+constexpr int RES = 16384;                   // resident keys per CTA
+
+struct alignas(128) Smem {
+    uint4 stage[NSTAGE][TILE_VEC];
+    alignas(16) uint16_t key[RES];           // the share's element keys, in index order
+    alignas(16) uint32_t h[2][256];          // this CTA's histograms of the row (peers read them)
+    uint32_t all[256];                       // a histogram summed over the cluster
+    uint32_t pre[2][256];                    // ... over the lower-ranked CTAs
+    uint32_t red[2][NT / 32];
+    uint32_t abort_flag;
+    unsigned long long full[NSTAGE];
+};
+
+template <class M>
+struct Share {
+    Smem &s;
+    const Params &p;
+    uint32_t C = 1, rank = 0, par = 0;
+    int32_t row = 0, L = 0;
+    int64_t V = 0, v0 = 0;
+    uint32_t n = 0;  // resident elements
+
+    __device__ Share(Smem &s_, const Params &p_) : s(s_), p(p_) {}
+
+    __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t &total) {
+        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+        const uint32_t inc = warp_incl_scan(x);
+        if (lane == 31) s.red[par][warp] = inc;
+        __syncthreads();
+        const uint32_t w = lane < NT / 32 ? s.red[par][lane] : 0u;
+        const uint32_t wi = warp_incl_scan(w);
+        total = __shfl_sync(0xFFFFFFFFu, wi, 31);
+        const uint32_t pre = __shfl_sync(0xFFFFFFFFu, wi - w, warp);
+        par ^= 1u;
+        return pre + inc;
+    }
+
+    // The keys of one tile's vectors, at their element positions in the share.
+    __device__ __forceinline__ void keep_tile(const uint4 *stg, int64_t tile_v0, int nv) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int pos = j * NT + static_cast<int>(threadIdx.x);
+            if (pos >= nv) break;
+            const int64_t v = tile_v0 + pos;
+            const uint32_t local = static_cast<uint32_t>(v - v0);
+            if constexpr (M::BLOCK) {
+                s.key[local] = static_cast<uint16_t>(BlockMode::key(stg[pos], v, V));
+            } else {
+                uint32_t ck[4];
+                TokenMode::clean(stg[pos], v, V, L, ck);  // packed pairs of keys, in element order
+                reinterpret_cast<uint4 *>(s.key)[local] = make_uint4(ck[0], ck[1], ck[2], ck[3]);
+            }
+        }
+    }
+
+    // Every CTA's histogram `which` complete (a cluster barrier), then its sum
+    // over the cluster and over the lower ranks.
+    __device__ __forceinline__ void gather(int which) {
+        const int tid = threadIdx.x;
+        if (C > 1) {
+            cluster_arrive();
+            cluster_wait();
+        } else {
+            __syncthreads();
+        }
+        uint32_t all = 0, pre = 0;
+        for (uint32_t r = 0; r < C; ++r) {
+            const uint32_t x = C > 1 ? ld_peer(peer_addr(&s.h[which][tid], r)) : s.h[which][tid];
+            all += x;
+            pre += r < rank ? x : 0u;
+        }
+        s.all[tid] = all;
+        s.pre[which][tid] = pre;
+        __syncthreads();
+    }
+
+    __device__ __forceinline__ void put(int32_t *orow, uint32_t slot, uint32_t local) const {
+        const int64_t e = M::BLOCK ? v0 + local : 8 * v0 + local;
+        orow[slot] = transform(p, row, static_cast<int32_t>(e));
+    }
+
+    __device__ void select_and_emit() {
+        const int tid = threadIdx.x;
+        const uint32_t k = static_cast<uint32_t>(p.k);
+        // Pass 1: high bytes. (Every lane of a warp runs every iteration: the
+        // warp-wide match in agg_add needs them all.)
+        for (uint32_t i0 = 0; i0 < n; i0 += NT) {
+            const uint32_t i = i0 + static_cast<uint32_t>(tid);
+            const uint32_t key = i < n ? s.key[i] : 0u;
+            agg_add(s.h[0], key >> 8, key != 0u);
+        }
+        gather(0);
+        uint32_t b1, above1, total;
+        const bool enough = find_bin256(s.all, k, b1, above1, total);
+        uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0;
+        const uint32_t lane = lane_id();
+        if (enough) {
+            // Pass 2: low bytes of the keys in bin b1.
+            for (uint32_t i0 = 0; i0 < n; i0 += NT) {
+                const uint32_t i = i0 + static_cast<uint32_t>(tid);
+                const uint32_t key = i < n ? s.key[i] : 0u;
+                agg_add(s.h[1], key & 0xFFu, key != 0u && (key >> 8) == b1);
+            }
+            gather(1);
+            uint32_t b2, above2, tot2;
+            find_bin256(s.all, k - above1, b2, above2, tot2);
+            T = (b1 << 8) | b2;
+            take = k - above1 - above2;
+            uint32_t x = 0;
+            for (uint32_t b = lane; b < 256u; b += 32u)
+                x += (b > b1 ? s.pre[0][b] : 0u) + (b > b2 ? s.pre[1][b] : 0u);
+            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
+            eq_prev = s.pre[1][b2];
+        } else {
+            // Fewer than k candidates in the row: every one of them.
+            uint32_t x = 0;
+            for (uint32_t b = lane; b < 256u; b += 32u) x += s.pre[0][b];
+            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
+            T = 0u;  // every key > 0
+        }
+        if (C > 1) cluster_arrive();  // done reading the peers' histograms
+        // This CTA's keys > T (after those of the lower ranks), then its quota
+        // of the lowest-index keys == T (after those of the lower ranks).
+        const uint32_t G = enough ? k - take : total;
+        const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
+        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        const uint32_t chunk = (n + NT - 1) / NT;  // contiguous per thread: ties in index order
+        const uint32_t lo = min(n, static_cast<uint32_t>(tid) * chunk), hi = min(n, lo + chunk);
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t i = lo; i < hi; ++i) {
+            const uint32_t key = s.key[i];
+            gt += key > T;
+            eq += key == T && T != 0u;
+        }
+        uint32_t tot;
+        const uint32_t incl = block_incl_scan(gt | (eq << 16), tot);
+        uint32_t rg = gt_prev + ((incl - (gt | (eq << 16))) & 0xFFFFu);
+        uint32_t re = (incl - (gt | (eq << 16))) >> 16;
+        for (uint32_t i = lo; i < hi; ++i) {
+            const uint32_t key = s.key[i];
+            if (key > T) put(orow, rg++, i);
+            else if (key == T && T != 0u) {
+                if (re < quota) put(orow, G + eq_prev + re, i);
+                ++re;
+            }
+        }
+        const uint32_t selected = enough ? k : total;
+        for (uint32_t i = selected + rank + static_cast<uint32_t>(tid) * C; i < k; i += NT * C) orow[i] = -1;
+        if (C > 1) cluster_wait();
+        else __syncthreads();
+        // Every peer is done with this row's histograms: zero them for the next.
+        s.h[0][tid] = 0u;
+        s.h[1][tid] = 0u;
+    }
+};
+
+template <class M>
+__global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const uint32_t C = cluster_size();
+    const uint32_t rank = cluster_rank();
+    const int32_t cid = static_cast<int32_t>(blockIdx.x / C);
+    const int32_t ncl = static_cast<int32_t>(gridDim.x / C);
+
+    grid_dependency_wait();
+    grid_dependents_release();
+    if (tid == 0) {
+        for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
+        fence_mbar_init();
+        s.abort_flag = 0u;
+    }
+    s.h[0][tid] = s.h[1][tid] = 0u;
+    __syncthreads();
+    Feed feed;
+    if (tid == 0) {
+        feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
+        for (int i = 0; i < NSTAGE && feed.row < p.rows; ++i) feed_issue(feed, s, i, p, M::BLOCK, ncl, C, rank);
+    }
+    if (C > 1) {  // every CTA started and zeroed before any distributed access
+        cluster_arrive();
+        cluster_wait();
+    }
+    Share<M> sh(s, p);
+    sh.C = C;
+    sh.rank = rank;
+    uint32_t seq = 0;
+    for (int32_t row = cid; row < p.rows; row += ncl) {
+        int32_t L;
+        int64_t V, v0, v1;
+        if (!row_share(p, M::BLOCK, row, C, rank, L, V, v0, v1)) {
+            const int32_t n = M::BLOCK ? (L + 7) >> 3 : L;
+            if (rank == 0) count_event(p, TOPK_CNT_BYPASS_ROWS);
+            const int32_t lo = static_cast<int32_t>(static_cast<int64_t>(p.k) * rank / C);
+            const int32_t hi = static_cast<int32_t>(static_cast<int64_t>(p.k) * (rank + 1) / C);
+            for (int32_t i = lo + tid; i < hi; i += NT)
+                p.out[static_cast<int64_t>(row) * p.k + i] = i < n ? transform(p, row, i) : -1;
+            continue;
+        }
+        sh.row = row;
+        sh.L = L;
+        sh.V = V;
+        sh.v0 = v0;
+        sh.n = static_cast<uint32_t>(M::BLOCK ? v1 - v0 : 8 * (v1 - v0));
+        const int ntiles = static_cast<int>((v1 - v0 + TILE_VEC - 1) / TILE_VEC);
+        for (int i = 0; i < ntiles; ++i, ++seq) {
+            const int st = static_cast<int>(seq % NSTAGE);
+            const int64_t tile_v0 = v0 + static_cast<int64_t>(i) * TILE_VEC;
+            const int nv = static_cast<int>(v1 - tile_v0 < TILE_VEC ? v1 - tile_v0 : TILE_VEC);
+            mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+            count_event(p, TOPK_CNT_ROUNDS);
+            sh.keep_tile(s.stage[st], tile_v0, nv);
+            __syncthreads();  // every thread is done with this stage
+            if (tid == 0 && feed.row < p.rows) {
+                fence_proxy_async();
+                feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);
+            }
+        }
+        if (rank == 0) count_event(p, TOPK_CNT_DIRECT_ROWS);
+        sh.select_and_emit();
+        __syncthreads();
+    }
+}
+
+}  // namespace direct
+
 // ------------------------------------------------------- one-tile rows kernel
 //
 // Rows whose valid prefix fits one tile (at most 2048 vectors) take a leaner
@@ -1861,7 +2102,6 @@ struct Row {
         for (int j = 0; j < NV; ++j) bal[j] = __ballot_sync(0xFFFFFFFFu, pass[j]);
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            const int pos = j * NT + static_cast<int>(threadIdx.x);
             if (pass[j]) s.queue[warp][q + __popc(bal[j] & lt)] = static_cast<uint8_t>((j << 5) | lane);
             q += __popc(bal[j]);
         }
@@ -2304,12 +2544,21 @@ Variant pick(bool block, bool) {
     return block ? variant<BlockMode, WIDE_NSTAGE, WIDE_CAP>() : variant<TokenMode, WIDE_NSTAGE, WIDE_CAP>();
 }
 
+// The resident-keys kernel (block rows wider than one tile).
+Variant pick_direct(bool block) {
+    return block ? Variant{reinterpret_cast<const void *>(&direct::topk_direct_kernel<BlockMode>),
+                           static_cast<int>(sizeof(direct::Smem))}
+                 : Variant{reinterpret_cast<const void *>(&direct::topk_direct_kernel<TokenMode>),
+                           static_cast<int>(sizeof(direct::Smem))};
+}
+
 struct DeviceInit {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int per_sm[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [block][wide]
     int per_sm_one[2][ONE_BUILDS] = {};    // the one-tile kernel, [block][build]
+    int per_sm_direct[2] = {0, 0};         // the resident-keys kernel, [block]
 };
 DeviceInit g_init[64];
 
@@ -2329,6 +2578,16 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                                                                       static_cast<size_t>(v.smem));
                 if (e == cudaSuccess && d.per_sm[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            const Variant v = pick_direct(b != 0);
+            e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_direct[b], v.fn, direct::NT,
+                                                                  static_cast<size_t>(v.smem));
+            if (e == cudaSuccess && d.per_sm_direct[b] < 1) e = cudaErrorInvalidConfiguration;
+        }
         for (int b = 0; b < 2 && e == cudaSuccess; ++b)
             for (int w = 0; w < ONE_BUILDS && e == cudaSuccess; ++w) {
                 const Variant v = pick_one(b != 0, w);
@@ -2344,40 +2603,49 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
     return d.err;
 }
 
+enum Kind { KIND_ONE = 0, KIND_STREAM = 1, KIND_DIRECT = 2 };
+
 struct Plan {
+    int kind;          // which kernel
     int cluster;
-    bool wide;         // the streamed kernel
     int build;         // one-tile rows: which build (see pick_one)
     int threads;
     int64_t clusters;  // persistent clusters launched
     bool spare;        // some resident slots stay free (the launch may overlap the previous one)
 };
 
-// One CTA per row when a row fits one stage. Wider rows: the smallest cluster
-// that puts about one CTA on every resident slot, at most 16, and never so many
-// CTAs that a share is below one stage. Clusters are persistent, so the grid
-// never exceeds what is resident at once.
-Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int forced) {
+// One CTA per row when a row fits one stage. Wider rows: block rows keep
+// their keys resident across the smallest cluster that holds them (the
+// direct kernel); token rows stream through a candidate buffer. Either way the
+// cluster grows, up to 16, while that puts about one CTA on every resident slot
+// and leaves every CTA at least one stage. Clusters are persistent, so the grid
+// never exceeds what is resident at once. path: 0 automatic, 1 streamed, 2 direct.
+Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int forced, int path) {
     const int64_t vecs = (static_cast<int64_t>(width) + 7) / 8;
-    Plan pl{1, vecs > TILE_VEC, 0, THREADS, 1, false};
-    if (forced > 0) {
-        pl.cluster = forced;
-        pl.wide = pl.wide || forced > 1;
-    } else if (pl.wide) {
-        const int64_t slots = static_cast<int64_t>(d.sms) * d.per_sm[block][1];
-        const int64_t stages = (vecs + TILE_VEC - 1) / TILE_VEC;
-        int c = 1;
-        while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages) c *= 2;
-        pl.cluster = c;
-    }
-    if (!pl.wide) {
+    const int64_t per_vec = block ? 1 : 8;  // elements per vector
+    Plan pl{KIND_ONE, 1, 0, THREADS, 1, false};
+    int c_res = 1;  // the smallest cluster whose shares fit as resident keys
+    while (c_res < 16 && (vecs + c_res - 1) / c_res * per_vec > direct::RES) c_res *= 2;
+    const bool fits = (vecs + c_res - 1) / c_res * per_vec <= direct::RES;
+    if (path == 2 && fits) pl.kind = KIND_DIRECT;
+    else if (path == 1 || vecs > TILE_VEC || forced > 1) pl.kind = block && fits && path != 1 ? KIND_DIRECT : KIND_STREAM;
+    if (pl.kind == KIND_ONE) {
         // Rows that leave SMs idle at one 512-thread CTA each take that build:
         // twice the threads on every row, so half the row's latency.
         pl.build = rows <= d.sms * d.per_sm_one[block][2] ? 2 : (k <= 1024 ? 0 : 1);
         pl.threads = pl.build == 2 ? 512 : 256;
     }
-    const int64_t slots = pl.wide ? static_cast<int64_t>(d.sms) * d.per_sm[block][1]
-                                  : static_cast<int64_t>(d.sms) * d.per_sm_one[block][pl.build];
+    const int per_sm = pl.kind == KIND_ONE ? d.per_sm_one[block][pl.build]
+                       : pl.kind == KIND_STREAM ? d.per_sm[block][1] : d.per_sm_direct[block];
+    const int64_t slots = static_cast<int64_t>(d.sms) * per_sm;
+    if (forced > 0) {
+        pl.cluster = pl.kind == KIND_DIRECT ? max(forced, c_res) : forced;
+    } else if (pl.kind != KIND_ONE) {
+        const int64_t stages = (vecs + TILE_VEC - 1) / TILE_VEC;
+        int c = pl.kind == KIND_DIRECT ? c_res : 1;
+        while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages) c *= 2;
+        pl.cluster = c;
+    }
     const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
     pl.spare = pl.clusters * pl.cluster < slots;
@@ -2414,6 +2682,8 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
                                   table_stride, page_size, out);
     if (st != TOPK_OK || rows == 0) return st;
     const int forced = opt ? opt->cluster : 0;
+    const int path = opt ? opt->path : 0;
+    if (path < 0 || path > 2) return TOPK_ERR_ARG;
     if (forced != 0 && forced != 1 && forced != 2 && forced != 4 && forced != 8 && forced != 16)
         return TOPK_ERR_ARG;
     int dev = 0;
@@ -2422,8 +2692,9 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     if (init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
 
     const bool block = mode == TOPK_BLOCK8;
-    const Plan pl = make_plan(rows, width, k, *d, block, forced);
-    const Variant v = pl.wide ? pick(block, true) : pick_one(block, pl.build);
+    const Plan pl = make_plan(rows, width, k, *d, block, forced, path);
+    const Variant v = pl.kind == KIND_ONE ? pick_one(block, pl.build)
+                      : pl.kind == KIND_STREAM ? pick(block, true) : pick_direct(block);
     const int threads = pl.threads;
 
     Params prm;
@@ -2514,13 +2785,14 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
     topk::DeviceInit *d = nullptr;
     if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
     if (topk::init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
-    const topk::Plan pl = topk::make_plan(rows, width, k, *d, mode == TOPK_BLOCK8, 0);
-    const topk::Variant v = pl.wide ? topk::pick(mode == TOPK_BLOCK8, true)
-                                    : topk::pick_one(mode == TOPK_BLOCK8, pl.build);
+    const bool block = mode == TOPK_BLOCK8;
+    const topk::Plan pl = topk::make_plan(rows, width, k, *d, block, 0, 0);
+    const topk::Variant v = pl.kind == topk::KIND_ONE ? topk::pick_one(block, pl.build)
+                            : pl.kind == topk::KIND_STREAM ? topk::pick(block, true) : topk::pick_direct(block);
     if (cluster) *cluster = pl.cluster;
     if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = v.smem;
-    if (variant) *variant = pl.wide ? 1 : 0;
+    if (variant) *variant = pl.kind;
     return TOPK_OK;
 }
 

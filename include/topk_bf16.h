@@ -100,6 +100,9 @@ typedef struct {
     int32_t cluster;        /* 0: automatic; else CTAs per row: 1, 2, 4, 8 or 16 */
     uint32_t *counters;     /* NULL, or device uint32 [TOPK_NUM_COUNTERS] that each
                                launch adds its path counts and cycle split to */
+    int32_t path;           /* rows wider than one stage: 0 automatic, 1 candidate buffer
+                               (streamed), 2 resident keys (direct; rows whose cluster
+                               shares fit 16384 keys per CTA) */
 } topk_bf16_options_t;
 
 /* Indices into topk_bf16_options_t.counters. */
@@ -137,6 +140,7 @@ enum {
     TOPK_CNT_CYC_F_FIND = 25,    /*   the buffer's k-th key for the next threshold */
     TOPK_CNT_CYC_F_LOOP = 26,    /*   end of tile: barrier and the next copy's issue */
     TOPK_CNT_TIE_FILLS = 27,     /* streamed first tiles completed with lowest-index ties at their cut */
+    TOPK_CNT_DIRECT_ROWS = 28,   /* rows selected from resident keys (the direct kernel) */
     TOPK_NUM_COUNTERS = 32
 };
 
@@ -151,7 +155,8 @@ topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, in
 /*
  * The launch topk_bf16_select would make for these sizes on the current device:
  * CTAs per row, threads per CTA, dynamic shared memory bytes and the kernel
- * variant (0 = one-tile rows, 1 = streamed rows). Any output pointer may be NULL.
+ * variant (0 = one-tile rows, 1 = streamed rows, 2 = resident keys). Any output
+ * pointer may be NULL.
  */
 topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t mode,
                              int32_t *cluster, int32_t *threads, int32_t *smem_bytes,

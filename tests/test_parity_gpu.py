@@ -153,3 +153,33 @@ def test_carried_cut_hits_and_misses(mode, width, k):
     c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
     assert c["guess_hit"] > 0 and c["guess_miss"] > 0, c
     assert tk.plan(case.rows, case.width, case.k, case.mode)["variant"] == "one-tile"
+
+
+@pytest.mark.parametrize("cluster", [0, 1, 4, 16])
+@pytest.mark.parametrize("mode", [W.TOKEN, W.BLOCK8])
+@pytest.mark.parametrize("k", [1, 300, 2048])
+def test_resident_keys_path(cluster, mode, k):
+    """The resident-keys kernel (two cluster-wide radix passes over the keys of
+    every share) on ragged rows, token and block, at several cluster sizes."""
+    case = W.ragged_case(seed=40 + k + cluster, rows=9, width=100003, row_stride=100008, k=k,
+                         mode=mode, with_table=True)
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    assert_same_sets(run_gpu(case, cluster=cluster, path=2, counters=counters), run_oracle(case), case.name)
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["direct_rows"] + c["bypass_rows"] == case.rows, c
+
+
+def test_resident_keys_crowded_and_edges():
+    check(W.config3(0, rows=64, width=150000), path=2)
+    for case in W.edge_cases(2, width=40000, k=512):
+        check(case, path=2)
+        check(case, path=2, cluster=4)
+
+
+def test_block_rows_streamed_path():
+    """Block rows wider than one stage take the resident-keys kernel; the
+    candidate-buffer kernel stays exact on them too."""
+    case = W.config4(0, rows=8, width=1 << 18)
+    assert tk.plan(case.rows, case.width, case.k, case.mode)["variant"] == "direct"
+    check(case, path=1)
+    check(case, path=1, cluster=2)

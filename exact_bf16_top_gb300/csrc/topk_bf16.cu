@@ -1588,27 +1588,51 @@ struct Share {
         orow[slot] = transform(p, row, static_cast<int32_t>(e));
     }
 
+    // Key h (0..7) of a group of eight packed in a uint4.
+    static __device__ __forceinline__ uint32_t key_of(const uint4 &w, int h) {
+        const uint32_t x = (h & 4) ? ((h & 2) ? w.w : w.z) : ((h & 2) ? w.y : w.x);
+        return (h & 1) ? (x >> 16) : (x & 0xFFFFu);
+    }
+
+    // The keys are read eight at a time (16 bytes, consecutive across lanes);
+    // groups past the share read as zero (no candidate).
     __device__ void select_and_emit() {
         const int tid = threadIdx.x;
         const uint32_t k = static_cast<uint32_t>(p.k);
+        const uint32_t groups = (n + 7u) / 8u;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(s.key);
+        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+        PhaseClock clk;
+        clk.start(p);
         // Pass 1: high bytes. (Every lane of a warp runs every iteration: the
         // warp-wide match in agg_add needs them all.)
-        for (uint32_t i0 = 0; i0 < n; i0 += NT) {
-            const uint32_t i = i0 + static_cast<uint32_t>(tid);
-            const uint32_t key = i < n ? s.key[i] : 0u;
-            agg_add(s.h[0], key >> 8, key != 0u);
+        for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
+            const uint32_t g = g0 + static_cast<uint32_t>(tid);
+            const uint4 w = g < groups ? k4[g] : zero4;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = key_of(w, h);
+                agg_add(s.h[0], key >> 8, key != 0u);
+            }
         }
         gather(0);
+        clk.stop(p, TOPK_CNT_CYC_CUT);
+        clk.start(p);
         uint32_t b1, above1, total;
         const bool enough = find_bin256(s.all, k, b1, above1, total);
         uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0;
         const uint32_t lane = lane_id();
         if (enough) {
-            // Pass 2: low bytes of the keys in bin b1.
-            for (uint32_t i0 = 0; i0 < n; i0 += NT) {
-                const uint32_t i = i0 + static_cast<uint32_t>(tid);
-                const uint32_t key = i < n ? s.key[i] : 0u;
-                agg_add(s.h[1], key & 0xFFu, key != 0u && (key >> 8) == b1);
+            // Pass 2: low bytes of the keys in bin b1 (a warp with none skips the match).
+            for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
+                const uint32_t g = g0 + static_cast<uint32_t>(tid);
+                const uint4 w = g < groups ? k4[g] : zero4;
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = key_of(w, h);
+                    const bool in = key != 0u && (key >> 8) == b1;
+                    if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.h[1], key & 0xFFu, in);
+                }
             }
             gather(1);
             uint32_t b2, above2, tot2;
@@ -1628,35 +1652,62 @@ struct Share {
             T = 0u;  // every key > 0
         }
         if (C > 1) cluster_arrive();  // done reading the peers' histograms
-        // This CTA's keys > T (after those of the lower ranks), then its quota
-        // of the lowest-index keys == T (after those of the lower ranks).
+        clk.stop(p, TOPK_CNT_CYC_EXACT);
+        clk.start(p);
+        // This CTA's keys > T (after those of the lower ranks, in any order),
+        // then its quota of the lowest-index keys == T (after those of the
+        // lower ranks). Each thread owns a contiguous run of groups, so ties
+        // rank in index order by thread, then within the run.
         const uint32_t G = enough ? k - take : total;
         const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
+        const bool ties = enough;  // T > 0: keys == T may be taken
         int32_t *orow = p.out + static_cast<int64_t>(row) * k;
-        const uint32_t chunk = (n + NT - 1) / NT;  // contiguous per thread: ties in index order
-        const uint32_t lo = min(n, static_cast<uint32_t>(tid) * chunk), hi = min(n, lo + chunk);
+        const uint32_t run = (groups + NT - 1) / NT;
+        const uint32_t g_lo = min(groups, static_cast<uint32_t>(tid) * run);
+        const uint32_t g_n = min(groups, g_lo + run) - g_lo;
         uint32_t gt = 0, eq = 0;
-        for (uint32_t i = lo; i < hi; ++i) {
-            const uint32_t key = s.key[i];
-            gt += key > T;
-            eq += key == T && T != 0u;
+        for (uint32_t j = 0; j < g_n; ++j) {
+            const uint32_t g = g_lo + (j + lane) % g_n;  // rotated: lanes spread over banks
+            const uint4 w = k4[g];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = key_of(w, h);
+                gt += key > T;
+                eq += ties && key == T;
+            }
         }
         uint32_t tot;
-        const uint32_t incl = block_incl_scan(gt | (eq << 16), tot);
-        uint32_t rg = gt_prev + ((incl - (gt | (eq << 16))) & 0xFFFFu);
-        uint32_t re = (incl - (gt | (eq << 16))) >> 16;
-        for (uint32_t i = lo; i < hi; ++i) {
-            const uint32_t key = s.key[i];
-            if (key > T) put(orow, rg++, i);
-            else if (key == T && T != 0u) {
-                if (re < quota) put(orow, G + eq_prev + re, i);
-                ++re;
+        const uint32_t packed = gt | (eq << 16);
+        const uint32_t ex = block_incl_scan(packed, tot) - packed;
+        uint32_t rg = gt_prev + (ex & 0xFFFFu);
+        if (gt) {
+            for (uint32_t j = 0; j < g_n; ++j) {
+                const uint32_t g = g_lo + (j + lane) % g_n;
+                const uint4 w = k4[g];
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if (key_of(w, h) > T) put(orow, rg++, 8u * g + static_cast<uint32_t>(h));
+            }
+        }
+        uint32_t re = ex >> 16;
+        if (eq && re < quota) {  // in index order
+            for (uint32_t j = 0; j < g_n && re < quota; ++j) {
+                const uint32_t g = g_lo + j;
+                const uint4 w = k4[g];
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    if (key_of(w, h) == T) {
+                        if (re < quota) put(orow, G + eq_prev + re, 8u * g + static_cast<uint32_t>(h));
+                        ++re;
+                    }
+                }
             }
         }
         const uint32_t selected = enough ? k : total;
         for (uint32_t i = selected + rank + static_cast<uint32_t>(tid) * C; i < k; i += NT * C) orow[i] = -1;
         if (C > 1) cluster_wait();
         else __syncthreads();
+        clk.stop(p, TOPK_CNT_CYC_FINISH);
         // Every peer is done with this row's histograms: zero them for the next.
         s.h[0][tid] = 0u;
         s.h[1][tid] = 0u;
@@ -1717,15 +1768,23 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
             const int st = static_cast<int>(seq % NSTAGE);
             const int64_t tile_v0 = v0 + static_cast<int64_t>(i) * TILE_VEC;
             const int nv = static_cast<int>(v1 - tile_v0 < TILE_VEC ? v1 - tile_v0 : TILE_VEC);
+            PhaseClock clk;
+            clk.start(p);
             mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+            clk.stop(p, TOPK_CNT_CYC_WAIT);
             count_event(p, TOPK_CNT_ROUNDS);
+            clk.start(p);
             sh.keep_tile(s.stage[st], tile_v0, nv);
             __syncthreads();  // every thread is done with this stage
+            clk.stop(p, TOPK_CNT_CYC_FILTER);
             if (tid == 0 && feed.row < p.rows) {
                 fence_proxy_async();
                 feed_issue(feed, s, st, p, M::BLOCK, ncl, C, rank);
             }
         }
+        if (tid == 0)  // the last group's keys past the share: no candidates
+            for (uint32_t i = sh.n; i < ((sh.n + 7u) & ~7u); ++i) s.key[i] = 0u;
+        __syncthreads();
         if (rank == 0) count_event(p, TOPK_CNT_DIRECT_ROWS);
         sh.select_and_emit();
         __syncthreads();

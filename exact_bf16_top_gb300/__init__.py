@@ -72,6 +72,9 @@ def load(path: str | None = None):
         lib.topk_bf16_select.argtypes = sel_args
         lib.topk_bf16_select.restype = ctypes.c_int
         lib.topk_bf16_select_ex.argtypes = sel_args + [ctypes.POINTER(_Options)]
+        lib.topk_bf16_select_paged.restype = ctypes.c_int
+        lib.topk_bf16_select_paged.argtypes = (sel_args[:10] + [ctypes.c_int32, ctypes.c_int32]
+                                               + sel_args[10:])
         lib.topk_bf16_select_ex.restype = ctypes.c_int
         lib.topk_bf16_status_string.argtypes = [ctypes.c_int]
         lib.topk_bf16_status_string.restype = ctypes.c_char_p
@@ -97,7 +100,8 @@ def _ptr(t) -> int | None:
 
 def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_size: int = 64,
            out=None, width: int | None = None, stream=None, *, force_direct: bool = False,
-           cluster: int = 0, counters=None, path: int = 0):
+           cluster: int = 0, counters=None, path: int = 0, block_rows: int | None = None,
+           rows_per_request: int = 1):
     """Exact top-k of every row of ``logits`` -> int32 [rows, k] on the same device.
 
     logits: CUDA bfloat16 (or int16/uint16 holding BF16 bits) [rows, row_stride]
@@ -105,6 +109,8 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
     block_table: None or CUDA int32 [rows, pages] (unit inner stride);
     width: logits per row that may be valid (default: logits.shape[1]);
     stream: a torch.cuda.Stream (default: the current stream);
+    block_rows / rows_per_request: the full transform (see topk_bf16_select_paged):
+    physical rows per page (default page_size) and rows sharing one table row;
     force_direct / cluster / counters / path: test hooks (see topk_bf16_select_ex).
     """
     import torch
@@ -129,10 +135,12 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
         raise ValueError("valid_len must be a contiguous CUDA int32 tensor with one entry per row")
     table_stride = 0
     if block_table is not None:
+        requests = -(-rows // max(int(rows_per_request), 1))
         if not (block_table.is_cuda and block_table.dtype == torch.int32 and block_table.dim() == 2
-                and block_table.shape[0] == rows and block_table.stride(1) == 1):
-            raise ValueError("block_table must be CUDA int32 [rows, pages] with unit inner stride")
-        table_stride = block_table.stride(0) if rows > 1 else block_table.shape[1]
+                and block_table.shape[0] >= requests and block_table.stride(1) == 1):
+            raise ValueError("block_table must be CUDA int32 [ceil(rows / rows_per_request), pages] "
+                             "with unit inner stride")
+        table_stride = block_table.stride(0) if block_table.shape[0] > 1 else block_table.shape[1]
     if out is None:
         out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
     elif not (out.is_cuda and out.dtype == torch.int32 and out.shape == (rows, k) and out.is_contiguous()):
@@ -144,7 +152,13 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
         args = (_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), int(mode),
                 _ptr(block_table), table_stride, int(page_size), _ptr(out),
                 ctypes.c_void_p(stream.cuda_stream))
-        if force_direct or cluster or counters is not None or path:
+        paged = (block_rows is not None and int(block_rows) != int(page_size)) or int(rows_per_request) != 1
+        if paged:
+            if force_direct or cluster or counters is not None or path:
+                raise ValueError("the test hooks do not combine with block_rows / rows_per_request")
+            st = lib.topk_bf16_select_paged(*args[:10], int(page_size if block_rows is None else block_rows),
+                                            int(rows_per_request), *args[10:])
+        elif force_direct or cluster or counters is not None or path:
             opt = _Options(1 if force_direct else 0, int(cluster),
                            None if counters is None else counters.data_ptr(), int(path))
             st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))

@@ -75,6 +75,8 @@ struct Params {
     int32_t k;
     const int32_t *table;
     int32_t table_stride, page_shift;
+    int32_t block_rows;                      // physical rows per page
+    int32_t rows_per_request;                // rows sharing one table row
     int32_t *out;
     uint32_t *counters;
     int32_t force_direct;
@@ -427,10 +429,18 @@ struct PhaseClock {
     }
 };
 
+// The table row of a row: its request's (IndexerSelect: request = row / q).
+__device__ __forceinline__ const int32_t *table_row(const Params &p, int32_t row) {
+    const int32_t request = p.rows_per_request == 1 ? row : row / p.rows_per_request;
+    return p.table + static_cast<int64_t>(request) * p.table_stride;
+}
+
+// Page of element i times the physical rows per page, plus i's offset in its
+// page (IndexerSelect.emit).
 __device__ __forceinline__ int32_t transform(const Params &p, int32_t row, int32_t i) {
     if (!p.table) return i;
-    const int32_t page = p.table[static_cast<int64_t>(row) * p.table_stride + (i >> p.page_shift)];
-    return (page << p.page_shift) | (i & ((1 << p.page_shift) - 1));
+    const int32_t page = table_row(p, row)[i >> p.page_shift];
+    return page * p.block_rows + (i & ((1 << p.page_shift) - 1));
 }
 
 // Warp-aggregated reservation of `n` slots (lane 0 adds; every lane gets base).
@@ -1930,7 +1940,7 @@ struct Row {
 
     __device__ __forceinline__ void put(uint32_t slot, uint32_t idx) const {
         int32_t v = static_cast<int32_t>(idx);
-        if (tab) v = (s.tab[idx >> p.page_shift] << p.page_shift) | (v & ((1 << p.page_shift) - 1));
+        if (tab) v = s.tab[idx >> p.page_shift] * p.block_rows + (v & ((1 << p.page_shift) - 1));
         else v = transform(p, row, v);
         orow[slot] = v;
     }
@@ -2337,7 +2347,7 @@ struct Row {
             const uint32_t npages = (nE + (1u << p.page_shift) - 1u) >> p.page_shift;
             if (npages <= static_cast<uint32_t>(TAB_CAP)) {
                 tab = true;
-                const int32_t *trow = p.table + static_cast<int64_t>(row) * p.table_stride;
+                const int32_t *trow = table_row(p, row);
                 if (tid < npages) t0 = __ldg(trow + tid);
             }
         }
@@ -2735,8 +2745,10 @@ topk_status_t check_args(const uint16_t *logits, int64_t row_stride, int32_t row
 
 topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
                      const int32_t *valid_len, int32_t k, topk_mode_t mode, const int32_t *table,
-                     int32_t table_stride, int32_t page_size, int32_t *out, void *stream,
-                     const topk_bf16_options_t *opt) {
+                     int32_t table_stride, int32_t page_size, int32_t block_rows, int32_t q,
+                     int32_t *out, void *stream, const topk_bf16_options_t *opt) {
+    if (q < 1) return TOPK_ERR_ARG;
+    if (table && (block_rows < page_size || (block_rows & (block_rows - 1)) != 0)) return TOPK_ERR_ARG;
     topk_status_t st = check_args(logits, row_stride, rows, width, valid_len, k, mode, table,
                                   table_stride, page_size, out);
     if (st != TOPK_OK || rows == 0) return st;
@@ -2765,6 +2777,8 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     prm.k = k;
     prm.table = table;
     prm.table_stride = table_stride;
+    prm.block_rows = block_rows;
+    prm.rows_per_request = q;
     prm.page_shift = 0;
     if (table)
         while ((1 << prm.page_shift) < page_size) ++prm.page_shift;
@@ -2810,7 +2824,16 @@ topk_status_t topk_bf16_select(const uint16_t *logits, int64_t row_stride, int32
                                int32_t table_stride, int32_t page_size, int32_t *out,
                                void *stream) {
     return topk::launch(logits, row_stride, rows, width, valid_len, k, mode, block_table,
-                        table_stride, page_size, out, stream, nullptr);
+                        table_stride, page_size, page_size, 1, out, stream, nullptr);
+}
+
+topk_status_t topk_bf16_select_paged(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                     int32_t width, const int32_t *valid_len, int32_t k,
+                                     topk_mode_t mode, const int32_t *block_table,
+                                     int32_t table_stride, int32_t page_size, int32_t block_rows,
+                                     int32_t rows_per_request, int32_t *out, void *stream) {
+    return topk::launch(logits, row_stride, rows, width, valid_len, k, mode, block_table,
+                        table_stride, page_size, block_rows, rows_per_request, out, stream, nullptr);
 }
 
 topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, int32_t rows,
@@ -2819,7 +2842,7 @@ topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, in
                                   int32_t table_stride, int32_t page_size, int32_t *out,
                                   void *stream, const topk_bf16_options_t *options) {
     return topk::launch(logits, row_stride, rows, width, valid_len, k, mode, block_table,
-                        table_stride, page_size, out, stream, options);
+                        table_stride, page_size, page_size, 1, out, stream, options);
 }
 
 const char *topk_bf16_status_string(topk_status_t status) {

@@ -87,6 +87,27 @@ topk_status_t topk_bf16_select(const uint16_t *logits, int64_t row_stride, int32
                                int32_t table_stride, int32_t page_size, int32_t *out,
                                void *stream);
 
+/*
+ * topk_bf16_select with the full block-table transform of the indexer page
+ * (vLLM kimi_k3 "dsa/indexer": IndexerSelect's docstring and kernel, and
+ * IndexerSelect.emit): rows come in requests of rows_per_request consecutive rows
+ * that share one table row (request = row / rows_per_request), and each page of
+ * page_size elements maps to block_rows physical rows:
+ *     physical = block_table[request * table_stride + i / page_size] * block_rows
+ *                + i % page_size.
+ * block_rows is a power of two >= page_size (64, or e.g. 2048 in hybrid models);
+ * the caller keeps page ids small enough that physical indices fit int32.
+ * block_table holds ceil(rows / rows_per_request) rows. topk_bf16_select is this
+ * call with rows_per_request = 1 and block_rows = page_size.
+ * Errors as topk_bf16_select, plus TOPK_ERR_ARG for rows_per_request < 1 or a bad
+ * block_rows (checked when block_table is not NULL).
+ */
+topk_status_t topk_bf16_select_paged(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                     int32_t width, const int32_t *valid_len, int32_t k,
+                                     topk_mode_t mode, const int32_t *block_table,
+                                     int32_t table_stride, int32_t page_size, int32_t block_rows,
+                                     int32_t rows_per_request, int32_t *out, void *stream);
+
 /* Human-readable name of a status (a static string). */
 const char *topk_bf16_status_string(topk_status_t status);
 

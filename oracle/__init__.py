@@ -54,6 +54,12 @@ def _bind(path: str):
                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int32]
+    g = lib.oracle_topk_bf16_paged
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32]
     return lib
 
 
@@ -69,13 +75,15 @@ def load(path: str | None = None):
 
 
 def topk(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_size: int = 64,
-         width: int | None = None, threads: int = 1, lib=None) -> np.ndarray:
+         width: int | None = None, threads: int = 1, lib=None, block_rows: int | None = None,
+         rows_per_request: int = 1) -> np.ndarray:
     """Exact top-k of every row; returns int32 [rows, k] (selected indices, then -1).
 
     logits: uint16/int16 array [rows, row_stride] of BF16 bits (a torch tensor
     of dtype bfloat16/int16 on the CPU is accepted too); valid_len: int [rows];
-    block_table: None (identity) or int32 [rows, pages]; width: the row width
-    (defaults to row_stride).
+    block_table: None (identity) or int32 [ceil(rows / rows_per_request), pages];
+    width: the row width (defaults to row_stride); block_rows: physical rows per
+    page (default page_size); rows_per_request: rows sharing one table row.
     """
     logits = _as_u16(logits)
     if logits.ndim != 2:
@@ -88,13 +96,15 @@ def topk(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_si
     table_ptr, table_stride = None, 0
     if block_table is not None:
         table = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
-        if table.ndim != 2 or table.shape[0] != rows:
-            raise ValueError("block_table must be [rows, pages]")
+        if table.ndim != 2 or table.shape[0] < -(-rows // rows_per_request):
+            raise ValueError("block_table needs ceil(rows / rows_per_request) rows of pages")
         table_ptr, table_stride = table.ctypes.data, table.shape[1]
     out = np.empty((rows, k), dtype=np.int32)
     lib = lib or load()
-    rc = lib.oracle_topk_bf16(logits.ctypes.data, stride, rows, width, valid.ctypes.data, k, mode,
-                              table_ptr, table_stride, page_size, out.ctypes.data, threads)
+    rc = lib.oracle_topk_bf16_paged(logits.ctypes.data, stride, rows, width, valid.ctypes.data, k,
+                                    mode, table_ptr, table_stride, page_size,
+                                    page_size if block_rows is None else block_rows,
+                                    rows_per_request, out.ctypes.data, threads)
     if rc != 0:
         raise RuntimeError("oracle_topk_bf16 failed (bad argument or out of memory)")
     return out

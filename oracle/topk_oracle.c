@@ -69,15 +69,21 @@ typedef struct {
     int32_t k, mode;
     const int32_t *table;
     int32_t table_stride, page;
+    int32_t block_rows, rows_per_request;
     int32_t *out;
     int32_t first_row, row_step;
     int status;
 } job_t;
 
-/* Block-table transform of a logical element index (IndexerSelect.emit). */
+/* Block-table transform of a logical element index (vLLM kimi_k3 "dsa/indexer",
+ * IndexerSelect: a row belongs to request row / q, whose table row it reads;
+ * IndexerSelect.emit: the page's id times the physical rows per page, plus the
+ * element's offset in its page). */
 static int32_t transform(const job_t *j, int32_t r, int32_t i) {
     if (!j->table) return i;
-    return j->table[(int64_t)r * j->table_stride + i / j->page] * j->page + i % j->page;
+    const int32_t request = r / j->rows_per_request;
+    const int64_t page_id = j->table[(int64_t)request * j->table_stride + i / j->page];
+    return (int32_t)(page_id * j->block_rows + i % j->page);
 }
 
 static int one_row(const job_t *j, int32_t r) {
@@ -138,24 +144,27 @@ static void *worker(void *arg) {
 
 /*
  * logits: BF16 bits, row r at logits + r * row_stride; valid_len: [rows];
- * block_table: NULL (identity) or [rows, table_stride] page ids, page elements
- * per page; out: [rows, k] int32. threads: worker threads over rows (<= 1: the
- * calling thread only). Returns 0, or 1 on a bad argument or allocation failure.
+ * block_table: NULL (identity) or [ceil(rows / rows_per_request), table_stride]
+ * page ids, page_size elements per page, block_rows physical rows per page;
+ * out: [rows, k] int32. threads: worker threads over rows (<= 1: the calling
+ * thread only). Returns 0, or 1 on a bad argument or allocation failure.
  */
-int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
-                     const int32_t *valid_len, int32_t k, int32_t mode,
-                     const int32_t *block_table, int32_t table_stride, int32_t page_size,
-                     int32_t *out, int32_t threads) {
+int oracle_topk_bf16_paged(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                           int32_t width, const int32_t *valid_len, int32_t k, int32_t mode,
+                           const int32_t *block_table, int32_t table_stride, int32_t page_size,
+                           int32_t block_rows, int32_t rows_per_request, int32_t *out,
+                           int32_t threads) {
     if (rows < 0 || width < 0 || k < 1 || row_stride < width) return 1;
     if (mode != ORACLE_TOKEN && mode != ORACLE_BLOCK8) return 1;
-    if (block_table && page_size < 1) return 1;
+    if (block_table && (page_size < 1 || block_rows < 1 || rows_per_request < 1)) return 1;
     if (rows == 0) return 0;
     if (!logits || !valid_len || !out) return 1;
     if (threads < 1) threads = 1;
     if (threads > rows) threads = rows;
 
     job_t base = {logits, row_stride, rows, width, valid_len, k, mode,
-                  block_table, table_stride, page_size, out, 0, 1, 0};
+                  block_table, table_stride, page_size, block_rows, rows_per_request,
+                  out, 0, 1, 0};
     if (threads == 1) {
         worker(&base);
         return base.status;
@@ -179,4 +188,14 @@ int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     free(jobs);
     free(tids);
     return status;
+}
+
+/* The transform with one table row per row and page_size physical rows per page. */
+int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                     const int32_t *valid_len, int32_t k, int32_t mode,
+                     const int32_t *block_table, int32_t table_stride, int32_t page_size,
+                     int32_t *out, int32_t threads) {
+    return oracle_topk_bf16_paged(logits, row_stride, rows, width, valid_len, k, mode,
+                                  block_table, table_stride, page_size, page_size, 1, out,
+                                  threads);
 }

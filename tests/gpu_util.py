@@ -22,6 +22,8 @@ def upload(case, device="cuda"):
 
 def run_gpu(case, **opts):
     logits, valid, table = upload(case)
+    if case.block_rows is not None or case.rows_per_request != 1:
+        opts = dict(opts, block_rows=case.block_rows, rows_per_request=case.rows_per_request)
     out = tk.select(logits, valid, case.k, case.mode, table, case.page_size, width=case.width, **opts)
     torch.cuda.synchronize()
     return out.cpu().numpy()
@@ -29,7 +31,8 @@ def run_gpu(case, **opts):
 
 def run_oracle(case):
     return oracle.topk(case.logits, case.valid_len, case.k, case.mode, case.block_table,
-                       case.page_size, width=case.width, threads=THREADS)
+                       case.page_size, width=case.width, threads=THREADS,
+                       block_rows=case.block_rows, rows_per_request=case.rows_per_request)
 
 
 def assert_same_sets(got, exp, name=""):

@@ -61,6 +61,27 @@ def check_golden(lib) -> list[str]:
         got = oracle.topk(row[None, :], [c["valid_len"]], c["k"], c["mode"], table, lib=lib)
         if sorted(got[0].tolist()) != c["expected"]:
             bad.append(f"golden {c['name']}: {sorted(got[0].tolist())} != {c['expected']}")
+    return bad + check_paged_golden(lib)
+
+
+def check_paged_golden(lib) -> list[str]:
+    """tests/golden/paged_cases.json: requests of several rows, block rows != page."""
+    with open(os.path.join(HERE, "golden", "paged_cases.json")) as fh:
+        data = json.load(fh)
+    bad = []
+    for c in data["cases"]:
+        rows = []
+        for r in c["rows"]:
+            row = np.full(c["width"], int(r["fill"], 16), np.uint16)
+            for pos, h in r.get("set", {}).items():
+                row[int(pos)] = int(h, 16)
+            rows.append(row)
+        got = oracle.topk(np.stack(rows), [r["valid_len"] for r in c["rows"]], c["k"], c["mode"],
+                          np.array(c["table"], np.int32), c["page_size"], lib=lib,
+                          block_rows=c["block_rows"], rows_per_request=c["rows_per_request"])
+        got = [sorted(g.tolist()) for g in got]
+        if got != c["expected"]:
+            bad.append(f"paged golden {c['name']}: {got} != {c['expected']}")
     return bad
 
 
@@ -234,7 +255,9 @@ MUTANTS = [
     ("newest block not pinned", [("if (i == n - 1) { nan = 0; key = KEY_POS_INF; }", "")]),
     ("-inf blocks not written as -1", [("j->mode == ORACLE_BLOCK8 && key == KEY_NEG_INF", "0")]),
     ("bypass misses n == k", [("if (n <= j->k) {", "if (n < j->k) {")]),
-    ("page offset dropped", [("* j->page + i % j->page", "* j->page")]),
+    ("page offset dropped", [("page_id * j->block_rows + i % j->page", "page_id * j->block_rows")]),
+    ("page size taken for block rows", [("page_id * j->block_rows + i % j->page", "page_id * j->page + i % j->page")]),
+    ("request ignored", [("const int32_t request = r / j->rows_per_request;", "const int32_t request = r;")]),
     ("valid_len not clamped", [("if (L > j->width) L = j->width;", "")]),
     ("block minimum instead of maximum", [("order_key(row[t]) > key", "order_key(row[t]) < key")]),
     ("block NaN not propagated", [("if (is_nan_bf16(row[t])) nan = 1;", "if (0) nan = 1;")]),

@@ -183,3 +183,14 @@ def test_block_rows_streamed_path():
     assert tk.plan(case.rows, case.width, case.k, case.mode)["variant"] == "direct"
     check(case, path=1)
     check(case, path=1, cluster=2)
+
+
+@pytest.mark.parametrize("mode,width,k", [(W.TOKEN, 16384, 512), (W.TOKEN, 100000, 512),
+                                          (W.BLOCK8, 16384, 100), (W.BLOCK8, 300000, 2048)])
+@pytest.mark.parametrize("q,block_rows", [(1, 2048), (2, 64), (4, 2048)])
+def test_requests_and_block_rows(mode, width, k, q, block_rows):
+    """The full transform: q rows per request sharing a table row, block_rows
+    physical rows per 64-element page, through every kernel (one-tile,
+    streamed, resident keys)."""
+    case = W.paged_case(60 + q, rows=37, width=width, k=k, mode=mode, q=q, block_rows=block_rows)
+    check(case)

@@ -35,9 +35,11 @@ class Case:
     valid_len: np.ndarray         # int32 [rows]
     k: int
     mode: int = TOKEN
-    block_table: np.ndarray | None = None   # int32 [rows, pages] or None
+    block_table: np.ndarray | None = None   # int32 [ceil(rows / rows_per_request), pages] or None
     page_size: int = PAGE
     notes: dict = field(default_factory=dict)
+    block_rows: int | None = None           # physical rows per page (None: page_size)
+    rows_per_request: int = 1               # rows sharing one table row
 
     @property
     def rows(self) -> int:
@@ -293,3 +295,17 @@ def shifting_rows(seed: int, rows: int = 3000, width: int = 8192, k: int = 512,
     n_width = width if mode == TOKEN else -(-width // 8)
     return Case(f"shifting {rows}x{width} k{k} mode{mode}", to_bf16_bits(x), width, valid, k,
                 mode, permuted_table(rng, rows, n_width))
+
+
+def paged_case(seed: int, rows: int, width: int, k: int, mode: int = TOKEN, q: int = 2,
+               block_rows: int = 2048, page: int = PAGE) -> Case:
+    """N(0,1) rows with ragged valid lengths, in requests of q rows that share a
+    table row of seeded-permuted page ids, block_rows physical rows per page."""
+    rng = rng_for(seed)
+    stride = -(-width // 8) * 8
+    logits = normal_bf16(rng, (rows, stride))
+    valid = rng.integers(0, width + 1, size=rows).astype(np.int32)
+    n_width = width if mode == TOKEN else -(-width // 8)
+    table = permuted_table(rng, -(-rows // q), n_width, page)
+    return Case(f"paged {rows}x{width} k{k} mode{mode} q{q} block_rows{block_rows}", logits, width,
+                valid, k, mode, table, page, block_rows=block_rows, rows_per_request=q)

@@ -1231,11 +1231,12 @@ struct Cta {
         const int tid = threadIdx.x;
         count_event(*p, TOPK_CNT_CLUSTER_MERGES);
         if (s->v_newthr) best_T = max(best_T, s->v_newthr - 1u);  // the last tile's find
-        s->hwin[1][tid] = 0u;  // the index radix's scratch (compact starts on a barrier)
+        s->hwin[1][tid] = 0u;  // the index radix's scratch
         run_ok = false;
-        compact(false);
+        // The whole buffer takes part (no compaction first): entries below the
+        // row's bound are skipped by the histograms and never selected.
         __syncthreads();
-        const uint32_t n = s->v_count;
+        const uint32_t n = min(s->v_count, static_cast<uint32_t>(CAP));
         const uint32_t my_max = buffer_max(n);
         if (tid == 0) {
             atomicMax(&s->shared_thr[slot], best_T);

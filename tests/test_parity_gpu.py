@@ -109,8 +109,10 @@ def test_repeatable():
 
 def test_path_counters_cover_every_path():
     counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    # the wide edge rows include an ascending one: every tile passes the threshold,
+    # so its buffer fills and is compacted while streaming
     for case in [W.config3(0, rows=64, width=60000), W.edge_cases(0)[0], W.edge_cases(0)[1],
-                 W.config4(0, rows=8, width=1 << 18)]:
+                 W.config4(0, rows=8, width=1 << 18), W.edge_cases(0, width=150000)[0]]:
         run_gpu(case, counters=counters)
         run_gpu(case, counters=counters, cluster=4)
     run_gpu(W.edge_cases(0)[0], counters=counters, force_direct=True)

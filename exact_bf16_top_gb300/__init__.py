@@ -80,7 +80,7 @@ def load(path: str | None = None):
         lib.topk_bf16_status_string.restype = ctypes.c_char_p
         i32p = ctypes.POINTER(ctypes.c_int32)
         lib.topk_bf16_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                       ctypes.c_int32, i32p, i32p, i32p, i32p]
+                                       ctypes.c_int32, i32p, i32p, i32p, i32p, i32p]
         lib.topk_bf16_plan.restype = ctypes.c_int
         lib.topk_bf16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
         lib.topk_bf16_device_status.restype = ctypes.c_int
@@ -178,12 +178,13 @@ def select_raw(logits_ptr: int, row_stride: int, rows: int, width: int, valid_le
 
 
 def plan(rows: int, width: int, k: int, mode: int = TOKEN) -> dict:
-    """The launch the library would make: CTAs per row, threads, shared bytes, variant."""
-    c, t, s, v = (ctypes.c_int32() for _ in range(4))
+    """The launch the library would make: CTAs per row, threads, shared bytes, variant,
+    CTAs launched."""
+    c, t, s, v, n = (ctypes.c_int32() for _ in range(5))
     _check(load().topk_bf16_plan(rows, width, k, mode, ctypes.byref(c), ctypes.byref(t),
-                                 ctypes.byref(s), ctypes.byref(v)))
+                                 ctypes.byref(s), ctypes.byref(v), ctypes.byref(n)))
     return {"cluster": c.value, "threads": t.value, "smem_bytes": s.value,
-            "variant": ("one-tile", "streamed", "direct")[v.value]}
+            "variant": ("one-tile", "streamed", "direct")[v.value], "ctas": n.value}
 
 
 def device_status(clear: bool = True) -> int:

@@ -211,6 +211,21 @@ __device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
     return v;
 }
 
+// Word w of every CTA of the cluster: the sum over all of them and over those
+// ranked below this one. The C loads are issued back to back (one round trip).
+__device__ __forceinline__ void cluster_sum(const uint32_t *w, uint32_t C, uint32_t rank, uint32_t &all,
+                                            uint32_t &pre) {
+    uint32_t x[16];
+#pragma unroll
+    for (uint32_t r = 0; r < 16; ++r) x[r] = r < C ? ld_peer(peer_addr(w, r)) : 0u;
+    all = pre = 0u;
+#pragma unroll
+    for (uint32_t r = 0; r < 16; ++r) {
+        all += x[r];
+        pre += r < rank ? x[r] : 0u;
+    }
+}
+
 __device__ __forceinline__ void red_max_peer(uint32_t addr, uint32_t v) {
     asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v)
                  : "memory");
@@ -1261,12 +1276,8 @@ struct Cta {
         cluster_arrive();
         cluster_wait();
         {
-            uint32_t all = 0, pre = 0;
-            for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t x = ld_peer(peer_addr(&s->h_merge[0][tid], r));
-                all += x;
-                pre += r < rank ? x : 0u;
-            }
+            uint32_t all, pre;
+            cluster_sum(&s->h_merge[0][tid], C, rank, all, pre);
             s->m_all[tid] = all;
             s->m_pre[0][tid] = pre;
         }
@@ -1295,12 +1306,8 @@ struct Cta {
             }
             cluster_arrive();
             cluster_wait();
-            uint32_t all = 0, pre = 0;
-            for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t x = ld_peer(peer_addr(&s->h_merge[1][tid], r));
-                all += x;
-                pre += r < rank ? x : 0u;
-            }
+            uint32_t all, pre;
+            cluster_sum(&s->h_merge[1][tid], C, rank, all, pre);
             s->m_all[tid] = all;
             s->m_pre[1][tid] = pre;
             __syncthreads();
@@ -1507,29 +1514,45 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
 // --------------------------------------------- resident-keys (direct) kernel
 //
 // Rows split over a cluster whose shares fit in shared memory as keys: the
-// DecodeTopK page's direct path (the exact k-th key from two cluster-wide 8-bit
-// radix histograms, then every CTA writes its own selected indices). Each CTA
-// streams its share through the stage ring once and keeps one 16-bit key per
-// element (0: not a candidate); no candidate buffer, no threshold, no
-// compaction. Used where a buffer would churn: block rows, whose k is large
-// next to a CTA's share.
+// DecodeTopK page's direct path, with its sample-based cutoff taken from
+// representatives. Each CTA streams its share through the stage ring once and
+// keeps one 16-bit key per element (0: not a candidate); no candidate buffer,
+// no threshold, no compaction. While the tiles stream in, every thread keeps the
+// largest key it saw in each tile (a representative) and adds its high byte to
+// a histogram. The row's k-th largest representative c (two cluster-wide 8-bit
+// passes over the representatives) is a lower bound of the k-th largest key:
+// at least k groups hold a key >= c. Only keys >= c (a few per cent) go on: a
+// cluster-wide histogram of key - c finds the exact k-th key, and every CTA
+// writes its own selected indices from its list of those keys. The exact
+// fallback (two 8-bit radix passes over every key) takes the rows where the
+// representatives cannot bound the k-th key. Used where a buffer would churn:
+// block rows, whose k is large next to a CTA's share.
 
 namespace direct {
 
 constexpr int NT = 256;
 constexpr int NSTAGE = 2;
 constexpr int RES = 16384;                   // resident keys per CTA
+constexpr int MAX_TILES = RES / TILE_VEC;    // stages per share (block rows; token rows take one)
+constexpr int LIST_CAP = 1280;               // keys >= the cut listed per CTA (more: emitted by a scan)
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][TILE_VEC];
     alignas(16) uint16_t key[RES];           // the share's element keys, in index order
-    alignas(16) uint32_t h[2][256];          // this CTA's histograms of the row (peers read them)
+    alignas(16) uint32_t h[3][256];          // this CTA's histograms of the row (peers read them):
+                                             // representatives' high / low bytes (or the exact
+                                             // passes' keys), then keys - cut
     uint32_t all[256];                       // a histogram summed over the cluster
     uint32_t pre[2][256];                    // ... over the lower-ranked CTAs
+    uint16_t rep[MAX_TILES * NT];            // the representative of each thread and tile
+    uint32_t list[LIST_CAP];                 // local index << 16 | key, for keys >= the cut
+    uint32_t n_list, cursor[2];
     uint32_t red[2][NT / 32];
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
 };
+// Two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
+static_assert(sizeof(Smem) + 1024 <= 233472 / 2, "two resident-keys CTAs must fit on an SM");
 
 template <class M>
 struct Share {
@@ -1555,8 +1578,11 @@ struct Share {
         return pre + inc;
     }
 
-    // The keys of one tile's vectors, at their element positions in the share.
-    __device__ __forceinline__ void keep_tile(const uint4 *stg, int64_t tile_v0, int nv) {
+    // The keys of one tile's vectors, at their element positions in the share;
+    // the thread's largest key of the tile becomes its representative, whose
+    // high byte goes into the representatives' histogram h[0].
+    __device__ __forceinline__ void keep_tile(const uint4 *stg, int64_t tile_v0, int nv, int tile) {
+        uint32_t best = 0;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int pos = j * NT + static_cast<int>(threadIdx.x);
@@ -1564,18 +1590,25 @@ struct Share {
             const int64_t v = tile_v0 + pos;
             const uint32_t local = static_cast<uint32_t>(v - v0);
             if constexpr (M::BLOCK) {
-                s.key[local] = static_cast<uint16_t>(BlockMode::key(stg[pos], v, V));
+                const uint32_t key = BlockMode::key(stg[pos], v, V);
+                s.key[local] = static_cast<uint16_t>(key);
+                best = max(best, key);
             } else {
                 uint32_t ck[4];
                 TokenMode::clean(stg[pos], v, V, L, ck);  // packed pairs of keys, in element order
                 reinterpret_cast<uint4 *>(s.key)[local] = make_uint4(ck[0], ck[1], ck[2], ck[3]);
+                best = max(best, umax_halves(umax2(umax2(ck[0], ck[1]), umax2(ck[2], ck[3]))));
             }
+        }
+        if (!p.force_direct) {  // (uniform: the exact passes start from an empty h[0])
+            s.rep[tile * NT + static_cast<int>(threadIdx.x)] = static_cast<uint16_t>(best);
+            agg_add(s.h[0], best >> 8, best != 0u);
         }
     }
 
     // Every CTA's histogram `which` complete (a cluster barrier), then its sum
-    // over the cluster and over the lower ranks.
-    __device__ __forceinline__ void gather(int which) {
+    // over the cluster (all) and, for pre_slot >= 0, over the lower ranks.
+    __device__ __forceinline__ void gather(int which, int pre_slot) {
         const int tid = threadIdx.x;
         if (C > 1) {
             cluster_arrive();
@@ -1583,14 +1616,10 @@ struct Share {
         } else {
             __syncthreads();
         }
-        uint32_t all = 0, pre = 0;
-        for (uint32_t r = 0; r < C; ++r) {
-            const uint32_t x = C > 1 ? ld_peer(peer_addr(&s.h[which][tid], r)) : s.h[which][tid];
-            all += x;
-            pre += r < rank ? x : 0u;
-        }
+        uint32_t all = s.h[which][tid], pre = 0;
+        if (C > 1) cluster_sum(&s.h[which][tid], C, rank, all, pre);
         s.all[tid] = all;
-        s.pre[which][tid] = pre;
+        if (pre_slot >= 0) s.pre[pre_slot][tid] = pre;
         __syncthreads();
     }
 
@@ -1605,74 +1634,19 @@ struct Share {
         return (h & 1) ? (x >> 16) : (x & 0xFFFFu);
     }
 
-    // The keys are read eight at a time (16 bytes, consecutive across lanes);
-    // groups past the share read as zero (no candidate).
-    __device__ void select_and_emit() {
+    // This CTA's keys > T at slots gt_prev + .. (after those of the lower ranks,
+    // in any order), then its quota of the lowest-index keys == T at slots
+    // G + eq_prev + .. (after those of the lower ranks). Each thread owns a
+    // contiguous run of groups, so ties rank in index order by thread, then
+    // within the run. ties = false: no key == T is taken.
+    __device__ void emit_scan(uint32_t T, uint32_t G, uint32_t gt_prev, uint32_t eq_prev,
+                              uint32_t take, bool ties) {
         const int tid = threadIdx.x;
-        const uint32_t k = static_cast<uint32_t>(p.k);
+        const uint32_t lane = lane_id();
         const uint32_t groups = (n + 7u) / 8u;
         const uint4 *k4 = reinterpret_cast<const uint4 *>(s.key);
-        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-        PhaseClock clk;
-        clk.start(p);
-        // Pass 1: high bytes. (Every lane of a warp runs every iteration: the
-        // warp-wide match in agg_add needs them all.)
-        for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
-            const uint32_t g = g0 + static_cast<uint32_t>(tid);
-            const uint4 w = g < groups ? k4[g] : zero4;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const uint32_t key = key_of(w, h);
-                agg_add(s.h[0], key >> 8, key != 0u);
-            }
-        }
-        gather(0);
-        clk.stop(p, TOPK_CNT_CYC_CUT);
-        clk.start(p);
-        uint32_t b1, above1, total;
-        const bool enough = find_bin256(s.all, k, b1, above1, total);
-        uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0;
-        const uint32_t lane = lane_id();
-        if (enough) {
-            // Pass 2: low bytes of the keys in bin b1 (a warp with none skips the match).
-            for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
-                const uint32_t g = g0 + static_cast<uint32_t>(tid);
-                const uint4 w = g < groups ? k4[g] : zero4;
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    const uint32_t key = key_of(w, h);
-                    const bool in = key != 0u && (key >> 8) == b1;
-                    if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.h[1], key & 0xFFu, in);
-                }
-            }
-            gather(1);
-            uint32_t b2, above2, tot2;
-            find_bin256(s.all, k - above1, b2, above2, tot2);
-            T = (b1 << 8) | b2;
-            take = k - above1 - above2;
-            uint32_t x = 0;
-            for (uint32_t b = lane; b < 256u; b += 32u)
-                x += (b > b1 ? s.pre[0][b] : 0u) + (b > b2 ? s.pre[1][b] : 0u);
-            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
-            eq_prev = s.pre[1][b2];
-        } else {
-            // Fewer than k candidates in the row: every one of them.
-            uint32_t x = 0;
-            for (uint32_t b = lane; b < 256u; b += 32u) x += s.pre[0][b];
-            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
-            T = 0u;  // every key > 0
-        }
-        if (C > 1) cluster_arrive();  // done reading the peers' histograms
-        clk.stop(p, TOPK_CNT_CYC_EXACT);
-        clk.start(p);
-        // This CTA's keys > T (after those of the lower ranks, in any order),
-        // then its quota of the lowest-index keys == T (after those of the
-        // lower ranks). Each thread owns a contiguous run of groups, so ties
-        // rank in index order by thread, then within the run.
-        const uint32_t G = enough ? k - take : total;
         const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
-        const bool ties = enough;  // T > 0: keys == T may be taken
-        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        int32_t *orow = p.out + static_cast<int64_t>(row) * p.k;
         const uint32_t run = (groups + NT - 1) / NT;
         const uint32_t g_lo = min(groups, static_cast<uint32_t>(tid) * run);
         const uint32_t g_n = min(groups, g_lo + run) - g_lo;
@@ -1714,14 +1688,244 @@ struct Share {
                 }
             }
         }
+    }
+
+    // The exact k-th key from two cluster-wide 8-bit radix passes over every
+    // resident key (h[0] and h[1] start empty), then the emission. The keys are
+    // read eight at a time (16 bytes, consecutive across lanes); groups past the
+    // share read as zero (no candidate). Rows with fewer than k candidates take
+    // them all and pad with -1.
+    __device__ void exact_select(PhaseClock &clk) {
+        const int tid = threadIdx.x;
+        const uint32_t k = static_cast<uint32_t>(p.k);
+        const uint32_t groups = (n + 7u) / 8u;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(s.key);
+        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+        // Pass 1: high bytes. (Every lane of a warp runs every iteration: the
+        // warp-wide match in agg_add needs them all.)
+        for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
+            const uint32_t g = g0 + static_cast<uint32_t>(tid);
+            const uint4 w = g < groups ? k4[g] : zero4;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = key_of(w, h);
+                agg_add(s.h[0], key >> 8, key != 0u);
+            }
+        }
+        gather(0, 0);
+        clk.stop(p, TOPK_CNT_CYC_CUT);
+        clk.start(p);
+        uint32_t b1, above1, total;
+        const bool enough = find_bin256(s.all, k, b1, above1, total);
+        uint32_t T = 0, take = 0, gt_prev = 0, eq_prev = 0;
+        const uint32_t lane = lane_id();
+        if (enough) {
+            // Pass 2: low bytes of the keys in bin b1 (a warp with none skips the match).
+            for (uint32_t g0 = 0; g0 < groups; g0 += NT) {
+                const uint32_t g = g0 + static_cast<uint32_t>(tid);
+                const uint4 w = g < groups ? k4[g] : zero4;
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = key_of(w, h);
+                    const bool in = key != 0u && (key >> 8) == b1;
+                    if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.h[1], key & 0xFFu, in);
+                }
+            }
+            gather(1, 1);
+            uint32_t b2, above2, tot2;
+            find_bin256(s.all, k - above1, b2, above2, tot2);
+            T = (b1 << 8) | b2;
+            take = k - above1 - above2;
+            uint32_t x = 0;
+            for (uint32_t b = lane; b < 256u; b += 32u)
+                x += (b > b1 ? s.pre[0][b] : 0u) + (b > b2 ? s.pre[1][b] : 0u);
+            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
+            eq_prev = s.pre[1][b2];
+        } else {
+            // Fewer than k candidates in the row: every one of them.
+            uint32_t x = 0;
+            for (uint32_t b = lane; b < 256u; b += 32u) x += s.pre[0][b];
+            gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
+            T = 0u;  // every key > 0
+        }
+        if (C > 1) cluster_arrive();  // done reading the peers' histograms
+        clk.stop(p, TOPK_CNT_CYC_EXACT);
+        clk.start(p);
+        emit_scan(T, enough ? k - take : total, gt_prev, eq_prev, take, enough);
         const uint32_t selected = enough ? k : total;
+        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
         for (uint32_t i = selected + rank + static_cast<uint32_t>(tid) * C; i < k; i += NT * C) orow[i] = -1;
+    }
+
+    // This CTA's keys >= c: listed (local index << 16 | key; past LIST_CAP only
+    // counted) and binned by key - c into h[2], the last bin holding every key
+    // >= c + 255. A counting pass over the thread's groups (g = j * NT + tid),
+    // one reservation per warp, then a writing pass over the groups that hold
+    // such keys.
+    __device__ __forceinline__ void list_survivors(uint32_t c) {
+        constexpr uint32_t GPT = RES / 8 / NT;  // groups per thread, at most
+        const uint32_t groups = (n + 7u) / 8u;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(s.key);
+        const uint32_t tid = threadIdx.x;
+        uint32_t cnt = 0, hold = 0;
+#pragma unroll
+        for (uint32_t j = 0; j < GPT; ++j) {
+            const uint32_t g = j * NT + tid;
+            if (g < groups) {
+                const uint4 w = k4[g];
+                if (umax_halves(umax2(umax2(w.x, w.y), umax2(w.z, w.w))) >= c) {
+                    hold |= 1u << j;
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) cnt += key_of(w, h) >= c;
+                }
+            }
+        }
+        const uint32_t inc = warp_incl_scan(cnt);
+        uint32_t at = warp_reserve(&s.n_list, __shfl_sync(0xFFFFFFFFu, inc, 31)) + inc - cnt;
+        while (hold) {
+            const uint32_t j = static_cast<uint32_t>(__ffs(hold) - 1);
+            hold &= hold - 1u;
+            const uint32_t g = j * NT + tid;
+            const uint4 w = k4[g];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = key_of(w, h);
+                if (key >= c) {
+                    if (at < static_cast<uint32_t>(LIST_CAP))
+                        s.list[at] = ((8u * g + static_cast<uint32_t>(h)) << 16) | key;
+                    ++at;
+                    atomicAdd(&s.h[2][min(key - c, 255u)], 1u);
+                }
+            }
+        }
+    }
+
+    // The selection from the representatives' cut; false (with nothing
+    // written) when the row needs the exact passes: fewer than k
+    // representatives, or the k-th key in the window's last bin. The answer is
+    // the same on every CTA of the cluster (it comes from cluster-wide sums).
+    __device__ bool cut_select(uint32_t ntiles, PhaseClock &clk) {
+        const int tid = threadIdx.x;
+        const uint32_t k = static_cast<uint32_t>(p.k);
+        const uint32_t lane = lane_id();
+        gather(0, -1);  // the representatives' high bytes
+        // Past that barrier no thread uses the previous row's list: reset it
+        // (the next barrier publishes the zeros).
+        if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
+        uint32_t b1, above1, total;
+        if (!find_bin256(s.all, k, b1, above1, total)) {
+            if (rank == 0) count_event(p, TOPK_CNT_TILE_UNBOUNDED);
+            return false;
+        }
+        // The low bytes of the representatives in bin b1.
+        for (uint32_t j = 0; j < ntiles; ++j) {
+            const uint32_t r = s.rep[j * NT + static_cast<uint32_t>(tid)];
+            const bool in = r != 0u && (r >> 8) == b1;
+            if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.h[1], r & 0xFFu, in);
+        }
+        gather(1, -1);
+        uint32_t b2, above2, tot2;
+        find_bin256(s.all, k - above1, b2, above2, tot2);
+        const uint32_t c = (b1 << 8) | b2;  // the row's k-th largest representative
+        clk.stop(p, TOPK_CNT_CYC_CUT);
+        clk.start(p);
+        list_survivors(c);
+        gather(2, 0);
+        clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
+        clk.start(p);
+        uint32_t t, above, tot3;
+        find_bin256(s.all, k, t, above, tot3);  // at least k keys are >= c
+        if (t == 255u) {  // the k-th key is >= c + 255: not resolved by the window
+            if (rank == 0) count_event(p, TOPK_CNT_TILE_OVERFLOW);
+            return false;
+        }
+        if (rank == 0) count_event(p, TOPK_CNT_TILE_SAMPLED);
+        const uint32_t T = c + t;       // the row's k-th largest key
+        const uint32_t take = k - above;  // keys == T to take, lowest indices first
+        uint32_t x = 0;
+        for (uint32_t b = lane; b < 256u; b += 32u) x += b > t ? s.pre[0][b] : 0u;
+        const uint32_t gt_prev = __reduce_add_sync(0xFFFFFFFFu, x);
+        const uint32_t eq_prev = s.pre[0][t];
+        const uint32_t my_eq = s.h[2][t];
+        if (C > 1) cluster_arrive();  // done reading the peers' histograms
+        clk.stop(p, TOPK_CNT_CYC_EXACT);
+        clk.start(p);
+        const uint32_t quota = take > eq_prev ? min(take - eq_prev, my_eq) : 0u;
+        const uint32_t listed = s.n_list;
+        const bool partial = quota != 0u && quota != my_eq;  // some of this CTA's ties, lowest first
+        if (listed > static_cast<uint32_t>(LIST_CAP) || (partial && my_eq > static_cast<uint32_t>(NT))) {
+            // Listed only in part, or too many ties to rank: from the resident keys.
+            emit_scan(T, above, gt_prev, eq_prev, take, true);
+            return true;
+        }
+        // From the list: keys > T at warp-reserved slots (the order within a
+        // class is free); keys == T likewise when this CTA takes all of them,
+        // else gathered (into pre[1], unused on this path) and ranked by index.
+        int32_t *orow = p.out + static_cast<int64_t>(row) * k;
+        uint32_t *ties = s.pre[1];
+        const uint32_t lt = (1u << lane) - 1u;
+        for (uint32_t i0 = 0; i0 < listed; i0 += NT) {
+            const uint32_t i = i0 + static_cast<uint32_t>(tid);
+            const uint32_t e = i < listed ? s.list[i] : 0u;
+            const uint32_t key = e & 0xFFFFu;
+            const bool gt = key > T, eq = quota != 0u && key == T;
+            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
+            const uint32_t og = warp_reserve(&s.cursor[0], __popc(bg));
+            const uint32_t oe = warp_reserve(&s.cursor[1], __popc(be)) + __popc(be & lt);
+            if (gt) put(orow, gt_prev + og + __popc(bg & lt), e >> 16);
+            if (eq) {
+                if (partial) ties[oe] = e >> 16;
+                else put(orow, above + eq_prev + oe, e >> 16);
+            }
+        }
+        if (partial) {
+            __syncthreads();
+            if (static_cast<uint32_t>(tid) < my_eq) {
+                const uint32_t mine = ties[tid];
+                uint32_t r = 0;
+                for (uint32_t j = 0; j < my_eq; ++j) r += ties[j] < mine;
+                if (r < quota) put(orow, above + eq_prev + r, mine);
+            }
+        }
+        return true;
+    }
+
+    __device__ void select_and_emit(uint32_t ntiles) {
+        const int tid = threadIdx.x;
+        PhaseClock clk;
+        clk.start(p);
+        bool done = false;
+        if (!p.force_direct) {
+            done = cut_select(ntiles, clk);
+            if (!done) {
+                // Every peer must be done reading h[0] and h[1] before the exact
+                // passes refill them.
+                if (C > 1) {
+                    cluster_arrive();
+                    cluster_wait();
+                } else {
+                    __syncthreads();
+                }
+                s.h[0][tid] = 0u;
+                s.h[1][tid] = 0u;
+                __syncthreads();
+                clk.start(p);
+            }
+        }
+        if (!done) {
+            if (rank == 0) count_event(p, TOPK_CNT_TILE_EXACT);
+            exact_select(clk);
+        }
         if (C > 1) cluster_wait();
         else __syncthreads();
         clk.stop(p, TOPK_CNT_CYC_FINISH);
-        // Every peer is done with this row's histograms: zero them for the next.
+        // Every peer is done with this row's histograms: clear them for the next.
+        // (The list and its cursors may still be in use by this CTA's slower
+        // warps: the wait above passes once every thread has arrived, which each
+        // did before emitting.)
         s.h[0][tid] = 0u;
         s.h[1][tid] = 0u;
+        s.h[2][tid] = 0u;
     }
 };
 
@@ -1742,7 +1946,8 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
         fence_mbar_init();
         s.abort_flag = 0u;
     }
-    s.h[0][tid] = s.h[1][tid] = 0u;
+    s.h[0][tid] = s.h[1][tid] = s.h[2][tid] = 0u;
+    if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
     __syncthreads();
     Feed feed;
     if (tid == 0) {
@@ -1785,7 +1990,7 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
             clk.stop(p, TOPK_CNT_CYC_WAIT);
             count_event(p, TOPK_CNT_ROUNDS);
             clk.start(p);
-            sh.keep_tile(s.stage[st], tile_v0, nv);
+            sh.keep_tile(s.stage[st], tile_v0, nv, i);
             __syncthreads();  // every thread is done with this stage
             clk.stop(p, TOPK_CNT_CYC_FILTER);
             if (tid == 0 && feed.row < p.rows) {
@@ -1797,7 +2002,7 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
             for (uint32_t i = sh.n; i < ((sh.n + 7u) & ~7u); ++i) s.key[i] = 0u;
         __syncthreads();
         if (rank == 0) count_event(p, TOPK_CNT_DIRECT_ROWS);
-        sh.select_and_emit();
+        sh.select_and_emit(static_cast<uint32_t>(ntiles));
         __syncthreads();
     }
 }
@@ -2629,7 +2834,32 @@ struct DeviceInit {
     int per_sm[2][2] = {{0, 0}, {0, 0}};   // resident CTAs per SM, [block][wide]
     int per_sm_one[2][ONE_BUILDS] = {};    // the one-tile kernel, [block][build]
     int per_sm_direct[2] = {0, 0};         // the resident-keys kernel, [block]
+    // Clusters of 1, 2, 4, 8, 16 CTAs resident at once, [direct][block][log2 size]
+    // (a cluster's CTAs share one GPC, so this can be less than the slots / size).
+    int cap[2][2][5] = {};
 };
+
+// Clusters of c CTAs of this kernel that fit on the device at once; 0 if none
+// (or if the runtime cannot say, e.g. a size above what the kernel allows).
+int cluster_capacity(const Variant &v, int threads, int c) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = static_cast<unsigned>(c);
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, v.fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
 DeviceInit g_init[64];
 
 cudaError_t init_device(int dev, DeviceInit *&out) {
@@ -2659,6 +2889,13 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
             if (e == cudaSuccess && d.per_sm_direct[b] < 1) e = cudaErrorInvalidConfiguration;
         }
         for (int b = 0; b < 2 && e == cudaSuccess; ++b)
+            for (int l = 0; l < 5; ++l) {
+                const int c = 1 << l;
+                d.cap[0][b][l] = l == 0 ? d.sms * d.per_sm[b][1] : cluster_capacity(pick(b != 0, true), THREADS, c);
+                d.cap[1][b][l] = l == 0 ? d.sms * d.per_sm_direct[b]
+                                        : cluster_capacity(pick_direct(b != 0), direct::NT, c);
+            }
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b)
             for (int w = 0; w < ONE_BUILDS && e == cudaSuccess; ++w) {
                 const Variant v = pick_one(b != 0, w);
                 e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
@@ -2687,9 +2924,11 @@ struct Plan {
 // One CTA per row when a row fits one stage. Wider rows: block rows keep
 // their keys resident across the smallest cluster that holds them (the
 // direct kernel); token rows stream through a candidate buffer. Either way the
-// cluster grows, up to 16, while that puts about one CTA on every resident slot
-// and leaves every CTA at least one stage. Clusters are persistent, so the grid
-// never exceeds what is resident at once. path: 0 automatic, 1 streamed, 2 direct.
+// cluster grows, up to 16, while that puts about one CTA on every resident slot,
+// keeps every row's cluster resident at once and leaves every CTA at least one
+// stage. Clusters are persistent, so the grid never exceeds what is resident at
+// once (clusters are placed whole, within one GPC: the runtime's count of
+// resident clusters, not the slots / size). path: 0 automatic, 1 streamed, 2 direct.
 Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int forced, int path) {
     const int64_t vecs = (static_cast<int64_t>(width) + 7) / 8;
     const int64_t per_vec = block ? 1 : 8;  // elements per vector
@@ -2708,15 +2947,24 @@ Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int 
     const int per_sm = pl.kind == KIND_ONE ? d.per_sm_one[block][pl.build]
                        : pl.kind == KIND_STREAM ? d.per_sm[block][1] : d.per_sm_direct[block];
     const int64_t slots = static_cast<int64_t>(d.sms) * per_sm;
+    auto resident = [&](int c) -> int64_t {
+        if (pl.kind == KIND_ONE) return slots;
+        int l = 0;
+        while ((1 << l) < c) ++l;
+        const int n = d.cap[pl.kind == KIND_DIRECT][block][l];
+        return n > 0 ? n : slots / c;
+    };
     if (forced > 0) {
         pl.cluster = pl.kind == KIND_DIRECT ? max(forced, c_res) : forced;
     } else if (pl.kind != KIND_ONE) {
         const int64_t stages = (vecs + TILE_VEC - 1) / TILE_VEC;
         int c = pl.kind == KIND_DIRECT ? c_res : 1;
-        while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages) c *= 2;
+        while (c < 16 && static_cast<int64_t>(rows) * c * 5 < slots * 4 && 2 * c <= stages &&
+               rows <= resident(2 * c))
+            c *= 2;
         pl.cluster = c;
     }
-    const int64_t max_clusters = slots / pl.cluster > 0 ? slots / pl.cluster : 1;
+    const int64_t max_clusters = resident(pl.cluster) > 0 ? resident(pl.cluster) : 1;
     pl.clusters = rows < max_clusters ? rows : max_clusters;
     pl.spare = pl.clusters * pl.cluster < slots;
     return pl;
@@ -2860,7 +3108,7 @@ const char *topk_bf16_status_string(topk_status_t status) {
 
 topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t mode,
                              int32_t *cluster, int32_t *threads, int32_t *smem_bytes,
-                             int32_t *variant) {
+                             int32_t *variant, int32_t *ctas) {
     if (rows < 0 || (mode != TOPK_TOKEN && mode != TOPK_BLOCK8)) return TOPK_ERR_ARG;
     if (k < 1 || k > TOPK_MAX_K) return TOPK_ERR_K;
     if (width < 0 || width > TOPK_MAX_WIDTH) return TOPK_ERR_WIDTH;
@@ -2876,6 +3124,7 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
     if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = v.smem;
     if (variant) *variant = pl.kind;
+    if (ctas) *ctas = static_cast<int32_t>(pl.clusters * pl.cluster);
     return TOPK_OK;
 }
 

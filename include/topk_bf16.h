@@ -175,13 +175,14 @@ topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, in
 
 /*
  * The launch topk_bf16_select would make for these sizes on the current device:
- * CTAs per row, threads per CTA, dynamic shared memory bytes and the kernel
- * variant (0 = one-tile rows, 1 = streamed rows, 2 = resident keys). Any output
- * pointer may be NULL.
+ * CTAs per row, threads per CTA, dynamic shared memory bytes, the kernel
+ * variant (0 = one-tile rows, 1 = streamed rows, 2 = resident keys) and the CTAs
+ * launched (persistent: at most what is resident at once; rows beyond that are
+ * taken in turn). Any output pointer may be NULL.
  */
 topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t mode,
                              int32_t *cluster, int32_t *threads, int32_t *smem_bytes,
-                             int32_t *variant);
+                             int32_t *variant, int32_t *ctas);
 
 /*
  * Device-side status word of the current device: nonzero bits record a bounded

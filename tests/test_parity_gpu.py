@@ -178,6 +178,23 @@ def test_resident_keys_crowded_and_edges():
         check(case, path=2, cluster=4)
 
 
+def test_resident_keys_cut_branches():
+    """The resident-keys selection from the per-thread maxima's cut: rows it
+    settles (listed or scanned emission, partial ties), rows whose k-th key lies
+    past the cut's window, and rows with fewer than k maxima, which take the
+    exact passes; each at several cluster sizes."""
+    case = W.resident_cut_rows(3)
+    exp = run_oracle(case)
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for cluster in (0, 8, 16):
+        assert_same_sets(run_gpu(case, cluster=cluster, counters=counters), exp, f"{case.name} c{cluster}")
+    short = W.config4(4, rows=6, width=1 << 15)   # two stages per row: 512 maxima < k
+    assert_same_sets(run_gpu(short, counters=counters), run_oracle(short), short.name)
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["tile_sampled"] > 0 and c["tile_overflow"] > 0 and c["tile_unbounded"] > 0, c
+    assert c["direct_rows"] == c["tile_sampled"] + c["tile_exact"], c
+
+
 def test_block_rows_streamed_path():
     """Block rows wider than one stage take the resident-keys kernel; the
     candidate-buffer kernel stays exact on them too."""

@@ -247,6 +247,27 @@ def _edge_block_rows(rng: np.random.Generator, width: int, k: int):
     return rows, lens
 
 
+def resident_cut_rows(seed: int = 0, width: int = 1 << 20, k: int = 2048) -> Case:
+    """Block rows for the resident-keys selection's branches (every row full).
+
+    Row 0: N(0,1). Row 1: N(0,1) with one aligned run of 2048 blocks near 200
+    (far above the rest: the k-th largest block sits far above the k-th largest
+    per-thread maximum). Row 2: the first 16384 blocks N(3, 0.25), the rest
+    N(0,1) (thousands of blocks of one CTA's share at or above the cut). Row 3:
+    N(0,1) sorted ascending. Row 4: constant 1.0 (ties everywhere).
+    """
+    rng = rng_for(seed)
+    nb = width // 8
+    logits = normal_bf16(rng, (5, width))
+    run = 2048 * int(rng.integers(0, nb // 2048))
+    logits[1, 8 * run:8 * (run + 2048)] = to_bf16_bits(200.0 + rng.standard_normal(8 * 2048, dtype=np.float32))
+    logits[2, :8 * 16384] = to_bf16_bits(3.0 + 0.25 * rng.standard_normal(8 * 16384, dtype=np.float32))
+    logits[3] = to_bf16_bits(np.sort(rng.standard_normal(width, dtype=np.float32)))
+    logits[4] = BF16_ONE
+    valid = np.full(5, width, np.int32)
+    return Case(f"resident-cut rows 5x{width} k{k}", logits, width, valid, k, BLOCK8)
+
+
 def edge_cases(seed: int = 0, width: int = 16384, k: int = 512) -> list[Case]:
     """Edge rows in token and block mode (one Case per mode)."""
     rng = rng_for(seed)

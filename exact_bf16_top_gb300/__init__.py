@@ -31,7 +31,7 @@ COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", 
                  "cyc_wait", "cyc_select", "cyc_filter", "cyc_finish", "cyc_compact",
                  "cyc_reps", "cyc_cut", "cyc_survivors", "cyc_exact", "guess_hit", "guess_miss",
                  "cyc_f_prep", "cyc_f_queue", "cyc_f_append", "cyc_f_sync", "cyc_f_find", "cyc_f_loop",
-                 "tie_fills", "direct_rows")
+                 "tie_fills", "direct_rows", "cyc_kernel", "cyc_align")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
            5: "CUDA error"}

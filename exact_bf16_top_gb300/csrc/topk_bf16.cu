@@ -392,6 +392,9 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 // warp that runs it gets the same answer. Returns false if the total is < q.
 __device__ __forceinline__ bool find_bin256(const uint32_t *hist, uint32_t q, uint32_t &bin,
                                             uint32_t &above, uint32_t &total) {
+    // A warp that reaches this diverged (after leader-only atomics, say) would
+    // run the scan below split in lane groups: reconverge first.
+    __syncwarp();
     const uint32_t lane = lane_id();
     const int lo_bin = 248 - 8 * static_cast<int>(lane);
     const uint4 a = *reinterpret_cast<const uint4 *>(hist + lo_bin);
@@ -476,6 +479,7 @@ __device__ __forceinline__ uint32_t warp_reserve(uint32_t *ctr, uint32_t n) {
 __device__ __forceinline__ void agg_add(uint32_t *hist, uint32_t bin, bool valid) {
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
     if (valid && lane_id() == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+    __syncwarp();  // reconverge after the leaders' atomics
 }
 
 template <class M, int NSTAGE, int CAP>
@@ -1808,7 +1812,11 @@ struct Share {
         const int tid = threadIdx.x;
         const uint32_t k = static_cast<uint32_t>(p.k);
         const uint32_t lane = lane_id();
+        clk.stop(p, TOPK_CNT_CYC_CUT);
+        clk.start(p);
         gather(0, -1);  // the representatives' high bytes
+        clk.stop(p, TOPK_CNT_CYC_ALIGN);
+        clk.start(p);
         // Past that barrier no thread uses the previous row's list: reset it
         // (the next barrier publishes the zeros).
         if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
@@ -1938,6 +1946,8 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
     const uint32_t rank = cluster_rank();
     const int32_t cid = static_cast<int32_t>(blockIdx.x / C);
     const int32_t ncl = static_cast<int32_t>(gridDim.x / C);
+    PhaseClock whole;
+    whole.start(p);
 
     grid_dependency_wait();
     grid_dependents_release();
@@ -2005,6 +2015,7 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
         sh.select_and_emit(static_cast<uint32_t>(ntiles));
         __syncthreads();
     }
+    whole.stop(p, TOPK_CNT_CYC_KERNEL);
 }
 
 }  // namespace direct
@@ -2153,7 +2164,8 @@ struct Row {
 
     // Representatives of groups of G elements of this thread's vectors
     // j * NT + tid (token: G logits, within a vector for G <= 8, else whole
-    // vectors; block: G blocks), fed to f(slot, key) in a fixed slot order.
+    // vectors; block: G blocks), fed to f(slot, r, key) in a fixed slot order
+    // (r: the thread's r-th representative, slot = r * NT + tid).
     template <int G, class F>
     __device__ __forceinline__ void reps(F &&f) const {
         const int tid = threadIdx.x;
@@ -2163,14 +2175,14 @@ struct Row {
                 uint32_t acc = 0;
 #pragma unroll
                 for (int i = 0; i < G; ++i) acc = max(acc, bkey((j + i) * NT + tid));
-                f((j / G) * NT + tid, acc);
+                f((j / G) * NT + tid, j / G, acc);
             }
         } else if constexpr (G == 4) {
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 const uint4 r = vec(j * NT + tid);
-                f((2 * j) * NT + tid, rep_key(smax_halves(smax2(r.x, r.y)), 1u));
-                f((2 * j + 1) * NT + tid, rep_key(smax_halves(smax2(r.z, r.w)), 1u));
+                f((2 * j) * NT + tid, 2 * j, rep_key(smax_halves(smax2(r.x, r.y)), 1u));
+                f((2 * j + 1) * NT + tid, 2 * j + 1, rep_key(smax_halves(smax2(r.z, r.w)), 1u));
             }
         } else {
             constexpr int PER = G / 8;  // whole vectors per group
@@ -2179,22 +2191,53 @@ struct Row {
                 uint32_t acc = vec_smax(vec(j * NT + tid));
 #pragma unroll
                 for (int i = 1; i < PER; ++i) acc = smax2(acc, vec_smax(vec((j + i) * NT + tid)));
-                f((j / PER) * NT + tid, rep_key(smax_halves(acc), 1u));
+                f((j / PER) * NT + tid, j / PER, rep_key(smax_halves(acc), 1u));
             }
         }
     }
 
-    // The exact k-th largest representative of groups of G: high byte over the
-    // representatives as they are formed (and stored), low byte over the
-    // stored ones. False when there are fewer than k representatives.
+    // A cut at most the k-th largest representative of groups of G, so that
+    // at least k keys are >= it. First a window of the 510 keys at and below
+    // the largest representative (two keys per bin, the lowest bin holding
+    // everything below): one pass with plain atomics, as the bins are spread;
+    // the cut is the lower key of the bin holding the k-th representative.
+    // When that bin is the lowest, two byte passes over the stored
+    // representatives give it exactly (high byte, then low byte within the
+    // high byte's bin). False when there are fewer than k representatives.
     template <int G>
     __device__ __forceinline__ bool rep_cut(uint32_t &c) {
-        constexpr int NREP = (M::BLOCK ? NV / G : (G >= 8 ? NV * 8 / G : NV * 2)) * NT;
+        constexpr int R = M::BLOCK ? NV / G : (G >= 8 ? NV * 8 / G : NV * 2);
+        constexpr int NREP = R * NT;
         static_assert(NREP <= REP_CAP, "representatives do not fit");
-        reps<G>([&](int slot, uint32_t key) {
+        uint32_t v[R];
+        reps<G>([&](int slot, int r, uint32_t key) {
             s.rep[slot] = static_cast<uint16_t>(key);
-            agg_add(s.hs[0], key >> 8, key != 0u);
+            v[r] = key;
         });
+        uint32_t top = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) top = max(top, v[r]);
+        top = __reduce_max_sync(0xFFFFFFFFu, top);
+        if (lane_id() == 0) s.red[par][threadIdx.x >> 5] = top;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) top = max(top, s.red[par][w]);
+        par ^= 1u;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (v[r] != 0u) atomicAdd(&s.hs[0][255u - min((top - v[r]) >> 1, 255u)], 1u);
+        __syncthreads();
+        warp0_find(s, s.hs[0], k);
+        __syncthreads();
+        if (s.bc[2] < k) return false;
+        if (s.bc[0] > 0u) {
+            c = static_cast<uint32_t>(max(static_cast<int>(top) - 2 * (255 - static_cast<int>(s.bc[0])) - 1, 1));
+            return true;
+        }
+        for (int i = threadIdx.x; i < NREP; i += NT) {
+            const uint32_t key = s.rep[i];
+            agg_add(s.hs[0], key >> 8, key != 0u);
+        }
         __syncthreads();
         warp0_find(s, s.hs[0], k);
         __syncthreads();
@@ -2443,6 +2486,7 @@ struct Row {
                 atomicAdd(&hw[min(key - c, 255u)], 1u);
                 ++at;
             }
+            __syncwarp();  // lanes left the loop above at different counts
         }
     }
 
@@ -2457,6 +2501,7 @@ struct Row {
     // first key). The caller's __syncthreads publishes both.
     __device__ __forceinline__ void warp0_cursors(uint32_t *h, uint32_t q) {
         if (threadIdx.x >= 32) return;
+        __syncwarp();  // (see find_bin256)
         const uint32_t lane = lane_id();
         uint4 *h4 = reinterpret_cast<uint4 *>(h + 248 - 8 * static_cast<int>(lane));
         const uint4 a = h4[0], b = h4[1];

@@ -162,6 +162,9 @@ enum {
     TOPK_CNT_CYC_F_LOOP = 26,    /*   end of tile: barrier and the next copy's issue */
     TOPK_CNT_TIE_FILLS = 27,     /* streamed first tiles completed with lowest-index ties at their cut */
     TOPK_CNT_DIRECT_ROWS = 28,   /* rows selected from resident keys (the direct kernel) */
+    TOPK_CNT_CYC_KERNEL = 29,    /* resident-keys kernel: entry to exit (thread 0 of each CTA) */
+    TOPK_CNT_CYC_ALIGN = 30,     /* resident-keys rows: the first cluster-wide sum after the
+                                    share is in (mostly waiting for the cluster's slowest CTA) */
     TOPK_NUM_COUNTERS = 32
 };
 

@@ -12,7 +12,8 @@ Pages followed (see the C file's header for the full statement):
   * sglang PR #39305 "Exact bf16 consumer top-k adapted from DeepSelect",
     Modifications (order key, NaN never selected);
   * vLLM kimi_k3 "dsa/indexer", IndexerSelect (lowest-index ties; emit's
-    block-table transform).
+    block-table transform; the ordered output with per-row counts) and
+    IndexerScore.rows_out (the per-8 maxima, "tops", the select is bounded by).
 """
 from __future__ import annotations
 
@@ -60,6 +61,16 @@ def _bind(path: str):
                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int32]
+    o = lib.oracle_topk_bf16_ordered
+    o.restype = ctypes.c_int
+    o.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    t = lib.oracle_tops
+    t.restype = ctypes.c_int
+    t.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
     return lib
 
 
@@ -107,6 +118,61 @@ def topk(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_si
                                     rows_per_request, out.ctypes.data, threads)
     if rc != 0:
         raise RuntimeError("oracle_topk_bf16 failed (bad argument or out of memory)")
+    return out
+
+
+def _table(block_table, rows: int, rows_per_request: int):
+    if block_table is None:
+        return None, 0, None
+    table = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if table.ndim != 2 or table.shape[0] < -(-rows // rows_per_request):
+        raise ValueError("block_table needs ceil(rows / rows_per_request) rows of pages")
+    return table.ctypes.data, table.shape[1], table
+
+
+def topk_ordered(logits, valid_len, k: int, block_table=None, page_size: int = 64,
+                 width: int | None = None, threads: int = 1, lib=None,
+                 block_rows: int | None = None, rows_per_request: int = 1):
+    """Token mode, IndexerSelect's output: (out, valid, ids) with out and ids
+    int32 [rows, k] (the selection in ascending index order, transformed / not,
+    then -1) and valid int32 [rows] (the counts). Arguments as topk()."""
+    logits = _as_u16(logits)
+    if logits.ndim != 2:
+        raise ValueError("logits must be 2-D [rows, row_stride]")
+    rows, stride = logits.shape
+    width = stride if width is None else int(width)
+    valid_len = np.ascontiguousarray(np.asarray(valid_len, dtype=np.int32).reshape(-1))
+    if valid_len.shape[0] != rows:
+        raise ValueError("valid_len must have one entry per row")
+    table_ptr, table_stride, _keep = _table(block_table, rows, rows_per_request)
+    out = np.empty((rows, k), dtype=np.int32)
+    ids = np.empty((rows, k), dtype=np.int32)
+    counts = np.empty(rows, dtype=np.int32)
+    lib = lib or load()
+    rc = lib.oracle_topk_bf16_ordered(logits.ctypes.data, stride, rows, width, valid_len.ctypes.data, k,
+                                      table_ptr, table_stride, page_size,
+                                      page_size if block_rows is None else block_rows,
+                                      rows_per_request, out.ctypes.data, counts.ctypes.data,
+                                      ids.ctypes.data, threads)
+    if rc != 0:
+        raise RuntimeError("oracle_topk_bf16_ordered failed (bad argument or out of memory)")
+    return out, counts, ids
+
+
+def tops(logits, valid_len, width: int | None = None, lib=None) -> np.ndarray:
+    """The per-8 maxima the ordered select is bounded by: uint16 [rows,
+    ceil(width / 8)], each aligned group's largest order key among its valid,
+    non-NaN logits (0 for none)."""
+    logits = _as_u16(logits)
+    rows, stride = logits.shape
+    width = stride if width is None else int(width)
+    valid_len = np.ascontiguousarray(np.asarray(valid_len, dtype=np.int32).reshape(-1))
+    groups = (width + 7) // 8
+    out = np.empty((rows, groups), dtype=np.uint16)
+    lib = lib or load()
+    if lib.oracle_tops(logits.ctypes.data, stride, rows, width, valid_len.ctypes.data,
+                       out.ctypes.data, groups) != 0:
+        raise RuntimeError("oracle_tops failed (bad argument)")
     return out
 
 

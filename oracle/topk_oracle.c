@@ -37,6 +37,20 @@
  * Method: for every candidate, one 64-bit word (key << 32) | (0xFFFFFFFF - i);
  * sorting those words in descending order sorts by key descending, then index
  * ascending. The first min(k, candidates) words are the selection.
+ *
+ * The ordered variant follows IndexerSelect on the kimi_k3 indexer page (class
+ * docstring and write_selected): the same selected set, written in ascending
+ * element-index order ("key order": the page's keys are token positions), -1
+ * past the row's count, the count itself per row, and optionally the
+ * untransformed indices in the same order. Token mode (the page's logits are
+ * one score per token). Reading: the ids past the count are -1, like out.
+ *
+ * The scorer's "tops" (IndexerScore.rows_out on the same page: each aligned
+ * group of 8 logits' largest order key) are defined here over the eligible
+ * elements of the group: below the row's valid length and not NaN; a group with
+ * none has top 0 (no key is 0, which is below every key a BF16 value has other
+ * than the NaN patterns: order_key never yields 0 for a non-NaN value since
+ * order_key(0xFFFF) = 0 and 0xFFFF is a NaN).
  */
 #include <pthread.h>
 #include <stdint.h>
@@ -73,7 +87,19 @@ typedef struct {
     int32_t *out;
     int32_t first_row, row_step;
     int status;
+    int ordered;     /* 1: ascending index order, counts in valid, indices in ids */
+    int32_t *valid;  /* [rows] when ordered */
+    int32_t *ids;    /* [rows, k] or NULL, when ordered */
 } job_t;
+
+static int cmp_asc_i32(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/* Ordered output of the selected logical indices sel_idx[0 .. sel) (sorted in
+   place): out and ids in ascending index order, -1 past the count. */
+static void write_ordered(const job_t *j, int32_t r, int32_t *sel_idx, int32_t sel);
 
 /* Block-table transform of a logical element index (vLLM kimi_k3 "dsa/indexer",
  * IndexerSelect: a row belongs to request row / q, whose table row it reads;
@@ -96,6 +122,11 @@ static int one_row(const job_t *j, int32_t r) {
 
     if (n <= j->k) { /* short row: 0 .. n-1 then -1, values never read */
         for (int32_t s = 0; s < j->k; ++s) out[s] = s < n ? transform(j, r, s) : -1;
+        if (j->ordered) {
+            j->valid[r] = n;
+            if (j->ids)
+                for (int32_t s = 0; s < j->k; ++s) j->ids[(int64_t)r * j->k + s] = s < n ? s : -1;
+        }
         return 0;
     }
 
@@ -124,6 +155,15 @@ static int one_row(const job_t *j, int32_t r) {
     qsort(cand, (size_t)m, sizeof(uint64_t), cmp_desc_u64);
 
     int32_t sel = m < j->k ? m : j->k;
+    if (j->ordered) {
+        int32_t *sel_idx = (int32_t *)malloc((size_t)(sel > 0 ? sel : 1) * sizeof(int32_t));
+        if (!sel_idx) { free(cand); return 1; }
+        for (int32_t s = 0; s < sel; ++s) sel_idx[s] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[s]);
+        write_ordered(j, r, sel_idx, sel);
+        free(sel_idx);
+        free(cand);
+        return 0;
+    }
     for (int32_t s = 0; s < sel; ++s) {
         uint16_t key = (uint16_t)(cand[s] >> 32);
         int32_t i = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[s]);
@@ -135,6 +175,15 @@ static int one_row(const job_t *j, int32_t r) {
     return 0;
 }
 
+static void write_ordered(const job_t *j, int32_t r, int32_t *sel_idx, int32_t sel) {
+    int32_t *out = j->out + (int64_t)r * j->k;
+    qsort(sel_idx, (size_t)sel, sizeof(int32_t), cmp_asc_i32);
+    for (int32_t s = 0; s < j->k; ++s) out[s] = s < sel ? transform(j, r, sel_idx[s]) : -1;
+    if (j->ids)
+        for (int32_t s = 0; s < j->k; ++s) j->ids[(int64_t)r * j->k + s] = s < sel ? sel_idx[s] : -1;
+    j->valid[r] = sel;
+}
+
 static void *worker(void *arg) {
     job_t *j = (job_t *)arg;
     for (int32_t r = j->first_row; r < j->rows; r += j->row_step)
@@ -142,29 +191,12 @@ static void *worker(void *arg) {
     return NULL;
 }
 
-/*
- * logits: BF16 bits, row r at logits + r * row_stride; valid_len: [rows];
- * block_table: NULL (identity) or [ceil(rows / rows_per_request), table_stride]
- * page ids, page_size elements per page, block_rows physical rows per page;
- * out: [rows, k] int32. threads: worker threads over rows (<= 1: the calling
- * thread only). Returns 0, or 1 on a bad argument or allocation failure.
- */
-int oracle_topk_bf16_paged(const uint16_t *logits, int64_t row_stride, int32_t rows,
-                           int32_t width, const int32_t *valid_len, int32_t k, int32_t mode,
-                           const int32_t *block_table, int32_t table_stride, int32_t page_size,
-                           int32_t block_rows, int32_t rows_per_request, int32_t *out,
-                           int32_t threads) {
-    if (rows < 0 || width < 0 || k < 1 || row_stride < width) return 1;
-    if (mode != ORACLE_TOKEN && mode != ORACLE_BLOCK8) return 1;
-    if (block_table && (page_size < 1 || block_rows < 1 || rows_per_request < 1)) return 1;
-    if (rows == 0) return 0;
-    if (!logits || !valid_len || !out) return 1;
+/* Rows over `threads` worker threads (<= 1: the calling thread). */
+static int run_jobs(job_t *base_in, int32_t threads) {
+    job_t base = *base_in;
+    const int32_t rows = base.rows;
     if (threads < 1) threads = 1;
     if (threads > rows) threads = rows;
-
-    job_t base = {logits, row_stride, rows, width, valid_len, k, mode,
-                  block_table, table_stride, page_size, block_rows, rows_per_request,
-                  out, 0, 1, 0};
     if (threads == 1) {
         worker(&base);
         return base.status;
@@ -190,6 +222,29 @@ int oracle_topk_bf16_paged(const uint16_t *logits, int64_t row_stride, int32_t r
     return status;
 }
 
+/*
+ * logits: BF16 bits, row r at logits + r * row_stride; valid_len: [rows];
+ * block_table: NULL (identity) or [ceil(rows / rows_per_request), table_stride]
+ * page ids, page_size elements per page, block_rows physical rows per page;
+ * out: [rows, k] int32. threads: worker threads over rows (<= 1: the calling
+ * thread only). Returns 0, or 1 on a bad argument or allocation failure.
+ */
+int oracle_topk_bf16_paged(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                           int32_t width, const int32_t *valid_len, int32_t k, int32_t mode,
+                           const int32_t *block_table, int32_t table_stride, int32_t page_size,
+                           int32_t block_rows, int32_t rows_per_request, int32_t *out,
+                           int32_t threads) {
+    if (rows < 0 || width < 0 || k < 1 || row_stride < width) return 1;
+    if (mode != ORACLE_TOKEN && mode != ORACLE_BLOCK8) return 1;
+    if (block_table && (page_size < 1 || block_rows < 1 || rows_per_request < 1)) return 1;
+    if (rows == 0) return 0;
+    if (!logits || !valid_len || !out) return 1;
+    job_t base = {logits, row_stride, rows, width, valid_len, k, mode,
+                  block_table, table_stride, page_size, block_rows, rows_per_request,
+                  out, 0, 1, 0, 0, NULL, NULL};
+    return run_jobs(&base, threads);
+}
+
 /* The transform with one table row per row and page_size physical rows per page. */
 int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
                      const int32_t *valid_len, int32_t k, int32_t mode,
@@ -198,4 +253,52 @@ int oracle_topk_bf16(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     return oracle_topk_bf16_paged(logits, row_stride, rows, width, valid_len, k, mode,
                                   block_table, table_stride, page_size, page_size, 1, out,
                                   threads);
+}
+
+/*
+ * The ordered variant (token mode): the selection of oracle_topk_bf16_paged in
+ * ascending element-index order, -1 past the count; valid: int32 [rows], the
+ * counts; ids: NULL or int32 [rows, k], the untransformed indices in the same
+ * order, -1 past the count.
+ */
+int oracle_topk_bf16_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                             int32_t width, const int32_t *valid_len, int32_t k,
+                             const int32_t *block_table, int32_t table_stride, int32_t page_size,
+                             int32_t block_rows, int32_t rows_per_request, int32_t *out,
+                             int32_t *valid, int32_t *ids, int32_t threads) {
+    if (rows < 0 || width < 0 || k < 1 || row_stride < width) return 1;
+    if (block_table && (page_size < 1 || block_rows < 1 || rows_per_request < 1)) return 1;
+    if (rows == 0) return 0;
+    if (!logits || !valid_len || !out || !valid) return 1;
+    job_t base = {logits, row_stride, rows, width, valid_len, k, ORACLE_TOKEN,
+                  block_table, table_stride, page_size, block_rows, rows_per_request,
+                  out, 0, 1, 0, 1, valid, ids};
+    return run_jobs(&base, threads);
+}
+
+/*
+ * The scorer's per-8 maxima: tops[r * tops_stride + g] for g < ceil(L / 8) is
+ * the largest order key among logits 8g .. 8g + 7 of row r that lie below its
+ * valid length L (clamped to [0, width]) and are not NaN, 0 when none is; the
+ * entries from ceil(L / 8) to ceil(width / 8) are 0. Returns 0, or 1 on a bad
+ * argument.
+ */
+int oracle_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                const int32_t *valid_len, uint16_t *tops, int64_t tops_stride) {
+    if (rows < 0 || width < 0 || row_stride < width) return 1;
+    const int32_t groups = (width + 7) / 8;
+    if (tops_stride < groups) return 1;
+    for (int32_t r = 0; r < rows; ++r) {
+        int32_t L = valid_len[r];
+        if (L < 0) L = 0;
+        if (L > width) L = width;
+        const uint16_t *row = logits + (int64_t)r * row_stride;
+        for (int32_t g = 0; g < groups; ++g) {
+            uint16_t top = 0;
+            for (int32_t t = 8 * g; t < 8 * g + 8 && t < L; ++t)
+                if (!is_nan_bf16(row[t]) && order_key(row[t]) > top) top = order_key(row[t]);
+            tops[(int64_t)r * tops_stride + g] = top;
+        }
+    }
+    return 0;
 }

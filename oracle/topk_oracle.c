@@ -92,6 +92,9 @@ typedef struct {
     int32_t *ids;    /* [rows, k] or NULL, when ordered */
 } job_t;
 
+/* The element index of a candidate word (key << 32) | (0xFFFFFFFF - i). */
+static int32_t cand_index(uint64_t w) { return (int32_t)(0xFFFFFFFFu - (uint32_t)w); }
+
 static int cmp_asc_i32(const void *a, const void *b) {
     int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
     return x < y ? -1 : (x > y ? 1 : 0);
@@ -158,7 +161,7 @@ static int one_row(const job_t *j, int32_t r) {
     if (j->ordered) {
         int32_t *sel_idx = (int32_t *)malloc((size_t)(sel > 0 ? sel : 1) * sizeof(int32_t));
         if (!sel_idx) { free(cand); return 1; }
-        for (int32_t s = 0; s < sel; ++s) sel_idx[s] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[s]);
+        for (int32_t s = 0; s < sel; ++s) sel_idx[s] = cand_index(cand[s]);
         write_ordered(j, r, sel_idx, sel);
         free(sel_idx);
         free(cand);
@@ -166,7 +169,7 @@ static int one_row(const job_t *j, int32_t r) {
     }
     for (int32_t s = 0; s < sel; ++s) {
         uint16_t key = (uint16_t)(cand[s] >> 32);
-        int32_t i = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[s]);
+        int32_t i = cand_index(cand[s]);
         if (j->mode == ORACLE_BLOCK8 && key == KEY_NEG_INF) out[s] = -1;
         else out[s] = transform(j, r, i);
     }

@@ -248,7 +248,7 @@ def test_threads_give_same_result():
 MUTANTS = [
     ("ties to the highest index",
      [("(uint64_t)(0xFFFFFFFFu - (uint32_t)i)", "(uint64_t)(uint32_t)i"),
-      ("(int32_t)(0xFFFFFFFFu - (uint32_t)cand[s])", "(int32_t)(uint32_t)cand[s]")]),
+      ("return (int32_t)(0xFFFFFFFFu - (uint32_t)w);", "return (int32_t)(uint32_t)w;")]),
     ("positive/negative key masks swapped", [("? 0xFFFFu : 0x8000u", "? 0x8000u : 0xFFFFu")]),
     ("negatives not reversed", [("? 0xFFFFu : 0x8000u", "? 0x7FFFu : 0x8000u")]),
     ("infinities taken for NaN", [("(x & 0x7FFFu) > 0x7F80u", "(x & 0x7FFFu) >= 0x7F80u")]),

@@ -25,13 +25,14 @@ TOKEN = 0
 BLOCK8 = 1
 MAX_K = 2048
 MAX_WIDTH = 1 << 20
-NUM_COUNTERS = 32
+NUM_COUNTERS = 40
 COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", "tile_overflow",
                  "tile_take_all", "compactions", "refills", "cluster_merges", "rounds",
                  "cyc_wait", "cyc_select", "cyc_filter", "cyc_finish", "cyc_compact",
                  "cyc_reps", "cyc_cut", "cyc_survivors", "cyc_exact", "guess_hit", "guess_miss",
                  "cyc_f_prep", "cyc_f_queue", "cyc_f_append", "cyc_f_sync", "cyc_f_find", "cyc_f_loop",
-                 "tie_fills", "direct_rows", "cyc_kernel", "cyc_align")
+                 "tie_fills", "direct_rows", "cyc_kernel", "cyc_align", "ordered_tops",
+                 "ordered_exact")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
            5: "CUDA error"}
@@ -76,6 +77,13 @@ def load(path: str | None = None):
         lib.topk_bf16_select_paged.argtypes = (sel_args[:10] + [ctypes.c_int32, ctypes.c_int32]
                                                + sel_args[10:])
         lib.topk_bf16_select_ex.restype = ctypes.c_int
+        lib.topk_bf16_tops.restype = ctypes.c_int
+        lib.topk_bf16_tops.argtypes = sel_args[:5] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        lib.topk_bf16_select_ordered.restype = ctypes.c_int
+        lib.topk_bf16_select_ordered.argtypes = (sel_args[:6] + [ctypes.c_void_p, ctypes.c_int64]
+                                                 + [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                    ctypes.c_int32, ctypes.c_int32]
+                                                 + [ctypes.c_void_p] * 4 + [ctypes.POINTER(_Options)])
         lib.topk_bf16_status_string.argtypes = [ctypes.c_int]
         lib.topk_bf16_status_string.restype = ctypes.c_char_p
         i32p = ctypes.POINTER(ctypes.c_int32)
@@ -114,6 +122,101 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
     force_direct / cluster / counters / path: test hooks (see topk_bf16_select_ex).
     """
     import torch
+    rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width,
+                                                    rows_per_request)
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    elif not (out.is_cuda and out.dtype == torch.int32 and out.shape == (rows, k) and out.is_contiguous()):
+        raise ValueError("out must be a contiguous CUDA int32 tensor [rows, k]")
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    lib = load()
+    with torch.cuda.device(logits.device):
+        args = (_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), int(mode),
+                _ptr(block_table), table_stride, int(page_size), _ptr(out),
+                ctypes.c_void_p(stream.cuda_stream))
+        paged = (block_rows is not None and int(block_rows) != int(page_size)) or int(rows_per_request) != 1
+        if paged:
+            if force_direct or cluster or counters is not None or path:
+                raise ValueError("the test hooks do not combine with block_rows / rows_per_request")
+            st = lib.topk_bf16_select_paged(*args[:10], int(page_size if block_rows is None else block_rows),
+                                            int(rows_per_request), *args[10:])
+        elif force_direct or cluster or counters is not None or path:
+            opt = _Options(1 if force_direct else 0, int(cluster),
+                           None if counters is None else counters.data_ptr(), int(path))
+            st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
+        else:
+            st = lib.topk_bf16_select(*args)
+    _check(st)
+    return out
+
+
+def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_size: int = 64,
+                   width: int | None = None, stream=None, *, block_rows: int | None = None,
+                   rows_per_request: int = 1, ids: bool = False, out=None, valid=None,
+                   counters=None, force_exact: bool = False):
+    """The ordered select of the indexer page (token mode): (out, valid, ids) with
+    out int32 [rows, k] the selection in ascending index order (transformed),
+    then -1; valid int32 [rows] the counts; ids int32 [rows, k] the untransformed
+    indices (None unless ``ids``). tops: None, or CUDA uint16/int16 [rows,
+    tops_stride] (unit inner stride, 16-byte aligned rows): each aligned group of
+    8 logits' largest order key among its valid non-NaN logits, 0 for none (see
+    topk_bf16_select_ordered). Other arguments as select(); counters /
+    force_exact: test hooks.
+    """
+    import torch
+    rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width,
+                                                    rows_per_request)
+    tops_stride = 0
+    if tops is not None:
+        if not (tops.is_cuda and tops.element_size() == 2 and tops.dim() == 2 and tops.shape[0] >= rows
+                and tops.stride(1) == 1):
+            raise ValueError("tops must be CUDA 16-bit [rows, tops_stride] with unit inner stride")
+        tops_stride = tops.stride(0) if tops.shape[0] > 1 else tops.shape[1]
+    dev = logits.device
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    if valid is None:
+        valid = torch.empty(rows, dtype=torch.int32, device=dev)
+    ids_t = torch.empty((rows, k), dtype=torch.int32, device=dev) if ids else None
+    for t, shape in ((out, (rows, k)), (valid, (rows,))):
+        if not (t.is_cuda and t.dtype == torch.int32 and tuple(t.shape) == shape and t.is_contiguous()):
+            raise ValueError("out / valid must be contiguous CUDA int32 [rows, k] / [rows]")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    opt = None
+    if counters is not None or force_exact:
+        opt = ctypes.byref(_Options(1 if force_exact else 0, 0,
+                                    None if counters is None else counters.data_ptr(), 0))
+    lib = load()
+    with torch.cuda.device(dev):
+        st = lib.topk_bf16_select_ordered(
+            _ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), _ptr(tops), tops_stride,
+            _ptr(block_table), table_stride, int(page_size),
+            int(page_size if block_rows is None else block_rows), int(rows_per_request),
+            _ptr(out), _ptr(valid), _ptr(ids_t), ctypes.c_void_p(stream.cuda_stream), opt)
+    _check(st)
+    return out, valid, ids_t
+
+
+def tops(logits, valid_len, width: int | None = None, stream=None):
+    """The per-8 maxima select_ordered is bounded by (topk_bf16_tops): int16
+    [rows, ceil(ceil(width / 8) / 8) * 8] holding uint16 order keys."""
+    import torch
+    rows, width, row_stride, _ = _inputs(logits, valid_len, None, width, 1)
+    stride = -(-(-(-width // 8)) // 8) * 8
+    out = torch.empty((rows, max(stride, 8)), dtype=torch.int16, device=logits.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    with torch.cuda.device(logits.device):
+        _check(load().topk_bf16_tops(_ptr(logits), row_stride, rows, width, _ptr(valid_len), _ptr(out),
+                                     out.shape[1], ctypes.c_void_p(stream.cuda_stream)))
+    return out
+
+
+def _inputs(logits, valid_len, block_table, width, rows_per_request):
+    """Checks shared by the entry points; returns (rows, width, row_stride, table_stride)."""
+    import torch
     if not (isinstance(logits, torch.Tensor) and logits.is_cuda):
         raise TypeError("logits must be a CUDA tensor")
     if logits.dtype not in (torch.bfloat16, torch.int16) and str(logits.dtype) != "torch.uint16":
@@ -141,31 +244,7 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
             raise ValueError("block_table must be CUDA int32 [ceil(rows / rows_per_request), pages] "
                              "with unit inner stride")
         table_stride = block_table.stride(0) if block_table.shape[0] > 1 else block_table.shape[1]
-    if out is None:
-        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
-    elif not (out.is_cuda and out.dtype == torch.int32 and out.shape == (rows, k) and out.is_contiguous()):
-        raise ValueError("out must be a contiguous CUDA int32 tensor [rows, k]")
-    if stream is None:
-        stream = torch.cuda.current_stream(logits.device)
-    lib = load()
-    with torch.cuda.device(logits.device):
-        args = (_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k), int(mode),
-                _ptr(block_table), table_stride, int(page_size), _ptr(out),
-                ctypes.c_void_p(stream.cuda_stream))
-        paged = (block_rows is not None and int(block_rows) != int(page_size)) or int(rows_per_request) != 1
-        if paged:
-            if force_direct or cluster or counters is not None or path:
-                raise ValueError("the test hooks do not combine with block_rows / rows_per_request")
-            st = lib.topk_bf16_select_paged(*args[:10], int(page_size if block_rows is None else block_rows),
-                                            int(rows_per_request), *args[10:])
-        elif force_direct or cluster or counters is not None or path:
-            opt = _Options(1 if force_direct else 0, int(cluster),
-                           None if counters is None else counters.data_ptr(), int(path))
-            st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
-        else:
-            st = lib.topk_bf16_select(*args)
-    _check(st)
-    return out
+    return rows, width, row_stride, table_stride
 
 
 def select_raw(logits_ptr: int, row_stride: int, rows: int, width: int, valid_len_ptr: int, k: int,

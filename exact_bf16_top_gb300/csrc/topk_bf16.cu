@@ -2827,6 +2827,554 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
 
 }  // namespace one
 
+// ------------------------------------------------------- ordered (tops) kernel
+//
+// The exact top-k of token rows in ascending index order, bounded by the
+// scorer's per-8 maxima ("tops"): vLLM kimi_k3 "dsa/indexer", IndexerSelect
+// (class docstring; write_selected). The k-th largest of a set of disjoint
+// groups' maxima bounds the row's k-th key from below (each such group holds a
+// key at least as large), so only the vectors whose top reaches that bound are
+// read. One CTA of 512 threads per row:
+//   1. representatives: maxima of groups of tops, each warp over its own
+//      contiguous range of tops (coalesced 16-byte reads); the cut c is the
+//      k-th largest representative, from a histogram of the 510 keys below the
+//      largest one (two byte passes when it lies lower);
+//   2. the vectors whose top is >= c, listed in index order (a second read of
+//      the tops: counts, a CTA scan, then the writes);
+//   3. every key >= c of those vectors, listed in index order (all threads load
+//      their run of listed vectors together), binned by key - c;
+//   4. the k-th key T from that histogram (or two byte passes over the list);
+//   5. the output in index order: each listed key's slot is the number of
+//      selected keys before it (keys above T, and ties at T while fewer than
+//      the quota precede them), from one CTA scan.
+// Rows whose lists would overflow, or whose representatives cannot bound the
+// k-th key, take the exact select over every key (two radix passes, then the
+// same ordered output from a scan of the row). Without tops every row does.
+namespace ordered {
+
+constexpr int NT = 512;
+constexpr int NW = NT / 32;
+constexpr int REP_CAP = 8192;    // representatives kept for the byte-pass fallback
+constexpr int VEC_CAP = 8192;    // candidate vectors listed
+constexpr int KEY_CAP = 8192;    // candidate keys listed
+
+struct OParams {
+    const uint16_t *logits;
+    int64_t row_stride;
+    int32_t rows, width;
+    const int32_t *valid_len;
+    int32_t k;
+    const uint16_t *tops;        // NULL: every row takes the exact select
+    int64_t tops_stride;
+    const int32_t *table;
+    int32_t table_stride, page_shift, block_rows, rows_per_request;
+    int32_t *out, *valid, *ids;
+    uint32_t *counters;
+};
+
+struct alignas(16) Smem {
+    alignas(16) uint32_t hs[2][256];  // byte-pass histograms (zero between uses)
+    alignas(16) uint32_t hw[256];     // the candidates' window (key - c)
+    uint16_t rep[REP_CAP];
+    uint32_t cvec[VEC_CAP];           // candidate vectors, in index order
+    uint32_t lidx[KEY_CAP];           // candidate keys' element indices, in index order
+    uint16_t lkey[KEY_CAP];
+    uint32_t red[2][NW];
+    uint32_t bc[4];
+};
+
+__device__ __forceinline__ void count_o(const OParams &p, int which, uint32_t v = 1u) {
+    if (p.counters && threadIdx.x == 0) atomicAdd(p.counters + which, v);
+}
+
+// The page transform of IndexerSelect.emit (request = row / q).
+__device__ __forceinline__ int32_t transform_o(const OParams &p, int32_t row, int32_t i) {
+    if (!p.table) return i;
+    const int32_t request = p.rows_per_request == 1 ? row : row / p.rows_per_request;
+    const int32_t page = p.table[static_cast<int64_t>(request) * p.table_stride + (i >> p.page_shift)];
+    return page * p.block_rows + (i & ((1 << p.page_shift) - 1));
+}
+
+// Slot `slot` of the row's outputs: element i (transformed, and as is in ids).
+__device__ __forceinline__ void put_o(const OParams &p, int32_t row, uint32_t slot, int32_t i) {
+    const int64_t at = static_cast<int64_t>(row) * p.k + slot;
+    p.out[at] = transform_o(p, row, i);
+    if (p.ids) p.ids[at] = i;
+}
+
+// CTA-wide inclusive scan (every thread gets its prefix and the total).
+__device__ __forceinline__ uint32_t cta_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    const uint32_t inc = warp_incl_scan(x);
+    if (lane == 31) s.red[par][warp] = inc;
+    __syncthreads();
+    const uint32_t w = lane < NW ? s.red[par][lane] : 0u;
+    const uint32_t wi = warp_incl_scan(w);
+    total = __shfl_sync(0xFFFFFFFFu, wi, 31);
+    const uint32_t pre = __shfl_sync(0xFFFFFFFFu, wi - w, warp);
+    par ^= 1u;
+    return pre + inc;
+}
+
+// CTA-wide maximum.
+__device__ __forceinline__ uint32_t cta_max(Smem &s, uint32_t &par, uint32_t x) {
+    x = __reduce_max_sync(0xFFFFFFFFu, x);
+    if (lane_id() == 0) s.red[par][threadIdx.x >> 5] = x;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < NW; ++w) x = max(x, s.red[par][w]);
+    par ^= 1u;
+    return x;
+}
+
+// Warp 0: the bin of hist holding the q-th largest, the count above it and
+// the total, to s.bc; the histogram is zeroed. The caller's barrier publishes.
+__device__ __forceinline__ void find_o(Smem &s, uint32_t *hist, uint32_t q) {
+    if (threadIdx.x < 32) {
+        uint32_t b, above, total;
+        find_bin256(hist, q, b, above, total);
+        reinterpret_cast<uint4 *>(hist)[2 * threadIdx.x] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(hist)[2 * threadIdx.x + 1] = make_uint4(0, 0, 0, 0);
+        if (threadIdx.x == 0) {
+            s.bc[0] = b;
+            s.bc[1] = above;
+            s.bc[2] = total;
+        }
+    }
+}
+
+// Bit h set when element h (0..7) of the vector has a key >= c (c >= 1);
+// lanes at or past `len` elements of the row are not eligible, nor NaN.
+__device__ __forceinline__ uint32_t mask_ge(const uint4 &r, uint32_t c, int32_t lanes) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t kk = key2(w[i]);
+        const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
+        const bool nlo = ((w[i] & 0x7FFFu) > 0x7F80u), nhi = (((w[i] >> 16) & 0x7FFFu) > 0x7F80u);
+        m |= (!nlo && lo >= c && 2 * i < lanes ? 1u : 0u) << (2 * i);
+        m |= (!nhi && hi >= c && 2 * i + 1 < lanes ? 1u : 0u) << (2 * i + 1);
+    }
+    return m;
+}
+
+__device__ __forceinline__ uint32_t key_of8(const uint4 &r, int h) {
+    const uint32_t w = (h & 4) ? ((h & 2) ? r.w : r.z) : ((h & 2) ? r.y : r.x);
+    return (key2(w) >> ((h & 1) * 16)) & 0xFFFFu;
+}
+
+struct RowO {
+    Smem &s;
+    const OParams &p;
+    uint32_t par = 0;
+    int32_t row = 0, L = 0, V = 0;     // valid logits; vectors (and groups of tops) holding them
+    uint32_t k = 0;
+    const uint4 *lrow = nullptr;       // the row's logits as 16-byte vectors
+    const uint4 *trow = nullptr;       // the row's tops, eight per 16 bytes
+
+    __device__ RowO(Smem &s_, const OParams &p_) : s(s_), p(p_) {}
+
+    __device__ __forceinline__ int32_t lanes_of(int32_t v) const { return min(8, L - 8 * v); }
+
+    // Top g of the piece t (tops 8 * piece .. 8 * piece + 7); 0 past the row.
+    __device__ __forceinline__ uint32_t top_at(const uint4 &t, int32_t piece, int e) const {
+        const uint32_t w = (e & 4) ? ((e & 2) ? t.w : t.z) : ((e & 2) ? t.y : t.x);
+        return 8 * piece + e < V ? (w >> ((e & 1) * 16)) & 0xFFFFu : 0u;
+    }
+
+    __device__ __forceinline__ void write_range_neg(uint32_t from) const {
+        for (uint32_t i = from + threadIdx.x; i < k; i += NT) {
+            const int64_t at = static_cast<int64_t>(row) * p.k + i;
+            p.out[at] = -1;
+            if (p.ids) p.ids[at] = -1;
+        }
+    }
+
+    // The k-th largest of the NREP = slots * NT representatives in s.rep (0 =
+    // none): a window of the 510 keys at and below the largest, top (two keys
+    // per bin), else two byte passes. The cut returned is at most it (the
+    // lower key of the window bin that holds it); 0 when there are fewer than
+    // k representatives.
+    __device__ uint32_t rep_cut(uint32_t slots, uint32_t top) {
+        const uint32_t tid = threadIdx.x;
+        for (uint32_t j = 0; j < slots; ++j) {
+            const uint32_t v = s.rep[j * NT + tid];
+            if (v) atomicAdd(&s.hw[255u - min((top - v) >> 1, 255u)], 1u);
+        }
+        __syncthreads();
+        find_o(s, s.hw, k);
+        __syncthreads();
+        if (s.bc[2] < k) return 0u;
+        const uint32_t b = s.bc[0];
+        __syncthreads();  // every thread has read s.bc
+        if (b > 0u) return static_cast<uint32_t>(max(static_cast<int>(top) - 2 * (255 - static_cast<int>(b)) - 1, 1));
+        for (uint32_t j = 0; j < slots; ++j) {
+            const uint32_t v = s.rep[j * NT + tid];
+            agg_add(s.hs[0], v >> 8, v != 0u);
+        }
+        __syncthreads();
+        find_o(s, s.hs[0], k);
+        __syncthreads();
+        const uint32_t hb = s.bc[0], ha = s.bc[1];
+        __syncthreads();
+        for (uint32_t j = 0; j < slots; ++j) {
+            const uint32_t v = s.rep[j * NT + tid];
+            const bool in = v != 0u && (v >> 8) == hb;
+            if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.hs[1], v & 0xFFu, in);
+        }
+        __syncthreads();
+        find_o(s, s.hs[1], k - ha);
+        __syncthreads();
+        const uint32_t c = (hb << 8) | s.bc[0];
+        __syncthreads();
+        return c;
+    }
+
+    // Step 1: the cut from the tops (0: none). Warp w walks pieces
+    // [w * ppw, (w + 1) * ppw) of the row's tops, lane l piece w * ppw + 32 i + l
+    // at step i. Rows of at most REP_CAP groups use every top as a
+    // representative; longer ones the maximum of a lane's pieces over r steps.
+    __device__ uint32_t cut_from_tops() {
+        const uint32_t tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+        const int32_t pieces = (V + 7) / 8;
+        const int32_t ppw = (pieces + NW - 1) / NW;
+        const int32_t steps = (ppw + 31) / 32;
+        const int32_t base = static_cast<int32_t>(warp) * ppw, end = min(base + ppw, pieces);
+        const bool each = V <= REP_CAP;
+        int32_t r = 1;
+        while (!each && (steps + r - 1) / r > REP_CAP / NT) r *= 2;
+        const uint32_t slots = each ? static_cast<uint32_t>(steps * 8) : static_cast<uint32_t>((steps + r - 1) / r);
+        uint32_t best = 0;
+        for (int32_t g = 0; g < static_cast<int32_t>(each ? steps : slots); ++g) {
+            uint32_t acc = 0;
+            for (int32_t i = each ? g : g * r; i < (each ? g + 1 : min(g * r + r, steps)); ++i) {
+                const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
+                const uint4 t = piece < end ? __ldg(trow + piece) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t top = piece < end ? top_at(t, piece, e) : 0u;
+                    if (each) s.rep[(8 * i + e) * NT + tid] = static_cast<uint16_t>(top);
+                    acc = max(acc, top);
+                }
+            }
+            if (!each) s.rep[g * NT + tid] = static_cast<uint16_t>(acc);
+            best = max(best, acc);
+        }
+        const uint32_t top = cta_max(s, par, best);
+        if (top == 0u) return 0u;  // no eligible key at all
+        return rep_cut(slots, top);
+    }
+
+    // Step 2: the vectors whose top is >= c, in index order, into s.cvec (the
+    // same walk as step 1). Returns their count (listed only up to VEC_CAP).
+    __device__ uint32_t list_vectors(uint32_t c) {
+        const uint32_t tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+        const int32_t pieces = (V + 7) / 8;
+        const int32_t ppw = (pieces + NW - 1) / NW;
+        const int32_t steps = (ppw + 31) / 32;
+        const int32_t base = static_cast<int32_t>(warp) * ppw, end = min(base + ppw, pieces);
+        uint32_t cnt = 0;
+        for (int32_t i = 0; i < steps; ++i) {
+            const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
+            if (piece < end) {
+                const uint4 t = __ldg(trow + piece);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cnt += top_at(t, piece, e) >= c;
+            }
+        }
+        const uint32_t wt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        if (lane == 0) s.red[par][warp] = wt;
+        __syncthreads();
+        uint32_t at = 0, total = 0;
+        for (uint32_t w = 0; w < static_cast<uint32_t>(NW); ++w) {
+            const uint32_t x = s.red[par][w];
+            at += w < warp ? x : 0u;
+            total += x;
+        }
+        par ^= 1u;
+        if (total > static_cast<uint32_t>(VEC_CAP)) return total;
+        for (int32_t i = 0; i < steps; ++i) {
+            const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
+            uint32_t m = 0;
+            if (piece < end) {
+                const uint4 t = __ldg(trow + piece);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m |= (top_at(t, piece, e) >= c ? 1u : 0u) << e;
+            }
+            const uint32_t n = __popc(m);
+            const uint32_t incl = warp_incl_scan(n);
+            uint32_t pos = at + incl - n;
+            for (; m; m &= m - 1u) s.cvec[pos++] = static_cast<uint32_t>(8 * piece + __ffs(m) - 1);
+            at += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        __syncthreads();
+        return total;
+    }
+
+    // Step 3: every key >= c of the nv listed vectors, in index order, into
+    // s.lkey / s.lidx, binned by key - c into s.hw (the last bin open-ended).
+    // Thread t takes listed vectors [t q, t q + q). Returns the count (listed
+    // only up to KEY_CAP).
+    __device__ uint32_t list_keys(uint32_t c, uint32_t nv) {
+        const uint32_t tid = threadIdx.x;
+        const uint32_t q = (nv + NT - 1) / NT;
+        const uint32_t j0 = min(tid * q, nv), j1 = min(j0 + q, nv);
+        uint32_t cnt = 0;
+        for (uint32_t j = j0; j < j1; j += 4) {
+            uint4 r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)  // the loads issue together
+                r[u] = j + u < j1 ? __ldg(lrow + s.cvec[j + u]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + u < j1) cnt += __popc(mask_ge(r[u], c, lanes_of(static_cast<int32_t>(s.cvec[j + u]))));
+        }
+        uint32_t total;
+        uint32_t at = cta_scan(s, par, cnt, total) - cnt;
+        if (total > static_cast<uint32_t>(KEY_CAP)) return total;
+        for (uint32_t j = j0; j < j1; j += 4) {
+            uint4 r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                r[u] = j + u < j1 ? __ldg(lrow + s.cvec[j + u]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j + u >= j1) continue;
+                const int32_t v = static_cast<int32_t>(s.cvec[j + u]);
+                for (uint32_t m = mask_ge(r[u], c, lanes_of(v)); m; m &= m - 1u) {
+                    const int h = __ffs(m) - 1;
+                    const uint32_t key = key_of8(r[u], h);
+                    s.lkey[at] = static_cast<uint16_t>(key);
+                    s.lidx[at] = static_cast<uint32_t>(8 * v + h);
+                    atomicAdd(&s.hw[min(key - c, 255u)], 1u);
+                    ++at;
+                }
+            }
+        }
+        __syncthreads();
+        return total;
+    }
+
+    // Step 5 (and the exact path's output): n_own entries of this thread, in
+    // index order, after those of lower threads; slot of each selected one =
+    // the selected entries before it in index order (keys above T, then ties
+    // at T while fewer than `take` precede them).
+    template <class Get>
+    __device__ __forceinline__ void write_ordered(uint32_t T, uint32_t take, bool all, uint32_t n_own, Get &&get) {
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t j = 0; j < n_own; ++j) {
+            uint32_t key;
+            int32_t idx;
+            get(j, key, idx);
+            gt += key > T || (all && key != 0u);
+            eq += !all && key == T && key != 0u;
+        }
+        uint32_t tg, te;
+        uint32_t pa = cta_scan(s, par, gt, tg) - gt;
+        uint32_t pt = cta_scan(s, par, eq, te) - eq;
+        if (gt == 0u && (eq == 0u || pt >= take)) return;
+        for (uint32_t j = 0; j < n_own; ++j) {
+            uint32_t key;
+            int32_t idx;
+            get(j, key, idx);
+            if (key == 0u) continue;
+            if (key > T || all) {
+                put_o(p, row, pa + min(pt, take), idx);
+                ++pa;
+            } else if (key == T) {
+                if (pt < take) put_o(p, row, pa + pt, idx);
+                ++pt;
+            }
+        }
+    }
+
+    // The exact select over every key of the row (two byte passes over all
+    // eligible keys), then the ordered output from a scan of the row: thread t
+    // takes vectors [t q, t q + q).
+    __device__ void exact_row() {
+        const uint32_t tid = threadIdx.x;
+        count_o(p, TOPK_CNT_ORDERED_EXACT);
+        for (int32_t v0 = 0; v0 < V; v0 += NT) {
+            const int32_t v = v0 + static_cast<int32_t>(tid);
+            const uint4 r = v < V ? __ldg(lrow + v) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t m = v < V ? mask_ge(r, 1u, lanes_of(v)) : 0u;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) agg_add(s.hs[0], key_of8(r, h) >> 8, (m >> h) & 1u);
+        }
+        __syncthreads();
+        find_o(s, s.hs[0], k);
+        __syncthreads();
+        const uint32_t hb = s.bc[0], ha = s.bc[1], total = s.bc[2];
+        __syncthreads();
+        uint32_t T = 0, take = 0;
+        const bool all = total <= k;  // every eligible key
+        if (!all) {
+            for (int32_t v0 = 0; v0 < V; v0 += NT) {
+                const int32_t v = v0 + static_cast<int32_t>(tid);
+                const uint4 r = v < V ? __ldg(lrow + v) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t m = v < V ? mask_ge(r, 1u, lanes_of(v)) : 0u;
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = key_of8(r, h);
+                    const bool in = ((m >> h) & 1u) && (key >> 8) == hb;
+                    if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.hs[1], key & 0xFFu, in);
+                }
+            }
+            __syncthreads();
+            find_o(s, s.hs[1], k - ha);
+            __syncthreads();
+            T = (hb << 8) | s.bc[0];
+            take = k - ha - s.bc[1];
+            __syncthreads();
+        }
+        const uint32_t q = (static_cast<uint32_t>(V) + NT - 1) / NT;
+        const uint32_t v0 = min(tid * q, static_cast<uint32_t>(V)), v1 = min(v0 + q, static_cast<uint32_t>(V));
+        write_ordered(T, take, all, (v1 - v0) * 8u, [&](uint32_t j, uint32_t &key, int32_t &idx) {
+            const int32_t v = static_cast<int32_t>(v0 + j / 8u);
+            const int h = static_cast<int>(j % 8u);
+            const uint4 r = __ldg(lrow + v);
+            key = ((mask_ge(r, 1u, lanes_of(v)) >> h) & 1u) ? key_of8(r, h) : 0u;
+            idx = 8 * v + h;
+        });
+        const uint32_t selected = all ? total : k;
+        write_range_neg(selected);
+        if (tid == 0) p.valid[row] = static_cast<int32_t>(selected);
+    }
+
+    __device__ void select(int32_t row_) {
+        const uint32_t tid = threadIdx.x;
+        row = row_;
+        k = static_cast<uint32_t>(p.k);
+        L = min(max(__ldg(p.valid_len + row), 0), p.width);
+        V = (L + 7) / 8;
+        lrow = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
+        if (static_cast<uint32_t>(L) <= k) {  // the whole row, values not read
+            count_o(p, TOPK_CNT_BYPASS_ROWS);
+            for (uint32_t i = tid; i < k; i += NT) {
+                const int64_t at = static_cast<int64_t>(row) * p.k + i;
+                p.out[at] = i < static_cast<uint32_t>(L) ? transform_o(p, row, static_cast<int32_t>(i)) : -1;
+                if (p.ids) p.ids[at] = i < static_cast<uint32_t>(L) ? static_cast<int32_t>(i) : -1;
+            }
+            if (tid == 0) p.valid[row] = L;
+            return;
+        }
+        if (!p.tops) {
+            exact_row();
+            return;
+        }
+        trow = reinterpret_cast<const uint4 *>(p.tops + static_cast<int64_t>(row) * p.tops_stride);
+        const uint32_t c = cut_from_tops();
+        if (c == 0u) {
+            exact_row();
+            return;
+        }
+        const uint32_t nv = list_vectors(c);
+        if (nv > static_cast<uint32_t>(VEC_CAP)) {
+            exact_row();
+            return;
+        }
+        const uint32_t nk = list_keys(c, nv);
+        if (nk > static_cast<uint32_t>(KEY_CAP) || nk < k) {  // (nk < k: tops not the row's maxima)
+            if (nk < k && tid == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+            if (tid < 256u) s.hw[tid] = 0u;
+            __syncthreads();
+            exact_row();
+            return;
+        }
+        count_o(p, TOPK_CNT_ORDERED_TOPS);
+        // Step 4: the k-th key T.
+        find_o(s, s.hw, k);
+        __syncthreads();
+        uint32_t b = s.bc[0], above = s.bc[1];
+        __syncthreads();
+        uint32_t T = c + b;
+        if (b == 255u) {  // at least c + 255: two byte passes over key - c of the list
+            for (uint32_t i0 = 0; i0 < nk; i0 += NT) {
+                const uint32_t i = i0 + tid;
+                const uint32_t d = i < nk ? static_cast<uint32_t>(s.lkey[i]) - c : 0u;
+                agg_add(s.hs[0], d >> 8, i < nk);
+            }
+            __syncthreads();
+            find_o(s, s.hs[0], k);
+            __syncthreads();
+            const uint32_t hb = s.bc[0], ha = s.bc[1];
+            __syncthreads();
+            for (uint32_t i0 = 0; i0 < nk; i0 += NT) {
+                const uint32_t i = i0 + tid;
+                const uint32_t d = i < nk ? static_cast<uint32_t>(s.lkey[i]) - c : 0u;
+                const bool in = i < nk && (d >> 8) == hb;
+                if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.hs[1], d & 0xFFu, in);
+            }
+            __syncthreads();
+            find_o(s, s.hs[1], k - ha);
+            __syncthreads();
+            T = c + ((hb << 8) | s.bc[0]);
+            above = ha + s.bc[1];
+            __syncthreads();
+        }
+        // Step 5: the ordered output; thread t takes list entries [t q, t q + q).
+        const uint32_t q = (nk + NT - 1) / NT;
+        const uint32_t i0 = min(tid * q, nk), i1 = min(i0 + q, nk);
+        write_ordered(T, k - above, false, i1 - i0, [&](uint32_t j, uint32_t &key, int32_t &idx) {
+            key = s.lkey[i0 + j];
+            idx = static_cast<int32_t>(s.lidx[i0 + j]);
+        });
+        if (tid == 0) p.valid[row] = static_cast<int32_t>(k);
+    }
+};
+
+__global__ void __launch_bounds__(NT, 1) topk_ordered_kernel(const OParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    grid_dependency_wait();
+    grid_dependents_release();
+    if (threadIdx.x < 256u) s.hs[0][threadIdx.x] = s.hs[1][threadIdx.x] = s.hw[threadIdx.x] = 0u;
+    __syncthreads();
+    RowO r(s, p);
+    for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += static_cast<int32_t>(gridDim.x)) {
+        r.select(row);
+        __syncthreads();
+    }
+}
+
+// The per-8 maxima: thread i of the grid takes piece i (8 groups of 8 logits)
+// of its row and writes their tops as one 16-byte store. A group's top is the
+// largest key among its logits below the row's valid length that are not NaN,
+// 0 when there is none.
+__global__ void __launch_bounds__(256) topk_tops_kernel(const uint16_t *logits, int64_t row_stride,
+                                                        int32_t rows, int32_t width,
+                                                        const int32_t *valid_len, uint16_t *tops,
+                                                        int64_t tops_stride, int32_t pieces) {
+    grid_dependency_wait();
+    grid_dependents_release();
+    const int64_t total = static_cast<int64_t>(rows) * pieces;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t row = static_cast<int32_t>(i / pieces), piece = static_cast<int32_t>(i % pieces);
+        const int32_t L = min(max(__ldg(valid_len + row), 0), width);
+        const uint4 *src = reinterpret_cast<const uint4 *>(logits + static_cast<int64_t>(row) * row_stride);
+        uint32_t t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int32_t v = 8 * piece + e;
+            uint32_t top = 0;
+            if (8 * v < L) {
+                const uint4 r = __ldg(src + v);
+                const uint32_t m = mask_ge(r, 1u, min(8, L - 8 * v));
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if ((m >> h) & 1u) top = max(top, key_of8(r, h));
+            }
+            t[e] = top;
+        }
+        reinterpret_cast<uint4 *>(tops + static_cast<int64_t>(row) * tops_stride)[piece] =
+            make_uint4(t[0] | (t[1] << 16), t[2] | (t[3] << 16), t[4] | (t[5] << 16), t[6] | (t[7] << 16));
+    }
+}
+
+}  // namespace ordered
+
 // ------------------------------------------------------------------ host side
 
 struct Variant {
@@ -2933,6 +3481,10 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                                                                   static_cast<size_t>(v.smem));
             if (e == cudaSuccess && d.per_sm_direct[b] < 1) e = cudaErrorInvalidConfiguration;
         }
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&ordered::topk_ordered_kernel),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(sizeof(ordered::Smem)));
         for (int b = 0; b < 2 && e == cudaSuccess; ++b)
             for (int l = 0; l < 5; ++l) {
                 const int c = 1 << l;
@@ -3108,9 +3660,109 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }
 
+// The ordered select: one CTA per row, as many rows at once as there are SMs.
+topk_status_t launch_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                             const int32_t *valid_len, int32_t k, const uint16_t *tops,
+                             int64_t tops_stride, const int32_t *table, int32_t table_stride,
+                             int32_t page_size, int32_t block_rows, int32_t q, int32_t *out,
+                             int32_t *valid, int32_t *ids, void *stream,
+                             const topk_bf16_options_t *opt) {
+    if (q < 1) return TOPK_ERR_ARG;
+    if (table && (block_rows < page_size || (block_rows & (block_rows - 1)) != 0)) return TOPK_ERR_ARG;
+    topk_status_t st = check_args(logits, row_stride, rows, width, valid_len, k, TOPK_TOKEN, table,
+                                  table_stride, page_size, out);
+    if (st != TOPK_OK || rows == 0) return st;
+    if (!valid) return TOPK_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(valid) & 3u) != 0 || (reinterpret_cast<uintptr_t>(ids) & 3u) != 0)
+        return TOPK_ERR_ALIGN;
+    if (tops) {
+        const int64_t groups = (static_cast<int64_t>(width) + 7) / 8;
+        if ((reinterpret_cast<uintptr_t>(tops) & 15u) != 0 || (tops_stride & 7) != 0) return TOPK_ERR_ALIGN;
+        if (tops_stride < (groups + 7) / 8 * 8) return TOPK_ERR_ARG;
+    }
+    int dev = 0;
+    DeviceInit *d = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
+
+    ordered::OParams prm;
+    prm.logits = logits;
+    prm.row_stride = row_stride;
+    prm.rows = rows;
+    prm.width = width;
+    prm.valid_len = valid_len;
+    prm.k = k;
+    prm.tops = (opt && opt->force_direct) ? nullptr : tops;
+    prm.tops_stride = tops_stride;
+    prm.table = table;
+    prm.table_stride = table_stride;
+    prm.page_shift = 0;
+    if (table)
+        while ((1 << prm.page_shift) < page_size) ++prm.page_shift;
+    prm.block_rows = block_rows;
+    prm.rows_per_request = q;
+    prm.out = out;
+    prm.valid = valid;
+    prm.ids = ids;
+    prm.counters = opt ? opt->counters : nullptr;
+
+    const int grid = rows < d->sms ? rows : d->sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(ordered::NT, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(ordered::Smem);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    unsigned n_attr = 0;
+    if (grid < d->sms) {  // SMs left free: the launch may overlap the previous kernel's tail
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    void *args[] = {&prm};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&ordered::topk_ordered_kernel), args);
+    return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
 }  // namespace topk
 
 extern "C" {
+
+topk_status_t topk_bf16_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                             const int32_t *valid_len, uint16_t *tops, int64_t tops_stride,
+                             void *stream) {
+    topk_status_t st = topk::check_args(logits, row_stride, rows, width, valid_len, 1, TOPK_TOKEN,
+                                        nullptr, 0, 0, reinterpret_cast<const int32_t *>(tops));
+    if (st != TOPK_OK || rows == 0) return st;
+    const int64_t groups = (static_cast<int64_t>(width) + 7) / 8;
+    const int64_t pieces = (groups + 7) / 8;
+    if ((reinterpret_cast<uintptr_t>(tops) & 15u) != 0 || (tops_stride & 7) != 0) return TOPK_ERR_ALIGN;
+    if (tops_stride < pieces * 8) return TOPK_ERR_ARG;
+    if (pieces == 0) return TOPK_OK;
+    int dev = 0;
+    topk::DeviceInit *d = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (topk::init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
+    const int64_t total = static_cast<int64_t>(rows) * pieces;
+    const int64_t want = (total + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(want < 8LL * d->sms ? want : 8LL * d->sms);
+    topk::ordered::topk_tops_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, row_stride, rows, width, valid_len, tops, tops_stride, static_cast<int32_t>(pieces));
+    return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+topk_status_t topk_bf16_select_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                       int32_t width, const int32_t *valid_len, int32_t k,
+                                       const uint16_t *tops, int64_t tops_stride,
+                                       const int32_t *block_table, int32_t table_stride,
+                                       int32_t page_size, int32_t block_rows, int32_t rows_per_request,
+                                       int32_t *out, int32_t *valid, int32_t *ids, void *stream,
+                                       const topk_bf16_options_t *options) {
+    return topk::launch_ordered(logits, row_stride, rows, width, valid_len, k, tops, tops_stride,
+                                block_table, table_stride, page_size, block_rows, rows_per_request,
+                                out, valid, ids, stream, options);
+}
 
 topk_status_t topk_bf16_select(const uint16_t *logits, int64_t row_stride, int32_t rows,
                                int32_t width, const int32_t *valid_len, int32_t k,

@@ -165,7 +165,9 @@ enum {
     TOPK_CNT_CYC_KERNEL = 29,    /* resident-keys kernel: entry to exit (thread 0 of each CTA) */
     TOPK_CNT_CYC_ALIGN = 30,     /* resident-keys rows: the first cluster-wide sum after the
                                     share is in (mostly waiting for the cluster's slowest CTA) */
-    TOPK_NUM_COUNTERS = 32
+    TOPK_CNT_ORDERED_TOPS = 31,  /* ordered rows selected from the tops' bound */
+    TOPK_CNT_ORDERED_EXACT = 32, /* ordered rows that took the exact select over every key */
+    TOPK_NUM_COUNTERS = 40
 };
 
 /* topk_bf16_select with options (NULL = defaults). Same arguments and errors,
@@ -175,6 +177,66 @@ topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, in
                                   topk_mode_t mode, const int32_t *block_table,
                                   int32_t table_stride, int32_t page_size, int32_t *out,
                                   void *stream, const topk_bf16_options_t *options);
+
+/*
+ * The ordered select of the indexer page (vLLM kimi_k3 "dsa/indexer":
+ * IndexerSelect's docstring, kernel and write_selected), token mode: the same
+ * selected set as topk_bf16_select_paged, written in ascending element-index
+ * order ("key order": the page's keys are token positions), bounded by the
+ * scorer's per-8 maxima so that only the vectors that can hold a selected key
+ * are read.
+ *
+ * tops         NULL, or device uint16 [rows, tops_stride], 16-byte aligned:
+ *              tops[r * tops_stride + g], for g < ceil(valid_len[r] / 8), is the
+ *              largest order key x ^ (x < 0 ? 0xFFFF : 0x8000) among logits
+ *              8g .. 8g + 7 of row r that lie below its valid length and are not
+ *              NaN, 0 when there is none (what IndexerScore.rows_out writes for
+ *              the select). They must be exactly that: a row is read only where
+ *              its tops reach the row's bound (wrong tops give a wrong result,
+ *              never an out-of-bounds access). NULL: every row takes the exact
+ *              select over all of its logits.
+ * tops_stride  a multiple of 8, at least ceil(ceil(width / 8) / 8) * 8 (whole
+ *              16-byte pieces of tops are read; entries past a row's valid
+ *              groups are ignored).
+ * out          device int32 [rows, k]: the selected indices in ascending index
+ *              order, transformed as in topk_bf16_select_paged, then -1.
+ * valid        device int32 [rows]: each row's count of selected indices: n
+ *              when n <= k (the row is taken whole without reading values, as
+ *              in topk_bf16_select), else k, or the row's non-NaN elements when
+ *              they are fewer.
+ * ids          NULL, or device int32 [rows, k]: the untransformed indices in the
+ *              same order, then -1.
+ * options      NULL, or test hooks: counters (TOPK_CNT_BYPASS_ROWS,
+ *              TOPK_CNT_ORDERED_TOPS, TOPK_CNT_ORDERED_EXACT), force_direct
+ *              (tops ignored: the exact select on every row). Other fields unused.
+ * The remaining arguments are those of topk_bf16_select_paged (mode is token).
+ * Errors as topk_bf16_select_paged, plus TOPK_ERR_ARG for a NULL valid or a
+ * short tops_stride and TOPK_ERR_ALIGN for misaligned tops, tops_stride, valid
+ * or ids.
+ */
+topk_status_t topk_bf16_select_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                       int32_t width, const int32_t *valid_len, int32_t k,
+                                       const uint16_t *tops, int64_t tops_stride,
+                                       const int32_t *block_table, int32_t table_stride,
+                                       int32_t page_size, int32_t block_rows, int32_t rows_per_request,
+                                       int32_t *out, int32_t *valid, int32_t *ids, void *stream,
+                                       const topk_bf16_options_t *options);
+
+/*
+ * The per-8 maxima topk_bf16_select_ordered is bounded by, for producers that
+ * do not write them (IndexerScore.rows_out on the indexer page writes them
+ * with the logits): tops[r * tops_stride + g] = the largest order key among
+ * logits 8g .. 8g + 7 of row r below valid_len[r] (clamped to [0, width]) that
+ * are not NaN, 0 when there is none, for every g < ceil(ceil(width / 8) / 8) * 8.
+ * logits, row_stride, rows, width, valid_len as in topk_bf16_select; tops:
+ * device uint16, 16-byte aligned; tops_stride: a multiple of 8, at least
+ * ceil(ceil(width / 8) / 8) * 8. Errors as topk_bf16_select for those
+ * arguments, TOPK_ERR_ALIGN for a misaligned tops or tops_stride, TOPK_ERR_ARG
+ * for a short tops_stride.
+ */
+topk_status_t topk_bf16_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                             const int32_t *valid_len, uint16_t *tops, int64_t tops_stride,
+                             void *stream);
 
 /*
  * The launch topk_bf16_select would make for these sizes on the current device:

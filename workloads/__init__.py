@@ -268,6 +268,18 @@ def resident_cut_rows(seed: int = 0, width: int = 1 << 20, k: int = 2048) -> Cas
     return Case(f"resident-cut rows 5x{width} k{k}", logits, width, valid, k, BLOCK8)
 
 
+def ordered_wide(seed: int = 0, rows: int = 64, width: int = 1 << 20, k: int = 2048) -> Case:
+    """Long token rows for the ordered select bounded by per-8 maxima (the
+    indexer's decode step: top-2048 of up to 1M keys per row): N(0,1) scores,
+    valid lengths uniform in [width/2, width], a seeded-permuted table of 64-token
+    pages."""
+    rng = rng_for(seed)
+    logits = normal_bf16(rng, (rows, width))
+    valid = rng.integers(width // 2, width + 1, size=rows).astype(np.int32)
+    table = permuted_table(rng, rows, width)
+    return Case(f"ordered {rows}x{width} k{k}", logits, width, valid, k, TOKEN, table)
+
+
 def edge_cases(seed: int = 0, width: int = 16384, k: int = 512) -> list[Case]:
     """Edge rows in token and block mode (one Case per mode)."""
     rng = rng_for(seed)

@@ -185,6 +185,45 @@ class GpuCase:
                   out=self.out, width=c.width)
 
 
+class OrderedGpuCase(GpuCase):
+    """The ordered select (bounded by per-8 maxima) on a resident workload: the
+    maxima of every copy are computed once, on the GPU, outside the timed
+    region (in the pages' decode step the scorer writes them with the logits)."""
+
+    def __init__(self, case, torch, device, min_copies: int = 1):
+        super().__init__(case, torch, device, min_copies)
+        import exact_bf16_top_gb300 as tk
+        self.tops = [tk.tops(self.logits[i], self.valid, width=case.width) for i in range(self.copies)]
+        self.valid_out = torch.empty(case.rows, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def launch(self, i: int, tk):
+        c = self.case
+        tk.select_ordered(self.logits[i % self.copies], self.valid, c.k, self.tops[i % self.copies],
+                          self.table, c.page_size, width=c.width, out=self.out, valid=self.valid_out)
+
+
+def gpu_case(name, case, torch, device, min_copies: int = 1):
+    if name.startswith("ordered"):
+        return OrderedGpuCase(case, torch, device, min_copies)
+    return GpuCase(case, torch, device, min_copies)
+
+
+def ordered_bytes(case) -> int:
+    """Bytes the ordered select must move: the maxima of every valid group of 8,
+    at least the k vectors that hold the selected keys, the valid lengths, the
+    output and the counts, and one table entry per page that can hold a
+    selected index (as algorithmic_bytes)."""
+    L = np.clip(case.valid_len.astype(np.int64), 0, case.width)
+    big = L > case.k
+    b = int((2 * ((L + 7) // 8) + 16 * np.minimum(case.k, L))[big].sum())
+    b += 4 * case.rows + 4 * case.rows * case.k + 4 * case.rows
+    if case.block_table is not None:
+        pages = -(-L // case.page_size)
+        b += int(4 * np.minimum(np.minimum(L, case.k), pages).sum())
+    return b
+
+
 def time_graph(gc, tk, torch, steps: int, warmup: int):
     """Mean microseconds per launch over `steps` launches replayed from a CUDA
     graph (events on the capture/replay stream)."""
@@ -289,7 +328,8 @@ def sweep_cases(full: bool):
     cases += [("config3 crowded 64x150000 k512", lambda: W.config3(0)),
               ("config4 block 32x1048576 k2048", lambda: W.config4(0)),
               ("config5a wide 256x524288 k512", lambda: W.config5a(0)),
-              ("config5b wide 64x1048576 k512", lambda: W.config5b(0))]
+              ("config5b wide 64x1048576 k512", lambda: W.config5b(0)),
+              ("ordered 64x1048576 k2048 (bounded by per-8 maxima)", lambda: W.ordered_wide(0))]
     return cases
 
 
@@ -297,9 +337,9 @@ def run_sweep(tk, torch, device, steps, warmup, peak, full):
     out = []
     for name, make in sweep_cases(full):
         case = make()
-        gc = GpuCase(case, torch, device)
+        gc = gpu_case(name, case, torch, device)
         us = time_graph(gc, tk, torch, steps, warmup)
-        ab = algorithmic_bytes(case)
+        ab = ordered_bytes(case) if name.startswith("ordered") else algorithmic_bytes(case)
         gbs = ab / (us * 1e-6) / 1e9
         out.append({"workload": name, "us_per_launch": round(us, 3),
                     "rows_per_s": round(case.rows / (us * 1e-6), 1),
@@ -319,7 +359,7 @@ def profile(args):
         raise SystemExit(f"no workload matches {args.profile!r}")
     name, make = matches[0]
     case = make()
-    gc = GpuCase(case, torch, torch.device("cuda", 0), min_copies=2)
+    gc = gpu_case(name, case, torch, torch.device("cuda", 0), min_copies=2)
     for i in range(args.warmup):
         gc.launch(i + 1, tk)
     torch.cuda.synchronize()
@@ -341,12 +381,16 @@ def diag(args):
             if want not in name:
                 continue
             case = make()
-            gc = GpuCase(case, torch, dev, min_copies=1)
+            gc = gpu_case(name, case, torch, dev, min_copies=1)
             gc.launch(0, tk)
             ctr = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device=dev)
             c = case
-            tk.select(gc.logits[0], gc.valid, c.k, c.mode, gc.table, c.page_size, out=gc.out,
-                      width=c.width, counters=ctr)
+            if name.startswith("ordered"):
+                tk.select_ordered(gc.logits[0], gc.valid, c.k, gc.tops[0], gc.table, c.page_size,
+                                  width=c.width, out=gc.out, valid=gc.valid_out, counters=ctr)
+            else:
+                tk.select(gc.logits[0], gc.valid, c.k, c.mode, gc.table, c.page_size, out=gc.out,
+                          width=c.width, counters=ctr)
             torch.cuda.synchronize()
             vals = ctr.cpu().numpy().view(np.uint32).tolist()
             print(json.dumps({"workload": name, "plan": tk.plan(c.rows, c.width, c.k, c.mode),

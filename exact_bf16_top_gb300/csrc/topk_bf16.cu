@@ -2854,9 +2854,11 @@ namespace ordered {
 
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
-constexpr int REP_CAP = 8192;    // representatives kept for the byte-pass fallback
+constexpr int REP_CAP = 16384;   // representatives: every top (rows of up to 16384 groups), else
+                                 // every piece's maximum (up to 16384 pieces: 1M logits)
 constexpr int VEC_CAP = 8192;    // candidate vectors listed
 constexpr int KEY_CAP = 8192;    // candidate keys listed
+constexpr int MAX_BATCHES = 4;   // 256-piece batches of a warp's range of tops (16384 pieces / 16 warps)
 
 struct OParams {
     const uint16_t *logits;
@@ -2991,15 +2993,17 @@ struct RowO {
         }
     }
 
-    // The k-th largest of the NREP = slots * NT representatives in s.rep (0 =
-    // none): a window of the 510 keys at and below the largest, top (two keys
-    // per bin), else two byte passes. The cut returned is at most it (the
-    // lower key of the window bin that holds it); 0 when there are fewer than
-    // k representatives.
-    __device__ uint32_t rep_cut(uint32_t slots, uint32_t top) {
+    // The k-th largest of the n representatives s.rep[0 .. n) (0 = none): a
+    // window of the 510 keys at and below the largest, top (two keys per bin),
+    // else two byte passes. The cut returned is at most it (the lower key of
+    // the window bin that holds it); 0 when there are fewer than k
+    // representatives.
+    __device__ uint32_t rep_cut(uint32_t n, uint32_t top) {
         const uint32_t tid = threadIdx.x;
+        const uint32_t slots = (n + NT - 1) / NT;
         for (uint32_t j = 0; j < slots; ++j) {
-            const uint32_t v = s.rep[j * NT + tid];
+            const uint32_t i = j * NT + tid;
+            const uint32_t v = i < n ? s.rep[i] : 0u;
             if (v) atomicAdd(&s.hw[255u - min((top - v) >> 1, 255u)], 1u);
         }
         __syncthreads();
@@ -3010,7 +3014,8 @@ struct RowO {
         __syncthreads();  // every thread has read s.bc
         if (b > 0u) return static_cast<uint32_t>(max(static_cast<int>(top) - 2 * (255 - static_cast<int>(b)) - 1, 1));
         for (uint32_t j = 0; j < slots; ++j) {
-            const uint32_t v = s.rep[j * NT + tid];
+            const uint32_t i = j * NT + tid;
+            const uint32_t v = i < n ? s.rep[i] : 0u;
             agg_add(s.hs[0], v >> 8, v != 0u);
         }
         __syncthreads();
@@ -3019,7 +3024,8 @@ struct RowO {
         const uint32_t hb = s.bc[0], ha = s.bc[1];
         __syncthreads();
         for (uint32_t j = 0; j < slots; ++j) {
-            const uint32_t v = s.rep[j * NT + tid];
+            const uint32_t i = j * NT + tid;
+            const uint32_t v = i < n ? s.rep[i] : 0u;
             const bool in = v != 0u && (v >> 8) == hb;
             if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.hs[1], v & 0xFFu, in);
         }
@@ -3031,81 +3037,146 @@ struct RowO {
         return c;
     }
 
-    // Step 1: the cut from the tops (0: none). Warp w walks pieces
-    // [w * ppw, (w + 1) * ppw) of the row's tops, lane l piece w * ppw + 32 i + l
-    // at step i. Rows of at most REP_CAP groups use every top as a
-    // representative; longer ones the maximum of a lane's pieces over r steps.
-    __device__ uint32_t cut_from_tops() {
-        const uint32_t tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
-        const int32_t pieces = (V + 7) / 8;
-        const int32_t ppw = (pieces + NW - 1) / NW;
-        const int32_t steps = (ppw + 31) / 32;
-        const int32_t base = static_cast<int32_t>(warp) * ppw, end = min(base + ppw, pieces);
-        const bool each = V <= REP_CAP;
-        int32_t r = 1;
-        while (!each && (steps + r - 1) / r > REP_CAP / NT) r *= 2;
-        const uint32_t slots = each ? static_cast<uint32_t>(steps * 8) : static_cast<uint32_t>((steps + r - 1) / r);
-        uint32_t best = 0;
-        for (int32_t g = 0; g < static_cast<int32_t>(each ? steps : slots); ++g) {
-            uint32_t acc = 0;
-            for (int32_t i = each ? g : g * r; i < (each ? g + 1 : min(g * r + r, steps)); ++i) {
-                const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
-                const uint4 t = piece < end ? __ldg(trow + piece) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t top = piece < end ? top_at(t, piece, e) : 0u;
-                    if (each) s.rep[(8 * i + e) * NT + tid] = static_cast<uint16_t>(top);
-                    acc = max(acc, top);
-                }
-            }
-            if (!each) s.rep[g * NT + tid] = static_cast<uint16_t>(acc);
-            best = max(best, acc);
-        }
-        const uint32_t top = cta_max(s, par, best);
-        if (top == 0u) return 0u;  // no eligible key at all
-        return rep_cut(slots, top);
+    // The walk over the row's tops shared by steps 1 and 2: warp w takes the
+    // pieces (8 tops, 16 bytes) [w * ppw, (w + 1) * ppw), in batches of 256,
+    // lane l pieces p0 .. p0 + 7 of batch b, p0 = w * ppw + 256 b + 8 l (the
+    // order of (b, l, u) is index order). Rows of at most REP_CAP groups keep
+    // every top in s.rep (s.rep[g] = top g); longer ones every piece's maximum
+    // (s.rep[piece]).
+    struct Walk {
+        int32_t pieces, ppw, base, end, batches;
+        bool each;
+    };
+    __device__ __forceinline__ Walk walk() const {
+        Walk w;
+        w.pieces = (V + 7) / 8;
+        w.ppw = (w.pieces + NW - 1) / NW;
+        w.base = static_cast<int32_t>(threadIdx.x >> 5) * w.ppw;
+        w.end = min(w.base + w.ppw, w.pieces);
+        w.batches = (w.ppw + 255) / 256;
+        w.each = V <= REP_CAP;
+        return w;
     }
 
-    // Step 2: the vectors whose top is >= c, in index order, into s.cvec (the
-    // same walk as step 1). Returns their count (listed only up to VEC_CAP).
-    __device__ uint32_t list_vectors(uint32_t c) {
-        const uint32_t tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
-        const int32_t pieces = (V + 7) / 8;
-        const int32_t ppw = (pieces + NW - 1) / NW;
-        const int32_t steps = (ppw + 31) / 32;
-        const int32_t base = static_cast<int32_t>(warp) * ppw, end = min(base + ppw, pieces);
-        uint32_t cnt = 0;
-        for (int32_t i = 0; i < steps; ++i) {
-            const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
-            if (piece < end) {
-                const uint4 t = __ldg(trow + piece);
+    // Step 1: the cut from the tops (0: none).
+    __device__ uint32_t cut_from_tops() {
+        const Walk w = walk();
+        if (w.batches > MAX_BATCHES) {  // (rows are at most 1M logits: cannot happen)
+            if (threadIdx.x == 0) atomicOr(&g_device_status, ERR_BOUNDS);
+            return 0u;
+        }
+        // Read coalesced: at round j lane l takes pieces base + 256 j + 32 u + l,
+        // u < 8 (the eight loads issue together); kept by piece index.
+        uint32_t best = 0;
+        for (int32_t b = 0; b < w.batches; ++b) {
+            uint4 t[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cnt += top_at(t, piece, e) >= c;
+            for (int u = 0; u < 8; ++u) {
+                const int32_t pc = w.base + 256 * b + 32 * u + static_cast<int32_t>(lane_id());
+                t[u] = pc < w.end ? __ldg(trow + pc) : make_uint4(0u, 0u, 0u, 0u);
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t pc = w.base + 256 * b + 32 * u + static_cast<int32_t>(lane_id());
+                if (pc >= w.end) continue;
+                uint32_t acc = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t top = top_at(t[u], pc, e);
+                    if (w.each) s.rep[8 * pc + e] = static_cast<uint16_t>(top);
+                    acc = max(acc, top);
+                }
+                if (!w.each) s.rep[pc] = static_cast<uint16_t>(acc);
+                best = max(best, acc);
+            }
+        }
+        const uint32_t top = cta_max(s, par, best);  // (its barrier also publishes s.rep)
+        if (top == 0u) return 0u;  // no eligible key at all
+        return rep_cut(static_cast<uint32_t>(w.each ? 8 * w.pieces : w.pieces), top);
+    }
+
+    // Step 2: the vectors whose top is >= c, in index order, into s.cvec: from
+    // the tops kept in s.rep, or, for long rows, from the pieces whose maximum
+    // in s.rep reaches c (only those are read again). A counting pass, the
+    // warps' offsets, then the writes. Returns the count (listed only up to
+    // VEC_CAP).
+    __device__ uint32_t list_vectors(uint32_t c) {
+        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+        const Walk w = walk();
+        uint64_t mk[MAX_BATCHES];  // bit 8u + e: top e of the lane's piece u of batch b is >= c
+        uint32_t cnt = 0;
+        if (w.each) {
+#pragma unroll
+            for (int b = 0; b < MAX_BATCHES; ++b) {
+                mk[b] = 0;
+                if (b >= w.batches) continue;
+                const int32_t p0 = w.base + 256 * b + 8 * static_cast<int32_t>(lane);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (p0 + u >= w.end) continue;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mk[b] |= static_cast<uint64_t>(s.rep[8 * (p0 + u) + e] >= c ? 1u : 0u) << (8 * u + e);
+                }
+                cnt += __popcll(mk[b]);
+            }
+        } else {
+            // Pieces whose maximum reaches c (bit 8b + u), then their tops, read
+            // four at a time with the loads issued together.
+            uint32_t flags = 0;
+#pragma unroll
+            for (int b = 0; b < MAX_BATCHES; ++b) {
+                mk[b] = 0;
+                const int32_t p0 = w.base + 256 * b + 8 * static_cast<int32_t>(lane);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (b < w.batches && p0 + u < w.end && s.rep[p0 + u] >= c) flags |= 1u << (8 * b + u);
+            }
+            while (flags) {
+                int f[4];
+                uint4 t[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    f[x] = flags ? __ffs(flags) - 1 : -1;
+                    if (flags) flags &= flags - 1u;
+                    const int32_t pc = w.base + 256 * (f[x] >> 3) + 8 * static_cast<int32_t>(lane) + (f[x] & 7);
+                    t[x] = f[x] >= 0 ? __ldg(trow + pc) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    if (f[x] < 0) continue;
+                    const int32_t pc = w.base + 256 * (f[x] >> 3) + 8 * static_cast<int32_t>(lane) + (f[x] & 7);
+                    uint64_t m = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m |= static_cast<uint64_t>(top_at(t[x], pc, e) >= c ? 1u : 0u) << e;
+#pragma unroll
+                    for (int b = 0; b < MAX_BATCHES; ++b)
+                        if ((f[x] >> 3) == b) mk[b] |= m << (8 * (f[x] & 7));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < MAX_BATCHES; ++b) cnt += __popcll(mk[b]);
         }
         const uint32_t wt = __reduce_add_sync(0xFFFFFFFFu, cnt);
         if (lane == 0) s.red[par][warp] = wt;
         __syncthreads();
         uint32_t at = 0, total = 0;
-        for (uint32_t w = 0; w < static_cast<uint32_t>(NW); ++w) {
-            const uint32_t x = s.red[par][w];
-            at += w < warp ? x : 0u;
-            total += x;
+        for (uint32_t x = 0; x < static_cast<uint32_t>(NW); ++x) {
+            const uint32_t y = s.red[par][x];
+            at += x < warp ? y : 0u;
+            total += y;
         }
         par ^= 1u;
         if (total > static_cast<uint32_t>(VEC_CAP)) return total;
-        for (int32_t i = 0; i < steps; ++i) {
-            const int32_t piece = base + 32 * i + static_cast<int32_t>(lane);
-            uint32_t m = 0;
-            if (piece < end) {
-                const uint4 t = __ldg(trow + piece);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m |= (top_at(t, piece, e) >= c ? 1u : 0u) << e;
-            }
-            const uint32_t n = __popc(m);
+        for (int b = 0; b < MAX_BATCHES; ++b) {
+            if (b >= w.batches) break;  // (uniform)
+            uint64_t m = mk[b];
+            const uint32_t n = __popcll(m);
             const uint32_t incl = warp_incl_scan(n);
             uint32_t pos = at + incl - n;
-            for (; m; m &= m - 1u) s.cvec[pos++] = static_cast<uint32_t>(8 * piece + __ffs(m) - 1);
+            const int32_t p0 = w.base + 256 * b + 8 * static_cast<int32_t>(lane);
+            for (; m; m &= m - 1u) s.cvec[pos++] = static_cast<uint32_t>(8 * p0 + __ffsll(m) - 1);
             at += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         __syncthreads();
@@ -3117,41 +3188,39 @@ struct RowO {
     // Thread t takes listed vectors [t q, t q + q). Returns the count (listed
     // only up to KEY_CAP).
     __device__ uint32_t list_keys(uint32_t c, uint32_t nv) {
+        constexpr uint32_t HOLD = 8;  // vectors a thread keeps in registers between the passes
         const uint32_t tid = threadIdx.x;
         const uint32_t q = (nv + NT - 1) / NT;
         const uint32_t j0 = min(tid * q, nv), j1 = min(j0 + q, nv);
+        uint4 r[HOLD];
+#pragma unroll
+        for (uint32_t u = 0; u < HOLD; ++u)  // the loads issue together
+            r[u] = j0 + u < j1 ? __ldg(lrow + s.cvec[j0 + u]) : make_uint4(0u, 0u, 0u, 0u);
         uint32_t cnt = 0;
-        for (uint32_t j = j0; j < j1; j += 4) {
-            uint4 r[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)  // the loads issue together
-                r[u] = j + u < j1 ? __ldg(lrow + s.cvec[j + u]) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (j + u < j1) cnt += __popc(mask_ge(r[u], c, lanes_of(static_cast<int32_t>(s.cvec[j + u]))));
+        for (uint32_t u = 0; u < HOLD; ++u)
+            if (j0 + u < j1) cnt += __popc(mask_ge(r[u], c, lanes_of(static_cast<int32_t>(s.cvec[j0 + u]))));
+        for (uint32_t j = j0 + HOLD; j < j1; ++j) {  // runs longer than HOLD (few rows)
+            const uint4 x = __ldg(lrow + s.cvec[j]);
+            cnt += __popc(mask_ge(x, c, lanes_of(static_cast<int32_t>(s.cvec[j]))));
         }
         uint32_t total;
         uint32_t at = cta_scan(s, par, cnt, total) - cnt;
         if (total > static_cast<uint32_t>(KEY_CAP)) return total;
-        for (uint32_t j = j0; j < j1; j += 4) {
-            uint4 r[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                r[u] = j + u < j1 ? __ldg(lrow + s.cvec[j + u]) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (j + u >= j1) continue;
-                const int32_t v = static_cast<int32_t>(s.cvec[j + u]);
-                for (uint32_t m = mask_ge(r[u], c, lanes_of(v)); m; m &= m - 1u) {
-                    const int h = __ffs(m) - 1;
-                    const uint32_t key = key_of8(r[u], h);
-                    s.lkey[at] = static_cast<uint16_t>(key);
-                    s.lidx[at] = static_cast<uint32_t>(8 * v + h);
-                    atomicAdd(&s.hw[min(key - c, 255u)], 1u);
-                    ++at;
-                }
+        auto put_keys = [&](const uint4 &x, int32_t v) {
+            for (uint32_t m = mask_ge(x, c, lanes_of(v)); m; m &= m - 1u) {
+                const int h = __ffs(m) - 1;
+                const uint32_t key = key_of8(x, h);
+                s.lkey[at] = static_cast<uint16_t>(key);
+                s.lidx[at] = static_cast<uint32_t>(8 * v + h);
+                atomicAdd(&s.hw[min(key - c, 255u)], 1u);
+                ++at;
             }
-        }
+        };
+#pragma unroll
+        for (uint32_t u = 0; u < HOLD; ++u)
+            if (j0 + u < j1) put_keys(r[u], static_cast<int32_t>(s.cvec[j0 + u]));
+        for (uint32_t j = j0 + HOLD; j < j1; ++j) put_keys(__ldg(lrow + s.cvec[j]), static_cast<int32_t>(s.cvec[j]));
         __syncthreads();
         return total;
     }

@@ -67,6 +67,10 @@ def _bind(path: str):
                   ctypes.c_void_p, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    wd = lib.oracle_topk_bf16_words
+    wd.restype = ctypes.c_int
+    wd.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     t = lib.oracle_tops
     t.restype = ctypes.c_int
     t.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -157,6 +161,24 @@ def topk_ordered(logits, valid_len, k: int, block_table=None, page_size: int = 6
     if rc != 0:
         raise RuntimeError("oracle_topk_bf16_ordered failed (bad argument or out of memory)")
     return out, counts, ids
+
+
+def topk_words(logits, valid_len, n: int, width: int | None = None, lib=None):
+    """Token mode, IndexerLocalTopk's output: (out, valid) with out int32
+    [rows, n + n / 32] (B' words of the selection: keys above the n-th largest in
+    index order, then the ties taken; then the plane of each index's bit 16) and
+    valid int32 [rows]."""
+    logits = _as_u16(logits)
+    rows, stride = logits.shape
+    width = stride if width is None else int(width)
+    valid_len = np.ascontiguousarray(np.asarray(valid_len, dtype=np.int32).reshape(-1))
+    out = np.empty((rows, n + n // 32), dtype=np.int32)
+    counts = np.empty(rows, dtype=np.int32)
+    lib = lib or load()
+    if lib.oracle_topk_bf16_words(logits.ctypes.data, stride, rows, width, valid_len.ctypes.data, n,
+                                  out.ctypes.data, counts.ctypes.data) != 0:
+        raise RuntimeError("oracle_topk_bf16_words failed (bad argument or out of memory)")
+    return out, counts
 
 
 def tops(logits, valid_len, width: int | None = None, lib=None) -> np.ndarray:

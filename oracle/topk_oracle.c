@@ -45,6 +45,17 @@
  * untransformed indices in the same order. Token mode (the page's logits are
  * one score per token). Reading: the ids past the count are -1, like out.
  *
+ * The words variant follows IndexerLocalTopk on the same page (class
+ * docstring and candidate): the local top-n of a token row as the DCP merge's
+ * B' words, out[r][j] = (key << 16) | (0xFFFF - (l & 0xFFFF)) for the j-th
+ * selected element l (0: empty), bit j % 32 of out[r][n + j / 32] = bit 16 of
+ * l, valid[r] = the count. Order: the selected elements whose key exceeds the
+ * n-th largest key, in index order, then the ties at it that are taken (the
+ * lowest indices), in index order. A row of at most n elements takes all of
+ * them in index order (their words hold their keys, whatever the values).
+ * Readings: NaN elements of longer rows are never selected; when fewer than n
+ * are eligible, all of them are taken, in index order.
+ *
  * The scorer's "tops" (IndexerScore.rows_out on the same page: each aligned
  * group of 8 logits' largest order key) are defined here over the eligible
  * elements of the group: below the row's valid length and not NaN; a group with
@@ -302,6 +313,66 @@ int oracle_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_
                 if (!is_nan_bf16(row[t]) && order_key(row[t]) > top) top = order_key(row[t]);
             tops[(int64_t)r * tops_stride + g] = top;
         }
+    }
+    return 0;
+}
+
+/* One B' word and its plane bit for selected element l at slot j of row r. */
+static void put_word(int32_t *orow, int32_t n, int32_t j, int32_t l, uint16_t key) {
+    orow[j] = (int32_t)(((uint32_t)key << 16) | (0xFFFFu - ((uint32_t)l & 0xFFFFu)));
+    if ((l >> 16) & 1) orow[n + j / 32] |= (int32_t)(1u << (j % 32));
+}
+
+/*
+ * The words variant (token mode): out int32 [rows, n + n / 32] as described at
+ * the top; valid int32 [rows]. n a positive multiple of 32; rows up to 131072
+ * elements wide (the plane holds bit 16 of an index). Returns 0, or 1 on a bad
+ * argument or allocation failure.
+ */
+int oracle_topk_bf16_words(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                           const int32_t *valid_len, int32_t n, int32_t *out, int32_t *valid) {
+    if (rows < 0 || width < 0 || n < 32 || n % 32 != 0 || row_stride < width || width > (1 << 17))
+        return 1;
+    if (rows == 0) return 0;
+    if (!logits || !valid_len || !out || !valid) return 1;
+    const int32_t words = n + n / 32;
+    for (int32_t r = 0; r < rows; ++r) {
+        const uint16_t *row = logits + (int64_t)r * row_stride;
+        int32_t *orow = out + (int64_t)r * words;
+        for (int32_t j = 0; j < words; ++j) orow[j] = 0;
+        int32_t L = valid_len[r];
+        if (L < 0) L = 0;
+        if (L > width) L = width;
+        if (L <= n) { /* every element, in index order */
+            for (int32_t l = 0; l < L; ++l) put_word(orow, n, l, l, order_key(row[l]));
+            valid[r] = L;
+            continue;
+        }
+        uint64_t *cand = (uint64_t *)malloc((size_t)L * sizeof(uint64_t));
+        if (!cand) return 1;
+        int32_t m = 0;
+        for (int32_t l = 0; l < L; ++l)
+            if (!is_nan_bf16(row[l]))
+                cand[m++] = ((uint64_t)order_key(row[l]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)l);
+        qsort(cand, (size_t)m, sizeof(uint64_t), cmp_desc_u64);
+        const int32_t sel = m < n ? m : n;
+        /* the n-th largest key; with fewer than n candidates every one is "above" */
+        const uint16_t T = (uint16_t)(sel == n ? (cand[n - 1] >> 32) : 0);
+        int32_t *idx = (int32_t *)malloc((size_t)(sel > 0 ? sel : 1) * sizeof(int32_t));
+        if (!idx) { free(cand); return 1; }
+        int32_t j = 0;
+        for (int pass = 0; pass < 2; ++pass) { /* above T, then ties at T */
+            int32_t c = 0;
+            for (int32_t s2 = 0; s2 < sel; ++s2) {
+                const uint16_t key = (uint16_t)(cand[s2] >> 32);
+                if ((pass == 0) == (sel < n || key > T)) idx[c++] = cand_index(cand[s2]);
+            }
+            qsort(idx, (size_t)c, sizeof(int32_t), cmp_asc_i32);
+            for (int32_t t = 0; t < c; ++t) put_word(orow, n, j++, idx[t], order_key(row[idx[t]]));
+        }
+        valid[r] = sel;
+        free(idx);
+        free(cand);
     }
     return 0;
 }

@@ -79,6 +79,9 @@ def load(path: str | None = None):
         lib.topk_bf16_select_ex.restype = ctypes.c_int
         lib.topk_bf16_tops.restype = ctypes.c_int
         lib.topk_bf16_tops.argtypes = sel_args[:5] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        lib.topk_bf16_select_words.restype = ctypes.c_int
+        lib.topk_bf16_select_words.argtypes = (sel_args[:6] + [ctypes.c_void_p, ctypes.c_int64]
+                                               + [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Options)])
         lib.topk_bf16_select_ordered.restype = ctypes.c_int
         lib.topk_bf16_select_ordered.argtypes = (sel_args[:6] + [ctypes.c_void_p, ctypes.c_int64]
                                                  + [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -197,6 +200,38 @@ def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_
             _ptr(out), _ptr(valid), _ptr(ids_t), ctypes.c_void_p(stream.cuda_stream), opt)
     _check(st)
     return out, valid, ids_t
+
+
+def select_words(logits, valid_len, n: int, tops=None, width: int | None = None, stream=None, *,
+                 out=None, valid=None, counters=None, force_exact: bool = False):
+    """The local top-n as B' words (topk_bf16_select_words): (out, valid) with out
+    int32 [rows, n + n / 32] and valid int32 [rows]. tops: None or the per-8
+    maxima (as for select_ordered); other arguments as select_ordered."""
+    import torch
+    rows, width, row_stride, _ = _inputs(logits, valid_len, None, width, 1)
+    tops_stride = 0
+    if tops is not None:
+        if not (tops.is_cuda and tops.element_size() == 2 and tops.dim() == 2 and tops.shape[0] >= rows
+                and tops.stride(1) == 1):
+            raise ValueError("tops must be CUDA 16-bit [rows, tops_stride] with unit inner stride")
+        tops_stride = tops.stride(0) if tops.shape[0] > 1 else tops.shape[1]
+    dev = logits.device
+    if out is None:
+        out = torch.empty((rows, n + n // 32), dtype=torch.int32, device=dev)
+    if valid is None:
+        valid = torch.empty(rows, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    opt = None
+    if counters is not None or force_exact:
+        opt = ctypes.byref(_Options(1 if force_exact else 0, 0,
+                                    None if counters is None else counters.data_ptr(), 0))
+    with torch.cuda.device(dev):
+        st = load().topk_bf16_select_words(_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(n),
+                                           _ptr(tops), tops_stride, _ptr(out), _ptr(valid),
+                                           ctypes.c_void_p(stream.cuda_stream), opt)
+    _check(st)
+    return out, valid
 
 
 def tops(logits, valid_len, width: int | None = None, stream=None):

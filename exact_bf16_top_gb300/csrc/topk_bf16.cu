@@ -2872,6 +2872,7 @@ struct OParams {
     int32_t table_stride, page_shift, block_rows, rows_per_request;
     int32_t *out, *valid, *ids;
     uint32_t *counters;
+    int32_t words;        // 1: out holds B' words [rows, k + k / 32] (IndexerLocalTopk)
 };
 
 struct alignas(16) Smem {
@@ -2883,6 +2884,7 @@ struct alignas(16) Smem {
     uint16_t lkey[KEY_CAP];
     uint32_t red[2][NW];
     uint32_t bc[4];
+    uint32_t plane[2048 / 32];        // B' words: bit 16 of each slot's index
 };
 
 __device__ __forceinline__ void count_o(const OParams &p, int which, uint32_t v = 1u) {
@@ -2897,8 +2899,17 @@ __device__ __forceinline__ int32_t transform_o(const OParams &p, int32_t row, in
     return page * p.block_rows + (i & ((1 << p.page_shift) - 1));
 }
 
-// Slot `slot` of the row's outputs: element i (transformed, and as is in ids).
-__device__ __forceinline__ void put_o(const OParams &p, int32_t row, uint32_t slot, int32_t i) {
+// Slot `slot` of the row's outputs: element i (transformed, and as is in ids);
+// for B' words, (key << 16) | (0xFFFF - (i & 0xFFFF)) and bit 16 of i into the
+// shared plane (written out with the row's last step).
+__device__ __forceinline__ void put_o(const OParams &p, Smem &s, int32_t row, uint32_t slot, int32_t i,
+                                      uint32_t key) {
+    if (p.words) {
+        p.out[static_cast<int64_t>(row) * (p.k + p.k / 32) + slot] =
+            static_cast<int32_t>((key << 16) | (0xFFFFu - (static_cast<uint32_t>(i) & 0xFFFFu)));
+        if ((i >> 16) & 1) atomicOr(&s.plane[slot >> 5], 1u << (slot & 31u));
+        return;
+    }
     const int64_t at = static_cast<int64_t>(row) * p.k + slot;
     p.out[at] = transform_o(p, row, i);
     if (p.ids) p.ids[at] = i;
@@ -2985,7 +2996,18 @@ struct RowO {
         return 8 * piece + e < V ? (w >> ((e & 1) * 16)) & 0xFFFFu : 0u;
     }
 
+    // Slots [from, k): -1 (words: 0); words also get the row's plane (the
+    // caller's barrier has ordered every plane bit before this) and clear it.
     __device__ __forceinline__ void write_range_neg(uint32_t from) const {
+        if (p.words) {
+            int32_t *orow = p.out + static_cast<int64_t>(row) * (p.k + p.k / 32);
+            for (uint32_t i = from + threadIdx.x; i < k; i += NT) orow[i] = 0;
+            if (threadIdx.x < k / 32) {
+                orow[k + threadIdx.x] = static_cast<int32_t>(s.plane[threadIdx.x]);
+                s.plane[threadIdx.x] = 0u;
+            }
+            return;
+        }
         for (uint32_t i = from + threadIdx.x; i < k; i += NT) {
             const int64_t at = static_cast<int64_t>(row) * p.k + i;
             p.out[at] = -1;
@@ -3248,11 +3270,13 @@ struct RowO {
             int32_t idx;
             get(j, key, idx);
             if (key == 0u) continue;
+            // Ordered: the selected keys before it in index order. Words:
+            // the keys above in index order, then the ties taken.
             if (key > T || all) {
-                put_o(p, row, pa + min(pt, take), idx);
+                put_o(p, s, row, p.words ? pa : pa + min(pt, take), idx, key);
                 ++pa;
             } else if (key == T) {
-                if (pt < take) put_o(p, row, pa + pt, idx);
+                if (pt < take) put_o(p, s, row, p.words ? k - take + pt : pa + pt, idx, key);
                 ++pt;
             }
         }
@@ -3307,6 +3331,7 @@ struct RowO {
             idx = 8 * v + h;
         });
         const uint32_t selected = all ? total : k;
+        if (p.words) __syncthreads();  // every plane bit set
         write_range_neg(selected);
         if (tid == 0) p.valid[row] = static_cast<int32_t>(selected);
     }
@@ -3318,6 +3343,29 @@ struct RowO {
         L = min(max(__ldg(p.valid_len + row), 0), p.width);
         V = (L + 7) / 8;
         lrow = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
+        if (p.words && static_cast<uint32_t>(L) <= k) {  // the whole row, its keys in the words
+            count_o(p, TOPK_CNT_BYPASS_ROWS);
+            const uint16_t *x = p.logits + static_cast<int64_t>(row) * p.row_stride;
+            int32_t *orow = p.out + static_cast<int64_t>(row) * (p.k + p.k / 32);
+            for (uint32_t j = tid; j < k; j += NT) {
+                uint32_t w = 0;
+                if (j < static_cast<uint32_t>(L)) {
+                    const uint32_t b = x[j];
+                    w = ((b ^ ((b & 0x8000u) ? 0xFFFFu : 0x8000u)) << 16) | (0xFFFFu - (j & 0xFFFFu));
+                }
+                orow[j] = static_cast<int32_t>(w);
+            }
+            for (uint32_t t = tid; t < k / 32; t += NT) {  // bit 16 of the indices 32 t .. 32 t + 31 below L
+                uint32_t m = 0;
+                for (uint32_t b = 0; b < 32; ++b) {
+                    const uint32_t j = 32 * t + b;
+                    m |= (j < static_cast<uint32_t>(L) && ((j >> 16) & 1u)) ? 1u << b : 0u;
+                }
+                orow[k + t] = static_cast<int32_t>(m);
+            }
+            if (tid == 0) p.valid[row] = L;
+            return;
+        }
         if (static_cast<uint32_t>(L) <= k) {  // the whole row, values not read
             count_o(p, TOPK_CNT_BYPASS_ROWS);
             for (uint32_t i = tid; i < k; i += NT) {
@@ -3389,6 +3437,10 @@ struct RowO {
             key = s.lkey[i0 + j];
             idx = static_cast<int32_t>(s.lidx[i0 + j]);
         });
+        if (p.words) {
+            __syncthreads();  // every plane bit set
+            write_range_neg(k);
+        }
         if (tid == 0) p.valid[row] = static_cast<int32_t>(k);
     }
 };
@@ -3399,6 +3451,7 @@ __global__ void __launch_bounds__(NT, 1) topk_ordered_kernel(const OParams p) {
     grid_dependency_wait();
     grid_dependents_release();
     if (threadIdx.x < 256u) s.hs[0][threadIdx.x] = s.hs[1][threadIdx.x] = s.hw[threadIdx.x] = 0u;
+    if (threadIdx.x < 2048u / 32u) s.plane[threadIdx.x] = 0u;
     __syncthreads();
     RowO r(s, p);
     for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += static_cast<int32_t>(gridDim.x)) {
@@ -3735,8 +3788,9 @@ topk_status_t launch_ordered(const uint16_t *logits, int64_t row_stride, int32_t
                              int64_t tops_stride, const int32_t *table, int32_t table_stride,
                              int32_t page_size, int32_t block_rows, int32_t q, int32_t *out,
                              int32_t *valid, int32_t *ids, void *stream,
-                             const topk_bf16_options_t *opt) {
+                             const topk_bf16_options_t *opt, bool words = false) {
     if (q < 1) return TOPK_ERR_ARG;
+    if (words && (k % 32 != 0 || width > (1 << 17) || table || ids)) return TOPK_ERR_ARG;
     if (table && (block_rows < page_size || (block_rows & (block_rows - 1)) != 0)) return TOPK_ERR_ARG;
     topk_status_t st = check_args(logits, row_stride, rows, width, valid_len, k, TOPK_TOKEN, table,
                                   table_stride, page_size, out);
@@ -3774,6 +3828,7 @@ topk_status_t launch_ordered(const uint16_t *logits, int64_t row_stride, int32_t
     prm.valid = valid;
     prm.ids = ids;
     prm.counters = opt ? opt->counters : nullptr;
+    prm.words = words ? 1 : 0;
 
     const int grid = rows < d->sms ? rows : d->sms;
     cudaLaunchConfig_t cfg = {};
@@ -3819,6 +3874,14 @@ topk_status_t topk_bf16_tops(const uint16_t *logits, int64_t row_stride, int32_t
     topk::ordered::topk_tops_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         logits, row_stride, rows, width, valid_len, tops, tops_stride, static_cast<int32_t>(pieces));
     return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+topk_status_t topk_bf16_select_words(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                     int32_t width, const int32_t *valid_len, int32_t n,
+                                     const uint16_t *tops, int64_t tops_stride, int32_t *out,
+                                     int32_t *valid, void *stream, const topk_bf16_options_t *options) {
+    return topk::launch_ordered(logits, row_stride, rows, width, valid_len, n, tops, tops_stride,
+                                nullptr, 0, 64, 64, 1, out, valid, nullptr, stream, options, true);
 }
 
 topk_status_t topk_bf16_select_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows,

@@ -223,6 +223,35 @@ topk_status_t topk_bf16_select_ordered(const uint16_t *logits, int64_t row_strid
                                        const topk_bf16_options_t *options);
 
 /*
+ * The local top-n of token rows as the DCP merge's B' words (vLLM kimi_k3
+ * "dsa/indexer": IndexerLocalTopk's docstring, kernel and candidate), one GPU's
+ * part: out[r * (n + n / 32) + j], j < n, is (key << 16) | (0xFFFF - (l & 0xFFFF))
+ * for the j-th selected element l of row r, with key = x ^ (x < 0 ? 0xFFFF :
+ * 0x8000) of its BF16 bits, or 0 for an empty slot; bit j % 32 of
+ * out[r * (n + n / 32) + n + j / 32] is bit 16 of l. Order: the selected
+ * elements whose key exceeds the row's n-th largest key, in index order, then
+ * the ties at it that are taken (the lowest indices), in index order. A row of at
+ * most n elements takes every one of them, in index order (their words hold
+ * their keys, whatever the values); in longer rows NaN is never selected, and
+ * when fewer than n are eligible all of them are taken, in index order.
+ * valid[r]: the count. The selection is the one topk_bf16_select makes.
+ *
+ * n            32 .. TOPK_MAX_K, a multiple of 32.
+ * width        0 .. 131072 (the plane holds bit 16 of an index).
+ * tops         NULL, or the per-8 maxima as for topk_bf16_select_ordered (the
+ *              bound that limits the vectors read); NULL: the exact select.
+ * out          device int32 [rows, n + n / 32]; valid: device int32 [rows].
+ * options      NULL, or test hooks as for topk_bf16_select_ordered.
+ * logits, row_stride, rows, valid_len, stream as in topk_bf16_select. Errors as
+ * topk_bf16_select_ordered, plus TOPK_ERR_ARG for n not a multiple of 32 or a
+ * width above 131072.
+ */
+topk_status_t topk_bf16_select_words(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                     int32_t width, const int32_t *valid_len, int32_t n,
+                                     const uint16_t *tops, int64_t tops_stride, int32_t *out,
+                                     int32_t *valid, void *stream, const topk_bf16_options_t *options);
+
+/*
  * The per-8 maxima topk_bf16_select_ordered is bounded by, for producers that
  * do not write them (IndexerScore.rows_out on the indexer page writes them
  * with the logits): tops[r * tops_stride + g] = the largest order key among

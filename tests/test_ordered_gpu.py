@@ -103,3 +103,40 @@ def test_ordered_edges_and_exact_path():
     assert_same(run_ordered(case, counters=counters), expected(case), case.name)
     c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
     assert c["ordered_tops"] > 0 and c["ordered_exact"] > 0 and c["bypass_rows"] > 0, c
+
+
+def run_words(case, n, use_tops=True, counters=None, force_exact=False):
+    logits, valid, _ = _dev(case)
+    tops = tk.tops(logits, valid, width=case.width) if use_tops else None
+    out, cnt = tk.select_words(logits, valid, n, tops, width=case.width, counters=counters,
+                               force_exact=force_exact)
+    torch.cuda.synchronize()
+    assert tk.device_status() == 0
+    return out.cpu().numpy(), cnt.cpu().numpy()
+
+
+@pytest.mark.parametrize("width,n", [(3000, 32), (20000, 512), (131072, 2048), (100000, 256)])
+def test_words_parity(width, n):
+    """The local top-n as B' words (every path: whole short rows, the bounded
+    select, the exact one), bit-exact against the oracle, index plane included."""
+    case = W.paged_case(110 + n, rows=24, width=width, k=n, q=1)
+    exp = oracle.topk_words(case.logits, case.valid_len, n, width=case.width)
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for kw in ({}, {"force_exact": True}, {"use_tops": False}):
+        got = run_words(case, n, counters=counters, **kw)
+        assert np.array_equal(got[1], exp[1]), (case.name, kw)
+        assert np.array_equal(got[0], exp[0]), (case.name, kw)
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["ordered_exact"] > 0 and c["ordered_tops"] > 0, c
+
+
+def test_words_edges():
+    """Edge rows, short ones (lengths 0, 1, 7, ...) taken whole among them."""
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for width, n in ((16384, 512), (70000, 64)):
+        case = W.edge_cases(5, width=width, k=n)[0]
+        exp = oracle.topk_words(case.logits, case.valid_len, n, width=case.width)
+        got = run_words(case, n, counters=counters)
+        assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1]), case.name
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["bypass_rows"] > 0, c

@@ -203,21 +203,40 @@ class OrderedGpuCase(GpuCase):
                           self.table, c.page_size, width=c.width, out=self.out, valid=self.valid_out)
 
 
+class WordsGpuCase(OrderedGpuCase):
+    """The local top-n as B' words on a resident workload (maxima precomputed)."""
+
+    def __init__(self, case, torch, device, min_copies: int = 1):
+        super().__init__(case, torch, device, min_copies)
+        self.out = torch.empty((case.rows, case.k + case.k // 32), dtype=torch.int32, device=device)
+
+    def launch(self, i: int, tk):
+        c = self.case
+        tk.select_words(self.logits[i % self.copies], self.valid, c.k, self.tops[i % self.copies],
+                        width=c.width, out=self.out, valid=self.valid_out)
+
+
 def gpu_case(name, case, torch, device, min_copies: int = 1):
     if name.startswith("ordered"):
         return OrderedGpuCase(case, torch, device, min_copies)
+    if name.startswith("words"):
+        return WordsGpuCase(case, torch, device, min_copies)
     return GpuCase(case, torch, device, min_copies)
 
 
-def ordered_bytes(case) -> int:
-    """Bytes the ordered select must move: the maxima of every valid group of 8,
-    at least the k vectors that hold the selected keys, the valid lengths, the
-    output and the counts, and one table entry per page that can hold a
-    selected index (as algorithmic_bytes)."""
+def ordered_bytes(case, words: bool = False) -> int:
+    """Bytes the ordered select (or the B' words) must move: the maxima of every
+    valid group of 8, at least the k vectors that hold the selected keys, the
+    valid lengths, the output (words: k + k / 32 per row) and the counts, and one
+    table entry per page that can hold a selected index (as algorithmic_bytes).
+    Rows of at most k elements: words read their logits, the ordered select
+    nothing."""
     L = np.clip(case.valid_len.astype(np.int64), 0, case.width)
     big = L > case.k
     b = int((2 * ((L + 7) // 8) + 16 * np.minimum(case.k, L))[big].sum())
-    b += 4 * case.rows + 4 * case.rows * case.k + 4 * case.rows
+    if words:
+        b += int((2 * L)[~big].sum())
+    b += 4 * case.rows + 4 * case.rows * (case.k + (case.k // 32 if words else 0)) + 4 * case.rows
     if case.block_table is not None:
         pages = -(-L // case.page_size)
         b += int(4 * np.minimum(np.minimum(L, case.k), pages).sum())
@@ -329,7 +348,8 @@ def sweep_cases(full: bool):
               ("config4 block 32x1048576 k2048", lambda: W.config4(0)),
               ("config5a wide 256x524288 k512", lambda: W.config5a(0)),
               ("config5b wide 64x1048576 k512", lambda: W.config5b(0)),
-              ("ordered 64x1048576 k2048 (bounded by per-8 maxima)", lambda: W.ordered_wide(0))]
+              ("ordered 64x1048576 k2048 (bounded by per-8 maxima)", lambda: W.ordered_wide(0)),
+              ("words 128x16384 n2048 (local top-n as B' words)", lambda: W.local_rows(0))]
     return cases
 
 
@@ -339,7 +359,8 @@ def run_sweep(tk, torch, device, steps, warmup, peak, full):
         case = make()
         gc = gpu_case(name, case, torch, device)
         us = time_graph(gc, tk, torch, steps, warmup)
-        ab = ordered_bytes(case) if name.startswith("ordered") else algorithmic_bytes(case)
+        ab = ordered_bytes(case, name.startswith("words")) if name.startswith(("ordered", "words")) \
+            else algorithmic_bytes(case)
         gbs = ab / (us * 1e-6) / 1e9
         out.append({"workload": name, "us_per_launch": round(us, 3),
                     "rows_per_s": round(case.rows / (us * 1e-6), 1),
@@ -388,6 +409,9 @@ def diag(args):
             if name.startswith("ordered"):
                 tk.select_ordered(gc.logits[0], gc.valid, c.k, gc.tops[0], gc.table, c.page_size,
                                   width=c.width, out=gc.out, valid=gc.valid_out, counters=ctr)
+            elif name.startswith("words"):
+                tk.select_words(gc.logits[0], gc.valid, c.k, gc.tops[0], width=c.width, out=gc.out,
+                                valid=gc.valid_out, counters=ctr)
             else:
                 tk.select(gc.logits[0], gc.valid, c.k, c.mode, gc.table, c.page_size, out=gc.out,
                           width=c.width, counters=ctr)

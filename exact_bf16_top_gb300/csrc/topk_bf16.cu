@@ -2858,6 +2858,7 @@ constexpr int REP_CAP = 16384;   // representatives: every top (rows of up to 16
                                  // every piece's maximum (up to 16384 pieces: 1M logits)
 constexpr int VEC_CAP = 8192;    // candidate vectors listed
 constexpr int KEY_CAP = 8192;    // candidate keys listed
+constexpr int STAGE_VECS = (VEC_CAP * 4 + KEY_CAP * 6) / 16;  // rows the exact select keeps in shared memory
 constexpr int MAX_BATCHES = 4;   // 256-piece batches of a warp's range of tops (16384 pieces / 16 warps)
 
 struct OParams {
@@ -2879,9 +2880,14 @@ struct alignas(16) Smem {
     alignas(16) uint32_t hs[2][256];  // byte-pass histograms (zero between uses)
     alignas(16) uint32_t hw[256];     // the candidates' window (key - c)
     uint16_t rep[REP_CAP];
-    uint32_t cvec[VEC_CAP];           // candidate vectors, in index order
-    uint32_t lidx[KEY_CAP];           // candidate keys' element indices, in index order
-    uint16_t lkey[KEY_CAP];
+    union {
+        struct {
+            uint32_t cvec[VEC_CAP];   // candidate vectors, in index order
+            uint32_t lidx[KEY_CAP];   // candidate keys' element indices, in index order
+            uint16_t lkey[KEY_CAP];
+        };
+        uint4 keys[STAGE_VECS];       // the exact select: a row's keys, 8 per vector (0: not eligible)
+    };
     uint32_t red[2][NW];
     uint32_t bc[4];
     uint32_t plane[2048 / 32];        // B' words: bit 16 of each slot's index
@@ -3282,18 +3288,43 @@ struct RowO {
         }
     }
 
+    // The keys of vector v (element h in half h of the result; 0: not eligible).
+    __device__ __forceinline__ uint4 packed_keys(int32_t v) const {
+        const uint4 r = __ldg(lrow + v);
+        const uint32_t m = mask_ge(r, 1u, lanes_of(v));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t kk = key2(w[i]);
+            o[i] = (((m >> (2 * i)) & 1u) ? kk & 0xFFFFu : 0u) | (((m >> (2 * i + 1)) & 1u) ? kk & 0xFFFF0000u : 0u);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+
+    static __device__ __forceinline__ uint32_t half8(const uint4 &kk, int h) {
+        const uint32_t w = (h & 4) ? ((h & 2) ? kk.w : kk.z) : ((h & 2) ? kk.y : kk.x);
+        return (w >> ((h & 1) * 16)) & 0xFFFFu;
+    }
+
     // The exact select over every key of the row (two byte passes over all
     // eligible keys), then the ordered output from a scan of the row: thread t
-    // takes vectors [t q, t q + q).
+    // takes vectors [t q, t q + q). Rows of at most STAGE_VECS vectors keep their
+    // keys in shared memory after the first pass (the lists are not in use).
     __device__ void exact_row() {
         const uint32_t tid = threadIdx.x;
         count_o(p, TOPK_CNT_ORDERED_EXACT);
+        const bool staged = V <= STAGE_VECS;
+        auto keys_of = [&](int32_t v) -> uint4 { return staged ? s.keys[v] : packed_keys(v); };
         for (int32_t v0 = 0; v0 < V; v0 += NT) {
             const int32_t v = v0 + static_cast<int32_t>(tid);
-            const uint4 r = v < V ? __ldg(lrow + v) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t m = v < V ? mask_ge(r, 1u, lanes_of(v)) : 0u;
+            const uint4 kk = v < V ? packed_keys(v) : make_uint4(0u, 0u, 0u, 0u);
+            if (staged && v < V) s.keys[v] = kk;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) agg_add(s.hs[0], key_of8(r, h) >> 8, (m >> h) & 1u);
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = half8(kk, h);
+                agg_add(s.hs[0], key >> 8, key != 0u);
+            }
         }
         __syncthreads();
         find_o(s, s.hs[0], k);
@@ -3305,12 +3336,11 @@ struct RowO {
         if (!all) {
             for (int32_t v0 = 0; v0 < V; v0 += NT) {
                 const int32_t v = v0 + static_cast<int32_t>(tid);
-                const uint4 r = v < V ? __ldg(lrow + v) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t m = v < V ? mask_ge(r, 1u, lanes_of(v)) : 0u;
+                const uint4 kk = v < V ? keys_of(v) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
-                    const uint32_t key = key_of8(r, h);
-                    const bool in = ((m >> h) & 1u) && (key >> 8) == hb;
+                    const uint32_t key = half8(kk, h);
+                    const bool in = key != 0u && (key >> 8) == hb;
                     if (__any_sync(0xFFFFFFFFu, in)) agg_add(s.hs[1], key & 0xFFu, in);
                 }
             }
@@ -3323,13 +3353,37 @@ struct RowO {
         }
         const uint32_t q = (static_cast<uint32_t>(V) + NT - 1) / NT;
         const uint32_t v0 = min(tid * q, static_cast<uint32_t>(V)), v1 = min(v0 + q, static_cast<uint32_t>(V));
-        write_ordered(T, take, all, (v1 - v0) * 8u, [&](uint32_t j, uint32_t &key, int32_t &idx) {
-            const int32_t v = static_cast<int32_t>(v0 + j / 8u);
-            const int h = static_cast<int>(j % 8u);
-            const uint4 r = __ldg(lrow + v);
-            key = ((mask_ge(r, 1u, lanes_of(v)) >> h) & 1u) ? key_of8(r, h) : 0u;
-            idx = 8 * v + h;
-        });
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t v = v0; v < v1; ++v) {
+            const uint4 kk = keys_of(static_cast<int32_t>(v));
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = half8(kk, h);
+                gt += key != 0u && (key > T || all);
+                eq += !all && key != 0u && key == T;
+            }
+        }
+        uint32_t tg, te;
+        uint32_t pa = cta_scan(s, par, gt, tg) - gt;
+        uint32_t pt = cta_scan(s, par, eq, te) - eq;
+        if (gt != 0u || (eq != 0u && pt < take)) {
+            for (uint32_t v = v0; v < v1; ++v) {
+                const uint4 kk = keys_of(static_cast<int32_t>(v));
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = half8(kk, h);
+                    if (key == 0u) continue;
+                    const int32_t idx = static_cast<int32_t>(8 * v) + h;
+                    if (key > T || all) {
+                        put_o(p, s, row, p.words ? pa : pa + min(pt, take), idx, key);
+                        ++pa;
+                    } else if (key == T) {
+                        if (pt < take) put_o(p, s, row, p.words ? k - take + pt : pa + pt, idx, key);
+                        ++pt;
+                    }
+                }
+            }
+        }
         const uint32_t selected = all ? total : k;
         if (p.words) __syncthreads();  // every plane bit set
         write_range_neg(selected);

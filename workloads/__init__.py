@@ -280,6 +280,16 @@ def ordered_wide(seed: int = 0, rows: int = 64, width: int = 1 << 20, k: int = 2
     return Case(f"ordered {rows}x{width} k{k}", logits, width, valid, k, TOKEN, table)
 
 
+def local_rows(seed: int = 0, rows: int = 128, width: int = 16384, n: int = 2048) -> Case:
+    """One GPU's part of a context split over several (DCP): rows of up to 16384
+    keys (a 128K context over 8 GPUs) whose local top-n (n 2048) goes out as
+    B' words; N(0,1), valid lengths uniform in [width/2, width], no table."""
+    rng = rng_for(seed)
+    logits = normal_bf16(rng, (rows, width))
+    valid = rng.integers(width // 2, width + 1, size=rows).astype(np.int32)
+    return Case(f"local {rows}x{width} n{n}", logits, width, valid, n, TOKEN)
+
+
 def edge_cases(seed: int = 0, width: int = 16384, k: int = 512) -> list[Case]:
     """Edge rows in token and block mode (one Case per mode)."""
     rng = rng_for(seed)

@@ -3307,15 +3307,20 @@ struct RowO {
         return (w >> ((h & 1) * 16)) & 0xFFFFu;
     }
 
-    // The exact select over every key of the row (two byte passes over all
-    // eligible keys), then the ordered output from a scan of the row: thread t
-    // takes vectors [t q, t q + q). Rows of at most STAGE_VECS vectors keep their
-    // keys in shared memory after the first pass (the lists are not in use).
+    // The exact select over every key of the row, then the ordered output from
+    // a scan of the row: thread t takes vectors [t q, t q + q). The k-th key:
+    // the row's largest key M and the eligible count (one pass), a histogram of
+    // the 512 keys below M in bins of two (the keys in it spread over the bins:
+    // plain atomics), then which of the bin's two keys it is (a count of the
+    // upper one); when it lies lower, two byte passes over every key. Rows of at
+    // most STAGE_VECS vectors keep their keys in shared memory after the first
+    // pass (the lists are not in use).
     __device__ void exact_row() {
         const uint32_t tid = threadIdx.x;
         count_o(p, TOPK_CNT_ORDERED_EXACT);
         const bool staged = V <= STAGE_VECS;
         auto keys_of = [&](int32_t v) -> uint4 { return staged ? s.keys[v] : packed_keys(v); };
+        uint32_t top = 0, mine = 0;
         for (int32_t v0 = 0; v0 < V; v0 += NT) {
             const int32_t v = v0 + static_cast<int32_t>(tid);
             const uint4 kk = v < V ? packed_keys(v) : make_uint4(0u, 0u, 0u, 0u);
@@ -3323,17 +3328,69 @@ struct RowO {
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
                 const uint32_t key = half8(kk, h);
-                agg_add(s.hs[0], key >> 8, key != 0u);
+                top = max(top, key);
+                mine += key != 0u;
             }
         }
-        __syncthreads();
-        find_o(s, s.hs[0], k);
-        __syncthreads();
-        const uint32_t hb = s.bc[0], ha = s.bc[1], total = s.bc[2];
-        __syncthreads();
+        uint32_t total;
+        cta_scan(s, par, mine, total);  // (its barrier also publishes the staged keys)
+        top = cta_max(s, par, top);
         uint32_t T = 0, take = 0;
         const bool all = total <= k;  // every eligible key
+        bool found = all;
         if (!all) {
+            const uint32_t lo = top > 511u ? top - 511u : 1u;  // the window: keys lo .. top
+            for (int32_t v0 = 0; v0 < V; v0 += NT) {
+                const int32_t v = v0 + static_cast<int32_t>(tid);
+                const uint4 kk = v < V ? keys_of(v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = half8(kk, h);
+                    if (key >= lo) atomicAdd(&s.hs[0][255u - ((top - key) >> 1)], 1u);
+                }
+            }
+            __syncthreads();
+            find_o(s, s.hs[0], k);
+            __syncthreads();
+            const uint32_t b = s.bc[0], above_b = s.bc[1], in_window = s.bc[2];
+            __syncthreads();
+            if (in_window >= k) {
+                // Bin b holds keys top - 2 (255 - b) - 1 and the one above it.
+                const uint32_t upper = top - 2u * (255u - b);
+                uint32_t n_up = 0;
+                for (int32_t v0 = 0; v0 < V; v0 += NT) {
+                    const int32_t v = v0 + static_cast<int32_t>(tid);
+                    const uint4 kk = v < V ? keys_of(v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) n_up += half8(kk, h) == upper;
+                }
+                uint32_t ups;
+                cta_scan(s, par, n_up, ups);
+                if (above_b + ups >= k) {
+                    T = upper;
+                    take = k - above_b;
+                } else {
+                    T = upper - 1u;
+                    take = k - above_b - ups;
+                }
+                found = true;
+            }
+        }
+        if (!found) {
+            for (int32_t v0 = 0; v0 < V; v0 += NT) {
+                const int32_t v = v0 + static_cast<int32_t>(tid);
+                const uint4 kk = v < V ? keys_of(v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = half8(kk, h);
+                    agg_add(s.hs[0], key >> 8, key != 0u);
+                }
+            }
+            __syncthreads();
+            find_o(s, s.hs[0], k);
+            __syncthreads();
+            const uint32_t hb = s.bc[0], ha = s.bc[1];
+            __syncthreads();
             for (int32_t v0 = 0; v0 < V; v0 += NT) {
                 const int32_t v = v0 + static_cast<int32_t>(tid);
                 const uint4 kk = v < V ? keys_of(v) : make_uint4(0u, 0u, 0u, 0u);

@@ -73,3 +73,41 @@ def test_bad_arguments_rejected_on_host(lib, kw, status):
 
 def test_zero_rows_is_a_no_op(lib):
     assert _call(lib, rows=0, logits=None, valid=None, out=None) == 0
+
+
+def _ordered(lib, logits=16, stride=8, rows=1, width=8, valid_len=16, k=1, tops=16, tops_stride=8,
+             table=None, table_stride=0, page=64, block_rows=64, q=1, out=16, valid=16, ids=None):
+    return lib.topk_bf16_select_ordered(logits, stride, rows, width, valid_len, k, tops, tops_stride,
+                                        table, table_stride, page, block_rows, q, out, valid, ids,
+                                        None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), 3), (dict(valid=None), 1), (dict(valid=18), 2), (dict(ids=18), 2),
+    (dict(tops=24), 2), (dict(tops_stride=12), 2), (dict(tops_stride=0), 1), (dict(q=0), 1),
+    (dict(table=16, table_stride=1, block_rows=32), 1), (dict(table=16, table_stride=1, block_rows=96), 1),
+    (dict(width=(1 << 20) + 8, stride=(1 << 20) + 8, tops_stride=1 << 17), 4),
+])
+def test_ordered_bad_arguments_rejected_on_host(lib, kw, status):
+    assert _ordered(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=33), 1), (dict(n=0), 3), (dict(n=4096), 3), (dict(width=(1 << 17) + 8, stride=(1 << 17) + 8,
+                                                              tops_stride=(1 << 14) + 8), 1),
+    (dict(valid=None), 1), (dict(tops=20), 2),
+])
+def test_words_bad_arguments_rejected_on_host(lib, kw, status):
+    a = dict(logits=16, stride=8, rows=1, width=8, valid_len=16, n=32, tops=16, tops_stride=8, out=16,
+             valid=16)
+    a.update(kw)
+    assert lib.topk_bf16_select_words(a["logits"], a["stride"], a["rows"], a["width"], a["valid_len"],
+                                      a["n"], a["tops"], a["tops_stride"], a["out"], a["valid"],
+                                      None, None) == status
+
+
+def test_tops_bad_arguments_rejected_on_host(lib):
+    assert lib.topk_bf16_tops(16, 8, 1, 8, 16, 24, 8, None) == 2    # misaligned tops
+    assert lib.topk_bf16_tops(16, 8, 1, 8, 16, 16, 4, None) == 2    # stride not a multiple of 8
+    assert lib.topk_bf16_tops(16, 8, 1, 80, 16, 16, 8, None) == 4   # width above the row stride
+    assert lib.topk_bf16_tops(16, 8, 0, 8, 16, 16, 8, None) == 0    # no rows: nothing to do

@@ -1409,8 +1409,8 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     const int32_t cid = static_cast<int32_t>(blockIdx.x / C);
     const int32_t ncl = static_cast<int32_t>(gridDim.x / C);
 
-    grid_dependency_wait();
-    grid_dependents_release();
+    // Shared-memory set-up first: it touches no global memory, so it overlaps
+    // the previous kernel's tail under programmatic dependent launch.
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
@@ -1422,6 +1422,8 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     for (int i = 0; i < 4; ++i) s.hwin[i][tid] = 0u;
     s.h_merge[0][tid] = s.h_merge[1][tid] = 0u;
     __syncthreads();
+    grid_dependency_wait();
+    grid_dependents_release();
     Feed feed;
     if (tid == 0) {
         feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
@@ -1949,9 +1951,7 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
     PhaseClock whole;
     whole.start(p);
 
-    grid_dependency_wait();
-    grid_dependents_release();
-    if (tid == 0) {
+    if (tid == 0) {  // (shared-memory set-up before the wait, as in topk_kernel)
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
         s.abort_flag = 0u;
@@ -1959,6 +1959,9 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
     s.h[0][tid] = s.h[1][tid] = s.h[2][tid] = 0u;
     if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
     __syncthreads();
+    grid_dependency_wait();
+    grid_dependents_release();
+
     Feed feed;
     if (tid == 0) {
         feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
@@ -2766,9 +2769,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     const int tid = threadIdx.x;
     const int32_t step = static_cast<int32_t>(gridDim.x);
 
-    grid_dependency_wait();
-    grid_dependents_release();
-    if (tid == 0) {
+    if (tid == 0) {  // (shared-memory set-up before the wait, as in topk_kernel)
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
         s.abort_flag = 0u;
@@ -2777,6 +2778,9 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     }
     for (int i = tid; i < 4 * 256; i += NT) (&s.hs[0][0])[i] = 0u;
     __syncthreads();
+    grid_dependency_wait();
+    grid_dependents_release();
+
     int32_t feed_row = p.rows;
     if (tid == 0) {
         int32_t V;
@@ -3559,11 +3563,12 @@ struct RowO {
 __global__ void __launch_bounds__(NT, 1) topk_ordered_kernel(const OParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
-    grid_dependency_wait();
-    grid_dependents_release();
     if (threadIdx.x < 256u) s.hs[0][threadIdx.x] = s.hs[1][threadIdx.x] = s.hw[threadIdx.x] = 0u;
     if (threadIdx.x < 2048u / 32u) s.plane[threadIdx.x] = 0u;
     __syncthreads();
+    grid_dependency_wait();
+    grid_dependents_release();
+
     RowO r(s, p);
     for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += static_cast<int32_t>(gridDim.x)) {
         r.select(row);

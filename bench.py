@@ -365,7 +365,11 @@ def run_sweep(tk, torch, device, steps, warmup, peak, full):
         out.append({"workload": name, "us_per_launch": round(us, 3),
                     "rows_per_s": round(case.rows / (us * 1e-6), 1),
                     "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
-                    "copies": gc.copies, "plan": tk.plan(case.rows, case.width, case.k, case.mode)})
+                    "copies": gc.copies,
+                    "plan": ({"variant": "ordered", "threads": 512,
+                              "ctas": min(case.rows, torch.cuda.get_device_properties(device).multi_processor_count)}
+                             if name.startswith(("ordered", "words"))
+                             else tk.plan(case.rows, case.width, case.k, case.mode))})
         del gc
         torch.cuda.empty_cache()
     return out

@@ -2577,11 +2577,12 @@ struct Row {
 
     // The cut for the next row: below the k-th key T by the distance that held
     // the n - k extra keys over [c, T], scaled to aim at about
-    // k + min(k / 4, (SURV_CAP - k) / 2) keys at or above it on a row like this
-    // one (measured: a margin of k / 4 left no row short of k keys on N(0,1)
-    // rows, k / 8 about one row in forty, each costing a second cut).
+    // k + min(max(k / 8, 128), (SURV_CAP - k) / 2) keys at or above it on a row
+    // like this one. The margin covers the spread of the count, which grows like
+    // its square root (measured on N(0,1) rows with k = 512: 128 left no row
+    // short of k keys, 64 about one row in forty, each costing a second cut).
     __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t n) {
-        const uint32_t want = min(k / 4u, (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
+        const uint32_t want = min(max(k / 8u, 128u), (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
         const uint32_t d = T > c ? max((want * (T - c)) / (n - k + 1u), 1u) : 16u;
         guess = T > d ? T - d : 1u;
     }

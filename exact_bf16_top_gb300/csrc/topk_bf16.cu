@@ -2291,20 +2291,75 @@ struct Row {
         return true;
     }
 
+    // Every candidate key its own representative (rows too short for groups):
+    // the exact k-th largest key, from a window of the 512 keys at and below
+    // the largest key (two keys per bin; the keys in it spread over the bins:
+    // plain atomics) and a count of the upper key of the bin that holds it
+    // (exact: a crowd of ties at it may be written by index-ordered rescans).
+    // When it lies lower, the radix passes of exact_cut; rows that select a
+    // quarter of their elements or more go there directly (their k-th key is
+    // far below the largest). False when the row has fewer than k candidates.
+    __device__ bool window_cut(uint32_t &c) {
+        const int tid = threadIdx.x;
+        if (4u * k >= static_cast<uint32_t>(M::BLOCK ? V : L)) return exact_cut(c);
+        uint32_t top = 0;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) top = max(top, key_at<M>(ck, h));
+        }
+        top = __reduce_max_sync(0xFFFFFFFFu, top);
+        if (lane_id() == 0) s.red[par][tid >> 5] = top;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) top = max(top, s.red[par][w]);
+        par ^= 1u;
+        if (top == 0u) return false;  // no candidate at all
+        const uint32_t lo = top > 511u ? top - 511u : 1u;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) {
+                const uint32_t key = key_at<M>(ck, h);
+                if (key >= lo) atomicAdd(&s.hs[0][255u - ((top - key) >> 1)], 1u);
+            }
+        }
+        __syncthreads();
+        warp0_find(s, s.hs[0], k);
+        __syncthreads();
+        const uint32_t b = s.bc[0], above_b = s.bc[1], in_window = s.bc[2];
+        __syncthreads();  // every thread has read s.bc
+        if (in_window < k) return exact_cut(c);
+        const uint32_t upper = top - 2u * (255u - b);  // bin b: keys upper - 1 and upper
+        uint32_t n_up = 0;
+        for (int j = 0; j < NV; ++j) {
+            uint32_t ck[4];
+            clean(j * NT + tid, ck);
+#pragma unroll
+            for (int h = 0; h < M::KPV; ++h) n_up += key_at<M>(ck, h) == upper;
+        }
+        uint32_t ups;
+        block_scan(s, par, n_up, ups);
+        c = above_b + ups >= k ? upper : upper - 1u;
+        return true;
+    }
+
     __device__ __forceinline__ bool cut_for(uint32_t g, uint32_t &c) {
         // (a group is at most a thread's NV vectors)
         if constexpr (M::BLOCK) {
             if constexpr (NV >= 8) if (g == 8u) return rep_cut<8>(c);
             if constexpr (NV >= 4) if (g == 4u) return rep_cut<4>(c);
             if (g == 2u) return rep_cut<2>(c);
-            return exact_cut(c);
+            return p.force_direct ? exact_cut(c) : window_cut(c);
         } else {
             if constexpr (NV >= 8) if (g == 64u) return rep_cut<64>(c);
             if constexpr (NV >= 4) if (g == 32u) return rep_cut<32>(c);
             if (g == 16u) return rep_cut<16>(c);
             if (g == 8u) return rep_cut<8>(c);
             if (g == 4u) return rep_cut<4>(c);
-            return exact_cut(c);
+            return p.force_direct ? exact_cut(c) : window_cut(c);
         }
     }
 

@@ -848,10 +848,16 @@ struct Cta {
     // of g logits (token) or g blocks (block), with key >= thr, or nothing;
     // g = 1 feeds every candidate key. Every lane of a warp feeds together.
     __device__ __forceinline__ void rep_pass(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, uint32_t hb) {
-        auto feed = [&](uint32_t key) {
+        rep_walk(stg, tile_v0, nv, g, [&](uint32_t key) {
             if (hb == ALL) agg_add(s->hwin[2], key >> 8, key != 0u);
             else agg_add(s->hwin[3], key & 0xFFu, key != 0u && (key >> 8) == hb);
-        };
+        });
+    }
+
+    // The tile's representatives (groups of g, keys >= thr, else 0) fed to
+    // feed(key), every lane of a warp together.
+    template <class F>
+    __device__ __forceinline__ void rep_walk(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g, F &&feed) {
         uint32_t acc = 0x80008000u;   // token: packed running maximum of a group
         uint32_t bacc = 0u;           // block: running maximum key of a group
         const uint32_t per = g >= 8u ? g >> 3 : 1u;  // vectors per token group
@@ -944,6 +950,51 @@ struct Cta {
         for (;;) {
             PhaseClock clk;
             clk.start(*p);
+            // First a window of the 510 keys at and below the largest
+            // representative (two keys per bin, the lowest bin holding every
+            // lower one; plain atomics: the representatives spread over it).
+            // The cut is the lower key of the bin holding the k-th
+            // representative; when that bin is crowded (more than k / 4 of
+            // them: rows of few distinct values), a count of its upper key
+            // makes it exactly the k-th representative, since a key lower by
+            // one can be a crowd of its own that later tiles would append.
+            uint32_t top = 0;
+            rep_walk(stg, tile_v0, nv, g, [&](uint32_t key) { top = max(top, key); });
+            top = __reduce_max_sync(0xFFFFFFFFu, top);
+            if (lane_id() == 0) s->red[parity][tid >> 5] = top;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w) top = max(top, s->red[parity][w]);
+            parity ^= 1u;
+            if (top != 0u) {
+                rep_walk(stg, tile_v0, nv, g, [&](uint32_t key) {
+                    if (key) atomicAdd(&s->hwin[2][255u - min((top - key) >> 1, 255u)], 1u);
+                });
+                __syncthreads();
+                uint32_t b, wabove, wtotal;
+                const bool ok = find_bin256(s->hwin[2], k, b, wabove, wtotal);
+                const uint32_t in_bin = ok ? s->hwin[2][b] : 0u;
+                __syncthreads();
+                s->hwin[2][tid] = 0u;
+                __syncthreads();
+                if (ok && b > 0u) {
+                    const uint32_t upper = top - 2u * (255u - b);  // bin b: keys upper - 1, upper
+                    uint32_t c = upper > 1u ? upper - 1u : 1u;
+                    if (in_bin > k / 4u) {
+                        uint32_t mine = 0;
+                        rep_walk(stg, tile_v0, nv, g, [&](uint32_t key) { mine += key == upper; });
+                        uint32_t ups;
+                        block_incl_scan(mine, ups);
+                        if (wabove + ups >= k) c = upper;
+                    }
+                    count_event(*p, g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
+                    first_c = c;
+                    thr = max(thr, c + 1u);
+                    publish(c);
+                    clk.stop(*p, TOPK_CNT_CYC_CUT);
+                    return;
+                }
+            }
             rep_pass(stg, tile_v0, nv, g, ALL);
             __syncthreads();
             clk.stop(*p, TOPK_CNT_CYC_REPS);

@@ -129,11 +129,14 @@ typedef struct {
 /* Indices into topk_bf16_options_t.counters. */
 enum {
     TOPK_CNT_BYPASS_ROWS = 0,    /* rows with n <= k */
-    TOPK_CNT_TILE_SAMPLED = 1,   /* first tiles cut by the k-th largest group representative */
-    TOPK_CNT_TILE_EXACT = 2,     /* first tiles cut by the exact path (every key its own
-                                    representative): forced, fallen back to, or k-sized groups */
+    TOPK_CNT_TILE_SAMPLED = 1,   /* first tiles (and resident-keys rows) cut by the k-th largest
+                                    group representative */
+    TOPK_CNT_TILE_EXACT = 2,     /* first tiles (and resident-keys rows) cut by the exact path
+                                    (every key its own representative): forced, fallen back to,
+                                    or rows too short for groups */
     TOPK_CNT_TILE_UNBOUNDED = 3, /* fewer than k usable representatives: exact path taken */
-    TOPK_CNT_TILE_OVERFLOW = 4,  /* more survivors than buffer room: exact path taken */
+    TOPK_CNT_TILE_OVERFLOW = 4,  /* more survivors than buffer room (resident-keys rows: the
+                                    k-th key past the cut's window): exact path taken */
     TOPK_CNT_TILE_TAKE_ALL = 5,  /* first tiles with at most k candidates */
     TOPK_CNT_COMPACTIONS = 6,    /* candidate-buffer compactions */
     TOPK_CNT_REFILLS = 7,        /* tiles that filled the buffer and resumed after a compaction */

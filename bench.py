@@ -428,6 +428,23 @@ def diag(args):
 
 # -------------------------------------------------------------------- main
 
+def job_figures(dist, torch, device, us: float, e2e_rows_per_s: float, world: int):
+    """Whole-job figures from this rank's own (every rank calls this).
+
+    Each rank processes the same per-GPU batch, so the job's step time is the
+    slowest rank's (a max over ranks) and its end-to-end rate is `world` times
+    the slowest rank's end-to-end rate (a min over ranks). One all-reduce, in
+    float64, over the process group `dist` (None when there is one rank).
+    Returns (step time in us, job end-to-end rows/s).
+    """
+    if dist is not None:
+        t = torch.tensor([float(us), -float(e2e_rows_per_s)], dtype=torch.float64,
+                         device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us, e2e_rows_per_s = float(t[0].item()), -float(t[1].item())
+    return us, world * e2e_rows_per_s
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -495,18 +512,11 @@ def main():
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    if dist:
-        t = torch.tensor([us], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us = float(t.item())
+    e2e_rank, bi, bo = time_e2e(case, tk, torch, device, args.e2e_steps, 3)
+    us, e2e_v = job_figures(dist, torch, device, us, e2e_rank, world)
     rows_per_s = world * case.rows / (us * 1e-6)
     ab = algorithmic_bytes(case)
     achieved = ab / (us * 1e-6) / 1e9
-    e2e_v, bi, bo = time_e2e(case, tk, torch, device, args.e2e_steps, 3)
-    if dist:
-        t = torch.tensor([e2e_v], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MIN)
-        e2e_v = float(t.item()) * world
     copies = gc.copies
     del gc
     torch.cuda.empty_cache()

@@ -46,7 +46,7 @@ class TopkError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("force_direct", ctypes.c_int32), ("cluster", ctypes.c_int32),
-                ("counters", ctypes.c_void_p), ("path", ctypes.c_int32)]
+                ("counters", ctypes.c_void_p), ("path", ctypes.c_int32), ("hold", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -112,7 +112,7 @@ def _ptr(t) -> int | None:
 def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_size: int = 64,
            out=None, width: int | None = None, stream=None, *, force_direct: bool = False,
            cluster: int = 0, counters=None, path: int = 0, block_rows: int | None = None,
-           rows_per_request: int = 1):
+           rows_per_request: int = 1, hold: bool = False):
     """Exact top-k of every row of ``logits`` -> int32 [rows, k] on the same device.
 
     logits: CUDA bfloat16 (or int16/uint16 holding BF16 bits) [rows, row_stride]
@@ -122,7 +122,9 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
     stream: a torch.cuda.Stream (default: the current stream);
     block_rows / rows_per_request: the full transform (see topk_bf16_select_paged):
     physical rows per page (default page_size) and rows sharing one table row;
-    force_direct / cluster / counters / path: test hooks (see topk_bf16_select_ex).
+    force_direct / cluster / counters / path: test hooks (see topk_bf16_select_ex);
+    hold: do not let the next kernel on the stream start before this one completes
+    (topk_bf16_options_t.hold).
     """
     import torch
     rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width,
@@ -140,13 +142,13 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
                 ctypes.c_void_p(stream.cuda_stream))
         paged = (block_rows is not None and int(block_rows) != int(page_size)) or int(rows_per_request) != 1
         if paged:
-            if force_direct or cluster or counters is not None or path:
-                raise ValueError("the test hooks do not combine with block_rows / rows_per_request")
+            if force_direct or cluster or counters is not None or path or hold:
+                raise ValueError("the options do not combine with block_rows / rows_per_request")
             st = lib.topk_bf16_select_paged(*args[:10], int(page_size if block_rows is None else block_rows),
                                             int(rows_per_request), *args[10:])
-        elif force_direct or cluster or counters is not None or path:
+        elif force_direct or cluster or counters is not None or path or hold:
             opt = _Options(1 if force_direct else 0, int(cluster),
-                           None if counters is None else counters.data_ptr(), int(path))
+                           None if counters is None else counters.data_ptr(), int(path), 1 if hold else 0)
             st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
         else:
             st = lib.topk_bf16_select(*args)
@@ -157,7 +159,7 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
 def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_size: int = 64,
                    width: int | None = None, stream=None, *, block_rows: int | None = None,
                    rows_per_request: int = 1, ids: bool = False, out=None, valid=None,
-                   counters=None, force_exact: bool = False):
+                   counters=None, force_exact: bool = False, hold: bool = False):
     """The ordered select of the indexer page (token mode): (out, valid, ids) with
     out int32 [rows, k] the selection in ascending index order (transformed),
     then -1; valid int32 [rows] the counts; ids int32 [rows, k] the untransformed
@@ -165,7 +167,7 @@ def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_
     tops_stride] (unit inner stride, 16-byte aligned rows): each aligned group of
     8 logits' largest order key among its valid non-NaN logits, 0 for none (see
     topk_bf16_select_ordered). Other arguments as select(); counters /
-    force_exact: test hooks.
+    force_exact: test hooks; hold as for select().
     """
     import torch
     rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width,
@@ -188,9 +190,9 @@ def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     opt = None
-    if counters is not None or force_exact:
+    if counters is not None or force_exact or hold:
         opt = ctypes.byref(_Options(1 if force_exact else 0, 0,
-                                    None if counters is None else counters.data_ptr(), 0))
+                                    None if counters is None else counters.data_ptr(), 0, 1 if hold else 0))
     lib = load()
     with torch.cuda.device(dev):
         st = lib.topk_bf16_select_ordered(
@@ -203,7 +205,7 @@ def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_
 
 
 def select_words(logits, valid_len, n: int, tops=None, width: int | None = None, stream=None, *,
-                 out=None, valid=None, counters=None, force_exact: bool = False):
+                 out=None, valid=None, counters=None, force_exact: bool = False, hold: bool = False):
     """The local top-n as B' words (topk_bf16_select_words): (out, valid) with out
     int32 [rows, n + n / 32] and valid int32 [rows]. tops: None or the per-8
     maxima (as for select_ordered); other arguments as select_ordered."""
@@ -223,9 +225,9 @@ def select_words(logits, valid_len, n: int, tops=None, width: int | None = None,
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     opt = None
-    if counters is not None or force_exact:
+    if counters is not None or force_exact or hold:
         opt = ctypes.byref(_Options(1 if force_exact else 0, 0,
-                                    None if counters is None else counters.data_ptr(), 0))
+                                    None if counters is None else counters.data_ptr(), 0, 1 if hold else 0))
     with torch.cuda.device(dev):
         st = load().topk_bf16_select_words(_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(n),
                                            _ptr(tops), tops_stride, _ptr(out), _ptr(valid),

@@ -80,6 +80,8 @@ struct Params {
     int32_t *out;
     uint32_t *counters;
     int32_t force_direct;
+    int32_t release;                         // 0: hold the next grid on the stream until this
+                                             // one completes (see grid_dependents_release)
 };
 
 template <int NSTAGE, int CAP>
@@ -235,7 +237,10 @@ __device__ __forceinline__ void red_max_peer(uint32_t addr, uint32_t v) {
 // wait for the preceding grid before reading inputs, let the next one start
 // early): the wait returns once the preceding grid has completed and its writes
 // are visible; the release lets the next grid's CTAs start their prologue on
-// free SMs while this one runs (they wait the same way before reading).
+// free SMs while this one runs (they wait the same way before reading). A
+// launch with the hold option skips the release, for a next kernel that reads
+// this one's output without waiting first (IndexerSelect's release flag on the
+// indexer page): that kernel then starts only once this grid has completed.
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -1474,7 +1479,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     s.h_merge[0][tid] = s.h_merge[1][tid] = 0u;
     __syncthreads();
     grid_dependency_wait();
-    grid_dependents_release();
+    if (p.release) grid_dependents_release();
     Feed feed;
     if (tid == 0) {
         feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
@@ -2011,7 +2016,7 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
     if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
     __syncthreads();
     grid_dependency_wait();
-    grid_dependents_release();
+    if (p.release) grid_dependents_release();
 
     Feed feed;
     if (tid == 0) {
@@ -2888,7 +2893,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     for (int i = tid; i < 4 * 256; i += NT) (&s.hs[0][0])[i] = 0u;
     __syncthreads();
     grid_dependency_wait();
-    grid_dependents_release();
+    if (p.release) grid_dependents_release();
 
     int32_t feed_row = p.rows;
     if (tid == 0) {
@@ -2987,6 +2992,7 @@ struct OParams {
     int32_t *out, *valid, *ids;
     uint32_t *counters;
     int32_t words;        // 1: out holds B' words [rows, k + k / 32] (IndexerLocalTopk)
+    int32_t release;      // as Params::release
 };
 
 struct alignas(16) Smem {
@@ -3676,7 +3682,7 @@ __global__ void __launch_bounds__(NT, 1) topk_ordered_kernel(const OParams p) {
     if (threadIdx.x < 2048u / 32u) s.plane[threadIdx.x] = 0u;
     __syncthreads();
     grid_dependency_wait();
-    grid_dependents_release();
+    if (p.release) grid_dependents_release();
 
     RowO r(s, p);
     for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += static_cast<int32_t>(gridDim.x)) {
@@ -3978,6 +3984,7 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     prm.out = out;
     prm.counters = opt ? opt->counters : nullptr;
     prm.force_direct = opt ? opt->force_direct : 0;
+    prm.release = (opt && opt->hold) ? 0 : 1;
 
     const int64_t blocks = pl.clusters * pl.cluster;
     cudaLaunchConfig_t cfg = {};
@@ -4054,6 +4061,7 @@ topk_status_t launch_ordered(const uint16_t *logits, int64_t row_stride, int32_t
     prm.ids = ids;
     prm.counters = opt ? opt->counters : nullptr;
     prm.words = words ? 1 : 0;
+    prm.release = (opt && opt->hold) ? 0 : 1;
 
     const int grid = rows < d->sms ? rows : d->sms;
     cudaLaunchConfig_t cfg = {};

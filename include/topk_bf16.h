@@ -112,8 +112,10 @@ topk_status_t topk_bf16_select_paged(const uint16_t *logits, int64_t row_stride,
 const char *topk_bf16_status_string(topk_status_t status);
 
 /*
- * Options for topk_bf16_select_ex: test and diagnosis hooks. They change which
- * internal path computes the result, never the result itself.
+ * Options for topk_bf16_select_ex (and the ordered select and B' words): test
+ * and diagnosis hooks, which change which internal path computes the result,
+ * never the result itself, and the hold flag, which changes only when the next
+ * kernel on the stream may start. Zero-initialise the whole struct.
  */
 typedef struct {
     int32_t force_direct;   /* 1: skip the group-representative cutoff; every first
@@ -124,6 +126,12 @@ typedef struct {
     int32_t path;           /* rows wider than one stage: 0 automatic, 1 candidate buffer
                                (streamed), 2 resident keys (direct; rows whose cluster
                                shares fit 16384 keys per CTA) */
+    int32_t hold;           /* 0: the kernel lets the next kernel on the stream start early
+                               (programmatic dependent launch; that kernel must wait for this
+                               grid before it reads the output). Nonzero: it does not, so a
+                               next kernel launched that way starts only once this grid has
+                               completed: for consumers that read the output before their
+                               wait (the indexer page, IndexerSelect's release flag). */
 } topk_bf16_options_t;
 
 /* Indices into topk_bf16_options_t.counters. */

@@ -48,6 +48,25 @@ def test_header_compiles_as_c(tmp_path):
                     "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
 
 
+def test_options_struct_layout_matches_the_header(tmp_path):
+    # The binding's ctypes mirror of topk_bf16_options_t must agree with the C
+    # compiler on its size and on every field's offset.
+    fields = [f for f, _ in tk._Options._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "topk_bf16.h"\n'
+                   'int main(void){printf("%zu", sizeof(topk_bf16_options_t));'
+                   + "".join('printf(" %%zu", offsetof(topk_bf16_options_t, %s));' % f for f in fields)
+                   + 'return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                    "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(tk._Options)
+    assert got[1:] == [getattr(tk._Options, f).offset for f in fields]
+    assert "hold" in fields
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert tk.status_string(s)

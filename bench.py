@@ -46,7 +46,9 @@ L2_BYTES = 129 * 1024 * 1024
 # k = 512, page transform included, CUDA graph with L2-rotated inputs, on a
 # B200 (sglang PR #39305, Benchmark). Another machine's number: context only.
 PAGES_US_2048 = 36.0
-KERNEL_SRC = os.path.join(ROOT, "exact_bf16_top_gb300", "csrc", "topk_bf16.cu")
+# The headline kernel's sources (its translation unit and the headers it includes).
+KERNEL_SRC = [os.path.join(ROOT, "exact_bf16_top_gb300", "csrc", f)
+              for f in ("one_tile.cu", "common.cuh", "params.h")]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "one_tile_kernel_2048x16384_k512.md")
 
 
@@ -80,8 +82,11 @@ def measured_traffic():
     source (else None)."""
     import hashlib
     try:
-        with open(KERNEL_SRC, "rb") as fh:
-            digest = hashlib.sha256(fh.read()).hexdigest()
+        h = hashlib.sha256()
+        for path in KERNEL_SRC:
+            with open(path, "rb") as fh:
+                h.update(fh.read())
+        digest = h.hexdigest()
         fields = {}
         with open(TRAFFIC_SUMMARY) as fh:
             for line in fh:

@@ -1,7 +1,7 @@
 """Exact per-row top-k of BF16 logits on GB300: Python binding of libtopk_bf16.
 
 Argument marshalling only: every step of the selection runs in the CUDA kernels
-of ``csrc/topk_bf16.cu`` behind the C ABI declared in ``include/topk_bf16.h``.
+of the kernels under ``csrc/`` behind the C ABI declared in ``include/topk_bf16.h``.
 Torch supplies device memory and the current stream. There is no CPU fallback:
 if the library is missing or the tensors are not on a CUDA device, the call
 raises.

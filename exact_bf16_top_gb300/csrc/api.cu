@@ -92,7 +92,7 @@ cudaError_t init_device(int dev, DeviceInit *&out) {
                 const Variant v = one_variant(b != 0, w);
                 e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
                 if (e == cudaSuccess)
-                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b][w], v.fn, w == 2 ? 512 : 256,
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm_one[b][w], v.fn, one_threads(w),
                                                                       static_cast<size_t>(v.smem));
                 if (e == cudaSuccess && d.per_sm_one[b][w] < 1) e = cudaErrorInvalidConfiguration;
             }
@@ -134,7 +134,7 @@ Plan make_plan(int rows, int width, int k, const DeviceInit &d, bool block, int 
         // Rows that leave SMs idle at one 512-thread CTA each take that build:
         // twice the threads on every row, so half the row's latency.
         pl.build = rows <= d.sms * d.per_sm_one[block][2] ? 2 : (k <= 1024 ? 0 : 1);
-        pl.threads = pl.build == 2 ? 512 : 256;
+        pl.threads = one_threads(pl.build);
     }
     const int per_sm = pl.kind == KIND_ONE ? d.per_sm_one[block][pl.build]
                        : pl.kind == KIND_STREAM ? d.per_sm[block][1] : d.per_sm_direct[block];

@@ -81,6 +81,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet may be
+// suspended for up to `hint_ns` (it resumes as soon as the phase completes), so
+// that a waiting CTA issues few instructions while others on the SM work.
+__device__ __forceinline__ bool mbar_try_wait_hint(unsigned long long *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for a stage: gives up after WAIT_LIMIT_NS (recording ERR_WAIT and
 // raising the CTA's abort flag, which ends every later wait at once).
 __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t parity,
@@ -89,6 +104,24 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return;
+        if (*abort) return;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort = 1u;
+            atomicOr(&g_device_status, ERR_WAIT);
+            return;
+        }
+    }
+}
+
+// mbar_wait for a CTA that shares its SM with others: each try may suspend
+// the waiting threads (up to 20 us, resumed at the phase's completion) instead
+// of spinning; the same 1 s limit.
+__device__ __forceinline__ void mbar_wait_sleep(unsigned long long *bar, uint32_t parity,
+                                                volatile uint32_t *abort) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return;
         if (*abort) return;
         if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
             *abort = 1u;

@@ -5,19 +5,90 @@
 // computes"); the order key and NaN rule: sglang PR #39305 "Exact bf16 consumer
 // top-k adapted from DeepSelect", Modifications; lowest-index ties and the
 // block-table transform: vLLM kimi_k3 "dsa/indexer", IndexerSelect.
+//
+// A CTA is persistent over rows; a row arrives by one bulk copy into a 32 KiB
+// shared stage. Per row:
+//   1. a cut c with at least k keys >= c (so c is at most the k-th key): the
+//      cut that held on the CTA's previous row, or the k-th largest of group
+//      representatives;
+//   2. survivors: every thread forms the 8-bit masks of its vectors' logits
+//      >= c with packed BF16 compares (NaN never passes), takes its slots from
+//      a warp scan of the counts and one shared atomic per warp, and appends
+//      (key << 16 | 0xFFFF - index) words to a list, reading each survivor back
+//      from the stage; each survivor is counted in a 256-bin window histogram
+//      (bin key - c);
+//   3. the k-th key T from the window (one warp), with the counts above it and
+//      at it; from here on only the list is read, so the stage takes the next
+//      row's copy at once;
+//   4. output by one CTA scan of (keys above T, ties at T) counts per thread:
+//      every thread writes its selected entries at its scanned slots (no
+//      per-key atomics); ties are ranked by index only when not all are taken.
+// Fallbacks keep it exact: too few or too many survivors drop the carried cut
+// for the representatives' cut, then the exact cut (every key its own
+// representative); a crowd of ties beyond the list is written by index-ordered
+// rescans of the row.
 
 #include "common.cuh"
 
 namespace topk {
 
-// ------------------------------------------------------- one-tile rows kernel
-//
-// Rows whose valid prefix fits one tile (at most 2048 vectors) take a leaner
-// path: 512 threads hold the row in registers (4 vectors each), the stage it
-// came through is handed back to the copy ring at once, and the selection runs
-// in a handful of barrier phases: representatives -> cut -> survivors -> exact
-// cut -> write. Same cutoff argument as the streamed kernel.
 namespace one {
+
+// ---------------------------------------------------------- packed BF16 tests
+
+// Packed BF16 maximum: a NaN half loses to a number (both NaN: NaN).
+static __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// 0xFFFF in each half where a >= b as BF16 numbers, else 0 (a NaN half: 0).
+static __device__ __forceinline__ uint32_t bge2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The BF16 bits of the value whose order key is `key` (0x7F..0xFF80).
+static __device__ __forceinline__ uint32_t key_value(uint32_t key) {
+    return key >= 0x8000u ? key - 0x8000u : key ^ 0xFFFFu;
+}
+
+// The order key of 16-bit BF16 bits x: x ^ (x < 0 ? 0xFFFF : 0x8000).
+static __device__ __forceinline__ uint32_t value_key(uint32_t x) {
+    return x ^ ((x & 0x8000u) ? 0xFFFFu : 0x8000u);
+}
+
+// The packed compare operand of cut c: a non-NaN value x has key(x) >= c
+// exactly when x >= value(c) as a BF16 number, for every c in [key(-inf),
+// key(+inf)] except key(+0), where the numbers -0 and +0 compare equal. So c is
+// clamped into that range (no eligible key lies outside it) and key(+0) is
+// lowered to key(-0): a lower cut is still a cut (more keys at or above it).
+static __device__ __forceinline__ uint32_t cut_operand(uint32_t &c) {
+    c = min(max(c, KEY_NEG_INF), KEY_POS_INF);
+    if (c == 0x8000u) c = 0x7FFFu;
+    const uint32_t v = key_value(c);
+    return v | (v << 16);
+}
+
+// Bit i of the result: the low half of word i of r is >= the operand; bit 4 + i:
+// its high half.
+static __device__ __forceinline__ uint32_t mask8(const uint4 &r, uint32_t cv) {
+    const uint32_t t = (bge2(r.x, cv) & 0x00010001u) | (bge2(r.y, cv) & 0x00020002u) |
+                       (bge2(r.z, cv) & 0x00040004u) | (bge2(r.w, cv) & 0x00080008u);
+    return (t | (t >> 12)) & 0xFFu;
+}
+
+// The key of the larger half of a packed pair (0 for NaN).
+static __device__ __forceinline__ uint32_t top_key(uint32_t m) {
+    const uint32_t x = bmax2(m, __byte_perm(m, 0, 0x1032)) & 0xFFFFu;
+    return (x & 0x7FFFu) > 0x7F80u ? 0u : value_key(x);
+}
+
+static __device__ __forceinline__ uint32_t vec_bmax(const uint4 &r) {
+    return bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w));
+}
 
 // Everything of the one-tile path for a CTA of NT_ threads (256: several CTAs
 // per SM for many rows; 512: one, for rows that do not fill the SMs, where a
@@ -32,36 +103,34 @@ static constexpr int NTILE = NT * NV;        // 2048 vectors
 static constexpr int NSTAGE = NT == 256 ? 1 : 2;  // 256: the other CTAs on the SM cover its copies
 static constexpr int SURV_CAP = SURV_;
 static constexpr int REP_CAP = 4096;         // stored representatives (groups of >= 4 logits)
-static constexpr int QN = 32 * NV;           // queue entries of one warp
-static constexpr int TAB_CAP = 256;         // page ids of a row staged in shared memory (<= NT)
+static constexpr int TAB_CAP = 256;          // page ids of a row staged in shared memory
+static constexpr int TPT = (TAB_CAP + NT - 1) / NT;  // page ids per thread
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
     union {                                  // the representatives are done before survivors start
-        struct {
-            uint32_t surv_idx[SURV_CAP + 4]; // + a spare slot for writes past the end
-            uint16_t surv_key[SURV_CAP + 8];
-        };
+        uint32_t surv[SURV_CAP + 4];         // (key << 16) | (0xFFFF - index); + a spare slot for
+                                             // writes past the end
         uint16_t rep[REP_CAP];               // the row's representatives (0 = none)
     };
     alignas(16) uint32_t hs[4][256];         // [0], [1]: the cut's byte passes (zero between
                                              // uses); [2 + row parity]: the row's window
-    uint32_t tie_idx[TIECAP];
-    uint8_t queue[NW][QN];                   // (j << 5) | lane of queued vectors j * NT + thread
+    alignas(16) uint32_t tie_idx[TIECAP];
     int32_t tab[TAB_CAP];
     uint32_t red[2][NW];
     uint32_t bc[4];
     uint32_t v_cnt[2];                       // survivor counts, by row parity
-    uint32_t v_smax, v_ntie;
+    uint32_t v_smax;
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
 };
 
 // Histograms are read and written as 16-byte vectors; stages are bulk-copy targets.
 static_assert(offsetof(Smem, hs) % 16 == 0 && offsetof(Smem, stage) % 128 == 0, "shared layout");
-static_assert(TAB_CAP <= NT, "one page id per thread");
+static_assert(TAB_CAP % NT == 0 || NT % TAB_CAP == 0, "page ids spread evenly over the threads");
+static_assert(SURV_CAP < 65536, "scanned counts are packed in 16 bits");
 
-
+// Inclusive scan over the CTA (one __syncthreads); total = the sum over all.
 static __device__ __forceinline__ uint32_t block_scan(Smem &s, uint32_t &par, uint32_t x, uint32_t &total) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t inc = warp_incl_scan(x);
@@ -91,12 +160,6 @@ static __device__ __forceinline__ void warp0_find(Smem &s, uint32_t *hist, uint3
     }
 }
 
-// The half h (0..7) of a vector as a 16-bit value.
-static __device__ __forceinline__ uint32_t half_of(const uint4 &r, int h) {
-    const uint32_t w = (h & 4) ? ((h & 2) ? r.w : r.z) : ((h & 2) ? r.y : r.x);
-    return (h & 1) ? (w >> 16) : (w & 0xFFFFu);
-}
-
 template <class M>
 struct Row {
     Smem &s;
@@ -109,19 +172,27 @@ struct Row {
     uint32_t guess = 0;   // the cut carried over from this CTA's previous row (0: none)
     uint32_t rp = 0;      // parity of the rows this CTA has selected
     bool tab = false;     // the row's page ids are in s.tab
+    // The copy ring (thread 0's view): the next row to load into a stage and
+    // its valid vectors; the stage of the current row; whether the current
+    // row's stage has been handed back to the ring.
+    int32_t feed_row = 0, feed_V = 0, step = 1;
+    int32_t cand_row = 0, cand_L = 0;  // the candidate after feed_row and its valid length
+                                       // (loaded ahead: nothing waits for it until its turn)
+    int st = 0;
+    bool fed = false;
 
     __device__ Row(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
-    // Vector at position pos: lanes without an element read as 0x8000 (a
-    // negative value no cut can select and no group maximum prefers). The
-    // row's last vector is masked in place by mask_tail.
+    // Vector at position pos: lanes without an element read as 0xFFFF (a NaN:
+    // no compare passes it, no maximum prefers it, its key is 0). The row's
+    // last vector is masked in place by mask_tail.
     __device__ __forceinline__ uint4 vec(int pos) const {
-        if (pos >= V) return make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+        if (pos >= V) return make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
         return stg[pos];
     }
 
     // Token mode: overwrite the lanes of the last vector past the valid length
-    // with 0x8000, by the thread that owns that position (every later reader of
+    // with 0xFFFF, by the thread that owns that position (every later reader of
     // it is that thread or, after a warp barrier, its warp).
     __device__ __forceinline__ void mask_tail() const {
         if (M::BLOCK || (L & 7) == 0 || static_cast<int>(threadIdx.x) != (V - 1) % NT) return;
@@ -130,9 +201,7 @@ struct Row {
         uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int h = 0; h < 8; ++h)
-            if (h >= lanes)
-                w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
-                            ((h & 1) ? 0x80000000u : 0x00008000u);
+            if (h >= lanes) w[h >> 1] |= (h & 1) ? 0xFFFF0000u : 0x0000FFFFu;
         stg[V - 1] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 
@@ -145,7 +214,13 @@ struct Row {
         else ck[0] = ck[1] = ck[2] = ck[3] = 0u;
     }
 
+    // Output slot `slot` of the row gets element idx through the transform. A
+    // slot past k would break an internal invariant: it is recorded, not written.
     __device__ __forceinline__ void put(uint32_t slot, uint32_t idx) const {
+        if (slot >= k) {
+            atomicOr(&g_device_status, ERR_BOUNDS);
+            return;
+        }
         int32_t v = static_cast<int32_t>(idx);
         if (tab) v = s.tab[idx >> p.page_shift] * p.block_rows + (v & ((1 << p.page_shift) - 1));
         else v = transform(p, row, v);
@@ -155,7 +230,8 @@ struct Row {
     // Representatives of groups of G elements of this thread's vectors
     // j * NT + tid (token: G logits, within a vector for G <= 8, else whole
     // vectors; block: G blocks), fed to f(slot, r, key) in a fixed slot order
-    // (r: the thread's r-th representative, slot = r * NT + tid).
+    // (r: the thread's r-th representative, slot = r * NT + tid). A token
+    // group's representative is its largest logit (0: none, all NaN).
     template <int G, class F>
     __device__ __forceinline__ void reps(F &&f) const {
         const int tid = threadIdx.x;
@@ -171,17 +247,17 @@ struct Row {
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 const uint4 r = vec(j * NT + tid);
-                f((2 * j) * NT + tid, 2 * j, rep_key(smax_halves(smax2(r.x, r.y)), 1u));
-                f((2 * j + 1) * NT + tid, 2 * j + 1, rep_key(smax_halves(smax2(r.z, r.w)), 1u));
+                f((2 * j) * NT + tid, 2 * j, top_key(bmax2(r.x, r.y)));
+                f((2 * j + 1) * NT + tid, 2 * j + 1, top_key(bmax2(r.z, r.w)));
             }
         } else {
             constexpr int PER = G / 8;  // whole vectors per group
 #pragma unroll
             for (int j = 0; j < NV; j += PER) {
-                uint32_t acc = vec_smax(vec(j * NT + tid));
+                uint32_t acc = vec_bmax(vec(j * NT + tid));
 #pragma unroll
-                for (int i = 1; i < PER; ++i) acc = smax2(acc, vec_smax(vec((j + i) * NT + tid)));
-                f((j / PER) * NT + tid, j / PER, rep_key(smax_halves(acc), 1u));
+                for (int i = 1; i < PER; ++i) acc = bmax2(acc, vec_bmax(vec((j + i) * NT + tid)));
+                f((j / PER) * NT + tid, j / PER, top_key(acc));
             }
         }
     }
@@ -351,7 +427,7 @@ struct Row {
     }
 
     // Every candidate of the row (at most k of them), in index order.
-    __device__ void take_all(int32_t t0) {
+    __device__ void take_all(const int32_t (&t0)[TPT]) {
         const int tid = threadIdx.x;
         stage_table(t0);
         uint32_t cnt = 0;
@@ -381,11 +457,13 @@ struct Row {
         const uint32_t tid = threadIdx.x;
         if (e <= static_cast<uint32_t>(TIECAP)) {
             if (tid < e) {
+                // (entries past e read as never-smaller; TIECAP is a multiple of 4)
                 const uint32_t mine = s.tie_idx[tid];
-                uint32_t r = tid;
-                if (take < e) {
-                    r = 0;
-                    for (uint32_t u = 0; u < e; ++u) r += s.tie_idx[u] < mine;
+                uint32_t r = 0;
+                for (uint32_t u = 0; u < e; u += 4) {
+                    const uint4 t4 = *reinterpret_cast<const uint4 *>(&s.tie_idx[u]);
+                    r += (t4.x < mine) + (u + 1 < e && t4.y < mine) + (u + 2 < e && t4.z < mine) +
+                         (u + 3 < e && t4.w < mine);
                 }
                 if (r < take) put(first + r, mine);
             }
@@ -411,15 +489,15 @@ struct Row {
         }
     }
 
-    // The q-th largest survivor when the window histogram cannot place it: a
-    // two-pass radix select over s.surv_key[0 .. n), all in [lo, hi].
+    // The q-th largest survivor key when the window histogram cannot place it:
+    // a two-pass radix select over the list's keys, all in [lo, hi].
     __device__ uint32_t survivor_select(uint32_t n, uint32_t lo, uint32_t hi, uint32_t q, uint32_t &above) {
         const uint32_t tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         const uint32_t mask = (1u << shift) - 1u;
         for (uint32_t i = tid; i < n; i += NT)
-            atomicAdd(&s.hs[0][min((static_cast<uint32_t>(s.surv_key[i]) - lo) >> shift, 255u)], 1u);
+            atomicAdd(&s.hs[0][min(((s.surv[i] >> 16) - lo) >> shift, 255u)], 1u);
         __syncthreads();
         warp0_find(s, s.hs[0], q);
         __syncthreads();
@@ -430,7 +508,7 @@ struct Row {
             return lo + b1;
         }
         for (uint32_t i = tid; i < n; i += NT) {
-            const uint32_t o = static_cast<uint32_t>(s.surv_key[i]) - lo;
+            const uint32_t o = (s.surv[i] >> 16) - lo;
             if ((o >> shift) == b1) atomicAdd(&s.hs[0][o & mask], 1u);
         }
         __syncthreads();
@@ -442,157 +520,113 @@ struct Row {
         return lo + (b1 << shift) + b2;
     }
 
-    // Survivors of cut c: every key >= c goes to the list, and to the window
+    // Token rows: survivors of cut c (cv = cut_operand(c)): every key >= c
+    // goes to the list as (key << 16) | (0xFFFF - index), and to the window
     // histogram hw (bin key - c, the top bin holding every key >= c + 255).
-    // Each thread tests its vectors' maxima; the vectors that may reach c are
-    // queued per warp and worked through by all its lanes; slots come from one
-    // warp scan and one shared atomic per round.
-    template <bool FAST>
-    __device__ __forceinline__ void survivors_t(uint32_t c, uint32_t *hw) {
-        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
-        const int32_t cs = static_cast<int32_t>(c) - 0x8000;
-        uint32_t q = 0;
-        bool pass[NV];  // every vector's test first: the loads issue together
+    // Each thread forms the 8-bit masks of all its vectors with packed BF16
+    // compares (independent, so they overlap), packed into one 64-bit word;
+    // slots come from a ballot prefix of the counts and one shared atomic per
+    // warp; then one loop over the thread's survivors reads each back from the
+    // stage as a 16-bit value (no per-vector loops, no register indexing).
+    __device__ __forceinline__ void survivors_tok(uint32_t c, uint32_t cv, uint32_t *hw) {
+        constexpr int MW = (NV + 3) / 4;  // mask words: bit 8 (j % 4) + b of word j / 4 is
+                                          // vector j's logit 2 (b & 3) + (b >> 2)
+        const uint32_t lane = lane_id(), tid = threadIdx.x;
+        uint32_t mw[MW] = {};
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int pos = j * NT + static_cast<int>(threadIdx.x);
-            if constexpr (FAST) pass[j] = pos < V && smax_halves(vec_smax(stg[pos])) >= cs;
-            else if constexpr (M::BLOCK) pass[j] = bkey(pos) >= c;
-            else pass[j] = pos < V && M::may_reach(stg[pos], 0u, c);
-        }
-        uint32_t bal[NV];  // every ballot first: the stores then only wait on popcounts
+        for (int j = 0; j < NV; ++j) mw[j / 4] |= mask8(vec(j * NT + static_cast<int>(tid)), cv) << (8 * (j % 4));
+        uint32_t cnt = 0;  // <= 8 NV
 #pragma unroll
-        for (int j = 0; j < NV; ++j) bal[j] = __ballot_sync(0xFFFFFFFFu, pass[j]);
+        for (int w = 0; w < MW; ++w) cnt += __popc(mw[w]);
+        const uint32_t lt = (1u << lane) - 1u;
+        (void)lt;
+        const uint32_t incl = warp_incl_scan(cnt);
+        const uint32_t before = incl - cnt, tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 0 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
+        uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + before;
+        const uint16_t *h16 = reinterpret_cast<const uint16_t *>(stg);
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if (pass[j]) s.queue[warp][q + __popc(bal[j] & lt)] = static_cast<uint8_t>((j << 5) | lane);
-            q += __popc(bal[j]);
-        }
-        __syncwarp();
-        // Non-negative cut (FAST): the keys >= c are the BF16 bits >= c - 0x8000
-        // as signed 16-bit integers, NaN excluded (its sign bit is set first).
-        const uint32_t csm = (static_cast<uint32_t>(cs - 1) & 0xFFFFu) * 0x10001u;
-        for (uint32_t e0 = 0; e0 < q; e0 += 32) {
-            const uint32_t e = e0 + lane;
-            uint32_t m = 0;
-            int pos = 0;
-            uint4 r = make_uint4(0, 0, 0, 0);
-            uint32_t ck[4] = {0u, 0u, 0u, 0u};
-            if (e < q) {
-                const uint32_t qe = s.queue[warp][e];
-                pos = static_cast<int>(qe >> 5) * NT + static_cast<int>(warp * 32u + (qe & 31u));
-                if constexpr (FAST) {
-                    // Bit i (i < 4): low half of word i; bit 4 + i: its high half.
-                    r = stg[pos];
-                    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-                    uint32_t u = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t x = w[i] | nan2(w[i]);
-                        const uint32_t g = smax2(x, csm) ^ csm;  // nonzero halves: x >= cs
-                        u |= ((((g & 0x7FFF7FFFu) + 0x7FFF7FFFu) | g) & 0x80008000u) >> (15 - i);
-                    }
-                    m = (u & 0xFu) | ((u >> 12) & 0xF0u);
-                } else {
-                    clean(pos, ck);
-#pragma unroll
-                    for (int h = 0; h < M::KPV; ++h) m |= (key_at<M>(ck, h) >= c ? 1u : 0u) << h;
-                }
-            }
-            const uint32_t cnt = __popc(m);
-            uint32_t tot;
-            const uint32_t before = warp_excl_small(cnt, tot);
-            uint32_t base = 0;
-            if (lane == 0 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
-            uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + before;
+        for (int w = 0; w < MW; ++w) {
 #pragma unroll 1
-            for (; m; m &= m - 1u) {
-                const int bit = __ffs(m) - 1;
-                uint32_t key, idx;
-                if constexpr (FAST) {
-                    const int i = bit & 3, hi = bit >> 2;
-                    const uint32_t w = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
-                    key = ((hi ? w >> 16 : w) & 0xFFFFu) + 0x8000u;
-                    idx = static_cast<uint32_t>(pos) * 8u + static_cast<uint32_t>(2 * i + hi);
-                } else if constexpr (M::BLOCK) {
-                    key = ck[0];
-                    idx = static_cast<uint32_t>(pos);
-                } else {
-                    const int i = bit >> 1;
-                    const uint32_t w = i == 0 ? ck[0] : i == 1 ? ck[1] : i == 2 ? ck[2] : ck[3];
-                    key = (bit & 1) ? (w >> 16) : (w & 0xFFFFu);
-                    idx = static_cast<uint32_t>(pos) * 8u + static_cast<uint32_t>(bit);
-                }
+            for (uint32_t mm = mw[w]; mm; mm &= mm - 1u) {
+                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                const uint32_t j = 4u * w + (bit >> 3), b = bit & 7u;
+                const uint32_t idx = (j * NT + tid) * 8u + 2u * (b & 3u) + (b >> 2);
+                const uint32_t key = value_key(h16[idx]);
                 // Past the list's end (the count then exceeds it and the pass is
                 // redone or replaced) writes go to the spare slot.
-                const uint32_t slot = min(at, static_cast<uint32_t>(SURV_CAP));
-                s.surv_key[slot] = static_cast<uint16_t>(key);
-                s.surv_idx[slot] = idx;
+                s.surv[min(at, static_cast<uint32_t>(SURV_CAP))] = (key << 16) | (0xFFFFu - idx);
                 atomicAdd(&hw[min(key - c, 255u)], 1u);
                 ++at;
             }
-            __syncwarp();  // lanes left the loop above at different counts
         }
     }
 
-    __device__ __forceinline__ void survivors(uint32_t c, uint32_t *hw) {
-        if (!M::BLOCK && c >= 0x8000u) survivors_t<!M::BLOCK>(c, hw);
-        else survivors_t<false>(c, hw);
-    }
-
-    // Warp 0: the bin b of window histogram h that holds the q-th largest key,
-    // the count above it and the count in it, to s.bc; every bin from b up
-    // becomes a cursor, the count of the bins above it (the output slot of its
-    // first key). The caller's __syncthreads publishes both.
-    __device__ __forceinline__ void warp0_cursors(uint32_t *h, uint32_t q) {
-        if (threadIdx.x >= 32) return;
-        __syncwarp();  // (see find_bin256)
-        const uint32_t lane = lane_id();
-        uint4 *h4 = reinterpret_cast<uint4 *>(h + 248 - 8 * static_cast<int>(lane));
-        const uint4 a = h4[0], b = h4[1];
-        const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t sum = 0;
+    // Block rows: survivors of cut c, as survivors_tok with one key per vector
+    // (bit j: vector j's key >= c; the key is formed again for the write).
+    __device__ __forceinline__ void survivors_blk(uint32_t c, uint32_t *hw) {
+        const uint32_t tid = threadIdx.x;
+        uint32_t m = 0, cnt = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum += v[i];
-        const uint32_t incl = warp_incl_scan(sum);
-        uint32_t acc = incl - sum, cur[8], bin = 0, above = 0, cnt = 0;
-        bool mine = false;
-#pragma unroll
-        for (int i = 7; i >= 0; --i) {
-            cur[i] = acc;
-            if (!mine && acc < q && acc + v[i] >= q) {
-                mine = true;
-                bin = 248u - 8u * lane + static_cast<uint32_t>(i);
-                above = acc;
-                cnt = v[i];
-            }
-            acc += v[i];
+        for (int j = 0; j < NV; ++j)
+            if (bkey(j * NT + static_cast<int>(tid)) >= c) m |= 1u << j;
+        cnt = __popc(m);
+        const uint32_t incl = warp_incl_scan(cnt);
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t base = 0;
+        if (lane_id() == 0 && tot) base = atomicAdd(&s.v_cnt[rp], tot);
+        uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - cnt;
+#pragma unroll 1
+        for (; m; m &= m - 1u) {
+            const uint32_t idx = static_cast<uint32_t>(__ffs(m) - 1) * NT + tid;
+            const uint32_t key = bkey(static_cast<int>(idx));
+            s.surv[min(at, static_cast<uint32_t>(SURV_CAP))] = (key << 16) | (0xFFFFu - idx);
+            atomicAdd(&hw[min(key - c, 255u)], 1u);
+            ++at;
         }
-        h4[0] = make_uint4(cur[0], cur[1], cur[2], cur[3]);
-        h4[1] = make_uint4(cur[4], cur[5], cur[6], cur[7]);
-        if (mine) {
-            s.bc[0] = bin;
-            s.bc[1] = above;
-            s.bc[2] = cnt;
-        }
-        if (lane == 0) s.v_ntie = 0u;
     }
 
-    // Output of the list against window h based at `base` (bins key - base)
-    // whose bin b holds the k-th key: keys in higher bins take their bin's
-    // next slot; keys in bin b too when every one of them is taken, otherwise
-    // their indices go to s.tie_idx (while they fit) to be ranked.
-    __device__ __forceinline__ void emit(uint32_t n, uint32_t *h, uint32_t base, uint32_t b, bool all_ties) {
-        for (uint32_t i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = s.surv_key[i];
-            if (key < base) continue;
-            const uint32_t bin = min(key - base, 255u);
-            if (bin > b || (bin == b && all_ties)) {
-                put(atomicAdd(&h[bin], 1u), s.surv_idx[i]);
-            } else if (bin == b) {
-                const uint32_t t = atomicAdd(&s.v_ntie, 1u);
-                if (t < static_cast<uint32_t>(TIECAP)) s.tie_idx[t] = s.surv_idx[i];
+    // Output of the list (n entries) given the k-th key T, the count above it
+    // and the ties to take: one CTA scan of each thread's (above T, equal to T)
+    // counts gives every selected entry its slot, keys above T first. Ties go
+    // straight to their slots when all of them are taken; otherwise they are
+    // ranked by index (write_ties).
+    __device__ __forceinline__ void emit(uint32_t n, uint32_t T, uint32_t above, uint32_t take) {
+        const uint32_t tid = threadIdx.x;
+        const uint32_t lo_e = T << 16, hi_e = (T + 1u) << 16;  // entries of key T: [lo_e, hi_e)
+        uint32_t cnt = 0;  // (ties << 16) | above, this thread's entries tid + u NT
+        for (uint32_t i0 = tid; i0 < n; i0 += 4u * NT) {
+            uint32_t x[4];  // four entries loaded together (0: none)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = i0 + u * NT < n ? s.surv[i0 + u * NT] : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cnt += x[u] >= hi_e ? 1u : x[u] >= lo_e ? 0x10000u : 0u;
+        }
+        uint32_t total;
+        const uint32_t pre = block_scan(s, par, cnt, total) - cnt;
+        const uint32_t e = total >> 16;  // the ties at T (and total & 0xFFFF == above)
+        const bool all = take == e;
+        uint32_t a_at = pre & 0xFFFFu, t_at = pre >> 16;
+        for (uint32_t i0 = tid; cnt != 0u && i0 < n; i0 += 4u * NT) {
+            uint32_t x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = i0 + u * NT < n ? s.surv[i0 + u * NT] : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t idx = 0xFFFFu - (x[u] & 0xFFFFu);
+                if (x[u] >= hi_e) {
+                    put(a_at++, idx);
+                } else if (x[u] >= lo_e) {
+                    if (all) put(above + t_at, idx);
+                    else if (t_at < static_cast<uint32_t>(TIECAP)) s.tie_idx[t_at] = idx;
+                    ++t_at;
+                }
             }
+        }
+        if (!all) {
+            __syncthreads();
+            write_ties(T, take, above, e);
         }
     }
 
@@ -625,14 +659,52 @@ struct Row {
     // short of k keys, 64 about one row in forty, each costing a second cut).
     __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t n) {
         const uint32_t want = min(max(k / 8u, 128u), (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
-        const uint32_t d = T > c ? max((want * (T - c)) / (n - k + 1u), 1u) : 16u;
+        const uint32_t d = T > c ? max(static_cast<uint32_t>(__fdividef(static_cast<float>(want * (T - c)),
+                                                                        static_cast<float>(n - k + 1u))), 1u)
+                                 : 16u;
         guess = T > d ? T - d : 1u;
+    }
+
+    // Hand the current row's stage back to the copy ring: thread 0 issues the
+    // next row's copy into it. Every thread must be done reading the stage
+    // (a barrier since its last read orders those reads before the fence).
+    __device__ __forceinline__ void feed() {
+        fed = true;
+        if (threadIdx.x == 0 && feed_row < p.rows) {
+            fence_proxy_async();
+            issue_row(s, st, p, feed_row, feed_V);
+            advance_feed();
+        }
+    }
+
+    // Thread 0: feed_row = the next row that reads logits (p.rows if none),
+    // from the prefetched candidate; then the next candidate's length is
+    // loaded ahead.
+    __device__ __forceinline__ void advance_feed() {
+        for (;;) {
+            if (cand_row >= p.rows) {
+                feed_row = p.rows;
+                return;
+            }
+            const int32_t L = min(max(cand_L, 0), p.width);
+            const int32_t n = M::BLOCK ? (L + 7) >> 3 : L;
+            const int32_t r = cand_row;
+            cand_row += step;
+            if (cand_row < p.rows) cand_L = __ldg(p.valid_len + cand_row);
+            if (n > p.k) {
+                feed_row = r;
+                feed_V = (L + 7) >> 3;
+                return;
+            }
+        }
     }
 
     // Store the page ids loaded at the start of select() (the caller
     // synchronises before the first put).
-    __device__ __forceinline__ void stage_table(int32_t t0) const {
-        if (tab && threadIdx.x < static_cast<uint32_t>(TAB_CAP)) s.tab[threadIdx.x] = t0;
+    __device__ __forceinline__ void stage_table(const int32_t (&t0)[TPT]) const {
+#pragma unroll
+        for (int u = 0; u < TPT; ++u)
+            if (tab && threadIdx.x + u * NT < static_cast<uint32_t>(TAB_CAP)) s.tab[threadIdx.x + u * NT] = t0[u];
     }
 
     __device__ void select() {
@@ -640,14 +712,16 @@ struct Row {
         const uint32_t nE = M::BLOCK ? static_cast<uint32_t>(V) : static_cast<uint32_t>(L);
         // The row's page ids, loaded now and staged in shared memory before the
         // first write (their latency hides behind the survivor pass).
-        int32_t t0 = 0;  // page id of this thread's entry (TAB_CAP <= NT)
+        int32_t t0[TPT] = {};  // page ids of this thread's entries tid + u NT
         tab = false;
         if (p.table) {
             const uint32_t npages = (nE + (1u << p.page_shift) - 1u) >> p.page_shift;
             if (npages <= static_cast<uint32_t>(TAB_CAP)) {
                 tab = true;
                 const int32_t *trow = table_row(p, row);
-                if (tid < npages) t0 = __ldg(trow + tid);
+#pragma unroll
+                for (int u = 0; u < TPT; ++u)
+                    if (tid + u * NT < npages) t0[u] = __ldg(trow + tid + u * NT);
             }
         }
         mask_tail();
@@ -660,12 +734,13 @@ struct Row {
         uint32_t g = 1;
         if (!p.force_direct) {
             // (groups are a thread's own vectors: at most NV blocks, 8 NV logits)
+            // (nE / (2 g) >= 2 k written as nE >= 4 g k, all below 2^32)
             if constexpr (M::BLOCK) {
-                while (g < min(8u, static_cast<uint32_t>(NV)) && nE / (2u * g) >= 2u * k) g *= 2u;
+                while (g < min(8u, static_cast<uint32_t>(NV)) && nE >= 4u * g * k) g *= 2u;
             } else {
                 g = 4;
-                while (g < min(64u, 8u * NV) && nE / (2u * g) >= 2u * k) g *= 2u;
-                if (nE / g < 2u * k) g = 1;  // too few groups of 4: exact path
+                while (g < min(64u, 8u * NV) && nE >= 4u * g * k) g *= 2u;
+                if (nE < 2u * g * k) g = 1;  // too few groups of 4: exact path
             }
         }
         // First try the previous row's cut: any c with at least k keys >= c
@@ -705,7 +780,12 @@ struct Row {
             }
             clk.stop(p, TOPK_CNT_CYC_CUT);
             clk.start(p);
-            survivors(c, hw);
+            // cs: the cut as the survivor pass applies it (c, or a lower key
+            // the packed compares can apply exactly); c stays the cut found.
+            uint32_t cs = c;
+            const uint32_t cv = cut_operand(cs);
+            if constexpr (M::BLOCK) survivors_blk(cs, hw);
+            else survivors_tok(cs, cv, hw);
             stage_table(t0);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
@@ -727,54 +807,44 @@ struct Row {
                     g = 1u;
                     continue;
                 }
-                emit_rescan(c);  // the exact cut, with a crowd of ties at it
+                emit_rescan(c);  // the exact cut (the k-th key), with a crowd of ties at it
                 guess = c > 16u ? c - 16u : 1u;
                 clk.stop(p, TOPK_CNT_CYC_FINISH);
                 return;
             }
             count_event(p, guessed ? TOPK_CNT_GUESS_HIT : g == 1u ? TOPK_CNT_TILE_EXACT : TOPK_CNT_TILE_SAMPLED);
-            warp0_cursors(hw, k);
+            if (tid < 32u) {  // warp 0: the k-th key's bin, the count above it and in it
+                uint32_t b0, a0, t0w;
+                find_bin256(hw, k, b0, a0, t0w);
+                if (tid == 0) {
+                    s.bc[0] = b0;
+                    s.bc[1] = a0;
+                    s.bc[3] = hw[b0];
+                }
+            }
             __syncthreads();
-            uint32_t b = s.bc[0], above = s.bc[1], e = s.bc[2];
-            uint32_t T = c + b, base = c;
-            uint32_t *h = hw;
+            uint32_t b = s.bc[0], above = s.bc[1];
+            uint32_t T = cs + b;
+            if (b < 255u && s.bc[3] <= static_cast<uint32_t>(TIECAP)) {
+                // From here on only the list and the tie buffer are read: the
+                // stage takes the next row's copy now, which overlaps the rest.
+                feed();
+            }
             if (b == 255u) {
                 // The k-th key is at least c + 255: find it by radix select over
-                // the list, then emit against a window based at it.
+                // the list.
                 uint32_t smax = 0;
-                for (uint32_t i = tid; i < n; i += NT) smax = max(smax, static_cast<uint32_t>(s.surv_key[i]));
+                for (uint32_t i = tid; i < n; i += NT) smax = max(smax, s.surv[i] >> 16);
                 smax = __reduce_max_sync(0xFFFFFFFFu, smax);
                 if (lane_id() == 0) atomicMax(&s.v_smax, smax);
                 __syncthreads();
-                uint32_t a2;
-                T = survivor_select(n, c, s.v_smax, k, a2);
+                T = survivor_select(n, cs, s.v_smax, k, above);
                 if (tid == 0) s.v_smax = 0u;
-                h = s.hs[1];
-                base = T;
-                for (uint32_t i = tid; i < n; i += NT) {
-                    const uint32_t key = s.surv_key[i];
-                    if (key >= T) atomicAdd(&h[min(key - T, 255u)], 1u);
-                }
-                __syncthreads();
-                warp0_cursors(h, k);
-                __syncthreads();
-                b = s.bc[0];
-                above = s.bc[1];
-                e = s.bc[2];
             }
             clk.stop(p, TOPK_CNT_CYC_EXACT);
             clk.start(p);
-            const uint32_t take = k - above;
-            next_guess(c, T, n);
-            emit(n, h, base, b, take == e);
-            if (take != e) {
-                __syncthreads();
-                write_ties(T, take, above, e);
-            }
-            if (h != hw) {  // the cut's histogram back to zero
-                __syncthreads();
-                if (tid < 256u) h[tid] = 0u;
-            }
+            next_guess(cs, T, n);
+            emit(n, T, above, k - above);
             clk.stop(p, TOPK_CNT_CYC_FINISH);
             return;
         }
@@ -788,25 +858,11 @@ static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &
     bulk_load(&s.stage[st][0], src, bytes, &s.full[st]);
 }
 
-// The next row of this CTA, from `row` on in steps of `step`, that reads
-// logits (p.rows when none is left); V = its valid vectors.
-static __device__ __forceinline__ int32_t next_loaded_row(const Params &p, bool block, int32_t row, int32_t step,
-                                                    int32_t &V) {
-    for (; row < p.rows; row += step) {
-        const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
-        const int32_t n = block ? (L + 7) >> 3 : L;
-        if (n > p.k) {
-            V = (L + 7) >> 3;
-            return row;
-        }
-    }
-    return p.rows;
-}
-
 };  // struct Tile
 
 template <class M, int NT, int SURV>
-__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) topk_one_tile_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, NT == 128 ? 5 : NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1)
+    topk_one_tile_kernel(const Params p) {
     using O = Tile<NT, SURV>;
     constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -814,7 +870,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     const int tid = threadIdx.x;
     const int32_t step = static_cast<int32_t>(gridDim.x);
 
-    if (tid == 0) {  // (shared-memory set-up before the wait, as in topk_kernel)
+    if (tid == 0) {  // (shared-memory set-up before the wait: it touches no global memory)
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&s.full[i], 1);
         fence_mbar_init();
         s.abort_flag = 0u;
@@ -826,18 +882,19 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
     grid_dependency_wait();
     if (p.release) grid_dependents_release();
 
-    int32_t feed_row = p.rows;
-    if (tid == 0) {
-        int32_t V;
-        feed_row = O::next_loaded_row(p, M::BLOCK, static_cast<int32_t>(blockIdx.x), step, V);
-        for (int i = 0; i < NSTAGE && feed_row < p.rows; ++i) {
-            O::issue_row(s, i, p, feed_row, V);
-            feed_row = O::next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
-        }
-    }
-
     typename O::template Row<M> r(s, p);
     r.k = static_cast<uint32_t>(p.k);
+    r.step = step;
+    r.feed_row = p.rows;
+    if (tid == 0) {
+        r.cand_row = static_cast<int32_t>(blockIdx.x);
+        if (r.cand_row < p.rows) r.cand_L = __ldg(p.valid_len + r.cand_row);
+        r.advance_feed();
+        for (int i = 0; i < NSTAGE && r.feed_row < p.rows; ++i) {
+            O::issue_row(s, i, p, r.feed_row, r.feed_V);
+            r.advance_feed();
+        }
+    }
     uint32_t seq = 0;
     for (int32_t row = static_cast<int32_t>(blockIdx.x); row < p.rows; row += step) {
         const int32_t L = min(max(__ldg(p.valid_len + row), 0), p.width);
@@ -853,24 +910,20 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
         r.L = L;
         r.V = (L + 7) >> 3;
         r.stg = s.stage[st];
+        r.st = st;
+        r.fed = false;
         r.orow = p.out + static_cast<int64_t>(row) * p.k;
         PhaseClock clk;
         clk.start(p);
-        mbar_wait(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
+        mbar_wait_sleep(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
         clk.stop(p, TOPK_CNT_CYC_WAIT);
         count_event(p, TOPK_CNT_ROUNDS);
         ++seq;
         clk.start(p);
         r.select();
-        __syncthreads();  // every thread is done with this stage
+        __syncthreads();  // every thread is done with this stage and the row's shared state
         clk.stop(p, TOPK_CNT_CYC_SELECT);
-        if (tid == 0 && feed_row < p.rows) {
-            int32_t V;
-            O::next_loaded_row(p, M::BLOCK, feed_row, step, V);
-            fence_proxy_async();
-            O::issue_row(s, st, p, feed_row, V);
-            feed_row = O::next_loaded_row(p, M::BLOCK, feed_row + step, step, V);
-        }
+        if (!r.fed) r.feed();
     }
 }
 
@@ -883,11 +936,12 @@ static Variant one_build() {
 }
 
 // build 0: 256 threads, k <= 1024; 1: 256 threads, larger k; 2: 512 threads
-// (rows that do not fill the SMs).
+// (rows that do not fill the SMs); 3: 128 threads, k <= 1024.
 Variant one_variant(bool block, int build) {
     switch (build) {
         case 0: return block ? one_build<BlockMode, 256, 2048>() : one_build<TokenMode, 256, 2048>();
         case 1: return block ? one_build<BlockMode, 256, 4096>() : one_build<TokenMode, 256, 4096>();
+        case 3: return block ? one_build<BlockMode, 128, 2048>() : one_build<TokenMode, 128, 2048>();
         default: return block ? one_build<BlockMode, 512, 4096>() : one_build<TokenMode, 512, 4096>();
     }
 }

@@ -861,8 +861,7 @@ static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &
 };  // struct Tile
 
 template <class M, int NT, int SURV>
-__global__ void __launch_bounds__(NT, NT == 128 ? 5 : NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1)
-    topk_one_tile_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) topk_one_tile_kernel(const Params p) {
     using O = Tile<NT, SURV>;
     constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -936,12 +935,11 @@ static Variant one_build() {
 }
 
 // build 0: 256 threads, k <= 1024; 1: 256 threads, larger k; 2: 512 threads
-// (rows that do not fill the SMs); 3: 128 threads, k <= 1024.
+// (rows that do not fill the SMs).
 Variant one_variant(bool block, int build) {
     switch (build) {
         case 0: return block ? one_build<BlockMode, 256, 2048>() : one_build<TokenMode, 256, 2048>();
         case 1: return block ? one_build<BlockMode, 256, 4096>() : one_build<TokenMode, 256, 4096>();
-        case 3: return block ? one_build<BlockMode, 128, 2048>() : one_build<TokenMode, 128, 2048>();
         default: return block ? one_build<BlockMode, 512, 4096>() : one_build<TokenMode, 512, 4096>();
     }
 }

@@ -72,8 +72,8 @@ struct Variant {
 // Defined by the kernels' translation units.
 Variant stream_variant(bool block);               // stream.cu: the streamed cluster kernel
 Variant direct_variant(bool block);               // direct.cu: the resident-keys kernel
-constexpr int ONE_BUILDS = 4;                     // one-tile builds (see one_variant)
-constexpr int one_threads(int build) { return build == 2 ? 512 : build == 3 ? 128 : 256; }
+constexpr int ONE_BUILDS = 3;                     // one-tile builds (see one_variant)
+constexpr int one_threads(int build) { return build == 2 ? 512 : 256; }
 Variant one_variant(bool block, int build);       // one_tile.cu: the one-tile kernel
 Variant ordered_variant();                        // ordered.cu: the ordered kernel
 cudaError_t launch_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,

@@ -248,9 +248,12 @@ def ordered_bytes(case, words: bool = False) -> int:
     return b
 
 
-def time_graph(gc, tk, torch, steps: int, warmup: int):
+def time_graph(gc, tk, torch, steps: int, warmup: int, repeats: int = 0, stats=None):
     """Mean microseconds per launch over `steps` launches replayed from a CUDA
-    graph (events on the capture/replay stream)."""
+    graph (events on the capture/replay stream). With repeats > 0, the graph is
+    then replayed `repeats` more times, each timed on its own, and `stats`
+    (a dict) receives the median, minimum and maximum microseconds per launch
+    over those replays (the spread of the figure; not the timed region)."""
     stream = torch.cuda.Stream()
     for i in range(max(3, warmup)):          # eager warm-up (also loads the library)
         gc.launch(gc.copies - 1 - (i % gc.copies), tk)
@@ -270,7 +273,23 @@ def time_graph(gc, tk, torch, steps: int, warmup: int):
         graph.replay()
         stop.record(stream)
     stop.synchronize()
-    return start.elapsed_time(stop) * 1e3 / steps
+    us = start.elapsed_time(stop) * 1e3 / steps
+    if repeats > 0 and stats is not None:
+        per = []
+        for _ in range(repeats):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            b.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / steps)
+        per.sort()
+        stats.update({"replays": repeats, "launches_per_replay": steps,
+                      "median_us": round(per[len(per) // 2], 3), "min_us": round(per[0], 3),
+                      "max_us": round(per[-1], 3)})
+    return us
 
 
 def flush_l2(torch, device, scratch=[]):
@@ -477,6 +496,8 @@ def main():
     case = W.config2(HEADLINE["rows"], HEADLINE["valid"], HEADLINE["k"], seed=0)
     workload = (f"consumer top-k: {case.rows} rows x {case.width} bf16, valid {HEADLINE['valid']}, "
                 f"k={case.k}, permuted 64-token page table")
+    config = {"workload": workload, "rows": case.rows, "width": case.width,
+              "valid_len": HEADLINE["valid"], "k": case.k, "parallelism": f"rows x{world}"}
     peak, peak_kind = peaks()
 
     if args.impl == "reference":
@@ -489,7 +510,8 @@ def main():
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": case.rows / v * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u16 keys (bf16 bits)", "data": "synthetic",
-            "config": {"workload": workload, "rows": case.rows, "width": case.width, "k": case.k},
+            "config": dict(config, l2="host memory (the CPU oracle)",
+                           timing="wall clock over bounded samples of the rows, on the host cores"),
             "cpu_baseline": base,
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
@@ -517,6 +539,10 @@ def main():
         if dist:
             dist.barrier()
     clk = clocks.summary()
+    # The spread of the figure: the same graph replayed ten more times, each
+    # timed on its own (outside the timed region above).
+    spread = {}
+    time_graph(gc, tk, torch, args.steps, 0, repeats=10, stats=spread)
     e2e_rank, bi, bo = time_e2e(case, tk, torch, device, args.e2e_steps, 3)
     us, e2e_v = job_figures(dist, torch, device, us, e2e_rank, world)
     rows_per_s = world * case.rows / (us * 1e-6)
@@ -532,11 +558,10 @@ def main():
         "us_per_launch": round(us, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": round(rows_per_s / (case.rows / (PAGES_US_2048 * 1e-6)), 4),
         "dtype": "u16 keys (bf16 bits), int32 indices", "data": "synthetic",
-        "config": {"workload": workload, "rows": case.rows, "width": case.width,
-                   "valid_len": HEADLINE["valid"], "k": case.k, "parallelism": f"rows x{world}",
-                   "l2": f"inputs rotated over {copies} copies (> 2x the 129 MB L2 read "
-                         f"between reuses of a copy)",
-                   "timing": "CUDA graph of `steps` launches, events on the replay stream"},
+        "config": dict(config,
+                       l2=f"inputs rotated over {copies} copies (> 2x the 129 MB L2 read "
+                          f"between reuses of a copy)",
+                       timing="CUDA graph of `steps` launches, events on the replay stream"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab},
@@ -544,6 +569,7 @@ def main():
                 "d2h_bytes_per_step": bo},
         "gpu_launches": args.steps,
         "clocks": clk,
+        "spread": spread,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(case)

@@ -172,21 +172,14 @@ def select_ordered(logits, valid_len, k: int, tops=None, block_table=None, page_
     import torch
     rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width,
                                                     rows_per_request)
-    tops_stride = 0
-    if tops is not None:
-        if not (tops.is_cuda and tops.element_size() == 2 and tops.dim() == 2 and tops.shape[0] >= rows
-                and tops.stride(1) == 1):
-            raise ValueError("tops must be CUDA 16-bit [rows, tops_stride] with unit inner stride")
-        tops_stride = tops.stride(0) if tops.shape[0] > 1 else tops.shape[1]
+    tops_stride = _tops_stride(tops, rows, width)
     dev = logits.device
     if out is None:
         out = torch.empty((rows, k), dtype=torch.int32, device=dev)
     if valid is None:
         valid = torch.empty(rows, dtype=torch.int32, device=dev)
     ids_t = torch.empty((rows, k), dtype=torch.int32, device=dev) if ids else None
-    for t, shape in ((out, (rows, k)), (valid, (rows,))):
-        if not (t.is_cuda and t.dtype == torch.int32 and tuple(t.shape) == shape and t.is_contiguous()):
-            raise ValueError("out / valid must be contiguous CUDA int32 [rows, k] / [rows]")
+    _outputs(out, valid, rows, k)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     opt = None
@@ -211,17 +204,13 @@ def select_words(logits, valid_len, n: int, tops=None, width: int | None = None,
     maxima (as for select_ordered); other arguments as select_ordered."""
     import torch
     rows, width, row_stride, _ = _inputs(logits, valid_len, None, width, 1)
-    tops_stride = 0
-    if tops is not None:
-        if not (tops.is_cuda and tops.element_size() == 2 and tops.dim() == 2 and tops.shape[0] >= rows
-                and tops.stride(1) == 1):
-            raise ValueError("tops must be CUDA 16-bit [rows, tops_stride] with unit inner stride")
-        tops_stride = tops.stride(0) if tops.shape[0] > 1 else tops.shape[1]
+    tops_stride = _tops_stride(tops, rows, width)
     dev = logits.device
     if out is None:
         out = torch.empty((rows, n + n // 32), dtype=torch.int32, device=dev)
     if valid is None:
         valid = torch.empty(rows, dtype=torch.int32, device=dev)
+    _outputs(out, valid, rows, n + n // 32)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     opt = None
@@ -249,6 +238,29 @@ def tops(logits, valid_len, width: int | None = None, stream=None):
         _check(load().topk_bf16_tops(_ptr(logits), row_stride, rows, width, _ptr(valid_len), _ptr(out),
                                      out.shape[1], ctypes.c_void_p(stream.cuda_stream)))
     return out
+
+
+def _tops_stride(tops, rows: int, width: int) -> int:
+    """Checks the per-8 maxima tensor of select_ordered / select_words and
+    returns its row stride (0 for None). Every row must hold the row's whole
+    16-byte pieces of maxima: ceil(ceil(width / 8) / 8) * 8 entries."""
+    if tops is None:
+        return 0
+    need = -(-(-(-width // 8)) // 8) * 8
+    if not (tops.is_cuda and tops.element_size() == 2 and tops.dim() == 2 and tops.shape[0] >= rows
+            and tops.stride(1) == 1 and tops.shape[1] >= need):
+        raise ValueError(f"tops must be CUDA 16-bit [rows, >= {need}] with unit inner stride")
+    return tops.stride(0) if tops.shape[0] > 1 else tops.shape[1]
+
+
+def _outputs(out, valid, rows: int, cols: int):
+    """Checks caller-provided output tensors (the kernels write rows x cols
+    int32 words to out and rows words to valid)."""
+    import torch
+    for t, shape in ((out, (rows, cols)), (valid, (rows,))):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
+                and tuple(t.shape) == shape and t.is_contiguous()):
+            raise ValueError(f"out / valid must be contiguous CUDA int32 {list((rows, cols))} / [{rows}]")
 
 
 def _inputs(logits, valid_len, block_table, width, rows_per_request):

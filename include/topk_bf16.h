@@ -4,9 +4,9 @@
  * The operation is the one the vLLM page "decode_topk_cute" states in its module
  * docstring ("What this module computes"): for each row, the indices of its k
  * largest elements, in any order. Exact: every index whose value exceeds the
- * k-th largest, then enough of those equal to it; ties at the k-th largest go to
- * the lowest indices (vLLM kimi_k3 "dsa/indexer", IndexerSelect: "ties at the
- * threshold go to the lowest key indices"), so the selected set is unique. A row
+ * k-th largest, then enough of those equal to it; among elements equal to the
+ * k-th largest, the ones with the smallest indices are taken (vLLM kimi_k3
+ * "dsa/indexer", IndexerSelect docstring), so the selected set is unique. A row
  * of at most k elements returns 0 .. n-1 and -1 padding without reading its
  * values. Values are compared through the order-preserving 16-bit key of their
  * BF16 bits, x ^ (x < 0 ? 0xFFFF : 0x8000) (sglang PR #39305, Modifications), so
@@ -20,6 +20,14 @@
  * All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  * stream). Calls are thread-safe; the first call on a device sets kernel
  * attributes once.
+ *
+ * Kernels are launched with programmatic dependent launch where they leave SMs
+ * free, and release the next grid on the stream early (unless the hold option
+ * is set). A successor launched with programmatic stream serialization may
+ * then run alongside the whole call: it must execute griddepcontrol.wait (or
+ * cudaGridDependencySynchronize) before it reads any output of this call AND
+ * before it writes any input of this call (logits, valid lengths, block table,
+ * per-8 maxima), or set hold on this call.
  */
 #ifndef TOPK_BF16_H
 #define TOPK_BF16_H
@@ -128,10 +136,12 @@ typedef struct {
                                shares fit 16384 keys per CTA) */
     int32_t hold;           /* 0: the kernel lets the next kernel on the stream start early
                                (programmatic dependent launch; that kernel must wait for this
-                               grid before it reads the output). Nonzero: it does not, so a
-                               next kernel launched that way starts only once this grid has
-                               completed: for consumers that read the output before their
-                               wait (the indexer page, IndexerSelect's release flag). */
+                               grid before it reads the output and before it writes any of
+                               this call's inputs). Nonzero: it does not, so a next kernel
+                               launched that way starts only once this grid has completed:
+                               for consumers that read the output, or producers that write
+                               the next step's inputs, before their wait (the indexer page,
+                               IndexerSelect's release flag). */
 } topk_bf16_options_t;
 
 /* Indices into topk_bf16_options_t.counters. */

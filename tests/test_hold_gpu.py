@@ -99,3 +99,44 @@ def test_hold_ordered_and_words():
         torch.cuda.synchronize()
         assert np.array_equal(cnt.cpu().numpy(), wexp[1]), hold
         assert np.array_equal(out.cpu().numpy(), wexp[0]), hold
+
+
+@pytest.fixture(scope="module")
+def early_consumer(tmp_path_factory):
+    """The test helper tests/pdl_consumer.cu built with nvcc (sm_103a)."""
+    import ctypes
+    import os
+    import subprocess
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "pdl_consumer.cu")
+    so = str(tmp_path_factory.mktemp("pdl") / "libpdl_consumer.so")
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    subprocess.run([nvcc if os.path.exists(nvcc) else "nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
+                    "-O2", "-shared", "-Xcompiler", "-fPIC", "-o", so, src], check=True, capture_output=True)
+    lib = ctypes.CDLL(so)
+    lib.launch_copy_early.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    lib.launch_copy_early.restype = ctypes.c_int
+    return lib
+
+
+def test_hold_keeps_an_early_reader_from_stale_output(early_consumer):
+    """A consumer that reads the output before waiting for the preceding grid
+    (launched with programmatic stream serialization) must see the finished
+    output when the select was launched with hold: the output is pre-filled
+    with a marker before every select, and the early copy must equal the
+    oracle's selection every time."""
+    case = W.config2(32, 9000, 512, seed=4)
+    ctas = tk.plan(case.rows, case.width, case.k, case.mode)["ctas"]
+    assert ctas < torch.cuda.get_device_properties(0).multi_processor_count  # a spare-slot launch
+    logits, valid, table = upload(case)
+    exp = np.sort(run_oracle(case), 1)
+    out = torch.empty((case.rows, case.k), dtype=torch.int32, device="cuda")
+    copy = torch.empty_like(out)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(20):
+            out.fill_(-7)
+            tk.select(logits, valid, case.k, case.mode, table, case.page_size, out=out, hold=True, stream=s)
+            assert early_consumer.launch_copy_early(out.data_ptr(), copy.data_ptr(), out.numel(),
+                                                    s.cuda_stream) == 0
+            s.synchronize()
+            assert np.array_equal(np.sort(copy.cpu().numpy(), 1), exp)

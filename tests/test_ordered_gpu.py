@@ -140,3 +140,33 @@ def test_words_edges():
         assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1]), case.name
     c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
     assert c["bypass_rows"] > 0, c
+
+
+def test_binding_rejects_bad_outputs_and_tops():
+    """Outputs and per-8 maxima the kernels would write or read past are refused
+    on the host, before any launch: a short or wrongly typed out / valid for
+    the B' words and the ordered select, and maxima narrower than the row's
+    whole 16-byte pieces."""
+    case = W.paged_case(3, rows=4, width=4000, k=256, q=1, block_rows=64)
+    logits, valid, _ = _dev(case)
+    tops = tk.tops(logits, valid, width=case.width)
+    n = 256
+    short = torch.empty((case.rows, n), dtype=torch.int32, device="cuda")   # needs n + n / 32
+    with pytest.raises(ValueError):
+        tk.select_words(logits, valid, n, tops, width=case.width, out=short)
+    with pytest.raises(ValueError):
+        tk.select_words(logits, valid, n, tops, width=case.width,
+                        valid=torch.empty(case.rows - 1, dtype=torch.int32, device="cuda"))
+    with pytest.raises(ValueError):
+        tk.select_words(logits, valid, n, tops, width=case.width,
+                        out=torch.empty((case.rows, n + n // 32), dtype=torch.int64, device="cuda"))
+    with pytest.raises(ValueError):
+        tk.select_ordered(logits, valid, n, tops, width=case.width,
+                          out=torch.empty((case.rows, n + 1), dtype=torch.int32, device="cuda"))
+    narrow = tops[:, :8]  # a column view: the row stride covers the row, the view does not
+    with pytest.raises(ValueError):
+        tk.select_ordered(logits, valid, n, narrow, width=case.width)
+    with pytest.raises(ValueError):
+        tk.select_words(logits, valid, n, narrow, width=case.width)
+    torch.cuda.synchronize()
+    assert tk.device_status() == 0

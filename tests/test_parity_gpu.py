@@ -122,6 +122,25 @@ def test_path_counters_cover_every_path():
         assert c[name] > 0, (name, c)
 
 
+def test_natural_fallbacks_fire():
+    """The sampled cut's own fallbacks fire without force_direct, on rows built
+    for them (workloads.fallback_rows): rows whose groups hold fewer than k
+    usable representatives take the exact cut (tile_unbounded), rows whose
+    representatives' cut lets more survivors through than the list holds
+    redo the cut exactly (tile_overflow, one-tile kernel) or fill the
+    streamed kernel's buffer, which is compacted and the tile resumed
+    (refills: the streamed kernel has no list to overflow). Results stay
+    exact."""
+    for width, opts, names in ((16384, {}, ("tile_unbounded", "tile_overflow")),
+                               (100000, {"path": 1, "cluster": 1}, ("tile_unbounded", "refills"))):
+        case = W.fallback_rows(0, rows=8, width=width, k=512)
+        counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+        assert_same_sets(run_gpu(case, counters=counters, **opts), run_oracle(case), case.name)
+        c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+        for name in names:
+            assert c[name] > 0, (width, name, c)
+
+
 def test_output_written_in_place():
     case = W.config2(32, 16384, 512)
     logits = torch.from_numpy(case.logits.view(np.int16)).cuda()

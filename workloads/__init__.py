@@ -352,3 +352,27 @@ def paged_case(seed: int, rows: int, width: int, k: int, mode: int = TOKEN, q: i
     table = permuted_table(rng, -(-rows // q), n_width, page)
     return Case(f"paged {rows}x{width} k{k} mode{mode} q{q} block_rows{block_rows}", logits, width,
                 valid, k, mode, table, page, block_rows=block_rows, rows_per_request=q)
+
+
+def fallback_rows(seed: int = 0, rows: int = 8, width: int = 16384, k: int = 512) -> Case:
+    """Token rows built so that a sample-style cut cannot serve them and the
+    exact fallbacks must run (the DecodeTopK page's direct path: the sample
+    misjudges the row). Even rows: N(0,1) where seven of every eight 16-byte
+    vectors are all NaN, so most groups of logits hold no usable representative
+    (fewer than k of them) while more than k logits are eligible. Odd rows:
+    every vector's eight logits equal (one N(0,1) draw per vector), so any cut
+    taken from group maxima lets whole vectors through, several times k
+    logits. Valid lengths = width; no table."""
+    rng = rng_for(seed)
+    vecs = -(-width // 8)
+    out = np.empty((rows, vecs * 8), np.uint16)
+    for r in range(rows):
+        if r % 2 == 0:
+            row = normal_bf16(rng, (vecs * 8,))
+            nan_vec = rng.random(vecs) < 7.0 / 8.0
+            row.reshape(vecs, 8)[nan_vec] = 0x7FC0
+        else:
+            row = np.repeat(normal_bf16(rng, (vecs,)), 8)
+        out[r] = row
+    return Case(f"fallback {rows}x{width} k{k}", out[:, :width].copy() if width % 8 else out, width,
+                np.full(rows, width, np.int32), k, TOKEN, None)

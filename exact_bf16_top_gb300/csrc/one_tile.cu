@@ -34,62 +34,6 @@ namespace topk {
 
 namespace one {
 
-// ---------------------------------------------------------- packed BF16 tests
-
-// Packed BF16 maximum: a NaN half loses to a number (both NaN: NaN).
-static __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// 0xFFFF in each half where a >= b as BF16 numbers, else 0 (a NaN half: 0).
-static __device__ __forceinline__ uint32_t bge2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// The BF16 bits of the value whose order key is `key` (0x7F..0xFF80).
-static __device__ __forceinline__ uint32_t key_value(uint32_t key) {
-    return key >= 0x8000u ? key - 0x8000u : key ^ 0xFFFFu;
-}
-
-// The order key of 16-bit BF16 bits x: x ^ (x < 0 ? 0xFFFF : 0x8000).
-static __device__ __forceinline__ uint32_t value_key(uint32_t x) {
-    return x ^ ((x & 0x8000u) ? 0xFFFFu : 0x8000u);
-}
-
-// The packed compare operand of cut c: a non-NaN value x has key(x) >= c
-// exactly when x >= value(c) as a BF16 number, for every c in [key(-inf),
-// key(+inf)] except key(+0), where the numbers -0 and +0 compare equal. So c is
-// clamped into that range (no eligible key lies outside it) and key(+0) is
-// lowered to key(-0): a lower cut is still a cut (more keys at or above it).
-static __device__ __forceinline__ uint32_t cut_operand(uint32_t &c) {
-    c = min(max(c, KEY_NEG_INF), KEY_POS_INF);
-    if (c == 0x8000u) c = 0x7FFFu;
-    const uint32_t v = key_value(c);
-    return v | (v << 16);
-}
-
-// Bit i of the result: the low half of word i of r is >= the operand; bit 4 + i:
-// its high half.
-static __device__ __forceinline__ uint32_t mask8(const uint4 &r, uint32_t cv) {
-    const uint32_t t = (bge2(r.x, cv) & 0x00010001u) | (bge2(r.y, cv) & 0x00020002u) |
-                       (bge2(r.z, cv) & 0x00040004u) | (bge2(r.w, cv) & 0x00080008u);
-    return (t | (t >> 12)) & 0xFFu;
-}
-
-// The key of the larger half of a packed pair (0 for NaN).
-static __device__ __forceinline__ uint32_t top_key(uint32_t m) {
-    const uint32_t x = bmax2(m, __byte_perm(m, 0, 0x1032)) & 0xFFFFu;
-    return (x & 0x7FFFu) > 0x7F80u ? 0u : value_key(x);
-}
-
-static __device__ __forceinline__ uint32_t vec_bmax(const uint4 &r) {
-    return bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w));
-}
-
 // Everything of the one-tile path for a CTA of NT_ threads (256: several CTAs
 // per SM for many rows; 512: one, for rows that do not fill the SMs, where a
 // row's latency is what counts) with a survivor list of SURV_ entries (2048

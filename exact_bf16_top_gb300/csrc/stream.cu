@@ -34,10 +34,11 @@
 // which rises whenever the buffer is compacted to its top-k and, in a cluster,
 // when a peer CTA publishes its own bound through distributed shared memory.
 //
-// A vector is first tested on its packed maximum; the vectors that may hold a
-// wanted key are queued per warp (ballots), and the warp's lanes work through
-// the queue together, so divergence does not multiply the work; a warp
-// reserves its slots with one shared atomic, never one per key. The C buffers
+// In token rows every thread forms the 8-bit masks of its vectors' logits at
+// or above the threshold with packed BF16 compares (NaN never passes), and a
+// warp reserves the slots of all its survivors with one shared atomic, never
+// one per key; block rows queue the candidate vectors per warp (ballots) and
+// the warp's lanes work through the queue together. The C buffers
 // of a row are merged with cluster-wide histograms over distributed shared
 // memory; ties at the row's k-th key are split across CTAs in index order, and
 // each CTA writes its part of the answer through the block table.
@@ -93,7 +94,6 @@ struct Cta {
     uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full, s->v_arrive
     uint32_t f_Q = 0, f_next = 0, f_lim = 0;  // this warp's queue, where its appends stopped, the limit
     uint32_t first_c = 0;    // the first tile's cut while its ties are pending (0: none)
-    bool f_fast = false;
     bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
     uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
 
@@ -344,80 +344,81 @@ struct Cta {
         if (C > 1 && lane < C && lane != rank) red_max_peer(peer_addr(&s->shared_thr[slot], lane), bound);
     }
 
-    // Token mode, lim >= 0x8000: the keys >= lim are the non-negative values
-    // whose BF16 bits, as signed 16-bit integers, are >= lim - 0x8000 (NaN is
-    // excluded by setting its sign bit first). These are build_queue and
-    // append_keys for that case, on raw bits: no key conversion per element.
-    __device__ __forceinline__ uint32_t build_queue_fast(const uint4 *stg, int nv, int32_t cs) {
-        const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-        const uint32_t lt = (1u << lane) - 1u;
-        uint32_t q = 0;
-        int32_t mx[VPT];  // every vector's maximum first: the loads issue together
+    // Token mode: append every key >= lim of the tile, with packed BF16
+    // compares: a non-NaN value x has key(x) >= lim exactly when x >= value(lim)
+    // as a BF16 number, for lim in [key(-inf), key(+inf)], except lim = key(+0),
+    // where -0 compares equal to +0 and is masked out apart. Below key(-inf)
+    // every eligible key qualifies, above key(+inf) none.
+    // Each thread forms the 8-bit masks of its vectors. The warp reserves the
+    // slots of all its survivors with one
+    // shared atomic (a ballot prefix of the counts, or a shuffle scan when a
+    // count exceeds 15), then each lane writes its own, reading the values
+    // back from the stage. Returns false if the buffer could not take them
+    // (the warp's slots are then dead and the warp redoes its part after a
+    // compaction), true otherwise.
+    __device__ __forceinline__ bool append_masks(const uint4 *stg, int64_t tile_v0, int nv, uint32_t lim) {
+        const uint32_t lane = lane_id(), tid = threadIdx.x;
+        const uint32_t lo = max(lim, KEY_NEG_INF);
+        const bool negz = lo == 0x8000u;  // keys >= key(+0): values >= 0 but -0
+        const uint32_t v = lo > KEY_POS_INF ? 0x7FC0u : key_value(lo), cv = v | (v << 16);
+        uint32_t mw[2] = {0u, 0u};  // bit 8 (j % 4) + b of word j / 4: vector j's logit 2 (b & 3) + (b >> 2)
+        // Every vector's mask, with no branch between them: the loads and the
+        // compares of the eight vectors overlap.
+        if (!negz) {
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int pos = j * THREADS + static_cast<int>(threadIdx.x);
-            mx[j] = pos < nv ? smax_halves(vec_smax(stg[pos])) : -32768;
-        }
-        uint32_t b[VPT];  // every ballot first: the stores then only wait on popcounts
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) b[j] = __ballot_sync(0xFFFFFFFFu, mx[j] >= cs);
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            if (mx[j] >= cs) s->queue[warp][q + __popc(b[j] & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
-            q += __popc(b[j]);
-        }
-        __syncwarp();
-        return q;
-    }
-
-    __device__ __forceinline__ uint32_t append_fast(const uint4 *stg, int64_t tile_v0, uint32_t Q,
-                                                 uint32_t from, uint32_t lim) {
-        const uint32_t lane = lane_id();
-        const int32_t cs = static_cast<int32_t>(lim) - 0x8000;
-        const uint32_t csm = (static_cast<uint32_t>(cs - 1) & 0xFFFFu) * 0x10001u;
-        for (uint32_t e0 = from; e0 < Q; e0 += 32) {
-            const uint32_t e = e0 + lane;
-            uint32_t m = 0;
-            int pos = 0;
-            uint4 r = make_uint4(0, 0, 0, 0);
-            if (e < Q) {
-                pos = queued_pos(e);
-                r = stg[pos];
-                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-                uint32_t u = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t x = w[i] | nan2(w[i]);
-                    const uint32_t g = smax2(x, csm) ^ csm;  // nonzero halves: x >= cs
-                    u |= ((((g & 0x7FFF7FFFu) + 0x7FFF7FFFu) | g) & 0x80008000u) >> (15 - i);
-                }
-                m = (u & 0xFu) | ((u >> 12) & 0xF0u);  // bit i: low half of word i; bit 4 + i: high half
+            for (int j = 0; j < VPT; ++j) {
+                const int pos = j * THREADS + static_cast<int>(tid);
+                const uint4 r = pos < nv ? stg[pos] : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+                mw[j / 4] |= mask8(r, cv) << (8 * (j % 4));
             }
-            const uint32_t cnt = __popc(m);
-            uint32_t total, at;
-            const uint32_t before = warp_excl_small(cnt, total);
-            if (!reserve(total, before, cnt, at)) return e0;  // full: the caller compacts and resumes here
-
-            const uint32_t idx0 = static_cast<uint32_t>(tile_v0 + pos) * 8u;
+        } else {  // (rare) keys >= key(+0): -0 halves out
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int pos = j * THREADS + static_cast<int>(tid);
+                const uint4 r = pos < nv ? stg[pos] : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+                const uint32_t t = (__vcmpeq2(r.x, 0x80008000u) & 0x00010001u) |
+                                   (__vcmpeq2(r.y, 0x80008000u) & 0x00020002u) |
+                                   (__vcmpeq2(r.z, 0x80008000u) & 0x00040004u) |
+                                   (__vcmpeq2(r.w, 0x80008000u) & 0x00080008u);
+                mw[j / 4] |= (mask8(r, cv) & ~((t | (t >> 12)) & 0xFFu)) << (8 * (j % 4));
+            }
+        }
+        const uint32_t cnt = __popc(mw[0]) + __popc(mw[1]);
+        uint32_t total, before;
+        if (__ballot_sync(0xFFFFFFFFu, cnt > 15u) == 0u) {
+            before = warp_excl_small(cnt, total);
+        } else {
+            const uint32_t incl = warp_incl_scan(cnt);
+            before = incl - cnt;
+            total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (total == 0u) return true;
+        uint32_t at;
+        if (!reserve(total, before, cnt, at)) return false;
+        const uint16_t *h16 = reinterpret_cast<const uint16_t *>(stg);
+        const uint32_t i0 = static_cast<uint32_t>(tile_v0) * 8u;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
 #pragma unroll 1
-            for (; m; m &= m - 1u) {
-                const int bit = __ffs(m) - 1;
-                const int i = bit & 3, hi = bit >> 2;
-                const uint32_t w = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
-                const uint32_t key = ((hi ? w >> 16 : w) & 0xFFFFu) + 0x8000u;
+            for (uint32_t mm = mw[w]; mm; mm &= mm - 1u) {
+                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                const uint32_t j = 4u * w + (bit >> 3), b = bit & 7u;
+                const uint32_t h = (j * THREADS + tid) * 8u + 2u * (b & 3u) + (b >> 2);
+                const uint32_t key = value_key(h16[h]);
                 s->buf_key[at] = static_cast<uint16_t>(key);
-                s->buf_idx[at] = idx0 + static_cast<uint32_t>(2 * i + hi);
+                s->buf_idx[at] = i0 + h;
                 if (run_ok) atomicAdd(&s->hwin[1][min(key - run_lo, 255u)], 1u);
                 ++at;
             }
         }
-        return Q;
+        (void)lane;
+        return true;
     }
 
-    // Token mode: the row's last vector, when partial, gets 0x8000 (a negative
-    // value no cut selects) in the lanes past the valid length, by the thread
-    // that owns its position in this tile (its warp reads it after a warp
-    // barrier).
+    // Token mode: the row's last vector, when partial, gets 0xFFFF (a NaN: no
+    // cut selects it, no maximum prefers it, its key is 0) in the lanes past
+    // the valid length, by the thread that owns its position in this tile (its
+    // warp reads it after a warp barrier).
     __device__ __forceinline__ void mask_tail(const uint4 *stg, int64_t tile_v0, int nv) const {
         if (M::BLOCK || (L & 7) == 0) return;
         const int64_t pos = V - 1 - tile_v0;
@@ -429,8 +430,7 @@ struct Cta {
 #pragma unroll
         for (int h = 0; h < 8; ++h)
             if (h >= lanes)
-                w[h >> 1] = (w[h >> 1] & ((h & 1) ? 0x0000FFFFu : 0xFFFF0000u)) |
-                            ((h & 1) ? 0x80000000u : 0x00008000u);
+                w[h >> 1] |= (h & 1) ? 0xFFFF0000u : 0x0000FFFFu;
         *v = make_uint4(w[0], w[1], w[2], w[3]);
     }
 
@@ -792,20 +792,25 @@ struct Cta {
             s->v_full[tpar ^ 1u] = 0u;
             s->v_arrive[tpar ^ 1u] = 0u;
         }
-        const bool fast = !M::BLOCK && lim >= 0x8000u && lim <= KEY_POS_INF;
         mask_tail(stg, tile_v0, nv);
         clk.stop(*p, TOPK_CNT_CYC_F_PREP);
         clk.start(*p);
-        const uint32_t Q = fast ? build_queue_fast(stg, nv, static_cast<int32_t>(lim) - 0x8000)
-                                : build_queue(stg, tile_v0, nv, lim);
-        clk.stop(*p, TOPK_CNT_CYC_F_QUEUE);
-        clk.start(*p);
-        const uint32_t next = fast ? append_fast(stg, tile_v0, Q, 0, lim) : append_keys(stg, tile_v0, Q, 0, lim);
+        // Token rows: packed masks, the warp's whole part of the tile as one
+        // entry (Q = 1); block rows: a queue of candidate vectors.
+        uint32_t Q, next;
+        if constexpr (!M::BLOCK) {
+            Q = 1u;
+            next = append_masks(stg, tile_v0, nv, lim) ? 1u : 0u;
+        } else {
+            Q = build_queue(stg, tile_v0, nv, lim);
+            clk.stop(*p, TOPK_CNT_CYC_F_QUEUE);
+            clk.start(*p);
+            next = append_keys(stg, tile_v0, Q, 0, lim);
+        }
         buf_lo = min(buf_lo, lim);
         f_Q = Q;
         f_next = next;
         f_lim = lim;
-        f_fast = fast;
         if (next < Q && lane_id() == 0) s->v_full[tpar] = 1u;
         clk.stop(*p, TOPK_CNT_CYC_F_APPEND);
         clk.start(*p);
@@ -861,7 +866,8 @@ struct Cta {
             count_event(*p, TOPK_CNT_REFILLS);
             compact(false);
             const uint32_t lim = max(f_lim, thr);  // the buffer now holds k keys >= thr
-            next = f_fast ? append_fast(stg, tile_v0, f_Q, next, lim) : append_keys(stg, tile_v0, f_Q, next, lim);
+            if constexpr (!M::BLOCK) next = next < f_Q ? (append_masks(stg, tile_v0, nv, lim) ? 1u : 0u) : next;
+            else next = append_keys(stg, tile_v0, f_Q, next, lim);
             if (tid == 0) s->v_flag = 0u;
             __syncthreads();
             if (next < f_Q && lane_id() == 0) s->v_flag = 1u;

@@ -42,7 +42,8 @@
 // of a row are merged with cluster-wide histograms over distributed shared
 // memory; ties at the row's k-th key are split across CTAs in index order, and
 // each CTA writes its part of the answer through the block table.
-// All selection arithmetic is on 16-bit integer keys; no floating point.
+// The packed BF16 compares decide exactly what a compare of the 16-bit keys
+// decides (NaN never passes); every count, cut and histogram is on the keys.
 
 #include "common.cuh"
 

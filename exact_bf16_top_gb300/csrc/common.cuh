@@ -19,6 +19,22 @@ namespace topk {
 // unit's status function. Kernels never trap.
 static __device__ uint32_t g_device_status;
 
+// Debug builds (-DTOPK_DEBUG): every shared-memory index a kernel computes from
+// data (a count, a scan, an atomic's result, a key) is checked before use with
+// TOPK_IDX_OK(i, n); an index outside [0, n) sets ERR_DEBUG_INDEX in the status
+// word and the access is skipped (no trap). Release builds compile the checks
+// away.
+#ifdef TOPK_DEBUG
+__device__ __forceinline__ bool debug_index_ok(uint64_t i, uint64_t n) {
+    if (i < n) return true;
+    atomicOr(&g_device_status, ERR_DEBUG_INDEX);
+    return false;
+}
+#define TOPK_IDX_OK(i, n) ::topk::debug_index_ok(static_cast<uint64_t>(i), static_cast<uint64_t>(n))
+#else
+#define TOPK_IDX_OK(i, n) true
+#endif
+
 static cudaError_t unit_status(uint32_t *v, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_device_status, sizeof(uint32_t));
     if (e == cudaSuccess && clear) {

@@ -88,17 +88,20 @@ struct Share {
             const uint32_t local = static_cast<uint32_t>(v - v0);
             if constexpr (M::BLOCK) {
                 const uint32_t key = BlockMode::key(stg[pos], v, V);
+                if (!TOPK_IDX_OK(local, RES)) continue;
                 s.key[local] = static_cast<uint16_t>(key);
                 best = max(best, key);
             } else {
                 uint32_t ck[4];
                 TokenMode::clean(stg[pos], v, V, L, ck);  // packed pairs of keys, in element order
+                if (!TOPK_IDX_OK(local, RES / 8)) continue;
                 reinterpret_cast<uint4 *>(s.key)[local] = make_uint4(ck[0], ck[1], ck[2], ck[3]);
                 best = max(best, umax_halves(umax2(umax2(ck[0], ck[1]), umax2(ck[2], ck[3]))));
             }
         }
         if (!p.force_direct) {  // (uniform: the exact passes start from an empty h[0])
-            s.rep[tile * NT + static_cast<int>(threadIdx.x)] = static_cast<uint16_t>(best);
+            if (TOPK_IDX_OK(tile * NT + static_cast<int>(threadIdx.x), MAX_TILES * NT))
+                s.rep[tile * NT + static_cast<int>(threadIdx.x)] = static_cast<uint16_t>(best);
             agg_add(s.h[0], best >> 8, best != 0u);
         }
     }
@@ -121,6 +124,7 @@ struct Share {
     }
 
     __device__ __forceinline__ void put(int32_t *orow, uint32_t slot, uint32_t local) const {
+        if (!TOPK_IDX_OK(orow - (p.out + static_cast<int64_t>(row) * p.k) + slot, p.k)) return;
         const int64_t e = M::BLOCK ? v0 + local : 8 * v0 + local;
         orow[slot] = transform(p, row, static_cast<int32_t>(e));
     }

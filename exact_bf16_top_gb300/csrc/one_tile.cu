@@ -166,7 +166,10 @@ struct Row {
             return;
         }
         int32_t v = static_cast<int32_t>(idx);
-        if (tab) v = s.tab[idx >> p.page_shift] * p.block_rows + (v & ((1 << p.page_shift) - 1));
+        if (tab) {
+            if (!TOPK_IDX_OK(idx >> p.page_shift, TAB_CAP)) return;
+            v = s.tab[idx >> p.page_shift] * p.block_rows + (v & ((1 << p.page_shift) - 1));
+        }
         else v = transform(p, row, v);
         orow[slot] = v;
     }
@@ -268,7 +271,7 @@ struct Row {
     // The exact path's cut: every candidate key is its own representative.
     __device__ bool exact_cut(uint32_t &c) {
         const int tid = threadIdx.x;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -282,7 +285,7 @@ struct Row {
         __syncthreads();
         const uint32_t hb = s.bc[0], habove = s.bc[1], nkeys = s.bc[2];
         if (nkeys < k) return false;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -310,7 +313,7 @@ struct Row {
         const int tid = threadIdx.x;
         if (4u * k >= static_cast<uint32_t>(M::BLOCK ? V : L)) return exact_cut(c);
         uint32_t top = 0;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -324,13 +327,14 @@ struct Row {
         par ^= 1u;
         if (top == 0u) return false;  // no candidate at all
         const uint32_t lo = top > 511u ? top - 511u : 1u;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
             for (int h = 0; h < M::KPV; ++h) {
                 const uint32_t key = key_at<M>(ck, h);
-                if (key >= lo) atomicAdd(&s.hs[0][255u - ((top - key) >> 1)], 1u);
+                if (key >= lo && TOPK_IDX_OK(255u - ((top - key) >> 1), 256u))
+                    atomicAdd(&s.hs[0][255u - ((top - key) >> 1)], 1u);
             }
         }
         __syncthreads();
@@ -341,7 +345,7 @@ struct Row {
         if (in_window < k) return exact_cut(c);
         const uint32_t upper = top - 2u * (255u - b);  // bin b: keys upper - 1 and upper
         uint32_t n_up = 0;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -375,7 +379,7 @@ struct Row {
         const int tid = threadIdx.x;
         stage_table(t0);
         uint32_t cnt = 0;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -383,7 +387,7 @@ struct Row {
         }
         uint32_t total;
         uint32_t at = block_scan(s, par, cnt, total) - cnt;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
 #pragma unroll
@@ -414,7 +418,7 @@ struct Row {
             return;
         }
         uint32_t before = 0;
-        for (int j = 0; j < NV && before < take; ++j) {
+        for (int j = 0; j < NV && j * NT < V && before < take; ++j) {
             uint32_t ck[4];
             clean(j * NT + static_cast<int>(tid), ck);
             uint32_t eq = 0;
@@ -497,6 +501,7 @@ struct Row {
                 const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
                 const uint32_t j = 4u * w + (bit >> 3), b = bit & 7u;
                 const uint32_t idx = (j * NT + tid) * 8u + 2u * (b & 3u) + (b >> 2);
+                if (!TOPK_IDX_OK(idx, static_cast<uint32_t>(V) * 8u)) continue;
                 const uint32_t key = value_key(h16[idx]);
                 // Past the list's end (the count then exceeds it and the pass is
                 // redone or replaced) writes go to the spare slot.
@@ -579,7 +584,7 @@ struct Row {
     __device__ void emit_rescan(uint32_t c) {
         const int tid = threadIdx.x;
         uint32_t before = 0;
-        for (int j = 0; j < NV; ++j) {
+        for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
             uint32_t ck[4];
             clean(j * NT + tid, ck);
             uint32_t gt = 0;

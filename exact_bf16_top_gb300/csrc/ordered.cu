@@ -79,6 +79,7 @@ __device__ __forceinline__ int32_t transform_o(const OParams &p, int32_t row, in
 // shared plane (written out with the row's last step).
 __device__ __forceinline__ void put_o(const OParams &p, Smem &s, int32_t row, uint32_t slot, int32_t i,
                                       uint32_t key) {
+    if (!TOPK_IDX_OK(slot, p.k)) return;
     if (p.words) {
         p.out[static_cast<int64_t>(row) * (p.k + p.k / 32) + slot] =
             static_cast<int32_t>((key << 16) | (0xFFFFu - (static_cast<uint32_t>(i) & 0xFFFFu)));
@@ -280,10 +281,10 @@ struct RowO {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const uint32_t top = top_at(t[u], pc, e);
-                    if (w.each) s.rep[8 * pc + e] = static_cast<uint16_t>(top);
+                    if (w.each && TOPK_IDX_OK(8 * pc + e, REP_CAP)) s.rep[8 * pc + e] = static_cast<uint16_t>(top);
                     acc = max(acc, top);
                 }
-                if (!w.each) s.rep[pc] = static_cast<uint16_t>(acc);
+                if (!w.each && TOPK_IDX_OK(pc, REP_CAP)) s.rep[pc] = static_cast<uint16_t>(acc);
                 best = max(best, acc);
             }
         }
@@ -373,7 +374,8 @@ struct RowO {
             const uint32_t incl = warp_incl_scan(n);
             uint32_t pos = at + incl - n;
             const int32_t p0 = w.base + 256 * b + 8 * static_cast<int32_t>(lane);
-            for (; m; m &= m - 1u) s.cvec[pos++] = static_cast<uint32_t>(8 * p0 + __ffsll(m) - 1);
+            for (; m; m &= m - 1u)
+                if (TOPK_IDX_OK(pos, VEC_CAP)) s.cvec[pos++] = static_cast<uint32_t>(8 * p0 + __ffsll(m) - 1);
             at += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         __syncthreads();
@@ -408,6 +410,7 @@ struct RowO {
             for (uint32_t m = mask_ge(x, c, lanes_of(v)); m; m &= m - 1u) {
                 const int h = __ffs(m) - 1;
                 const uint32_t key = key_of8(x, h);
+                if (!TOPK_IDX_OK(at, KEY_CAP)) continue;
                 s.lkey[at] = static_cast<uint16_t>(key);
                 s.lidx[at] = static_cast<uint32_t>(8 * v + h);
                 atomicAdd(&s.hw[min(key - c, 255u)], 1u);

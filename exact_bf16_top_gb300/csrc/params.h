@@ -20,7 +20,7 @@ constexpr uint32_t KEY_NEG_INF = 0x007Fu;    // key of -inf
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a stage wait gives up after 1 s
 constexpr uint32_t ALL = 0xFFFFFFFFu;        // "every tie" / "no cut"
 
-enum : uint32_t { ERR_WAIT = 1u, ERR_BOUNDS = 2u };
+enum : uint32_t { ERR_WAIT = 1u, ERR_BOUNDS = 2u, ERR_DEBUG_INDEX = 4u };
 
 struct Params {
     const uint16_t *logits;

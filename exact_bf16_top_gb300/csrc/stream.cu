@@ -272,7 +272,8 @@ struct Cta {
                 pass = M::may_reach(raw, M::BLOCK ? BlockMode::key(raw, tile_v0 + pos, V) : 0u, lim);
             }
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pass) s->queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
+            if (pass && TOPK_IDX_OK(q + __popc(b & lt), QCAP))
+                s->queue[warp][q + __popc(b & lt)] = static_cast<uint16_t>(j * THREADS + static_cast<int>(threadIdx.x));
             q += __popc(b);
         }
         __syncwarp();
@@ -310,7 +311,7 @@ struct Cta {
 #pragma unroll
                 for (int h = 0; h < KPV; ++h) {
                     const uint32_t key = key_at<M>(ck, h);
-                    if (key >= lim) {
+                    if (key >= lim && TOPK_IDX_OK(at, CAP)) {
                         s->buf_key[at] = static_cast<uint16_t>(key);
                         s->buf_idx[at] = M::elem(tile_v0 + pos, h);
                         if (run_ok) atomicAdd(&s->hwin[1][min(key - run_lo, 255u)], 1u);
@@ -405,6 +406,7 @@ struct Cta {
                 const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
                 const uint32_t j = 4u * w + (bit >> 3), b = bit & 7u;
                 const uint32_t h = (j * THREADS + tid) * 8u + 2u * (b & 3u) + (b >> 2);
+                if (!TOPK_IDX_OK(h, static_cast<uint32_t>(nv) * 8u) || !TOPK_IDX_OK(at, CAP)) continue;
                 const uint32_t key = value_key(h16[h]);
                 s->buf_key[at] = static_cast<uint16_t>(key);
                 s->buf_idx[at] = i0 + h;
@@ -510,6 +512,7 @@ struct Cta {
             for (int h = 0; h < KPV; ++h) {
                 if (key_at<M>(ck, h) == c) {
                     if (r < take) {
+                        if (!TOPK_IDX_OK(first + r, CAP)) continue;
                         s->buf_key[first + r] = static_cast<uint16_t>(c);
                         s->buf_idx[first + r] = M::elem(tile_v0 + pos, h);
                     }
@@ -647,7 +650,7 @@ struct Cta {
                 const bool sel = key[e] != 0u && (key[e] > T || (key[e] == T && idx[e] <= cut));
                 const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
                 const uint32_t at = warp_reserve(&s->v_emit, __popc(b)) + __popc(b & lt);
-                if (sel) {
+                if (sel && TOPK_IDX_OK(at, n)) {
                     s->buf_key[at] = static_cast<uint16_t>(key[e]);
                     s->buf_idx[at] = idx[e];
                 }
@@ -677,7 +680,7 @@ struct Cta {
             const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
             const uint32_t ag = warp_reserve(&s->v_emit, __popc(bg)) + __popc(bg & lt);
             const uint32_t at = warp_reserve(&s->v_ntie, __popc(bt)) + __popc(bt & lt);
-            if (gt) orow[ag] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
+            if (gt && TOPK_IDX_OK(offset + ag, k)) orow[ag] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
             if (tie && at < static_cast<uint32_t>(TIECAP)) s->tie_idx[at] = s->buf_idx[i];
         }
         __syncthreads();
@@ -691,7 +694,7 @@ struct Cta {
                     for (uint32_t u = 0; u < e; ++u) r += s->tie_idx[u] < mine;
                 else
                     r = static_cast<uint32_t>(tid);
-                if (r < take) orow[ngt + r] = transform(*p, row, static_cast<int32_t>(mine));
+                if (r < take && TOPK_IDX_OK(offset + ngt + r, k)) orow[ngt + r] = transform(*p, row, static_cast<int32_t>(mine));
             }
             return ngt + min(take, e);
         }
@@ -704,7 +707,7 @@ struct Cta {
             const bool sel = i < n && s->buf_key[i] == T && s->buf_idx[i] <= cut;
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, sel);
             const uint32_t at = warp_reserve(&s->v_ntie, __popc(b)) + __popc(b & lt);
-            if (sel) orow[ngt + at] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
+            if (sel && TOPK_IDX_OK(offset + ngt + at, k)) orow[ngt + at] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
         }
         return ngt + min(take, e);
     }

@@ -301,8 +301,10 @@ topk_status_t topk_bf16_plan(int32_t rows, int32_t width, int32_t k, topk_mode_t
 
 /*
  * Device-side status word of the current device: nonzero bits record a bounded
- * wait that gave up (bit 0) or an internal capacity or range check that failed
- * (bit 1); neither happens in correct operation, and the kernels never trap.
+ * wait that gave up (bit 0), an internal capacity or range check that failed
+ * (bit 1), or, in a library built with -DTOPK_DEBUG, a shared-memory index out
+ * of range (bit 2, the access skipped); none happens in correct operation, and
+ * the kernels never trap.
  * Synchronises the device. clear != 0 resets the word afterwards.
  */
 topk_status_t topk_bf16_device_status(uint32_t *flags, int32_t clear);

@@ -316,7 +316,8 @@ def plan(rows: int, width: int, k: int, mode: int = TOKEN) -> dict:
 
 
 def device_status(clear: bool = True) -> int:
-    """Device-side status bits (bounded wait gave up = 1, bound check = 2); syncs the device."""
+    """Device-side status bits (bounded wait gave up = 1, capacity or range check = 2,
+    shared-memory index out of range in a -DTOPK_DEBUG build = 4); syncs the device."""
     flags = ctypes.c_uint32()
     _check(load().topk_bf16_device_status(ctypes.byref(flags), 1 if clear else 0))
     return flags.value

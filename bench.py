@@ -332,6 +332,17 @@ def time_e2e(case, tk, torch, device, steps: int, warmup: int):
     sec = start.elapsed_time(stop) / 1e3 / steps
     bi = h_logits.numel() * 2 + h_valid.numel() * 4 + (0 if h_table is None else h_table.numel() * 4)
     bo = h_out.numel() * 4
+    # The host link alone: the same pinned logits copied host -> device, nothing
+    # else (the rate the end-to-end figure is measured against).
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        d_logits.copy_(h_logits, non_blocking=True)
+    b.record(stream)
+    b.synchronize()
+    link_gbs = h_logits.numel() * 2 * steps / (a.elapsed_time(b) / 1e3) / 1e9
+    time_e2e.link_gbs = link_gbs
     return case.rows / sec, bi, bo
 
 
@@ -566,7 +577,9 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab},
         "e2e": {"value": round(e2e_v, 1), "unit": "rows/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
+                "d2h_bytes_per_step": bo,
+                "h2d_link_gbs": round(getattr(time_e2e, "link_gbs", 0.0), 1),
+                "h2d_gbs": round(bi * e2e_v / case.rows / 1e9, 1)},
         "gpu_launches": args.steps,
         "clocks": clk,
         "spread": spread,

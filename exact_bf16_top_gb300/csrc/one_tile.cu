@@ -9,7 +9,8 @@
 // A CTA is persistent over rows; a row arrives by one bulk copy into a 32 KiB
 // shared stage. Per row:
 //   1. a cut c with at least k keys >= c (so c is at most the k-th key): the
-//      cut that held on the CTA's previous row, or the k-th largest of group
+//      cut that held on the CTA's previous row (for its first row, the one its
+//      slot ended the last launch with), or the k-th largest of group
 //      representatives;
 //   2. survivors: every thread forms the 8-bit masks of its vectors' logits
 //      >= c with packed BF16 compares (NaN never passes), takes its slots from
@@ -33,6 +34,17 @@
 namespace topk {
 
 namespace one {
+
+// The cut each CTA slot ended its last launch with, per device: (k << 16) |
+// cut, bit 31 set for block rows (0: none). A launch's CTA starts from it when
+// k and the mode match (decode steps see rows alike from one step to the
+// next), so its first row usually skips the representatives' pass. Only a
+// starting point: the survivor pass counts exactly the keys at or above any
+// cut it tries and falls back on a miss, so results never depend on it.
+// Launches running at once (other streams) may overwrite each other's words:
+// a 32-bit store is indivisible, and any value is a valid starting point.
+constexpr int CARRY_SLOTS = 1024;
+static __device__ uint32_t g_carry[CARRY_SLOTS];
 
 // Everything of the one-tile path for a CTA of NT_ threads (256: several CTAs
 // per SM for many rows; 512: one, for rows that do not fill the SMs, where a
@@ -832,6 +844,11 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
 
     typename O::template Row<M> r(s, p);
     r.k = static_cast<uint32_t>(p.k);
+    const uint32_t carry_tag = (M::BLOCK ? 0x80000000u : 0u) | (static_cast<uint32_t>(p.k) << 16);
+    {
+        const uint32_t cw = g_carry[blockIdx.x % CARRY_SLOTS];
+        if ((cw & 0xFFFF0000u) == carry_tag && !p.force_direct) r.guess = cw & 0xFFFFu;
+    }
     r.step = step;
     r.feed_row = p.rows;
     if (tid == 0) {
@@ -873,6 +890,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
         clk.stop(p, TOPK_CNT_CYC_SELECT);
         if (!r.fed) r.feed();
     }
+    if (tid == 0 && r.guess != 0u) g_carry[blockIdx.x % CARRY_SLOTS] = carry_tag | r.guess;
 }
 
 }  // namespace one

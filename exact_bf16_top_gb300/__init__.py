@@ -35,7 +35,7 @@ COUNTER_NAMES = ("bypass_rows", "tile_sampled", "tile_exact", "tile_unbounded", 
                  "ordered_exact")
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned", 3: "bad k", 4: "bad width",
-           5: "CUDA error"}
+           5: "CUDA error", 6: "more rows or wider rows than select_static takes"}
 
 
 class TopkError(RuntimeError):
@@ -77,6 +77,8 @@ def load(path: str | None = None):
         lib.topk_bf16_select_paged.argtypes = (sel_args[:10] + [ctypes.c_int32, ctypes.c_int32]
                                                + sel_args[10:])
         lib.topk_bf16_select_ex.restype = ctypes.c_int
+        lib.topk_bf16_select_static.argtypes = sel_args
+        lib.topk_bf16_select_static.restype = ctypes.c_int
         lib.topk_bf16_tops.restype = ctypes.c_int
         lib.topk_bf16_tops.argtypes = sel_args[:5] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         lib.topk_bf16_select_words.restype = ctypes.c_int
@@ -152,6 +154,32 @@ def select(logits, valid_len, k: int, mode: int = TOKEN, block_table=None, page_
             st = lib.topk_bf16_select_ex(*args, ctypes.byref(opt))
         else:
             st = lib.topk_bf16_select(*args)
+    _check(st)
+    return out
+
+
+def select_static(logits, valid_len, k: int, out, mode: int = TOKEN, block_table=None,
+                  page_size: int = 64, width: int | None = None, stream=None):
+    """select() through topk_bf16_select_static: no allocation on the call.
+
+    For callers that cannot allocate device memory, so ``out`` (a contiguous CUDA
+    int32 [rows, k]) is required. Rows of at most 16384 logits, at most 65536
+    rows; each row starts from the cut that held for the same row index in the
+    library's previous call of this entry point on the device (a static table
+    of the library; results are exact whatever it holds). Other arguments as
+    select().
+    """
+    import torch
+    rows, width, row_stride, table_stride = _inputs(logits, valid_len, block_table, width, 1)
+    if not (out.is_cuda and out.dtype == torch.int32 and out.shape == (rows, k) and out.is_contiguous()):
+        raise ValueError("out must be a contiguous CUDA int32 tensor [rows, k]")
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    lib = load()
+    with torch.cuda.device(logits.device):
+        st = lib.topk_bf16_select_static(_ptr(logits), row_stride, rows, width, _ptr(valid_len), int(k),
+                                         int(mode), _ptr(block_table), table_stride, int(page_size),
+                                         _ptr(out), ctypes.c_void_p(stream.cuda_stream))
     _check(st)
     return out
 

@@ -256,6 +256,64 @@ topk_status_t launch(const uint16_t *logits, int64_t row_stride, int32_t rows, i
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }
 
+// topk_bf16_select_static: the one-tile kernel with per-row starting cuts in
+// the library's static table (no allocation anywhere on this path).
+topk_status_t launch_static(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
+                            const int32_t *valid_len, int32_t k, topk_mode_t mode, const int32_t *table,
+                            int32_t table_stride, int32_t page_size, int32_t *out, void *stream) {
+    topk_status_t st = check_args(logits, row_stride, rows, width, valid_len, k, mode, table, table_stride,
+                                  page_size, out);
+    if (st != TOPK_OK) return st;
+    if (rows > TOPK_STATIC_MAX_ROWS || width > TOPK_STATIC_MAX_WIDTH) return TOPK_ERR_SIZE;
+    if (rows == 0) return TOPK_OK;
+    int dev = 0;
+    DeviceInit *d = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (init_device(dev, d) != cudaSuccess) return TOPK_ERR_CUDA;
+    uint32_t *row_carry = nullptr;
+    if (static_row_carry(dev, &row_carry) != cudaSuccess || row_carry == nullptr) return TOPK_ERR_CUDA;
+
+    const bool block = mode == TOPK_BLOCK8;
+    const Plan pl = make_plan(rows, width, k, *d, block, 0, 0);
+    if (pl.kind != KIND_ONE) return TOPK_ERR_SIZE;  // (cannot happen within the width limit)
+    const Variant v = one_static_variant(block, pl.build);
+
+    Params prm;
+    prm.logits = logits;
+    prm.row_stride = row_stride;
+    prm.rows = rows;
+    prm.width = width;
+    prm.valid_len = valid_len;
+    prm.k = k;
+    prm.table = table;
+    prm.table_stride = table_stride;
+    prm.block_rows = page_size;
+    prm.rows_per_request = 1;
+    prm.page_shift = 0;
+    if (table)
+        while ((1 << prm.page_shift) < page_size) ++prm.page_shift;
+    prm.out = out;
+    prm.counters = nullptr;
+    prm.force_direct = 0;
+    prm.release = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.clusters), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(v.smem);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    unsigned n_attr = 0;
+    if (pl.spare) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    void *args[] = {&prm, &row_carry};
+    return cudaLaunchKernelExC(&cfg, v.fn, args) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
 // The ordered select: one CTA per row, as many rows at once as there are SMs.
 topk_status_t launch_ordered(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
                              const int32_t *valid_len, int32_t k, const uint16_t *tops,
@@ -390,6 +448,15 @@ topk_status_t topk_bf16_select_paged(const uint16_t *logits, int64_t row_stride,
                         table_stride, page_size, block_rows, rows_per_request, out, stream, nullptr);
 }
 
+topk_status_t topk_bf16_select_static(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                      int32_t width, const int32_t *valid_len, int32_t k,
+                                      topk_mode_t mode, const int32_t *block_table,
+                                      int32_t table_stride, int32_t page_size, int32_t *out,
+                                      void *stream) {
+    return topk::launch_static(logits, row_stride, rows, width, valid_len, k, mode, block_table,
+                               table_stride, page_size, out, stream);
+}
+
 topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, int32_t rows,
                                   int32_t width, const int32_t *valid_len, int32_t k,
                                   topk_mode_t mode, const int32_t *block_table,
@@ -407,6 +474,7 @@ const char *topk_bf16_status_string(topk_status_t status) {
         case TOPK_ERR_K: return "k outside [1, 2048]";
         case TOPK_ERR_WIDTH: return "width outside [0, 1048576] or row_stride < width";
         case TOPK_ERR_CUDA: return "CUDA error";
+        case TOPK_ERR_SIZE: return "more rows or wider rows than topk_bf16_select_static takes";
     }
     return "unknown status";
 }

@@ -29,6 +29,8 @@
 // representative); a crowd of ties beyond the list is written by index-ordered
 // rescans of the row.
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace topk {
@@ -821,8 +823,11 @@ static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &
 
 };  // struct Tile
 
+// The kernel's body. row_carry: NULL, or a table of per-row starting cuts
+// ((k << 16) | cut, bit 31 for block rows) read before each row and rewritten
+// after it (topk_bf16_select_static's variant).
 template <class M, int NT, int SURV>
-__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) topk_one_tile_kernel(const Params p) {
+__device__ __forceinline__ void one_tile_body(const Params &p, uint32_t *row_carry) {
     using O = Tile<NT, SURV>;
     constexpr int NSTAGE = O::NSTAGE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -878,6 +883,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
         r.st = st;
         r.fed = false;
         r.orow = p.out + static_cast<int64_t>(row) * p.k;
+        if (row_carry != nullptr) {  // this row's own starting cut, when it has one for this k
+            const uint32_t cw = row_carry[row];
+            if ((cw & 0xFFFF0000u) == carry_tag && !p.force_direct) r.guess = cw & 0xFFFFu;
+        }
         PhaseClock clk;
         clk.start(p);
         mbar_wait_sleep(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
@@ -889,9 +898,30 @@ __global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) to
         __syncthreads();  // every thread is done with this stage and the row's shared state
         clk.stop(p, TOPK_CNT_CYC_SELECT);
         if (!r.fed) r.feed();
+        if (row_carry != nullptr && tid == 0 && r.guess != 0u) row_carry[row] = carry_tag | r.guess;
     }
     if (tid == 0 && r.guess != 0u) g_carry[blockIdx.x % CARRY_SLOTS] = carry_tag | r.guess;
 }
+
+template <class M, int NT, int SURV>
+__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1) topk_one_tile_kernel(const Params p) {
+    one_tile_body<M, NT, SURV>(p, nullptr);
+}
+
+// topk_bf16_select_static's kernel: the same, with per-row starting cuts in
+// the static table below (its device address is passed in, see
+// static_row_carry).
+template <class M, int NT, int SURV>
+__global__ void __launch_bounds__(NT, NT == 256 ? (SURV <= 2048 ? 4 : 3) : 1)
+    topk_one_tile_static_kernel(const Params p, uint32_t *row_carry) {
+    one_tile_body<M, NT, SURV>(p, row_carry);
+}
+
+// The per-row starting cuts of topk_bf16_select_static: TOPK_STATIC_MAX_ROWS
+// words (256 KiB) in every device that loads the library, for the life of the
+// process. Hints only (a stale, foreign or raced entry costs speed, never
+// correctness), so nothing in it has to start at zero.
+static __device__ __align__(256) uint32_t g_row_carry[TOPK_STATIC_MAX_ROWS];
 
 }  // namespace one
 
@@ -912,5 +942,43 @@ Variant one_variant(bool block, int build) {
 }
 
 cudaError_t status_one(uint32_t *v, bool clear) { return unit_status(v, clear); }
+
+template <class M, int NT, int SURV>
+static Variant one_static_build() {
+    return Variant{reinterpret_cast<const void *>(&one::topk_one_tile_static_kernel<M, NT, SURV>),
+                   static_cast<int>(sizeof(typename one::Tile<NT, SURV>::Smem))};
+}
+
+Variant one_static_variant(bool block, int build) {
+    switch (build) {
+        case 0: return block ? one_static_build<BlockMode, 256, 2048>() : one_static_build<TokenMode, 256, 2048>();
+        case 1: return block ? one_static_build<BlockMode, 256, 4096>() : one_static_build<TokenMode, 256, 4096>();
+        default: return block ? one_static_build<BlockMode, 512, 4096>() : one_static_build<TokenMode, 512, 4096>();
+    }
+}
+
+// Set-up of topk_bf16_select_static on device `dev` (which must be current),
+// once per device: the device address of the static table (host code sees
+// only a stand-in for it, never to be passed to a kernel) and the kernels'
+// shared-memory attribute. Returns the first call's result on every call.
+cudaError_t static_row_carry(int dev, uint32_t **table) {
+    static std::once_flag once[64];
+    static uint32_t *addr[64];
+    static cudaError_t err[64];
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev]() {
+        void *a = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&a, one::g_row_carry);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b)
+            for (int w = 0; w < ONE_BUILDS && e == cudaSuccess; ++w) {
+                const Variant v = one_static_variant(b != 0, w);
+                e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+            }
+        addr[dev] = static_cast<uint32_t *>(a);
+        err[dev] = e;
+    });
+    *table = addr[dev];
+    return err[dev];
+}
 
 }  // namespace topk

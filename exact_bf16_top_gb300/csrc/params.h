@@ -75,6 +75,8 @@ Variant direct_variant(bool block);               // direct.cu: the resident-key
 constexpr int ONE_BUILDS = 3;                     // one-tile builds (see one_variant)
 constexpr int one_threads(int build) { return build == 2 ? 512 : 256; }
 Variant one_variant(bool block, int build);       // one_tile.cu: the one-tile kernel
+Variant one_static_variant(bool block, int build);  // one_tile.cu: topk_bf16_select_static's kernel
+cudaError_t static_row_carry(int dev, uint32_t **table);  // one_tile.cu: its table, set up once per device
 Variant ordered_variant();                        // ordered.cu: the ordered kernel
 cudaError_t launch_tops(const uint16_t *logits, int64_t row_stride, int32_t rows, int32_t width,
                         const int32_t *valid_len, uint16_t *tops, int64_t tops_stride, int32_t pieces,

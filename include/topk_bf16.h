@@ -53,11 +53,15 @@ typedef enum {
     TOPK_ERR_ALIGN = 2,  /* logits not 16-byte aligned, or row_stride not a multiple of 8 */
     TOPK_ERR_K = 3,      /* k outside [1, TOPK_MAX_K] */
     TOPK_ERR_WIDTH = 4,  /* width outside [0, TOPK_MAX_WIDTH], or row_stride < width */
-    TOPK_ERR_CUDA = 5    /* a CUDA call failed (launch or attribute); see cudaGetLastError */
+    TOPK_ERR_CUDA = 5,   /* a CUDA call failed (launch or attribute); see cudaGetLastError */
+    TOPK_ERR_SIZE = 6    /* topk_bf16_select_static: more rows than its table holds, or rows
+                            wider than one 16384-logit stage */
 } topk_status_t;
 
 #define TOPK_MAX_K 2048
 #define TOPK_MAX_WIDTH (1 << 20)
+#define TOPK_STATIC_MAX_ROWS 65536   /* rows per call of topk_bf16_select_static */
+#define TOPK_STATIC_MAX_WIDTH 16384  /* logits per row of topk_bf16_select_static */
 
 /*
  * Exact top-k of every row (the operation described at the top of this file).
@@ -198,6 +202,40 @@ topk_status_t topk_bf16_select_ex(const uint16_t *logits, int64_t row_stride, in
                                   topk_mode_t mode, const int32_t *block_table,
                                   int32_t table_stride, int32_t page_size, int32_t *out,
                                   void *stream, const topk_bf16_options_t *options);
+
+/*
+ * topk_bf16_select_static: the same selection as topk_bf16_select, for rows of
+ * at most TOPK_STATIC_MAX_WIDTH logits (one 32 KiB stage), where each row
+ * starts from the cut that worked for the same row index in the previous call.
+ * No source page has a counterpart. A per-row table like this is scratch that
+ * would normally be a buffer the caller allocates and passes in; this entry
+ * point serves callers that cannot allocate device memory at all (code running
+ * inside a stream capture that must not record allocations, programs under a
+ * fixed device-memory budget with no allocator, plug-ins whose host owns every
+ * allocation). The table lives in the library itself: TOPK_STATIC_MAX_ROWS
+ * 32-bit words (256 KiB) in a static array of every device that loads the
+ * library, held until the process exits; the call allocates nothing and the
+ * caller passes only inputs and outputs, as for topk_bf16_select.
+ *
+ * The table holds per-row starting cuts for decode loops, where row r of one
+ * call is the same request as row r of the last: a starting cut is checked by
+ * an exact count like any other and dropped when it does not hold, so results
+ * are always exact. Every call on a device shares the table and leaves its own
+ * cuts in it; nothing needs clearing, and calls that overlap on the GPU (other
+ * streams) race on it harmlessly (any entry is a valid starting point).
+ *
+ * The first call on a device takes the table's device address and sets the
+ * kernels' attributes (once per device, with that device current): make that
+ * first call before capturing a stream into a CUDA graph.
+ *
+ * Arguments and outputs as topk_bf16_select. Errors as topk_bf16_select, plus
+ * TOPK_ERR_SIZE for rows > TOPK_STATIC_MAX_ROWS or width > TOPK_STATIC_MAX_WIDTH.
+ */
+topk_status_t topk_bf16_select_static(const uint16_t *logits, int64_t row_stride, int32_t rows,
+                                      int32_t width, const int32_t *valid_len, int32_t k,
+                                      topk_mode_t mode, const int32_t *block_table,
+                                      int32_t table_stride, int32_t page_size, int32_t *out,
+                                      void *stream);
 
 /*
  * The ordered select of the indexer page (vLLM kimi_k3 "dsa/indexer":

@@ -68,7 +68,7 @@ def test_options_struct_layout_matches_the_header(tmp_path):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert tk.status_string(s)
 
 

@@ -540,6 +540,7 @@ struct Cta {
             count_event(*p, TOPK_CNT_TILE_TAKE_ALL);
             return;
         }
+        if (!M::BLOCK && !p->force_direct && nE / 8u >= 2u * k && vector_cut(stg, tile_v0, nv)) return;
         uint32_t g = 1;
         if (!p->force_direct)
             while (g < static_cast<uint32_t>(M::GMAX) && nE / (4u * g) >= 2u * k) g *= 4u;
@@ -626,6 +627,65 @@ struct Cta {
         }
     }
 
+    // Token rows: first_cut with every vector (8 logits) a group, its
+    // representative the largest of its logits (an element of the vector: the
+    // packed maximum returns one of its operands and skips NaN halves), all of
+    // them held in registers after one pass over the stage. The same window
+    // as first_cut's; returns false, with nothing changed, when the k-th
+    // largest representative lies below the window (first_cut's general path
+    // then takes the row).
+    __device__ __forceinline__ bool vector_cut(const uint4 *stg, int64_t tile_v0, int nv) {
+        const int tid = threadIdx.x;
+        PhaseClock clk;
+        clk.start(*p);
+        mask_tail(stg, tile_v0, nv);  // this thread's own vector, read back below
+        uint32_t rk[VPT];
+        uint32_t top = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int pos = j * THREADS + tid;
+            rk[j] = pos < nv ? top_key(vec_bmax(stg[pos])) : 0u;
+            top = max(top, rk[j]);
+        }
+        top = __reduce_max_sync(0xFFFFFFFFu, top);
+        if (lane_id() == 0) s->red[parity][tid >> 5] = top;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) top = max(top, s->red[parity][w]);
+        parity ^= 1u;
+        if (top == 0u) return false;
+        // Bins of two keys below the top (bin 255: top - 1, top); lower keys
+        // are not counted, so a k-th representative below the window shows as
+        // too few representatives.
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            if (rk[j] != 0u && top - rk[j] < 510u) atomicAdd(&s->hwin[2][255u - ((top - rk[j]) >> 1)], 1u);
+        __syncthreads();
+        uint32_t b, wabove, wtotal;
+        const bool ok = find_bin256(s->hwin[2], k, b, wabove, wtotal);
+        const uint32_t in_bin = ok ? s->hwin[2][b] : 0u;
+        __syncthreads();
+        s->hwin[2][tid] = 0u;
+        __syncthreads();
+        if (!ok) return false;
+        const uint32_t upper = top - 2u * (255u - b);  // bin b: keys upper - 1, upper
+        uint32_t c = upper > 1u ? upper - 1u : 1u;
+        if (in_bin > k / 4u) {  // a crowded bin: c exactly the k-th representative
+            uint32_t mine = 0;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) mine += rk[j] == upper;
+            uint32_t ups;
+            block_incl_scan(mine, ups);
+            if (wabove + ups >= k) c = upper;
+        }
+        count_event(*p, TOPK_CNT_TILE_SAMPLED);
+        first_c = c;
+        thr = max(thr, c + 1u);
+        publish(c);
+        clk.stop(*p, TOPK_CNT_CYC_CUT);
+        return true;
+    }
+
     // Keep the buffer entries [0, n) that are selected (key > T, or key == T
     // with index <= cut) at the front of the buffer, in any order. Returns how
     // many were kept.
@@ -668,24 +728,31 @@ struct Cta {
         const uint32_t lt = (1u << lane_id()) - 1u;
         int32_t *orow = p->out + static_cast<int64_t>(row) * k + offset;
         __syncthreads();
-        if (tid == 0) {
-            s->v_emit = 0u;
-            s->v_ntie = 0u;
+        // Each thread counts its entries (tid, tid + THREADS, ...) above T and
+        // tied at T, packed (ties << 16) | above (n <= CAP < 2^16); one CTA
+        // scan gives every thread its first output slot and tie slot, and a
+        // second pass writes them: no atomic per entry or per warp.
+        uint32_t cnt = 0;
+        for (uint32_t i = tid; i < n; i += THREADS) {
+            const uint32_t key = s->buf_key[i];
+            cnt += key > T ? 1u : (take != 0u && key == T ? 0x10000u : 0u);
         }
-        __syncthreads();
-        for (uint32_t i0 = 0; i0 < n; i0 += THREADS) {
-            const uint32_t i = i0 + tid;
-            const uint32_t key = i < n ? s->buf_key[i] : 0u;
-            const bool gt = key > T, tie = take && key == T;
-            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), bt = __ballot_sync(0xFFFFFFFFu, tie);
-            const uint32_t ag = warp_reserve(&s->v_emit, __popc(bg)) + __popc(bg & lt);
-            const uint32_t at = warp_reserve(&s->v_ntie, __popc(bt)) + __popc(bt & lt);
-            if (gt && TOPK_IDX_OK(offset + ag, k)) orow[ag] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
-            if (tie && at < static_cast<uint32_t>(TIECAP)) s->tie_idx[at] = s->buf_idx[i];
+        uint32_t total;
+        const uint32_t excl = block_incl_scan(cnt, total) - cnt;
+        uint32_t ag = excl & 0xFFFFu, at = excl >> 16;
+        for (uint32_t i = tid; i < n; i += THREADS) {
+            const uint32_t key = s->buf_key[i];
+            if (key > T) {
+                if (TOPK_IDX_OK(offset + ag, k)) orow[ag] = transform(*p, row, static_cast<int32_t>(s->buf_idx[i]));
+                ++ag;
+            } else if (take != 0u && key == T) {
+                if (at < static_cast<uint32_t>(TIECAP)) s->tie_idx[at] = s->buf_idx[i];
+                ++at;
+            }
         }
-        __syncthreads();
-        const uint32_t ngt = s->v_emit, e = s->v_ntie;
+        const uint32_t ngt = total & 0xFFFFu, e = total >> 16;
         if (take == 0u) return ngt;
+        __syncthreads();  // every tie index is written
         if (e <= static_cast<uint32_t>(TIECAP)) {
             if (static_cast<uint32_t>(tid) < e) {
                 const uint32_t mine = s->tie_idx[tid];
@@ -713,16 +780,44 @@ struct Cta {
     }
 
     // The largest key of buffer entries [0, n) (0 for none), in every thread.
+    // (Callers order the buffer's writes before it with a barrier.)
     __device__ __forceinline__ uint32_t buffer_max(uint32_t n) {
         uint32_t m = 0;
         for (uint32_t i = threadIdx.x; i < n; i += THREADS) m = max(m, static_cast<uint32_t>(s->buf_key[i]));
         m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane_id() == 0) s->red[parity][threadIdx.x >> 5] = m;
         __syncthreads();
-        if (threadIdx.x == 0) s->v_bufmax = 0u;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) m = max(m, s->red[parity][w]);
+        parity ^= 1u;
+        return m;
+    }
+
+    // The k-th largest key T of buffer entries [0, n) and the count above it,
+    // given a lower bound LB >= 1 of T, when every key >= LB lies within 255 of
+    // it: one histogram of those keys only (the buffer's stale entries below LB
+    // are skipped). Returns false when a key lies further up or fewer than k
+    // keys reach LB (the caller then takes window_select). Uses s->hwin[2]
+    // (zero on entry and on exit).
+    __device__ __forceinline__ bool bound_select(uint32_t n, uint32_t LB, uint32_t *T_out, uint32_t *above_out) {
+        const int tid = threadIdx.x;
+        bool wide = false;
+        for (uint32_t i = tid; i < n; i += THREADS) {
+            const uint32_t key = s->buf_key[i];
+            if (key >= LB) {
+                if (key - LB > 255u) wide = true;
+                else atomicAdd(&s->hwin[2][key - LB], 1u);
+            }
+        }
+        const bool any_wide = __syncthreads_or(wide) != 0;
+        uint32_t b = 0, above = 0, total;
+        const bool ok = !any_wide && find_bin256(s->hwin[2], k, b, above, total);
         __syncthreads();
-        if (lane_id() == 0 && m) atomicMax(&s->v_bufmax, m);
+        s->hwin[2][tid] = 0u;
         __syncthreads();
-        return s->v_bufmax;
+        *T_out = LB + b;
+        *above_out = above;
+        return ok;
     }
 
     // Reduce the buffer to its exact top-k. strict: every buffered key precedes
@@ -740,7 +835,8 @@ struct Cta {
         PhaseClock clk;
         clk.start(*p);
         uint32_t T, above;
-        window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
+        if (!bound_select(n, max(thr, 2u) - 1u, &T, &above))  // thr - 1: see emit_single
+            window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
         const uint32_t take = k - above;
         const uint32_t cut = tie_cut(n, T, take);
         const uint32_t kept = keep_selected(n, T, cut);
@@ -888,8 +984,13 @@ struct Cta {
         const uint32_t n = s->v_count;
         uint32_t T = 0, take = 0;
         if (n > k) {
+            // thr - 1 bounds the buffer's k-th key from below (thr is one above a
+            // cut, a compaction's k-th key or a find's F), and so does the last
+            // tile's find (v_newthr - 1).
+            const uint32_t LB = max(max(thr, s->v_newthr), 2u) - 1u;
             uint32_t above;
-            window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
+            if (!bound_select(n, LB, &T, &above))
+                window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
             take = k - above;
         }
         const uint32_t written = emit_selected(n, T, take, 0);

@@ -129,11 +129,15 @@ def test_natural_fallbacks_fire():
     representatives' cut lets more survivors through than the list holds
     redo the cut exactly (tile_overflow, one-tile kernel) or fill the
     streamed kernel's buffer, which is compacted and the tile resumed
-    (refills: the streamed kernel has no list to overflow). Results stay
-    exact."""
-    for width, opts, names in ((16384, {}, ("tile_unbounded", "tile_overflow")),
-                               (100000, {"path": 1, "cluster": 1}, ("tile_unbounded", "refills"))):
-        case = W.fallback_rows(0, rows=8, width=width, k=512)
+    (refills: the streamed kernel has no list to overflow). The streamed
+    kernel's first cut takes one representative per 8-logit vector while
+    the tile holds 2k of them (k <= 1024), one per half vector above that: on
+    these rows at most 8 (k - 1) keys, then 4 (k - 1), pass it, which a
+    4096-entry buffer holds for k <= 512 and k = 1024; k = 2048 there.
+    Results stay exact."""
+    for width, k, opts, names in ((16384, 512, {}, ("tile_unbounded", "tile_overflow")),
+                                  (100000, 2048, {"path": 1, "cluster": 1}, ("tile_unbounded", "refills"))):
+        case = W.fallback_rows(0, rows=8, width=width, k=k)
         counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
         assert_same_sets(run_gpu(case, counters=counters, **opts), run_oracle(case), case.name)
         c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))

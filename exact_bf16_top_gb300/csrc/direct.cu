@@ -30,6 +30,13 @@ namespace topk {
 namespace direct {
 
 constexpr int NSTAGE = 2;
+// Carried cuts: each cluster slot keeps the k-th key of the last row it
+// selected (tagged with the mode and k); its next row, in this launch or the
+// next, first tries that key lowered by CARRY_MARGIN as its cut, which the
+// row's own window sums then accept or reject (a starting point only).
+constexpr int CARRY_SLOTS = 256;
+constexpr uint32_t CARRY_MARGIN = 32;
+static __device__ uint32_t g_carry[CARRY_SLOTS];
 constexpr int MAX_TILES = RES / TILE_VEC;    // stages per share (block rows; token rows take one)
 constexpr int LIST_CAP = 1280;               // keys >= the cut listed per CTA (more: emitted by a scan)
 
@@ -44,6 +51,7 @@ struct alignas(128) Smem {
     uint16_t rep[MAX_TILES * NT];            // the representative of each thread and tile
     uint32_t list[LIST_CAP];                 // local index << 16 | key, for keys >= the cut
     uint32_t n_list, cursor[2];
+    uint32_t carry_word;                     // rank 0: the carried cut this launch starts from
     uint32_t red[2][NT / 32];
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
@@ -59,6 +67,8 @@ struct Share {
     int32_t row = 0, L = 0;
     int64_t V = 0, v0 = 0;
     uint32_t n = 0;  // resident elements
+    uint32_t kth = 0;    // the row's k-th key once selected (0: none)
+    uint32_t guess = 0;  // a carried cut to try first (0: none)
 
     __device__ Share(Smem &s_, const Params &p_) : s(s_), p(p_) {}
 
@@ -236,6 +246,7 @@ struct Share {
             uint32_t b2, above2, tot2;
             find_bin256(s.all, k - above1, b2, above2, tot2);
             T = (b1 << 8) | b2;
+            kth = T;
             take = k - above1 - above2;
             uint32_t x = 0;
             for (uint32_t b = lane; b < 256u; b += 32u)
@@ -334,18 +345,33 @@ struct Share {
         const uint32_t c = (b1 << 8) | b2;  // the row's k-th largest representative
         clk.stop(p, TOPK_CNT_CYC_CUT);
         clk.start(p);
+        const int r = select_from(c, clk);  // at least k keys are >= c
+        if (r != 0) {  // the k-th key is >= c + 255: not resolved by the window
+            if (rank == 0) count_event(p, TOPK_CNT_TILE_OVERFLOW);
+            return false;
+        }
+        if (rank == 0) count_event(p, TOPK_CNT_TILE_SAMPLED);
+        return true;
+    }
+
+    // The selection from a cut c: this CTA's keys >= c listed and binned by
+    // key - c, the window summed over the cluster, the k-th key T = c + bin,
+    // then the emission. Returns 1 (nothing written) when fewer than k keys of
+    // the row reach c, 2 when the k-th key lies past the window (>= c + 255),
+    // 0 when done. Every CTA of the cluster returns the same.
+    __device__ int select_from(uint32_t c, PhaseClock &clk) {
+        const int tid = threadIdx.x;
+        const uint32_t k = static_cast<uint32_t>(p.k);
+        const uint32_t lane = lane_id();
         list_survivors(c);
         gather(2, 0);
         clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
         clk.start(p);
         uint32_t t, above, tot3;
-        find_bin256(s.all, k, t, above, tot3);  // at least k keys are >= c
-        if (t == 255u) {  // the k-th key is >= c + 255: not resolved by the window
-            if (rank == 0) count_event(p, TOPK_CNT_TILE_OVERFLOW);
-            return false;
-        }
-        if (rank == 0) count_event(p, TOPK_CNT_TILE_SAMPLED);
+        if (!find_bin256(s.all, k, t, above, tot3)) return 1;
+        if (t == 255u) return 2;
         const uint32_t T = c + t;       // the row's k-th largest key
+        kth = T;
         const uint32_t take = k - above;  // keys == T to take, lowest indices first
         uint32_t x = 0;
         for (uint32_t b = lane; b < 256u; b += 32u) x += b > t ? s.pre[0][b] : 0u;
@@ -361,7 +387,7 @@ struct Share {
         if (listed > static_cast<uint32_t>(LIST_CAP) || (partial && my_eq > static_cast<uint32_t>(NT))) {
             // Listed only in part, or too many ties to rank: from the resident keys.
             emit_scan(T, above, gt_prev, eq_prev, take, true);
-            return true;
+            return 0;
         }
         // From the list: keys > T at warp-reserved slots (the order within a
         // class is free); keys == T likewise when this CTA takes all of them,
@@ -392,7 +418,29 @@ struct Share {
                 if (r < quota) put(orow, above + eq_prev + r, mine);
             }
         }
-        return true;
+        return 0;
+    }
+
+    // The carried cut first: on a miss, every peer is done reading this CTA's
+    // window sums before they are cleared, and the row goes on as without it.
+    __device__ bool guess_select(PhaseClock &clk) {
+        const int tid = threadIdx.x;
+        if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
+        __syncthreads();
+        if (select_from(guess, clk) == 0) {
+            if (rank == 0) count_event(p, TOPK_CNT_GUESS_HIT);
+            return true;
+        }
+        if (rank == 0) count_event(p, TOPK_CNT_GUESS_MISS);
+        if (C > 1) {
+            cluster_arrive();
+            cluster_wait();
+        } else {
+            __syncthreads();
+        }
+        s.h[2][tid] = 0u;
+        __syncthreads();
+        return false;
     }
 
     __device__ void select_and_emit(uint32_t ntiles) {
@@ -400,8 +448,10 @@ struct Share {
         PhaseClock clk;
         clk.start(p);
         bool done = false;
+        kth = 0u;
         if (!p.force_direct) {
-            done = cut_select(ntiles, clk);
+            if (guess != 0u) done = guess_select(clk);
+            if (!done) done = cut_select(ntiles, clk);
             if (!done) {
                 // Every peer must be done reading h[0] and h[1] before the exact
                 // passes refill them.
@@ -458,17 +508,28 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
     if (p.release) grid_dependents_release();
 
     Feed feed;
+    const uint32_t carry_tag = (M::BLOCK ? 0x80000000u : 0u) | (static_cast<uint32_t>(p.k) << 16);
     if (tid == 0) {
         feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
         for (int i = 0; i < NSTAGE && feed.row < p.rows; ++i) feed_issue(feed, s, i, p, M::BLOCK, ncl, C, rank);
+        // Read once, by rank 0, so that the whole cluster starts from the same
+        // word whatever other launches write meanwhile.
+        if (rank == 0) s.carry_word = g_carry[cid % CARRY_SLOTS];
     }
     if (C > 1) {  // every CTA started and zeroed before any distributed access
         cluster_arrive();
         cluster_wait();
+    } else {
+        __syncthreads();
     }
     Share<M> sh(s, p);
     sh.C = C;
     sh.rank = rank;
+    {
+        const uint32_t cw = C > 1 ? ld_peer(peer_addr(&s.carry_word, 0u)) : s.carry_word;
+        const uint32_t cut = cw & 0xFFFFu;
+        if ((cw & 0xFFFF0000u) == carry_tag && cut > CARRY_MARGIN) sh.guess = cut - CARRY_MARGIN;
+    }
     uint32_t seq = 0;
     for (int32_t row = cid; row < p.rows; row += ncl) {
         int32_t L;
@@ -511,8 +572,10 @@ __global__ void __launch_bounds__(NT, 2) topk_direct_kernel(const Params p) {
         __syncthreads();
         if (rank == 0) count_event(p, TOPK_CNT_DIRECT_ROWS);
         sh.select_and_emit(static_cast<uint32_t>(ntiles));
+        if (sh.kth > CARRY_MARGIN) sh.guess = sh.kth - CARRY_MARGIN;  // (uniform: from cluster sums)
         __syncthreads();
     }
+    if (rank == 0 && tid == 0 && sh.kth != 0u) g_carry[cid % CARRY_SLOTS] = carry_tag | sh.kth;
     whole.stop(p, TOPK_CNT_CYC_KERNEL);
 }
 

@@ -174,10 +174,13 @@ enum {
     TOPK_CNT_CYC_CUT = 16,       /*   the representatives' cut */
     TOPK_CNT_CYC_SURVIVORS = 17, /*   the survivor pass */
     TOPK_CNT_CYC_EXACT = 18,     /*   the exact cut among survivors and the tie appends */
-    TOPK_CNT_GUESS_HIT = 19,     /* one-tile rows cut by the cut of the CTA's previous row
-                                    (checked by the exact survivor counts) */
+    TOPK_CNT_GUESS_HIT = 19,     /* rows cut by a carried-over cut: one-tile rows by the cut of
+                                    the CTA's previous row, resident-keys rows by the k-th key
+                                    of the cluster's previous row less a margin (checked by
+                                    the exact survivor counts or the window sums) */
     TOPK_CNT_GUESS_MISS = 20,    /* carried-over cuts dropped: fewer than k keys at or above
-                                    it, or more survivors than buffer room */
+                                    it, more survivors than buffer room, or (resident-keys
+                                    rows) the k-th key past the cut's window */
     /* streamed rows, later tiles, split (thread 0 of each CTA): */
     TOPK_CNT_CYC_F_PREP = 21,    /*   threshold update, compaction, running-histogram rebuild */
     TOPK_CNT_CYC_F_QUEUE = 22,   /*   candidate-vector queue */

@@ -63,6 +63,11 @@ static constexpr int SURV_CAP = SURV_;
 static constexpr int REP_CAP = 4096;         // stored representatives (groups of >= 4 logits)
 static constexpr int TAB_CAP = 256;          // page ids of a row staged in shared memory
 static constexpr int TPT = (TAB_CAP + NT - 1) / NT;  // page ids per thread
+// The build for large k (256 threads, 4096-entry list) also carries the window
+// shift of its cuts and measures their distance in value near zero (see
+// next_guess): rows that select about half their elements need both. The
+// other builds keep the plain distance in keys.
+static constexpr bool DENSE_GUESS = NT == 256 && SURV_ == 4096;
 
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][NTILE];
@@ -79,6 +84,8 @@ struct alignas(128) Smem {
     uint32_t bc[4];
     uint32_t v_cnt[2];                       // survivor counts, by row parity
     uint32_t v_smax;
+    uint32_t v_hint;                         // exact_cut: a cut for the next row (see next_guess)
+    uint32_t v_carry[NSTAGE];                // a carried cut for the row in each stage (see issue_row)
     uint32_t abort_flag;
     unsigned long long full[NSTAGE];
 };
@@ -128,12 +135,15 @@ struct Row {
     int32_t *orow = nullptr;      // the row's k output slots
     uint32_t k = 0;
     uint32_t guess = 0;   // the cut carried over from this CTA's previous row (0: none)
+    uint32_t gshift = 0;  // its window's bin width, log2 keys (DENSE_GUESS builds; else 0)
+    uint32_t hint = 0;    // exact_cut's cut for the next row (DENSE_GUESS builds; 0: none)
     uint32_t rp = 0;      // parity of the rows this CTA has selected
     bool tab = false;     // the row's page ids are in s.tab
     // The copy ring (thread 0's view): the next row to load into a stage and
     // its valid vectors; the stage of the current row; whether the current
     // row's stage has been handed back to the ring.
     int32_t feed_row = 0, feed_V = 0, step = 1;
+    uint32_t *row_carry = nullptr;  // topk_bf16_select_static's per-row cuts (else NULL)
     int32_t cand_row = 0, cand_L = 0;  // the candidate after feed_row and its valid length
                                        // (loaded ahead: nothing waits for it until its turn)
     int st = 0;
@@ -295,8 +305,20 @@ struct Row {
             }
         }
         __syncthreads();
+        if constexpr (DENSE_GUESS) {
+            if (tid < 32) {
+                // The lowest key of the high byte holding the (k + want)-th
+                // largest key: k + want keys at or above it on this row, a cut
+                // for the next row counted in ranks; every key (cut 1) when the
+                // row has fewer.
+                uint32_t b, above, total;
+                const bool ok = find_bin256(s.hs[0], k + guess_want(), b, above, total);
+                if (tid == 0) s.v_hint = ok ? max(b << 8, 1u) : 1u;
+            }
+        }
         warp0_find(s, s.hs[0], k);
         __syncthreads();
+        if constexpr (DENSE_GUESS) hint = s.v_hint;
         const uint32_t hb = s.bc[0], habove = s.bc[1], nkeys = s.bc[2];
         if (nkeys < k) return false;
         for (int j = 0; j < NV && j * NT < V; ++j) {  // (vectors past V hold nothing)
@@ -451,15 +473,18 @@ struct Row {
         }
     }
 
-    // The q-th largest survivor key when the window histogram cannot place it:
-    // a two-pass radix select over the list's keys, all in [lo, hi].
+    // The q-th largest of the list's keys in [lo, hi] (others are not
+    // counted; q at most their number), by a radix select over the list: one
+    // pass when hi - lo < 256, else two.
     __device__ uint32_t survivor_select(uint32_t n, uint32_t lo, uint32_t hi, uint32_t q, uint32_t &above) {
         const uint32_t tid = threadIdx.x;
         const uint32_t range = hi - lo;
         const int shift = range < 256u ? 0 : (32 - __clz(static_cast<int>(range))) - 8;
         const uint32_t mask = (1u << shift) - 1u;
-        for (uint32_t i = tid; i < n; i += NT)
-            atomicAdd(&s.hs[0][min(((s.surv[i] >> 16) - lo) >> shift, 255u)], 1u);
+        for (uint32_t i = tid; i < n; i += NT) {
+            const uint32_t o = (s.surv[i] >> 16) - lo;  // (keys below lo wrap past range)
+            if (o <= range) atomicAdd(&s.hs[0][min(o >> shift, 255u)], 1u);
+        }
         __syncthreads();
         warp0_find(s, s.hs[0], q);
         __syncthreads();
@@ -490,7 +515,7 @@ struct Row {
     // slots come from a ballot prefix of the counts and one shared atomic per
     // warp; then one loop over the thread's survivors reads each back from the
     // stage as a 16-bit value (no per-vector loops, no register indexing).
-    __device__ __forceinline__ void survivors_tok(uint32_t c, uint32_t cv, uint32_t *hw) {
+    __device__ __forceinline__ void survivors_tok(uint32_t c, uint32_t cv, uint32_t *hw, uint32_t sh) {
         constexpr int MW = (NV + 3) / 4;  // mask words: bit 8 (j % 4) + b of word j / 4 is
                                           // vector j's logit 2 (b & 3) + (b >> 2)
         const uint32_t lane = lane_id(), tid = threadIdx.x;
@@ -520,7 +545,7 @@ struct Row {
                 // Past the list's end (the count then exceeds it and the pass is
                 // redone or replaced) writes go to the spare slot.
                 s.surv[min(at, static_cast<uint32_t>(SURV_CAP))] = (key << 16) | (0xFFFFu - idx);
-                atomicAdd(&hw[min(key - c, 255u)], 1u);
+                atomicAdd(&hw[min((key - c) >> sh, 255u)], 1u);
                 ++at;
             }
         }
@@ -528,7 +553,7 @@ struct Row {
 
     // Block rows: survivors of cut c, as survivors_tok with one key per vector
     // (bit j: vector j's key >= c; the key is formed again for the write).
-    __device__ __forceinline__ void survivors_blk(uint32_t c, uint32_t *hw) {
+    __device__ __forceinline__ void survivors_blk(uint32_t c, uint32_t *hw, uint32_t sh) {
         const uint32_t tid = threadIdx.x;
         uint32_t m = 0, cnt = 0;
 #pragma unroll
@@ -545,7 +570,7 @@ struct Row {
             const uint32_t idx = static_cast<uint32_t>(__ffs(m) - 1) * NT + tid;
             const uint32_t key = bkey(static_cast<int>(idx));
             s.surv[min(at, static_cast<uint32_t>(SURV_CAP))] = (key << 16) | (0xFFFFu - idx);
-            atomicAdd(&hw[min(key - c, 255u)], 1u);
+            atomicAdd(&hw[min((key - c) >> sh, 255u)], 1u);
             ++at;
         }
     }
@@ -620,11 +645,36 @@ struct Row {
     // like this one. The margin covers the spread of the count, which grows like
     // its square root (measured on N(0,1) rows with k = 512: 128 left no row
     // short of k keys, 64 about one row in forty, each costing a second cut).
+    //
+    // DENSE_GUESS builds: around zero BF16 keys step through tiny magnitudes,
+    // where a distance in keys says nothing about ranks, so within 1/8 of zero
+    // the distance is taken in value; after the exact cut (T = c: no spacing
+    // measured) the cut is exact_cut's hint. The next row's window histogram
+    // is then binned 2^gshift keys wide, so that T - cut spans at most 127
+    // bins (up to 256 keys per bin: the list's radix select places the k-th
+    // key inside its bin).
+    __device__ __forceinline__ uint32_t guess_want() const {
+        return min(max(k / 8u, 128u), (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
+    }
+
     __device__ __forceinline__ void next_guess(uint32_t c, uint32_t T, uint32_t n) {
-        const uint32_t want = min(max(k / 8u, 128u), (static_cast<uint32_t>(SURV_CAP) - k) / 2u);
-        const uint32_t d = T > c ? max(static_cast<uint32_t>(__fdividef(static_cast<float>(want * (T - c)),
-                                                                        static_cast<float>(n - k + 1u))), 1u)
-                                 : 16u;
+        const uint32_t want = guess_want();
+        uint32_t d = T > c ? max(static_cast<uint32_t>(__fdividef(static_cast<float>(want * (T - c)),
+                                                                  static_cast<float>(n - k + 1u))), 1u)
+                           : 16u;
+        if constexpr (DENSE_GUESS) {
+            if (T > c && T - 0x41FFu < 0x7C01u) {  // T's value in [-1/8, 1/8)
+                const float vT = __uint_as_float(key_value(T) << 16), vc = __uint_as_float(key_value(c) << 16);
+                const float vg = vT - (vT - vc) * __fdividef(static_cast<float>(want), static_cast<float>(n - k + 1u));
+                const uint32_t kg = value_key(__float_as_uint(vg) >> 16);  // (the key below covers truncation)
+                if (isfinite(vg) && kg > 1u && kg <= T) d = T - (kg - 1u);
+            } else if (T <= c && hint != 0u && hint < T) {
+                d = T - hint;
+            }
+            d = min(d, 127u << 8);  // (gshift <= 8)
+            gshift = 0u;
+            while ((d >> gshift) > 127u) ++gshift;
+        }
         guess = T > d ? T - d : 1u;
     }
 
@@ -635,7 +685,7 @@ struct Row {
         fed = true;
         if (threadIdx.x == 0 && feed_row < p.rows) {
             fence_proxy_async();
-            issue_row(s, st, p, feed_row, feed_V);
+            issue_row(s, st, p, feed_row, feed_V, row_carry != nullptr ? row_carry[feed_row] : 0u);
             advance_feed();
         }
     }
@@ -711,6 +761,7 @@ struct Row {
         // exactly those keys; a cut with too few of them or more than the list
         // holds is dropped for the representatives' cut.
         bool guessed = guess != 0u && !p.force_direct;
+        hint = 0u;
         // This row counts in s.v_cnt[rp] and s.hs[2 + rp], zeroed while the
         // previous row ran; the other pair, last used before the barrier that
         // ended the previous row, is zeroed now for the next one. A retry
@@ -747,8 +798,9 @@ struct Row {
             // the packed compares can apply exactly); c stays the cut found.
             uint32_t cs = c;
             const uint32_t cv = cut_operand(cs);
-            if constexpr (M::BLOCK) survivors_blk(cs, hw);
-            else survivors_tok(cs, cv, hw);
+            const uint32_t sh = DENSE_GUESS && guessed ? gshift : 0u;  // the window's bins: 2^sh keys
+            if constexpr (M::BLOCK) survivors_blk(cs, hw, sh);
+            else survivors_tok(cs, cv, hw, sh);
             stage_table(t0);
             __syncthreads();
             clk.stop(p, TOPK_CNT_CYC_SURVIVORS);
@@ -772,6 +824,7 @@ struct Row {
                 }
                 emit_rescan(c);  // the exact cut (the k-th key), with a crowd of ties at it
                 guess = c > 16u ? c - 16u : 1u;
+                gshift = 0u;
                 clk.stop(p, TOPK_CNT_CYC_FINISH);
                 return;
             }
@@ -787,8 +840,18 @@ struct Row {
             }
             __syncthreads();
             uint32_t b = s.bc[0], above = s.bc[1];
-            uint32_t T = cs + b;
-            if (b < 255u && s.bc[3] <= static_cast<uint32_t>(TIECAP)) {
+            uint32_t T = cs + (b << sh), at_T = s.bc[3];
+            if (sh != 0u && b < 255u) {
+                // Wide bins: the k-th key lies in [T, T + 2^sh), which the
+                // list's radix select places (its first barrier follows every
+                // thread's read of s.bc). The ties at it are not counted: the
+                // stage stays until the row is written.
+                uint32_t a2;
+                T = survivor_select(n, T, T + (1u << sh) - 1u, k - above, a2);
+                above += a2;
+                at_T = static_cast<uint32_t>(TIECAP) + 1u;
+            }
+            if (b < 255u && at_T <= static_cast<uint32_t>(TIECAP)) {
                 // From here on only the list and the tie buffer are read: the
                 // stage takes the next row's copy now, which overlaps the rest.
                 feed();
@@ -814,7 +877,13 @@ struct Row {
     }
 };
 
-static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int32_t V) {
+// Thread 0: the copy of a row into stage st, with the carried word for that
+// row (0: none) in s.v_carry[st]. The copy's arrival on the stage's barrier
+// releases the word, so every thread that waits for the stage reads the same
+// one, whatever other launches write to the carry tables meanwhile.
+static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &p, int32_t row, int32_t V,
+                                                 uint32_t carried) {
+    s.v_carry[st] = carried;
     const uint32_t bytes = static_cast<uint32_t>(V) * 16u;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.logits + static_cast<int64_t>(row) * p.row_stride);
     mbar_expect_tx(&s.full[st], bytes);
@@ -823,9 +892,13 @@ static __device__ __forceinline__ void issue_row(Smem &s, int st, const Params &
 
 };  // struct Tile
 
+// Carried words: bit 31 block rows, bits 27-30 the cut's window shift
+// (DENSE_GUESS builds), bits 16-26 k - 1, bits 0-15 the cut.
+static constexpr uint32_t CARRY_TAG_MASK = 0x87FF0000u;
+
 // The kernel's body. row_carry: NULL, or a table of per-row starting cuts
-// ((k << 16) | cut, bit 31 for block rows) read before each row and rewritten
-// after it (topk_bf16_select_static's variant).
+// (carried words) read as each row's copy is issued and rewritten after the
+// row (topk_bf16_select_static's variant).
 template <class M, int NT, int SURV>
 __device__ __forceinline__ void one_tile_body(const Params &p, uint32_t *row_carry) {
     using O = Tile<NT, SURV>;
@@ -849,19 +922,21 @@ __device__ __forceinline__ void one_tile_body(const Params &p, uint32_t *row_car
 
     typename O::template Row<M> r(s, p);
     r.k = static_cast<uint32_t>(p.k);
-    const uint32_t carry_tag = (M::BLOCK ? 0x80000000u : 0u) | (static_cast<uint32_t>(p.k) << 16);
-    {
-        const uint32_t cw = g_carry[blockIdx.x % CARRY_SLOTS];
-        if ((cw & 0xFFFF0000u) == carry_tag && !p.force_direct) r.guess = cw & 0xFFFFu;
-    }
+    const uint32_t carry_tag = (M::BLOCK ? 0x80000000u : 0u) | ((static_cast<uint32_t>(p.k) - 1u) << 16);
     r.step = step;
     r.feed_row = p.rows;
+    r.row_carry = row_carry;
     if (tid == 0) {
         r.cand_row = static_cast<int32_t>(blockIdx.x);
         if (r.cand_row < p.rows) r.cand_L = __ldg(p.valid_len + r.cand_row);
         r.advance_feed();
+        // The first row carries the cut this CTA slot ended the last launch
+        // with (or, static variant, the row's own when it has one for this k).
+        uint32_t first = g_carry[blockIdx.x % CARRY_SLOTS];
         for (int i = 0; i < NSTAGE && r.feed_row < p.rows; ++i) {
-            O::issue_row(s, i, p, r.feed_row, r.feed_V);
+            uint32_t w = row_carry != nullptr ? row_carry[r.feed_row] : 0u;
+            if ((w & CARRY_TAG_MASK) != carry_tag) w = i == 0 ? first : 0u;
+            O::issue_row(s, i, p, r.feed_row, r.feed_V, w);
             r.advance_feed();
         }
     }
@@ -883,14 +958,17 @@ __device__ __forceinline__ void one_tile_body(const Params &p, uint32_t *row_car
         r.st = st;
         r.fed = false;
         r.orow = p.out + static_cast<int64_t>(row) * p.k;
-        if (row_carry != nullptr) {  // this row's own starting cut, when it has one for this k
-            const uint32_t cw = row_carry[row];
-            if ((cw & 0xFFFF0000u) == carry_tag && !p.force_direct) r.guess = cw & 0xFFFFu;
-        }
         PhaseClock clk;
         clk.start(p);
         mbar_wait_sleep(&s.full[st], (seq / NSTAGE) & 1u, &s.abort_flag);
         clk.stop(p, TOPK_CNT_CYC_WAIT);
+        {  // the row's carried cut, when it has one for this k and mode (see issue_row)
+            const uint32_t cw = s.v_carry[st];
+            if ((cw & CARRY_TAG_MASK) == carry_tag && !p.force_direct) {
+                r.guess = cw & 0xFFFFu;
+                if constexpr (O::DENSE_GUESS) r.gshift = min((cw >> 27) & 15u, 8u);
+            }
+        }
         count_event(p, TOPK_CNT_ROUNDS);
         ++seq;
         clk.start(p);
@@ -898,9 +976,9 @@ __device__ __forceinline__ void one_tile_body(const Params &p, uint32_t *row_car
         __syncthreads();  // every thread is done with this stage and the row's shared state
         clk.stop(p, TOPK_CNT_CYC_SELECT);
         if (!r.fed) r.feed();
-        if (row_carry != nullptr && tid == 0 && r.guess != 0u) row_carry[row] = carry_tag | r.guess;
+        if (row_carry != nullptr && tid == 0 && r.guess != 0u) row_carry[row] = carry_tag | (r.gshift << 27) | r.guess;
     }
-    if (tid == 0 && r.guess != 0u) g_carry[blockIdx.x % CARRY_SLOTS] = carry_tag | r.guess;
+    if (tid == 0 && r.guess != 0u) g_carry[blockIdx.x % CARRY_SLOTS] = carry_tag | (r.gshift << 27) | r.guess;
 }
 
 template <class M, int NT, int SURV>

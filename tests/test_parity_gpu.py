@@ -167,6 +167,22 @@ def test_carried_cut_across_launches():
     assert c["guess_hit"] > 0 and c["guess_miss"] > 0, c
 
 
+def test_dense_cut_carried_across_launches():
+    """Rows that select about half their elements (2048 of 4096, k-th key near
+    zero, where BF16 keys are dense in value) on the large-k build: after the
+    first launch each row starts from a cut set in value, whose window
+    histogram has bins wider than one key and whose k-th key the list's radix
+    select places inside its bin. Launches over different draws stay exact and
+    reuse the carried cut."""
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for seed in range(3):
+        case = W.config2(2048, 4096, 2048, seed=20 + seed)
+        assert tk.plan(case.rows, case.width, case.k, case.mode)["threads"] == 256
+        assert_same_sets(run_gpu(case, counters=counters), run_oracle(case), f"dense {seed}")
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["guess_hit"] > 2048, c
+
+
 def test_carried_cut_across_launches_resident_keys():
     """The resident-keys kernel (wide block rows) starts each cluster's row from
     the k-th key its cluster slot selected last, lowered by a margin, and keeps

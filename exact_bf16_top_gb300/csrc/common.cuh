@@ -194,6 +194,11 @@ __device__ __forceinline__ void cluster_sum(const uint32_t *w, uint32_t C, uint3
     }
 }
 
+__device__ __forceinline__ void red_add_peer(uint32_t addr, uint32_t v) {
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v)
+                 : "memory");
+}
+
 __device__ __forceinline__ void red_max_peer(uint32_t addr, uint32_t v) {
     asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v)
                  : "memory");

@@ -49,6 +49,15 @@
 
 namespace topk {
 
+// Carried thresholds: each cluster slot keeps the k-th key of the last row it
+// selected (tagged with the mode and k). A launch whose clusters take at most
+// one row each starts every row at that key less STREAM_CARRY_MARGIN, which
+// the row's own buffers then accept (k keys at or above it) or reject (the row
+// is streamed again without it): a starting point only.
+constexpr int STREAM_CARRY_SLOTS = 512;
+constexpr uint32_t STREAM_CARRY_MARGIN = 16;
+static __device__ uint32_t g_stream_carry[STREAM_CARRY_SLOTS];
+
 template <int NSTAGE, int CAP>
 struct alignas(128) Smem {
     uint4 stage[NSTAGE][TILE_VEC];           // streamed logits
@@ -72,6 +81,9 @@ struct alignas(128) Smem {
     uint32_t shared_max[2];                  // largest candidate key of the row (max), by row parity
     uint32_t thr_snap;                       // shared_thr as every thread sees it this tile
     uint32_t abort_flag;                     // a bounded wait gave up
+    uint32_t carry_word;                     // rank 0: the carried word this launch starts from
+    uint32_t guess_cnt, guess_nv;            // rank 0: keys at or above it in the first tiles, and
+                                             // those tiles' elements (sums over the cluster)
     uint16_t queue[WARPS][QCAP];             // per-warp vector queues (tile positions)
     unsigned long long full[NSTAGE];         // stage mbarriers
 };
@@ -95,6 +107,7 @@ struct Cta {
     uint32_t tpar = 0;       // parity of the filter tiles: picks s->v_full, s->v_arrive
     uint32_t f_Q = 0, f_next = 0, f_lim = 0;  // this warp's queue, where its appends stopped, the limit
     uint32_t first_c = 0;    // the first tile's cut while its ties are pending (0: none)
+    uint32_t row_T = 0;      // the row's k-th key once selected (0: none)
     bool run_ok = false;     // s->hwin[1] counts every buffer key >= run_lo, in bins key - run_lo
     uint32_t run_lo = 0;     // (the top bin also holding every key >= run_lo + 255)
 
@@ -416,6 +429,54 @@ struct Cta {
         }
         (void)lane;
         return true;
+    }
+
+    // A carried threshold g for this row, checked on the first tile of every
+    // CTA of the cluster before anything is appended: the keys >= g there,
+    // scaled to the row's length, must come to between k and 8k (fewer: g is
+    // likely above the row's k-th key; more: the buffer would churn). Either
+    // way the row then goes on without g, from this same tile. An estimate
+    // only: a row that passes and still has fewer than k keys >= g is caught
+    // at the end (and streamed again). The same answer on every CTA of the
+    // cluster (sums over it, one cluster barrier).
+    __device__ __forceinline__ bool guess_holds(const uint4 *stg, int64_t tile_v0, int nv, uint32_t g) {
+        const int tid = threadIdx.x;
+        mask_tail(stg, tile_v0, nv);  // (this thread's own vector; filter_tile repeats it)
+        uint32_t cnt = 0;
+        if constexpr (M::BLOCK) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int pos = j * THREADS + tid;
+                if (pos < nv) cnt += BlockMode::key(stg[pos], tile_v0 + pos, V) >= g;
+            }
+        } else {
+            uint32_t lo = max(g, KEY_NEG_INF);
+            const uint32_t cv = cut_operand(lo);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int pos = j * THREADS + tid;
+                cnt += __popc(mask8(pos < nv ? stg[pos] : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+                                                                   0xFFFFFFFFu), cv));
+            }
+        }
+        uint32_t total;
+        block_incl_scan(cnt, total);
+        const uint32_t elems = static_cast<uint32_t>(
+            M::BLOCK ? nv : min(static_cast<int64_t>(nv) * 8, static_cast<int64_t>(L) - 8 * tile_v0));
+        uint64_t sum_cnt = total, sum_el = elems;
+        if (C > 1) {
+            if (tid == 0) {
+                red_add_peer(peer_addr(&s->guess_cnt, 0u), total);
+                red_add_peer(peer_addr(&s->guess_nv, 0u), elems);
+            }
+            cluster_arrive();
+            cluster_wait();
+            sum_cnt = ld_peer(peer_addr(&s->guess_cnt, 0u));
+            sum_el = ld_peer(peer_addr(&s->guess_nv, 0u));
+        }
+        const uint64_t row_el = M::BLOCK ? static_cast<uint64_t>(V) : static_cast<uint64_t>(L);
+        const uint64_t est = sum_el ? sum_cnt * row_el / sum_el : 0u;
+        return est >= k && est <= 8ull * k;
     }
 
     // Token mode: the row's last vector, when partial, gets 0xFFFF (a NaN: no
@@ -977,11 +1038,15 @@ struct Cta {
     }
 
     // C == 1: the buffer holds the row's candidates; write its top-k.
-    __device__ __forceinline__ void emit_single() {
+    // guessed: the row started from a carried threshold; with fewer than k
+    // keys at or above it, nothing is written and false is returned (the row
+    // is streamed again without it).
+    __device__ __forceinline__ bool emit_single(bool guessed) {
         s->hwin[1][threadIdx.x] = 0u;  // the index radix's scratch (ordered by the barriers below)
         run_ok = false;
         __syncthreads();
-        const uint32_t n = s->v_count;
+        const uint32_t n = min(s->v_count, static_cast<uint32_t>(CAP));
+        if (guessed && n < k) return false;
         uint32_t T = 0, take = 0;
         if (n > k) {
             // thr - 1 bounds the buffer's k-th key from below (thr is one above a
@@ -992,15 +1057,19 @@ struct Cta {
             if (!bound_select(n, LB, &T, &above))
                 window_select(0, n, buf_lo, max(buffer_max(n), buf_lo), k, &T, &above);
             take = k - above;
+            row_T = T;
         }
         const uint32_t written = emit_selected(n, T, take, 0);
         int32_t *orow = p->out + static_cast<int64_t>(row) * k;
         for (uint32_t i = written + threadIdx.x; i < k; i += THREADS) orow[i] = -1;
+        return true;
     }
 
     // Cluster merge: the C buffers (each its CTA's top-k) give the row's k-th
     // key; ties at it go to the lowest indices, lower-ranked CTAs first.
-    __device__ __forceinline__ void merge_and_emit() {
+    // guessed: as emit_single (the cluster-wide count decides, the same on
+    // every CTA of the cluster).
+    __device__ __forceinline__ bool merge_and_emit(bool guessed) {
         const int tid = threadIdx.x;
         count_event(*p, TOPK_CNT_CLUSTER_MERGES);
         if (s->v_newthr) best_T = max(best_T, s->v_newthr - 1u);  // the last tile's find
@@ -1080,18 +1149,22 @@ struct Cta {
             eq_prev = s->m_pre[1][b2];
         }
         cluster_arrive();  // done reading the peers' shared memory
-        // This CTA's part: keys > T, and its quota of the lowest-index ties.
-        const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
-        const uint32_t offset = gt_prev + min(eq_prev, take);
-        if (!enough) {
-            emit_selected(n, LB - 1u, 0u, offset);  // every key >= LB
-        } else {
-            emit_selected(n, T, quota, offset);
+        const bool missed = guessed && !enough;
+        if (!missed) {
+            // This CTA's part: keys > T, and its quota of the lowest-index ties.
+            const uint32_t quota = take > eq_prev ? take - eq_prev : 0u;
+            const uint32_t offset = gt_prev + min(eq_prev, take);
+            if (!enough) {
+                emit_selected(n, LB - 1u, 0u, offset);  // every key >= LB
+            } else {
+                emit_selected(n, T, quota, offset);
+                row_T = T;
+            }
+            const uint32_t selected_total = enough ? k : total;
+            int32_t *orow = p->out + static_cast<int64_t>(row) * k;
+            for (uint32_t i = selected_total + rank + static_cast<uint32_t>(tid) * C; i < k; i += THREADS * C)
+                orow[i] = -1;
         }
-        const uint32_t selected_total = enough ? k : total;
-        int32_t *orow = p->out + static_cast<int64_t>(row) * k;
-        for (uint32_t i = selected_total + rank + static_cast<uint32_t>(tid) * C; i < k; i += THREADS * C)
-            orow[i] = -1;
         cluster_wait();
         // Every peer is done with this row's shared words: reset them for the
         // row after next (the next row uses the other parity).
@@ -1101,6 +1174,7 @@ struct Cta {
             s->shared_thr[slot] = 0u;
             s->shared_max[slot] = 0u;
         }
+        return !missed;
     }
 };
 
@@ -1124,6 +1198,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         s.shared_max[0] = s.shared_max[1] = 0u;
         s.thr_snap = 0u;
         s.abort_flag = 0u;
+        s.guess_cnt = s.guess_nv = 0u;
     }
     for (int i = 0; i < 4; ++i) s.hwin[i][tid] = 0u;
     s.h_merge[0][tid] = s.h_merge[1][tid] = 0u;
@@ -1131,16 +1206,32 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     grid_dependency_wait();
     if (p.release) grid_dependents_release();
     Feed feed;
+    // One row per cluster at most: a row that misses its carried threshold is
+    // streamed again (the ring has nothing of another row in flight).
+    const bool one_row = ncl >= p.rows;
+    const uint32_t carry_tag = (M::BLOCK ? 0x80000000u : 0u) | (static_cast<uint32_t>(p.k) << 16);
     if (tid == 0) {
         feed_seek(feed, p, M::BLOCK, cid, ncl, C, rank);
         for (int i = 0; i < NSTAGE && feed.row < p.rows; ++i) feed_issue(feed, s, i, p, M::BLOCK, ncl, C, rank);
+        // Read once, by rank 0, so that the whole cluster starts from the same
+        // word whatever other launches write meanwhile.
+        if (rank == 0) s.carry_word = one_row && !p.force_direct ? g_stream_carry[cid % STREAM_CARRY_SLOTS] : 0u;
     }
     if (C > 1) {
         // Every CTA of the cluster has started and zeroed its shared words
         // before any distributed shared memory access.
         cluster_arrive();
         cluster_wait();
+    } else {
+        __syncthreads();
     }
+    uint32_t guess = 0;  // the carried threshold (0: none), the same on every CTA of the cluster
+    {
+        const uint32_t cw = C > 1 ? ld_peer(peer_addr(&s.carry_word, 0u)) : s.carry_word;
+        if ((cw & 0xFFFF0000u) == carry_tag && (cw & 0xFFFFu) > STREAM_CARRY_MARGIN)
+            guess = (cw & 0xFFFFu) - STREAM_CARRY_MARGIN;
+    }
+    uint32_t last_T = 0;
 
     const Params prm = p;
     Cta<M, NSTAGE, CAP> cta;
@@ -1163,12 +1254,17 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
                 p.out[static_cast<int64_t>(row) * p.k + i] = i < n ? transform(p, row, i) : -1;
             continue;
         }
+        // (V >= C: every CTA of the cluster has a share, so every one checks
+        // the threshold on its first tile and meets the others there)
+        bool guessed = guess != 0u && V >= static_cast<int64_t>(C);
+        for (;;) {  // (twice only when a carried threshold misses)
         cta.row = row;
         cta.L = L;
         cta.V = V;
-        cta.thr = M::KMIN;
+        cta.thr = guessed ? max(guess, static_cast<uint32_t>(M::KMIN)) : M::KMIN;
         cta.buf_lo = 0xFFFFu;
         cta.best_T = 0;
+        cta.row_T = 0;
         cta.slot = it & 1u;
         cta.run_ok = false;
         if (tid == 0) {
@@ -1194,8 +1290,13 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             clk.start(p);
             const uint4 *stg = s.stage[st];
             if (i == 0) {
+                if (guessed && !cta.guess_holds(stg, tile_v0, nv, guess)) {
+                    guessed = false;  // the row goes on without the carried threshold
+                    cta.thr = M::KMIN;
+                    if (rank == 0) count_event(p, TOPK_CNT_GUESS_MISS);
+                }
                 cta.thr = max(cta.thr, cta.effective_thr());
-                cta.first_cut(stg, tile_v0, nv);
+                if (!guessed) cta.first_cut(stg, tile_v0, nv);
                 clk.stop(p, TOPK_CNT_CYC_SELECT);
                 clk.start(p);
             }
@@ -1213,14 +1314,29 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         }
         PhaseClock fin;
         fin.start(p);
-        if (C == 1) {
-            cta.emit_single();
-        } else {
-            cta.merge_and_emit();
-        }
+        const bool done = C == 1 ? cta.emit_single(guessed) : cta.merge_and_emit(guessed);
         __syncthreads();
         fin.stop(p, TOPK_CNT_CYC_FINISH);
+        if (guessed && rank == 0) count_event(p, done ? TOPK_CNT_GUESS_HIT : TOPK_CNT_GUESS_MISS);
+        if (done) break;
+        // The carried threshold missed (fewer than k keys at or above it):
+        // stream the row again without it, with the other parity's shared
+        // words. Every thread is past its last read of the stages.
+        guessed = false;
+        ++it;
+        if (tid == 0) {
+            fence_proxy_async();
+            feed_seek(feed, p, M::BLOCK, row, ncl, C, rank);
+            for (int i = 0; i < NSTAGE && feed.row == row; ++i)
+                feed_issue(feed, s, static_cast<int>((seq + i) % NSTAGE), p, M::BLOCK, ncl, C, rank);
+        }
+        cta.snapshot_shared();
+        __syncthreads();
+        }
+        if (cta.row_T != 0u) last_T = cta.row_T;
     }
+    if (rank == 0 && tid == 0 && last_T != 0u && !p.force_direct)
+        g_stream_carry[cid % STREAM_CARRY_SLOTS] = carry_tag | last_T;
 }
 
 constexpr int WIDE_NSTAGE = 2, WIDE_CAP = 4096;

@@ -175,12 +175,16 @@ enum {
     TOPK_CNT_CYC_SURVIVORS = 17, /*   the survivor pass */
     TOPK_CNT_CYC_EXACT = 18,     /*   the exact cut among survivors and the tie appends */
     TOPK_CNT_GUESS_HIT = 19,     /* rows cut by a carried-over cut: one-tile rows by the cut of
-                                    the CTA's previous row, resident-keys rows by the k-th key
-                                    of the cluster's previous row less a margin (checked by
-                                    the exact survivor counts or the window sums) */
+                                    the CTA's previous row, resident-keys and streamed rows by
+                                    the k-th key of the cluster's previous row less a margin
+                                    (checked by the exact survivor counts, the window sums or
+                                    the buffers' final counts) */
     TOPK_CNT_GUESS_MISS = 20,    /* carried-over cuts dropped: fewer than k keys at or above
-                                    it, more survivors than buffer room, or (resident-keys
-                                    rows) the k-th key past the cut's window */
+                                    it, more survivors than buffer room, (resident-keys rows)
+                                    the k-th key past the cut's window, or (streamed rows) a
+                                    first tile whose count above it, scaled to the row, is
+                                    below k or above 8k, or a row streamed again after ending
+                                    with fewer than k keys above it */
     /* streamed rows, later tiles, split (thread 0 of each CTA): */
     TOPK_CNT_CYC_F_PREP = 21,    /*   threshold update, compaction, running-histogram rebuild */
     TOPK_CNT_CYC_F_QUEUE = 22,   /*   candidate-vector queue */

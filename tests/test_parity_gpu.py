@@ -183,6 +183,34 @@ def test_dense_cut_carried_across_launches():
     assert c["guess_hit"] > 2048, c
 
 
+@pytest.mark.parametrize("cluster", [1, 4])
+def test_carried_threshold_across_launches_streamed(cluster):
+    """Streamed rows (one per cluster) start from the k-th key their cluster
+    slot selected last, less a margin, once the first tile's keys above it
+    look like a row's worth; a row that passes that check and still ends with
+    fewer than k keys above it is streamed again. Launches that alternate
+    distributions (N(0,1); 4 N(0,1) - 20; N(0,1) / 4; a few distinct values;
+    ascending rows, whose first tile says nothing about the rest) stay exact,
+    with hits and misses."""
+    rng = np.random.default_rng(41)
+    rows, width = 12, 150000
+    kinds = []
+    for f in (lambda x: x, lambda x: 4.0 * x - 20.0, lambda x: 0.25 * x, lambda x: np.round(3.0 * x) / 2.0,
+              lambda x: np.sort(x, axis=1)):
+        x = f(rng.standard_normal((rows, width), dtype=np.float32))
+        valid = rng.integers(width // 2, width + 1, size=rows).astype(np.int32)
+        kinds.append(W.Case("carry-streamed", W.to_bf16_bits(x), width, valid, 512, W.TOKEN, None))
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    for rep in range(2):
+        for case in kinds:
+            exp = run_oracle(case)
+            for twice in range(2):
+                assert_same_sets(run_gpu(case, counters=counters, path=1, cluster=cluster), exp,
+                                 f"carry-streamed c{cluster} {rep} {twice}")
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    assert c["guess_hit"] > 0 and c["guess_miss"] > 0, c
+
+
 def test_carried_cut_across_launches_resident_keys():
     """The resident-keys kernel (wide block rows) starts each cluster's row from
     the k-th key its cluster slot selected last, lowered by a margin, and keeps

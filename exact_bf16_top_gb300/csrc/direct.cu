@@ -35,7 +35,7 @@ constexpr int NSTAGE = 2;
 // next, first tries that key lowered by CARRY_MARGIN as its cut, which the
 // row's own window sums then accept or reject (a starting point only).
 constexpr int CARRY_SLOTS = 256;
-constexpr uint32_t CARRY_MARGIN = 32;
+constexpr uint32_t CARRY_MARGIN = 12;
 static __device__ uint32_t g_carry[CARRY_SLOTS];
 constexpr int MAX_TILES = RES / TILE_VEC;    // stages per share (block rows; token rows take one)
 constexpr int LIST_CAP = 1280;               // keys >= the cut listed per CTA (more: emitted by a scan)
@@ -112,7 +112,7 @@ struct Share {
         if (!p.force_direct) {  // (uniform: the exact passes start from an empty h[0])
             if (TOPK_IDX_OK(tile * NT + static_cast<int>(threadIdx.x), MAX_TILES * NT))
                 s.rep[tile * NT + static_cast<int>(threadIdx.x)] = static_cast<uint16_t>(best);
-            agg_add(s.h[0], best >> 8, best != 0u);
+            if (guess == 0u) agg_add(s.h[0], best >> 8, best != 0u);  // (else only on a miss)
         }
     }
 
@@ -423,7 +423,7 @@ struct Share {
 
     // The carried cut first: on a miss, every peer is done reading this CTA's
     // window sums before they are cleared, and the row goes on as without it.
-    __device__ bool guess_select(PhaseClock &clk) {
+    __device__ bool guess_select(uint32_t ntiles, PhaseClock &clk) {
         const int tid = threadIdx.x;
         if (tid == 0) s.n_list = s.cursor[0] = s.cursor[1] = 0u;
         __syncthreads();
@@ -439,6 +439,11 @@ struct Share {
             __syncthreads();
         }
         s.h[2][tid] = 0u;
+        // The representatives' high bytes, which the stream left out.
+        for (uint32_t j = 0; j < ntiles; ++j) {
+            const uint32_t r = s.rep[j * NT + static_cast<uint32_t>(tid)];
+            agg_add(s.h[0], r >> 8, r != 0u);
+        }
         __syncthreads();
         return false;
     }
@@ -450,7 +455,7 @@ struct Share {
         bool done = false;
         kth = 0u;
         if (!p.force_direct) {
-            if (guess != 0u) done = guess_select(clk);
+            if (guess != 0u) done = guess_select(ntiles, clk);
             if (!done) done = cut_select(ntiles, clk);
             if (!done) {
                 // Every peer must be done reading h[0] and h[1] before the exact

@@ -53,9 +53,14 @@ namespace topk {
 // selected (tagged with the mode and k). A launch whose clusters take at most
 // one row each starts every row at that key less STREAM_CARRY_MARGIN, which
 // the row's own buffers then accept (k keys at or above it) or reject (the row
-// is streamed again without it): a starting point only.
+// is streamed again without it): a starting point only. A word whose row
+// dropped its threshold carries STREAM_CARRY_DROPPED: the next launch does not
+// try it (rows whose distribution changes from launch to launch then pay the
+// first-tile check every other launch only).
 constexpr int STREAM_CARRY_SLOTS = 512;
 constexpr uint32_t STREAM_CARRY_MARGIN = 16;
+constexpr uint32_t STREAM_CARRY_DROPPED = 1u << 30;
+constexpr uint32_t STREAM_CARRY_TAG_MASK = 0x8FFF0000u;  // mode (bit 31) and k (bits 16-27)
 static __device__ uint32_t g_stream_carry[STREAM_CARRY_SLOTS];
 
 template <int NSTAGE, int CAP>
@@ -1228,10 +1233,12 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
     uint32_t guess = 0;  // the carried threshold (0: none), the same on every CTA of the cluster
     {
         const uint32_t cw = C > 1 ? ld_peer(peer_addr(&s.carry_word, 0u)) : s.carry_word;
-        if ((cw & 0xFFFF0000u) == carry_tag && (cw & 0xFFFFu) > STREAM_CARRY_MARGIN)
+        if ((cw & STREAM_CARRY_TAG_MASK) == carry_tag && !(cw & STREAM_CARRY_DROPPED) &&
+            (cw & 0xFFFFu) > STREAM_CARRY_MARGIN)
             guess = (cw & 0xFFFFu) - STREAM_CARRY_MARGIN;
     }
     uint32_t last_T = 0;
+    bool dropped = false;  // a row of this cluster dropped its carried threshold
 
     const Params prm = p;
     Cta<M, NSTAGE, CAP> cta;
@@ -1292,6 +1299,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
             if (i == 0) {
                 if (guessed && !cta.guess_holds(stg, tile_v0, nv, guess)) {
                     guessed = false;  // the row goes on without the carried threshold
+                    dropped = true;
                     cta.thr = M::KMIN;
                     if (rank == 0) count_event(p, TOPK_CNT_GUESS_MISS);
                 }
@@ -1323,6 +1331,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         // stream the row again without it, with the other parity's shared
         // words. Every thread is past its last read of the stages.
         guessed = false;
+        dropped = true;
         ++it;
         if (tid == 0) {
             fence_proxy_async();
@@ -1336,7 +1345,7 @@ __global__ void __launch_bounds__(THREADS, NSTAGE <= 2 ? 2 : 1) topk_kernel(cons
         if (cta.row_T != 0u) last_T = cta.row_T;
     }
     if (rank == 0 && tid == 0 && last_T != 0u && !p.force_direct)
-        g_stream_carry[cid % STREAM_CARRY_SLOTS] = carry_tag | last_T;
+        g_stream_carry[cid % STREAM_CARRY_SLOTS] = carry_tag | (dropped ? STREAM_CARRY_DROPPED : 0u) | last_T;
 }
 
 constexpr int WIDE_NSTAGE = 2, WIDE_CAP = 4096;

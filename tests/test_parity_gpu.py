@@ -212,6 +212,34 @@ def test_carried_threshold_across_launches_streamed(cluster):
     assert c["guess_hit"] > 0 and c["guess_miss"] > 0, c
 
 
+@pytest.mark.parametrize("cluster", [1, 4])
+def test_streamed_row_again_after_a_late_miss(cluster):
+    """A carried threshold that passes the first-tile check but leaves fewer
+    than k keys above it by the row's end: the rows start from N(0,1) rows'
+    k-th key (about 2.7), and each CTA's first tile holds 120 logits of 4.0
+    among values of 0.25 N(0,1) (at most about 1.3), so the first tiles
+    predict about 2k keys above the threshold while the row holds 480 < k.
+    Every such row is streamed again without it, exactly."""
+    rng = np.random.default_rng(43)
+    rows, width, k = 8, 150000, 512
+    warm = W.Case("warm", W.to_bf16_bits(rng.standard_normal((rows, width), dtype=np.float32)), width,
+                  np.full(rows, width, np.int32), k, W.TOKEN, None)
+    x = 0.25 * rng.standard_normal((rows, width), dtype=np.float32)
+    V = width // 8
+    for r in range(rows):
+        for rank in range(4):  # the first tile of each of four equal shares
+            start = 8 * (V * rank // 4)
+            x[r, start + rng.choice(8000, size=120, replace=False)] = 4.0
+    late = W.Case("late", W.to_bf16_bits(x), width, np.full(rows, width, np.int32), k, W.TOKEN, None)
+    for _ in range(3):
+        assert_same_sets(run_gpu(warm, path=1, cluster=cluster), run_oracle(warm), "warm")
+    counters = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    assert_same_sets(run_gpu(late, counters=counters, path=1, cluster=cluster), run_oracle(late), "late")
+    c = dict(zip(tk.COUNTER_NAMES, counters.cpu().numpy().tolist()))
+    # every row missed once and was streamed twice (tiles counted per CTA)
+    assert c["guess_miss"] == rows and c["rounds"] >= 2 * rows * cluster * (V // cluster // 2048), c
+
+
 def test_carried_cut_across_launches_resident_keys():
     """The resident-keys kernel (wide block rows) starts each cluster's row from
     the k-th key its cluster slot selected last, lowered by a margin, and keeps

@@ -24,8 +24,10 @@ namespace topk {
 // cluster-wide histogram of key - c finds the exact k-th key, and every CTA
 // writes its own selected indices from its list of those keys. The exact
 // fallback (two 8-bit radix passes over every key) takes the rows where the
-// representatives cannot bound the k-th key. Used where a buffer would churn:
-// block rows, whose k is large next to a CTA's share.
+// representatives cannot bound the k-th key. Before all that, a cluster tries
+// the k-th key its slot selected last, less a margin, as c (see g_carry); the
+// representatives' histogram is then built only if that cut misses. Used where
+// a buffer would churn: block rows, whose k is large next to a CTA's share.
 
 namespace direct {
 

@@ -21,18 +21,20 @@
 // there are many.
 //
 // The first stage ("tile": 256 threads x 8 vectors) of a CTA's share is
-// selected exactly. Its cutoff comes from group representatives: each thread
-// splits its logits into groups of g and takes one element of each group, the
-// packed signed maximum of its BF16 bits (the group maximum whenever the group
-// holds a non-negative value). The k-th largest representative, found with a
-// 12-bit histogram, bounds the tile's k-th key from below, because k distinct
-// elements reach it; keys above it sit in about k groups, so they are few. Those
-// survivors go to the buffer and their exact k-th comes from a histogram
-// relative to the cutoff. When the representatives cannot bound the tile, or
-// the survivors overflow, every key becomes its own representative (g = 1): the
-// exact path. Later tiles append every key at or above a running threshold,
-// which rises whenever the buffer is compacted to its top-k and, in a cluster,
-// when a peer CTA publishes its own bound through distributed shared memory.
+// selected exactly. Its cutoff comes from group representatives: one element
+// of each group (token rows with room for 2k of them: every 16-byte vector, its
+// largest logit, held in registers; otherwise groups of 4 to 64 elements). The
+// k-th largest representative bounds the tile's k-th key from below, because k
+// distinct elements reach it; keys above it sit in about k groups, so they are
+// few. Those survivors go to the buffer and their exact k-th comes from a
+// histogram relative to the cutoff. When the representatives cannot bound the
+// tile, or the survivors overflow, every key becomes its own representative
+// (g = 1): the exact path. Later tiles append every key at or above a running
+// threshold, which rises whenever the buffer is compacted to its top-k and, in
+// a cluster, when a peer CTA publishes its own bound through distributed shared
+// memory. A launch whose clusters take one row each may instead start every
+// row at the threshold its cluster slot carried over from the previous launch
+// (see g_stream_carry), checked on the first tiles and by the final counts.
 //
 // In token rows every thread forms the 8-bit masks of its vectors' logits at
 // or above the threshold with packed BF16 compares (NaN never passes), and a
@@ -41,7 +43,8 @@
 // the warp's lanes work through the queue together. The C buffers
 // of a row are merged with cluster-wide histograms over distributed shared
 // memory; ties at the row's k-th key are split across CTAs in index order, and
-// each CTA writes its part of the answer through the block table.
+// each CTA writes its part of the answer through the block table, every
+// output slot from one CTA scan of (ties, above) counts.
 // The packed BF16 compares decide exactly what a compare of the 16-bit keys
 // decides (NaN never passes); every count, cut and histogram is on the keys.
 
